@@ -1,0 +1,474 @@
+// decode.cu -- batch-1..8 decode path: embedding gather, RMSNorm-fused split
+// GEMV with its epilogues (bias, residual add, SwiGLU, LM head + argmax),
+// split-KV flash-decoding GQA attention with the fused q/k-norm + RoPE + KV
+// write, and the end-of-step argmax write-back / cursor advance.
+//
+// Pages: ember scripts/reference_forward.py forward() (the per-token layer
+// loop this path runs, one token per sequence); ember internals "kv cache"
+// (cursor advances after all layers, explicit positions) and "grouped-query
+// attention" (query head h reads kv head h / G).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ember {
+
+// ============================================================== embedding ==
+__global__ void k_embed(EmbedArgs a) {
+    const int t = blockIdx.x;
+    __shared__ int s_id;
+    if (threadIdx.x == 0) {
+        int id = a.ids[t];
+        int ok = 1;
+        if (id < 0 || id >= a.V) {          // Falcon-H1 logits(): token outside vocabulary
+            raise_status(a.status, EMBER_ERR_TOKEN);
+            id = 0;
+            ok = 0;
+        }
+        if (a.seqs) {
+            const int seq = a.seqs[t], pos = a.positions[t];
+            if (seq < 0 || seq >= a.max_seqs) {
+                raise_status(a.status, EMBER_ERR_INVALID_ARG);
+                ok = 0;
+            } else if (pos < 0 || pos >= a.max_len) {
+                raise_status(a.status, EMBER_ERR_CAPACITY);
+                ok = 0;
+            } else if (pos != a.cursor[seq]) {  // ember internals: explicit pos == cursor
+                raise_status(a.status, EMBER_ERR_STATE);
+            }
+            a.tok_ok[t] = ok;
+        }
+        if (t == 0 && a.pf_seq >= 0 && a.cursor[a.pf_seq] != a.pf_start)
+            raise_status(a.status, EMBER_ERR_STATE);
+        s_id = id;
+    }
+    __syncthreads();
+    const uint16_t* row = a.E + (size_t)s_id * a.H;
+    float* out = a.x + (size_t)t * a.H;
+    for (int i = threadIdx.x; i < a.H; i += blockDim.x) out[i] = bf16_to_f32(row[i]);
+}
+
+void launch_embed(const EmbedArgs& a, cudaStream_t s) {
+    k_embed<<<a.n, 256, 0, s>>>(a);
+}
+
+// =================================================================== GEMV ==
+// One CTA of 256 threads handles tiles of R = 256/TPR consecutive weight rows;
+// TPR threads share a row, each issuing up to MAXJ independent 16-byte loads
+// before any arithmetic so that ~R*K*2 bytes per CTA are in flight.  The grid
+// is persistent (a few CTAs per SM striding over tiles) so the RMSNorm
+// statistics of the nb input rows are computed once per CTA.
+constexpr int GEMV_THREADS = 256;
+constexpr int GEMV_MAXJ = 8;
+
+template <int TPR, int NB>
+__global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
+    constexpr int R = GEMV_THREADS / TPR;
+    constexpr int GL = TPR < 32 ? TPR : 32;       // lanes reduced by shuffles
+    constexpr int WPR = TPR > 32 ? TPR / 32 : 1;  // warps per row
+    __shared__ float s_red[32];
+    __shared__ float s_rinv[NB];
+    __shared__ float s_part[R][WPR][NB];
+    __shared__ unsigned long long s_key[NB];
+
+    const int tid = threadIdx.x;
+    const int r = tid / TPR, sub = tid % TPR;
+    const int K8 = a.K >> 3;
+    const int nb = a.nb;
+
+    // RMSNorm statistics of every input row (ember reference_forward.py rmsnorm()).
+    for (int b = 0; b < NB; ++b) {
+        float rinv = 1.f;
+        if (a.norm_w && b < nb) {
+            const float* xb = a.x + (size_t)b * a.ldx;
+            float ss = 0.f;
+            for (int i = tid; i < a.K; i += GEMV_THREADS) ss += xb[i] * xb[i];
+            ss = block_sum(ss, s_red);
+            rinv = rsqrtf(ss / (float)a.K + a.eps);
+        }
+        if (tid == 0) s_rinv[b] = rinv;
+    }
+    if (tid < NB) s_key[tid] = 0ull;
+    __syncthreads();
+
+    unsigned long long best[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) best[b] = 0ull;
+
+    const int n_tiles = (a.N + R - 1) / R;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int row = tile * R + r;
+        const bool rv = row < a.N;
+        const uint4* wrow = reinterpret_cast<const uint4*>(a.W + (size_t)(rv ? row : 0) * a.K);
+        uint4 w[GEMV_MAXJ];
+#pragma unroll
+        for (int j = 0; j < GEMV_MAXJ; ++j) {
+            const int c = sub + j * TPR;
+            if (rv && c < K8) w[j] = ld_stream(wrow + c);
+        }
+        float acc[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+#pragma unroll
+        for (int j = 0; j < GEMV_MAXJ; ++j) {
+            const int c = sub + j * TPR;
+            if (rv && c < K8) {
+                float wf[8];
+                unpack8(w[j], wf);
+                if (a.norm_w) {
+                    const float4 n0 = reinterpret_cast<const float4*>(a.norm_w)[2 * c];
+                    const float4 n1 = reinterpret_cast<const float4*>(a.norm_w)[2 * c + 1];
+                    wf[0] *= n0.x; wf[1] *= n0.y; wf[2] *= n0.z; wf[3] *= n0.w;
+                    wf[4] *= n1.x; wf[5] *= n1.y; wf[6] *= n1.z; wf[7] *= n1.w;
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    if (b < nb) {
+                        const float4* xp =
+                            reinterpret_cast<const float4*>(a.x + (size_t)b * a.ldx) + 2 * c;
+                        const float4 x0 = xp[0], x1 = xp[1];
+                        float s = acc[b];
+                        s = fmaf(wf[0], x0.x, s); s = fmaf(wf[1], x0.y, s);
+                        s = fmaf(wf[2], x0.z, s); s = fmaf(wf[3], x0.w, s);
+                        s = fmaf(wf[4], x1.x, s); s = fmaf(wf[5], x1.y, s);
+                        s = fmaf(wf[6], x1.z, s); s = fmaf(wf[7], x1.w, s);
+                        acc[b] = s;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+            for (int o = GL / 2; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(FULL_MASK, acc[b], o);
+        }
+        if ((tid & (GL - 1)) == 0) {
+            const int wp = TPR > 32 ? (sub >> 5) : 0;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) s_part[r][wp][b] = acc[b];
+        }
+        __syncthreads();
+        // Epilogue: thread e handles (row r_e, token b_e).
+        if (tid < R * NB) {
+            const int re = tid / NB, be = tid % NB;
+            const int rowe = tile * R + re;
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < WPR; ++q) v += s_part[re][q][be];
+            v *= s_rinv[be];
+            if (rowe < a.N && be < nb) {
+                float* o = a.out + (size_t)be * a.ldo;
+                if (a.mode == EPI_STORE) {
+                    o[rowe] = a.bias ? v + a.bias[rowe] : v;
+                } else if (a.mode == EPI_RESID) {
+                    o[rowe] += v;
+                } else if (a.mode == EPI_ARGMAX) {
+                    if (a.out) o[rowe] = v;
+                    const unsigned long long k = argmax_key(v, (uint32_t)rowe);
+                    best[be] = k > best[be] ? k : best[be];
+                }
+            }
+            if (a.mode == EPI_SWIGLU) s_part[re][0][be] = v;   // re-used below
+        }
+        if (a.mode == EPI_SWIGLU) {
+            __syncthreads();
+            // rows 2i (gate) and 2i+1 (up): act_i = silu(gate) * up
+            if (tid < (R / 2) * NB) {
+                const int pi = tid / NB, be = tid % NB;
+                const int rg = tile * R + 2 * pi;
+                if (rg + 1 < a.N && be < nb) {
+                    const float g = s_part[2 * pi][0][be], u = s_part[2 * pi + 1][0][be];
+                    a.out[(size_t)be * a.ldo + (rg >> 1)] = g / (1.f + __expf(-g)) * u;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    if (a.mode == EPI_ARGMAX) {
+        if (tid < R * NB) {
+            const int be = tid % NB;
+            if (be < nb) atomicMax(&s_key[be], best[be]);
+        }
+        __syncthreads();
+        if (tid < nb) atomicMax(&a.keys[tid], s_key[tid]);
+    }
+}
+
+template <int TPR>
+static void gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
+    if (a.nb <= 1) k_gemv<TPR, 1><<<grid, GEMV_THREADS, 0, s>>>(a);
+    else if (a.nb <= 2) k_gemv<TPR, 2><<<grid, GEMV_THREADS, 0, s>>>(a);
+    else if (a.nb <= 4) k_gemv<TPR, 4><<<grid, GEMV_THREADS, 0, s>>>(a);
+    else k_gemv<TPR, 8><<<grid, GEMV_THREADS, 0, s>>>(a);
+}
+
+void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
+    const int K8 = a.K >> 3;
+    int tpr = 8;
+    while (tpr * GEMV_MAXJ < K8) tpr <<= 1;   // <= 8 loads per thread
+    // SwiGLU pairs rows 2i / 2i+1 inside one tile: at least two rows per tile
+    // (model validation keeps K <= 8192 for that projection).
+    if (a.mode == EPI_SWIGLU && tpr > 128) tpr = 128;
+    const int R = GEMV_THREADS / tpr;
+    const int tiles = (a.N + R - 1) / R;
+    const int grid = tiles < num_sms * 8 ? tiles : num_sms * 8;
+    switch (tpr) {
+        case 8: gemv_nb<8>(a, s, grid); break;
+        case 16: gemv_nb<16>(a, s, grid); break;
+        case 32: gemv_nb<32>(a, s, grid); break;
+        case 64: gemv_nb<64>(a, s, grid); break;
+        case 128: gemv_nb<128>(a, s, grid); break;
+        default: gemv_nb<256>(a, s, grid); break;
+    }
+}
+
+// ========================================================= decode attention ==
+// CTA (split s, kv head g, token b), 128 threads.  Keys [0, pos] are divided
+// evenly over gridDim.x splits; each split streams its K/V rows through
+// shared memory in tiles of 64 and keeps an online softmax (running max m,
+// sum l, output acc) per query head, in the base-2 domain.
+constexpr int ATT_THREADS = 128;
+constexpr int ATT_TK = 64;
+constexpr int ATT_MAXG = 16;
+
+template <int D>
+__global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
+    constexpr int H2 = D / 2;
+    constexpr int KP = D + 2;   // padded K row (bf16 elements): conflict-free row reads
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int S = gridDim.x;
+    const int G = a.NH / a.NKV;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    __shared__ float s_q[ATT_MAXG][D];
+    __shared__ __align__(16) uint16_t s_k[ATT_TK][KP];
+    __shared__ __align__(16) uint16_t s_v[ATT_TK][D];
+    __shared__ float s_sc[ATT_MAXG][ATT_TK];
+    __shared__ float s_m[ATT_MAXG], s_l[ATT_MAXG], s_scale[ATT_MAXG];
+    __shared__ float s_kv[2][D];
+    __shared__ int s_last;
+
+    if (!a.tok_ok[b]) return;   // the embed kernel flagged this token
+    const int pos = a.positions[b];
+    const int seq = a.seqs[b];
+    const int n_keys = pos + 1;
+    const int per = (n_keys + S - 1) / S;
+    const int lo = split * per;
+    const int hi = min(n_keys, lo + per);
+    const float* qkv = a.qkv + (size_t)b * a.ld_qkv;
+    const float* cs = a.cos_t + (size_t)pos * H2;
+    const float* sn = a.sin_t + (size_t)pos * H2;
+    const size_t head_off = (((size_t)seq * a.L + a.layer) * a.NKV + g) * (size_t)a.max_len * D;
+    uint16_t* kc = a.kc + head_off;
+    uint16_t* vc = a.vc + head_off;
+    // log2(e)/sqrt(D): scores in the base-2 domain
+    const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+
+    // ---- q of the G heads: optional per-head RMSNorm, then RoPE ----
+    for (int e = tid; e < G * D; e += ATT_THREADS) s_q[e / D][e % D] = qkv[(g * G) * D + e];
+    for (int e = tid; e < 2 * D; e += ATT_THREADS) {
+        const int which = e / D, d = e % D;   // 0: k, 1: v
+        s_kv[which][d] = qkv[a.NH * D + which * a.NKV * D + g * D + d];
+    }
+    __syncthreads();
+    if (a.q_norm) {   // PII-Tracer forward(): per-head RMSNorm before RoPE
+        for (int h = warp; h < G + 1; h += ATT_THREADS / 32) {
+            float* v = h < G ? s_q[h] : s_kv[0];
+            const float* w = h < G ? a.q_norm : a.k_norm;
+            float ss = 0.f;
+            for (int d = lane; d < D; d += 32) ss += v[d] * v[d];
+            ss = warp_sum(ss);
+            const float ri = rsqrtf(ss / (float)D + a.eps);
+            __syncwarp();
+            for (int d = lane; d < D; d += 32) v[d] = v[d] * ri * w[d];
+        }
+        __syncthreads();
+    }
+    // RoPE of q (kept f32, pre-scaled) and of k (rounded to bf16 = the cache value)
+    for (int e = tid; e < (G + 1) * H2; e += ATT_THREADS) {
+        const int h = e / H2, i = e % H2;
+        float* v = h < G ? s_q[h] : s_kv[0];
+        float r0, r1;
+        rope_pair(v[i], v[i + H2], cs[i], sn[i], r0, r1);
+        if (h < G) {
+            v[i] = r0 * qscale;
+            v[i + H2] = r1 * qscale;
+        } else {
+            v[i] = r0;
+            v[i + H2] = r1;
+        }
+    }
+    __syncthreads();
+    // The split that owns position pos writes the new K/V row before reading.
+    if (pos >= lo && pos < hi) {
+        for (int d = tid; d < D; d += ATT_THREADS) {
+            kc[(size_t)pos * D + d] = f32_to_bf16(s_kv[0][d]);
+            vc[(size_t)pos * D + d] = f32_to_bf16(s_kv[1][d]);
+        }
+    }
+    if (tid < G) {
+        s_m[tid] = -INFINITY;
+        s_l[tid] = 0.f;
+    }
+    __syncthreads();
+
+    // each thread owns output elements e = tid + i*128 of the [G][D] block
+    constexpr int MAXE = (ATT_MAXG * D + ATT_THREADS - 1) / ATT_THREADS;
+    float acc[MAXE];
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) acc[i] = 0.f;
+
+    for (int t0 = lo; t0 < hi; t0 += ATT_TK) {
+        const int nt = min(ATT_TK, hi - t0);
+        // stage K (padded rows) and V
+        constexpr int C8 = D / 8;
+        for (int e = tid; e < nt * C8; e += ATT_THREADS) {
+            const int j = e / C8, c = e % C8;
+            const uint4 kv4 = *reinterpret_cast<const uint4*>(kc + (size_t)(t0 + j) * D + c * 8);
+            const uint4 vv4 = *reinterpret_cast<const uint4*>(vc + (size_t)(t0 + j) * D + c * 8);
+            uint32_t* kd = reinterpret_cast<uint32_t*>(&s_k[j][c * 8]);
+            kd[0] = kv4.x; kd[1] = kv4.y; kd[2] = kv4.z; kd[3] = kv4.w;
+            *reinterpret_cast<uint4*>(&s_v[j][c * 8]) = vv4;
+        }
+        __syncthreads();
+        // scores: thread -> key j = tid % 64, heads h = tid/64, +2, ...
+        {
+            const int j = tid % ATT_TK;
+            for (int h = tid / ATT_TK; h < G; h += ATT_THREADS / ATT_TK) {
+                float sc = -INFINITY;
+                if (j < nt) {
+                    const uint32_t* kr = reinterpret_cast<const uint32_t*>(s_k[j]);
+                    float dot = 0.f;
+#pragma unroll 8
+                    for (int d2 = 0; d2 < H2; ++d2) {
+                        const uint32_t kk = kr[d2];
+                        dot = fmaf(s_q[h][2 * d2], bf16_lo(kk), dot);
+                        dot = fmaf(s_q[h][2 * d2 + 1], bf16_hi(kk), dot);
+                    }
+                    sc = dot;
+                }
+                s_sc[h][j] = sc;
+            }
+        }
+        __syncthreads();
+        // online softmax update, one warp per head
+        for (int h = warp; h < G; h += ATT_THREADS / 32) {
+            const float v0 = s_sc[h][lane], v1 = s_sc[h][lane + 32];
+            const float tm = warp_max(fmaxf(v0, v1));
+            const float mo = s_m[h];
+            const float mn = fmaxf(mo, tm);
+            const float p0 = exp2f(v0 - mn), p1 = exp2f(v1 - mn);
+            const float ps = warp_sum(p0 + p1);
+            s_sc[h][lane] = p0;
+            s_sc[h][lane + 32] = p1;
+            __syncwarp();
+            if (lane == 0) {
+                const float sc = exp2f(mo - mn);   // 0 when mo == -inf
+                s_scale[h] = sc;
+                s_l[h] = s_l[h] * sc + ps;
+                s_m[h] = mn;
+            }
+        }
+        __syncthreads();
+        // acc = acc*scale + P V
+#pragma unroll
+        for (int i = 0; i < MAXE; ++i) {
+            const int e = tid + i * ATT_THREADS;
+            if (e < G * D) {
+                const int h = e / D, d = e % D;
+                float s = acc[i] * s_scale[h];
+                for (int j = 0; j < nt; ++j) s = fmaf(s_sc[h][j], bf16_to_f32(s_v[j][d]), s);
+                acc[i] = s;
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- write this split's partial (m, l, acc) ----
+    float* part = a.part + ((((size_t)b * a.NKV + g) * S + split) * G) * (D + 2);
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+        const int e = tid + i * ATT_THREADS;
+        if (e < G * D) part[(size_t)(e / D) * (D + 2) + 2 + (e % D)] = acc[i];
+    }
+    if (tid < G) {
+        part[(size_t)tid * (D + 2) + 0] = s_m[tid];
+        part[(size_t)tid * (D + 2) + 1] = s_l[tid];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned done = atomicAdd(&a.counters[b * a.NKV + g], 1u);
+        s_last = (done == (unsigned)(S - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last split: merge all S partials (log-sum-exp rescale) ----
+    const float* pb = a.part + (((size_t)b * a.NKV + g) * S) * G * (D + 2);
+    for (int e = tid; e < G * D; e += ATT_THREADS) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < S; ++s2) {
+            const volatile float* ps = pb + ((size_t)s2 * G + h) * (D + 2);
+            if (ps[1] > 0.f) M = fmaxf(M, ps[0]);
+        }
+        float L = 0.f, O = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+            const volatile float* ps = pb + ((size_t)s2 * G + h) * (D + 2);
+            const float l = ps[1];
+            if (l > 0.f) {   // empty splits contribute nothing (no NaN)
+                const float f = exp2f(ps[0] - M);
+                L += l * f;
+                O += ps[2 + d] * f;
+            }
+        }
+        const size_t oi = (size_t)b * a.NH * D + (size_t)(g * G + h) * D + d;
+        if (a.att_b) a.att_b[oi] = f32_to_bf16(O / L);
+        else a.att[oi] = O / L;
+    }
+    if (tid == 0) a.counters[b * a.NKV + g] = 0u;
+}
+
+void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s) {
+    dim3 grid(a.splits, a.NKV, a.nb);
+    switch (a.D) {
+        case 16: k_attn_decode<16><<<grid, ATT_THREADS, 0, s>>>(a); break;
+        case 32: k_attn_decode<32><<<grid, ATT_THREADS, 0, s>>>(a); break;
+        case 64: k_attn_decode<64><<<grid, ATT_THREADS, 0, s>>>(a); break;
+        case 128: k_attn_decode<128><<<grid, ATT_THREADS, 0, s>>>(a); break;
+        default: break;   // rejected by model validation
+    }
+}
+
+// ================================================================== finish ==
+__global__ void k_finish(FinishArgs a) {
+    const int b = threadIdx.x;
+    if (b < a.nb) {
+        if (a.argmax) a.argmax[b] = argmax_key_index(a.keys[b]);
+        a.keys[b] = 0ull;
+        if (a.seqs && a.tok_ok[b]) a.cursor[a.seqs[b]] = a.positions[b] + 1;
+    }
+    if (b == 0 && a.pf_seq >= 0) a.cursor[a.pf_seq] = a.pf_end;
+}
+
+void launch_finish(const FinishArgs& a, cudaStream_t s) {
+    const int th = a.nb < 32 ? 32 : ((a.nb + 31) / 32) * 32;
+    k_finish<<<1, th, 0, s>>>(a);
+}
+
+// ================================================================ repack ==
+__global__ void k_bf16_to_f32(const uint16_t* in, float* out, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = bf16_to_f32(in[i]);
+}
+
+void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s) {
+    if (n <= 0) return;
+    long long blocks = (n + 255) / 256;
+    k_bf16_to_f32<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n);
+}
+
+}  // namespace ember

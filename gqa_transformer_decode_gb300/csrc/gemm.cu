@@ -1,0 +1,378 @@
+// gemm.cu -- tcgen05 / TMEM tensor-core GEMM fed by TMA, with the fused
+// epilogues of the projections (bias, residual add, SwiGLU).
+//
+//   D[M,N] = A[M,K] . B[N,K]^T      A: activations (bf16, K contiguous)
+//                                   B: weights, HF [out, in] (bf16, K contiguous)
+//
+// One CTA computes a BM x BN tile (BM = 128 rows of A = 128 TMEM lanes, BN f32
+// accumulator columns).  Warp roles:
+//   warp 0   one thread issues the TMA loads of A and B k-blocks (BK = 64
+//            elements = one 128-byte swizzle span) into a STAGES-deep ring;
+//   warp 1   allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
+//            K=16 per instruction, 4 per k-block) and commits each stage back
+//            to the producer, then commits the finished accumulator;
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//            32*(w%4)..+31), apply the fused epilogue, store to global.
+// Every mbarrier wait is bounded (~1 s of clock64); a timeout raises
+// EMBER_ERR_TIMEOUT, waits (bounded) for copies still in flight, frees TMEM
+// and returns.
+//
+// The projections this serves: q/k/v (+bias), o_proj (+residual), gate/up
+// (SwiGLU) and down (+residual) of ember scripts/reference_forward.py
+// forward(), in the whole-sequence form of LowLlamaBasic reference.py.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ember {
+
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BK = 64;
+constexpr int GEMM_THREADS = 192;
+constexpr long long WAIT_CYCLES = 1ll << 31;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(addr, parity)) {
+        if (clock64() - t0 > WAIT_CYCLES) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(tm), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride
+// byte offset), descriptor version 1, layout SWIZZLE_128B.  The leading byte
+// offset is unused for this layout.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3ffffu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              int M, int N, int K, GemmEpilogue e, int* status) {
+    constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+    constexpr int B_BYTES = BN * GEMM_BK * 2;
+    constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+    int* sflag = reinterpret_cast<int*>(tmem_slot + 1);   // [0] failed, [1] issued, [2] consumed
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * GEMM_BM;
+    const int nk = (K + GEMM_BK - 1) / GEMM_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        sflag[0] = 0;
+        sflag[1] = 0;
+        sflag[2] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_u32(tmem_slot)),
+            "r"((uint32_t)BN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer
+            int kb = 0;
+            for (; kb < nk; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t it = (uint32_t)(kb / STAGES);
+                if (!mbar_wait(&empty[s], (it & 1u) ^ 1u)) {
+                    sflag[0] = 1;
+                    break;
+                }
+                uint8_t* sa = smem + s * STAGE_BYTES;
+                mbar_expect_tx(&full[s], STAGE_BYTES);
+                tma_load_2d(sa, &tmA, kb * GEMM_BK, m0, &full[s]);
+                tma_load_2d(sa + A_BYTES, &tmB, kb * GEMM_BK, n0, &full[s]);
+            }
+            sflag[1] = kb;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16(GEMM_BM, BN);
+            int kb = 0;
+            for (; kb < nk; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t it = (uint32_t)(kb / STAGES);
+                if (!mbar_wait(&full[s], it & 1u)) {
+                    sflag[0] = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+                const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < GEMM_BK / 16; ++k) {
+                    umma_bf16(tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                              (kb > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);   // frees the stage once these MMAs have read it
+            }
+            sflag[2] = kb;
+            umma_commit(tfull);           // accumulator complete (after all issued MMAs)
+        }
+    } else {   // ---------------- epilogue warps 2..5
+        const int q = warp & 3;
+        const int row = m0 + q * 32 + lane;
+        if (!mbar_wait(tfull, 0)) {
+            sflag[0] = 1;
+        } else {
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld16(tbase + c, r);
+                tmem_ld16(tbase + c + 16, r + 16);
+                tmem_ld_wait();
+                const int n = n0 + c;
+                if (row >= M || n >= N) continue;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                const bool fullc = (n + 32 <= N);
+                if (e.mode == EPI_SWIGLU) {
+                    // columns 2i / 2i+1 = gate_i / up_i -> output column n/2 + i
+                    uint16_t* o = e.out_bf16 + (size_t)row * e.ldo + (n >> 1);
+                    if (fullc) {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float g0 = v[4 * i], u0 = v[4 * i + 1];
+                            const float g1 = v[4 * i + 2], u1 = v[4 * i + 3];
+                            pk[i] = pack_bf16x2(g0 / (1.f + __expf(-g0)) * u0,
+                                                g1 / (1.f + __expf(-g1)) * u1);
+                        }
+                        uint4* o4 = reinterpret_cast<uint4*>(o);
+                        o4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        o4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    } else {
+                        for (int i = 0; i < 16 && n + 2 * i + 1 < N; ++i) {
+                            const float g = v[2 * i], u = v[2 * i + 1];
+                            o[i] = f32_to_bf16(g / (1.f + __expf(-g)) * u);
+                        }
+                    }
+                } else {
+                    float* o = e.out_f32 + (size_t)row * e.ldo + n;
+                    if (e.mode == EPI_STORE && e.bias) {
+                        for (int i = 0; i < 32; ++i)
+                            if (n + i < N) v[i] += e.bias[n + i];
+                    }
+                    if (fullc) {
+                        float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float4 t = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                            if (e.mode == EPI_RESID) {
+                                const float4 x = o4[i];
+                                t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
+                            }
+                            o4[i] = t;
+                        }
+                    } else {
+                        for (int i = 0; i < 32 && n + i < N; ++i)
+                            o[i] = (e.mode == EPI_RESID) ? o[i] + v[i] : v[i];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && sflag[0]) raise_status(status, EMBER_ERR_TIMEOUT);
+    if (warp == 0 && lane == 0 && sflag[0]) {
+        // drain TMA copies that were issued but never consumed
+        for (int kb = sflag[2]; kb < sflag[1]; ++kb)
+            (void)mbar_wait(&full[kb % STAGES], (uint32_t)(kb / STAGES) & 1u);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)BN));
+    }
+}
+
+// ------------------------------------------------------------------- host --
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+static bool make_map(void* out, const uint16_t* ptr, int rows, int ld, int K, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld % 8) || (K % 8)) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)GEMM_BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<uint16_t*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int pick_bn(int N) {
+    if (N <= 64) return 64;
+    if (N <= 1024) return 128;
+    return 256;
+}
+
+bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16_t* B, int N,
+                    int ldb, int K) {
+    static_assert(sizeof(CUtensorMap) <= sizeof(p.tmA), "tensor map size");
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bn = pick_bn(N);
+    p.ok = make_map(p.tmA, A, M, lda, K, GEMM_BM) && make_map(p.tmB, B, N, ldb, K, p.bn);
+    return p.ok;
+}
+
+template <int BN, int STAGES>
+static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
+                      cudaStream_t s) {
+    constexpr int STAGE_BYTES = (GEMM_BM + BN) * GEMM_BK * 2;
+    constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_gemm_tc<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM);
+        attr = true;
+    }
+    dim3 grid((p.N + BN - 1) / BN, (m_rows + GEMM_BM - 1) / GEMM_BM);
+    const CUtensorMap* ta = reinterpret_cast<const CUtensorMap*>(p.tmA);
+    const CUtensorMap* tb = reinterpret_cast<const CUtensorMap*>(p.tmB);
+    k_gemm_tc<BN, STAGES><<<grid, GEMM_THREADS, SMEM, s>>>(*ta, *tb, m_rows, p.N, p.K, e, status);
+}
+
+void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
+                 cudaStream_t s) {
+    if (m_rows <= 0) return;
+    switch (p.bn) {
+        case 64: launch_bn<64, 8>(p, m_rows, e, status, s); break;
+        case 128: launch_bn<128, 6>(p, m_rows, e, status, s); break;
+        default: launch_bn<256, 4>(p, m_rows, e, status, s); break;
+    }
+}
+
+}  // namespace ember

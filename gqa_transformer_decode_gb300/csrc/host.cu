@@ -1,0 +1,861 @@
+// host.cu -- the C ABI of include/ember.h: configuration checks, weight
+// repack into the device layout, workspace and KV-cache ownership, and the
+// launch sequences of prefill, decode and encode.
+//
+// Shape of the interface: ember internals, "ForwardModel trait"
+// (create_cache(max_seq_len); forward_with_cache(ids, cache, start_pos)) and
+// "kv cache" (one block per layer, cursor advanced after all layers, explicit
+// positions); argument errors after Falcon-H1-0.5B-Rust Config::validate,
+// logits() and generate().
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace ember;
+
+namespace {
+
+thread_local std::string g_err;
+
+ember_status fail(ember_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define CK(call)                                                                          \
+    do {                                                                                  \
+        cudaError_t e_ = (call);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return fail(EMBER_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                              \
+    } while (0)
+
+constexpr int MAX_DECODE_BATCH = 64;   // tokens of one decode step
+constexpr int GEMV_MAX_BATCH = 8;      // above this the step runs on the GEMM path
+constexpr int MAX_SPLITS = 32;         // split-KV partials per (token, kv head)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bump allocator over one cudaMalloc'd block, 256-byte aligned pieces.
+struct Arena {
+    size_t off = 0;
+    std::vector<std::pair<void**, size_t>> items;
+    template <class T>
+    void add(T** p, size_t count) {
+        items.push_back({reinterpret_cast<void**>(p), count * sizeof(T)});
+    }
+    cudaError_t commit(void** base) {
+        size_t total = 0;
+        for (auto& it : items) total = align_up(total, 256) + it.second;
+        total = align_up(total, 256);
+        cudaError_t e = cudaMalloc(base, total ? total : 256);
+        if (e != cudaSuccess) return e;
+        size_t o = 0;
+        for (auto& it : items) {
+            o = align_up(o, 256);
+            *it.first = static_cast<char*>(*base) + o;
+            o += it.second;
+        }
+        return cudaSuccess;
+    }
+};
+
+// RoPE tables: inv_freq_i = theta^(-2i/D) in double, llama3 scaling per
+// LowLlamaBasic rotary_cos_sin(), then cos/sin of pos*inv_freq_i rounded to f32.
+void rope_tables(const ember_config& c, int npos, std::vector<float>& cs, std::vector<float>& sn) {
+    const int half = c.head_dim / 2;
+    std::vector<double> inv(half);
+    for (int i = 0; i < half; ++i) {
+        double f = std::pow(c.rope_theta, -(2.0 * i) / (double)c.head_dim);
+        if (c.rope_llama3) {
+            const double pi = 3.14159265358979323846;
+            double z = ((double)c.rs_orig_max_pos * f / (2.0 * pi) - c.rs_low) / (c.rs_high - c.rs_low);
+            z = z < 0.0 ? 0.0 : (z > 1.0 ? 1.0 : z);
+            const double lo = 1.0 / c.rs_factor;
+            f *= lo + z * (1.0 - lo);
+        }
+        inv[i] = f;
+    }
+    cs.resize((size_t)npos * half);
+    sn.resize((size_t)npos * half);
+    for (int p = 0; p < npos; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double a = (double)p * inv[i];
+            cs[(size_t)p * half + i] = (float)std::cos(a);
+            sn[(size_t)p * half + i] = (float)std::sin(a);
+        }
+}
+
+struct LayerDev {
+    uint16_t *wqkv, *wo, *wgu, *wd;
+    float *attn_norm, *mlp_norm, *bqkv, *q_norm, *k_norm;
+    GemmPlan p_qkv, p_o, p_gu, p_d;
+};
+
+struct GraphEntry {
+    int batch;
+    const void *seqs, *ids, *pos, *logits, *argmax;
+    cudaGraphExec_t exec;
+};
+
+}  // namespace
+
+struct ember_model {
+    ember_config c;
+    int q, kv, qkv_n, G, T, sms;
+    void* wblock = nullptr;
+    void* ablock = nullptr;
+    uint16_t* embed = nullptr;
+    uint16_t* cls_w = nullptr;
+    float *final_norm = nullptr, *cls_b = nullptr;
+    std::vector<LayerDev> layers;
+    // workspace
+    float *x, *qkv, *att_f, *act_f, *hbuf, *part;
+    uint16_t *xb, *qr, *att_b, *act_b, *enc_k, *enc_v, *hb;
+    unsigned* counters;
+    unsigned long long* keys;
+    int *tok_ok, *status;
+    float *enc_cos = nullptr, *enc_sin = nullptr;
+    int enc_positions = 0;
+    GemmPlan p_head;   // tied head on bf16 final states (encode without labels)
+    std::vector<GraphEntry> graphs;
+    bool use_graphs = true;
+    std::mutex mu;
+};
+
+struct ember_kv {
+    ember_model* m;
+    int max_seqs, max_len;
+    uint16_t *k = nullptr, *v = nullptr;
+    int32_t* cursor = nullptr;
+    float *cos_t = nullptr, *sin_t = nullptr;
+};
+
+static ember_status validate(const ember_config* c) {
+    if (!c) return fail(EMBER_ERR_INVALID_ARG, "config is NULL");
+    if (c->vocab <= 0 || c->hidden <= 0 || c->layers <= 0 || c->n_heads <= 0 ||
+        c->n_kv_heads <= 0 || c->head_dim <= 0 || c->ff <= 0)
+        return fail(EMBER_ERR_INVALID_ARG, "zero dimension");
+    if (c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0)
+        return fail(EMBER_ERR_INVALID_ARG, "invalid GQA/RoPE shape: heads %% kv_heads or odd head_dim");
+    if (c->head_dim != 16 && c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+        return fail(EMBER_ERR_UNSUPPORTED, "head_dim must be 16, 32, 64 or 128");
+    if (c->n_heads / c->n_kv_heads > 16) return fail(EMBER_ERR_UNSUPPORTED, "GQA group > 16");
+    if (c->hidden % 8 || c->ff % 8) return fail(EMBER_ERR_UNSUPPORTED, "hidden and ff must be multiples of 8");
+    if (c->hidden > 8192 || c->ff > 16384 || c->n_heads * c->head_dim > 16384)
+        return fail(EMBER_ERR_UNSUPPORTED, "hidden > 8192, ff > 16384 or heads*head_dim > 16384");
+    if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0))
+        return fail(EMBER_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+    if (c->rope_llama3 && (!(c->rs_factor > 0.0) || c->rs_high == c->rs_low || c->rs_orig_max_pos <= 0))
+        return fail(EMBER_ERR_INVALID_ARG, "invalid llama3 rope scaling");
+    if (c->n_labels < 0 || c->max_tokens < 0 || c->max_positions < 0)
+        return fail(EMBER_ERR_INVALID_ARG, "negative n_labels / max_tokens / max_positions");
+    return EMBER_OK;
+}
+
+extern "C" {
+
+const char* ember_last_error(void) { return g_err.c_str(); }
+
+size_t ember_kv_bytes(const ember_config* c, int32_t max_seqs, int32_t max_len) {
+    if (!c || max_seqs <= 0 || max_len <= 0) return 0;
+    return (size_t)c->layers * 2 * c->n_kv_heads * (size_t)max_len * c->head_dim * 2 *
+           (size_t)max_seqs;
+}
+
+ember_status ember_model_create(const ember_config* cfg, const ember_weights* w, ember_model** out) {
+    if (!out) return fail(EMBER_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    ember_status st = validate(cfg);
+    if (st != EMBER_OK) return st;
+    if (!w || !w->embed || !w->final_norm || !w->layers)
+        return fail(EMBER_ERR_INVALID_ARG, "missing weight: embed, final_norm or layers");
+    const ember_config& c = *cfg;
+    if (c.n_labels > 0 && !w->cls_w) return fail(EMBER_ERR_INVALID_ARG, "missing weight: cls_w");
+    for (int l = 0; l < c.layers; ++l) {
+        const ember_layer_weights& L = w->layers[l];
+        if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.mlp_norm || !L.w_gate ||
+            !L.w_up || !L.w_down)
+            return fail(EMBER_ERR_INVALID_ARG, "missing weight in layer %d", l);
+        if (c.qkv_bias && (!L.bq || !L.bk || !L.bv))
+            return fail(EMBER_ERR_INVALID_ARG, "missing q/k/v bias in layer %d", l);
+        if (c.qk_norm && (!L.q_norm || !L.k_norm))
+            return fail(EMBER_ERR_INVALID_ARG, "missing q/k norm in layer %d", l);
+    }
+
+    ember_model* m = new ember_model();
+    m->c = c;
+    if (m->c.max_tokens == 0) m->c.max_tokens = 4096;
+    if (m->c.max_positions == 0) m->c.max_positions = m->c.max_tokens;
+    const int H = c.hidden, D = c.head_dim, F = c.ff, V = c.vocab, NKV = c.n_kv_heads;
+    m->q = c.n_heads * D;
+    m->kv = NKV * D;
+    m->qkv_n = m->q + 2 * m->kv;
+    m->G = c.n_heads / NKV;
+    m->T = m->c.max_tokens;
+    m->use_graphs = !(getenv("EMBER_NO_GRAPH") && atoi(getenv("EMBER_NO_GRAPH")));
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
+    m->layers.resize(c.layers);
+
+    // ---- weights ----
+    Arena wa;
+    wa.add(&m->embed, (size_t)V * H);
+    wa.add(&m->final_norm, H);
+    if (c.n_labels > 0) {
+        wa.add(&m->cls_w, (size_t)c.n_labels * H);
+        wa.add(&m->cls_b, c.n_labels);
+    }
+    for (auto& L : m->layers) {
+        wa.add(&L.wqkv, (size_t)m->qkv_n * H);
+        wa.add(&L.wo, (size_t)H * m->q);
+        wa.add(&L.wgu, (size_t)2 * F * H);
+        wa.add(&L.wd, (size_t)H * F);
+        wa.add(&L.attn_norm, H);
+        wa.add(&L.mlp_norm, H);
+        wa.add(&L.bqkv, m->qkv_n);
+        wa.add(&L.q_norm, D);
+        wa.add(&L.k_norm, D);
+    }
+    // ---- workspace ----
+    const int T = m->T, B = MAX_DECODE_BATCH;
+    Arena aa;
+    aa.add(&m->x, (size_t)T * H);
+    aa.add(&m->xb, (size_t)T * H);
+    aa.add(&m->qkv, (size_t)T * m->qkv_n);
+    aa.add(&m->qr, (size_t)T * m->q);
+    aa.add(&m->att_b, (size_t)T * m->q);
+    aa.add(&m->act_b, (size_t)T * F);
+    aa.add(&m->hbuf, (size_t)T * H);
+    aa.add(&m->hb, (size_t)T * H);
+    aa.add(&m->att_f, (size_t)B * m->q);
+    aa.add(&m->act_f, (size_t)GEMV_MAX_BATCH * F);
+    aa.add(&m->part, (size_t)B * NKV * MAX_SPLITS * m->G * (D + 2));
+    aa.add(&m->counters, (size_t)B * NKV);
+    aa.add(&m->keys, (size_t)B);
+    aa.add(&m->tok_ok, (size_t)B);
+    aa.add(&m->status, 1);
+    if (!c.causal) {
+        aa.add(&m->enc_k, (size_t)T * m->kv);
+        aa.add(&m->enc_v, (size_t)T * m->kv);
+        aa.add(&m->enc_cos, (size_t)m->c.max_positions * (D / 2));
+        aa.add(&m->enc_sin, (size_t)m->c.max_positions * (D / 2));
+    }
+
+    auto cleanup = [&](ember_status s) {
+        if (m->wblock) cudaFree(m->wblock);
+        if (m->ablock) cudaFree(m->ablock);
+        delete m;
+        return s;
+    };
+    if (wa.commit(&m->wblock) != cudaSuccess) {
+        cudaGetLastError();
+        return cleanup(fail(EMBER_ERR_OOM, "weight allocation failed"));
+    }
+    if (aa.commit(&m->ablock) != cudaSuccess) {
+        cudaGetLastError();
+        return cleanup(fail(EMBER_ERR_OOM, "workspace allocation failed"));
+    }
+
+    cudaStream_t s = nullptr;
+    const auto D2D = cudaMemcpyDeviceToDevice;
+    cudaError_t e = cudaSuccess;
+    auto cp = [&](void* dst, const void* src, size_t bytes) {
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, D2D, s);
+    };
+    cp(m->embed, w->embed, (size_t)V * H * 2);
+    launch_bf16_to_f32(w->final_norm, m->final_norm, H, s);
+    if (c.n_labels > 0) {
+        cp(m->cls_w, w->cls_w, (size_t)c.n_labels * H * 2);
+        if (w->cls_b) launch_bf16_to_f32(w->cls_b, m->cls_b, c.n_labels, s);
+        else if (e == cudaSuccess) e = cudaMemsetAsync(m->cls_b, 0, c.n_labels * 4, s);
+    }
+    for (int l = 0; l < c.layers; ++l) {
+        const ember_layer_weights& W = w->layers[l];
+        LayerDev& L = m->layers[l];
+        // fused [q; k; v] rows
+        cp(L.wqkv, W.wq, (size_t)m->q * H * 2);
+        cp(L.wqkv + (size_t)m->q * H, W.wk, (size_t)m->kv * H * 2);
+        cp(L.wqkv + (size_t)(m->q + m->kv) * H, W.wv, (size_t)m->kv * H * 2);
+        cp(L.wo, W.wo, (size_t)H * m->q * 2);
+        // gate / up interleaved by row: row 2i = gate_i, row 2i+1 = up_i
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(L.wgu, (size_t)4 * H, W.w_gate, (size_t)2 * H, (size_t)2 * H, F,
+                                  D2D, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(L.wgu + H, (size_t)4 * H, W.w_up, (size_t)2 * H, (size_t)2 * H, F,
+                                  D2D, s);
+        cp(L.wd, W.w_down, (size_t)H * F * 2);
+        launch_bf16_to_f32(W.attn_norm, L.attn_norm, H, s);
+        launch_bf16_to_f32(W.mlp_norm, L.mlp_norm, H, s);
+        if (c.qkv_bias) {
+            launch_bf16_to_f32(W.bq, L.bqkv, m->q, s);
+            launch_bf16_to_f32(W.bk, L.bqkv + m->q, m->kv, s);
+            launch_bf16_to_f32(W.bv, L.bqkv + m->q + m->kv, m->kv, s);
+        } else if (e == cudaSuccess) {
+            e = cudaMemsetAsync(L.bqkv, 0, (size_t)m->qkv_n * 4, s);
+        }
+        if (c.qk_norm) {
+            launch_bf16_to_f32(W.q_norm, L.q_norm, D, s);
+            launch_bf16_to_f32(W.k_norm, L.k_norm, D, s);
+        }
+        // tensor-core plans of the whole-prompt projections
+        bool ok = make_gemm_plan(L.p_qkv, m->xb, T, H, L.wqkv, m->qkv_n, H, H) &&
+                  make_gemm_plan(L.p_o, m->att_b, T, m->q, L.wo, H, m->q, m->q) &&
+                  make_gemm_plan(L.p_gu, m->xb, T, H, L.wgu, 2 * F, H, H) &&
+                  make_gemm_plan(L.p_d, m->act_b, T, F, L.wd, H, F, F);
+        if (!ok) return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (layer %d)", l));
+    }
+    if (!make_gemm_plan(m->p_head, m->hb, T, H, m->embed, V, H, H))
+        return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (head)"));
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->counters, 0, (size_t)B * NKV * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->keys, 0, (size_t)B * 8, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, 4, s);
+    if (e == cudaSuccess && !c.causal) {
+        std::vector<float> cs, sn;
+        rope_tables(m->c, m->c.max_positions, cs, sn);
+        e = cudaMemcpy(m->enc_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(m->enc_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cleanup(fail(EMBER_ERR_CUDA, "weight repack failed: %s", cudaGetErrorString(e)));
+    *out = m;
+    return EMBER_OK;
+}
+
+void ember_model_destroy(ember_model* m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
+    if (m->wblock) cudaFree(m->wblock);
+    if (m->ablock) cudaFree(m->ablock);
+    delete m;
+}
+
+ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, ember_kv** out) {
+    if (!m || !out) return fail(EMBER_ERR_INVALID_ARG, "model or out is NULL");
+    *out = nullptr;
+    if (max_seqs <= 0 || max_len <= 0) return fail(EMBER_ERR_INVALID_ARG, "max_seqs and max_len must be > 0");
+    if (!m->c.causal) return fail(EMBER_ERR_INVALID_ARG, "a bidirectional encoder has no KV cache");
+    const size_t half = ember_kv_bytes(&m->c, max_seqs, max_len) / 2;
+    ember_kv* kv = new ember_kv();
+    kv->m = m;
+    kv->max_seqs = max_seqs;
+    kv->max_len = max_len;
+    const int h2 = m->c.head_dim / 2;
+    cudaError_t e = cudaMalloc(&kv->k, half);
+    if (e == cudaSuccess) e = cudaMalloc(&kv->v, half);
+    if (e == cudaSuccess) e = cudaMalloc(&kv->cursor, (size_t)max_seqs * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&kv->cos_t, (size_t)max_len * h2 * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&kv->sin_t, (size_t)max_len * h2 * 4);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        ember_kv_free(kv);
+        return fail(EMBER_ERR_OOM, "KV cache allocation of %zu bytes failed", 2 * half);
+    }
+    std::vector<float> cs, sn;
+    rope_tables(m->c, max_len, cs, sn);
+    e = cudaMemset(kv->k, 0, half);
+    if (e == cudaSuccess) e = cudaMemset(kv->v, 0, half);
+    if (e == cudaSuccess) e = cudaMemset(kv->cursor, 0, (size_t)max_seqs * 4);
+    if (e == cudaSuccess) e = cudaMemcpy(kv->cos_t, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(kv->sin_t, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        ember_kv_free(kv);
+        return fail(EMBER_ERR_CUDA, "KV cache init failed: %s", cudaGetErrorString(e));
+    }
+    *out = kv;
+    return EMBER_OK;
+}
+
+void ember_kv_free(ember_kv* kv) {
+    if (!kv) return;
+    cudaDeviceSynchronize();
+    cudaFree(kv->k);
+    cudaFree(kv->v);
+    cudaFree(kv->cursor);
+    cudaFree(kv->cos_t);
+    cudaFree(kv->sin_t);
+    delete kv;
+}
+
+ember_status ember_kv_reset(ember_kv* kv, int32_t seq, ember_stream_t stream) {
+    if (!kv) return fail(EMBER_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(EMBER_ERR_INVALID_ARG, "seq %d out of range", seq);
+    CK(cudaMemsetAsync(kv->cursor + seq, 0, 4, (cudaStream_t)stream));
+    return EMBER_OK;
+}
+
+ember_status ember_kv_layout(const ember_kv* kv, const uint16_t** k_base, const uint16_t** v_base,
+                             int64_t strides[4]) {
+    if (!kv || !k_base || !v_base || !strides) return fail(EMBER_ERR_INVALID_ARG, "NULL argument");
+    const ember_config& c = kv->m->c;
+    *k_base = kv->k;
+    *v_base = kv->v;
+    strides[2] = (int64_t)kv->max_len * c.head_dim;
+    strides[1] = strides[2] * c.n_kv_heads;
+    strides[0] = strides[1] * c.layers;
+    strides[3] = c.head_dim;
+    return EMBER_OK;
+}
+
+ember_status ember_sync_status(ember_model* m, ember_stream_t stream) {
+    if (!m) return fail(EMBER_ERR_INVALID_ARG, "model is NULL");
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    CK(cudaGetLastError());
+    int st = 0;
+    CK(cudaMemcpy(&st, m->status, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(m->status, 0, 4));
+    if (st != 0) return fail((ember_status)st, "device reported status %d", st);
+    return EMBER_OK;
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------- launch sequences --
+// One decoder layer over n tokens already embedded in m->x, on the
+// tensor-core path (whole-prompt prefill, encode, and decode batches > 8).
+struct CacheView {
+    uint16_t *k, *v;              // base of sequence z = 0, layer 0 handled by caller
+    long long seq_stride, head_stride;
+    int T_per_seq, pos0, causal;
+    const float *cos_t, *sin_t;
+};
+
+static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStream_t s) {
+    const ember_config& c = m->c;
+    LayerDev& L = m->layers[l];
+    const float eps = (float)c.rms_eps;
+    launch_rmsnorm_bf16(m->x, L.attn_norm, eps, n, c.hidden, m->xb, s);
+    GemmEpilogue e{};
+    e.mode = EPI_STORE;
+    e.out_f32 = m->qkv;
+    e.ldo = m->qkv_n;
+    e.bias = c.qkv_bias ? L.bqkv : nullptr;
+    launch_gemm(L.p_qkv, n, e, m->status, s);
+    RopeKVArgs r{};
+    r.qkv = m->qkv;
+    r.ld_qkv = m->qkv_n;
+    r.n = n;
+    r.NH = c.n_heads;
+    r.NKV = c.n_kv_heads;
+    r.D = c.head_dim;
+    r.T_per_seq = cv.T_per_seq;
+    r.pos0 = cv.pos0;
+    r.cos_t = cv.cos_t;
+    r.sin_t = cv.sin_t;
+    r.q_norm = c.qk_norm ? L.q_norm : nullptr;
+    r.k_norm = c.qk_norm ? L.k_norm : nullptr;
+    r.eps = eps;
+    r.q_out = m->qr;
+    r.kc = cv.k;
+    r.vc = cv.v;
+    r.seq_stride = cv.seq_stride;
+    r.head_stride = cv.head_stride;
+    launch_rope_kv(r, s);
+    AttnPrefillArgs a{};
+    a.q = m->qr;
+    a.n = n;
+    a.NH = c.n_heads;
+    a.NKV = c.n_kv_heads;
+    a.D = c.head_dim;
+    a.T_per_seq = cv.T_per_seq;
+    a.pos0 = cv.pos0;
+    a.causal = cv.causal;
+    a.kc = cv.k;
+    a.vc = cv.v;
+    a.seq_stride = cv.seq_stride;
+    a.head_stride = cv.head_stride;
+    a.att = m->att_b;
+    launch_attn_prefill(a, s);
+    e = GemmEpilogue{};
+    e.mode = EPI_RESID;
+    e.out_f32 = m->x;
+    e.ldo = c.hidden;
+    launch_gemm(L.p_o, n, e, m->status, s);
+    launch_rmsnorm_bf16(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, s);
+    e = GemmEpilogue{};
+    e.mode = EPI_SWIGLU;
+    e.out_bf16 = m->act_b;
+    e.ldo = c.ff;
+    launch_gemm(L.p_gu, n, e, m->status, s);
+    e = GemmEpilogue{};
+    e.mode = EPI_RESID;
+    e.out_f32 = m->x;
+    e.ldo = c.hidden;
+    launch_gemm(L.p_d, n, e, m->status, s);
+}
+
+extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq, const int32_t* ids,
+                                      int32_t n, int32_t start_pos, float* logits, int32_t* argmax,
+                                      float* hidden, ember_stream_t stream) {
+    if (!m || !kv || !ids) return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv or ids");
+    if (kv->m != m) return fail(EMBER_ERR_INVALID_ARG, "kv belongs to another model");
+    if (n <= 0) return fail(EMBER_ERR_INVALID_ARG, "input_ids must not be empty");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(EMBER_ERR_INVALID_ARG, "seq %d out of range", seq);
+    if (start_pos < 0) return fail(EMBER_ERR_INVALID_ARG, "negative start_pos");
+    if (n > m->T) return fail(EMBER_ERR_CAPACITY, "n = %d > max_tokens = %d", n, m->T);
+    if ((long long)start_pos + n > kv->max_len)
+        return fail(EMBER_ERR_CAPACITY, "sequence too long: %d + %d > max_len %d", start_pos, n, kv->max_len);
+    std::lock_guard<std::mutex> lock(m->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    const ember_config& c = m->c;
+    EmbedArgs ea{};
+    ea.E = m->embed;
+    ea.V = c.vocab;
+    ea.H = c.hidden;
+    ea.ids = ids;
+    ea.n = n;
+    ea.x = m->x;
+    ea.status = m->status;
+    ea.pf_seq = seq;
+    ea.pf_start = start_pos;
+    ea.cursor = kv->cursor;
+    launch_embed(ea, s);
+    const long long head_stride = (long long)kv->max_len * c.head_dim;
+    for (int l = 0; l < c.layers; ++l) {
+        CacheView cv{};
+        const long long off = (((long long)seq * c.layers + l) * c.n_kv_heads) * head_stride;
+        cv.k = kv->k + off;
+        cv.v = kv->v + off;
+        cv.seq_stride = 0;
+        cv.head_stride = head_stride;
+        cv.T_per_seq = n;
+        cv.pos0 = start_pos;
+        cv.causal = 1;
+        cv.cos_t = kv->cos_t;
+        cv.sin_t = kv->sin_t;
+        layer_tc(m, l, n, cv, s);
+    }
+    if (hidden) launch_rmsnorm_f32(m->x, m->final_norm, (float)c.rms_eps, n, c.hidden, hidden, s);
+    GemvArgs g{};
+    g.W = m->embed;
+    g.N = c.vocab;
+    g.K = c.hidden;
+    g.x = m->x + (size_t)(n - 1) * c.hidden;
+    g.ldx = c.hidden;
+    g.norm_w = m->final_norm;
+    g.eps = (float)c.rms_eps;
+    g.out = logits;
+    g.ldo = c.vocab;
+    g.nb = 1;
+    g.mode = EPI_ARGMAX;
+    g.keys = m->keys;
+    g.status = m->status;
+    launch_gemv(g, s, m->sms);
+    FinishArgs f{};
+    f.nb = 1;
+    f.keys = m->keys;
+    f.argmax = argmax;
+    f.cursor = kv->cursor;
+    f.pf_seq = seq;
+    f.pf_end = start_pos + n;
+    launch_finish(f, s);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+// Kernel sequence of one decode step (captured into a graph when possible).
+static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* seqs,
+                           const int32_t* ids, const int32_t* positions, float* logits,
+                           int32_t* argmax, cudaStream_t s) {
+    const ember_config& c = m->c;
+    const float eps = (float)c.rms_eps;
+    EmbedArgs ea{};
+    ea.E = m->embed;
+    ea.V = c.vocab;
+    ea.H = c.hidden;
+    ea.ids = ids;
+    ea.n = B;
+    ea.x = m->x;
+    ea.status = m->status;
+    ea.seqs = seqs;
+    ea.positions = positions;
+    ea.cursor = kv->cursor;
+    ea.max_seqs = kv->max_seqs;
+    ea.max_len = kv->max_len;
+    ea.tok_ok = m->tok_ok;
+    ea.pf_seq = -1;
+    launch_embed(ea, s);
+    const bool gemv = B <= GEMV_MAX_BATCH;
+    int splits = (2 * m->sms + B * c.n_kv_heads - 1) / (B * c.n_kv_heads);
+    splits = splits < 1 ? 1 : (splits > MAX_SPLITS ? MAX_SPLITS : splits);
+    for (int l = 0; l < c.layers; ++l) {
+        LayerDev& L = m->layers[l];
+        if (gemv) {
+            GemvArgs g{};
+            g.W = L.wqkv;
+            g.N = m->qkv_n;
+            g.K = c.hidden;
+            g.x = m->x;
+            g.ldx = c.hidden;
+            g.norm_w = L.attn_norm;
+            g.eps = eps;
+            g.bias = c.qkv_bias ? L.bqkv : nullptr;
+            g.out = m->qkv;
+            g.ldo = m->qkv_n;
+            g.nb = B;
+            g.mode = EPI_STORE;
+            g.status = m->status;
+            launch_gemv(g, s, m->sms);
+        } else {
+            launch_rmsnorm_bf16(m->x, L.attn_norm, eps, B, c.hidden, m->xb, s);
+            GemmEpilogue e{};
+            e.mode = EPI_STORE;
+            e.out_f32 = m->qkv;
+            e.ldo = m->qkv_n;
+            e.bias = c.qkv_bias ? L.bqkv : nullptr;
+            launch_gemm(L.p_qkv, B, e, m->status, s);
+        }
+        AttnDecodeArgs a{};
+        a.qkv = m->qkv;
+        a.ld_qkv = m->qkv_n;
+        a.nb = B;
+        a.NH = c.n_heads;
+        a.NKV = c.n_kv_heads;
+        a.D = c.head_dim;
+        a.L = c.layers;
+        a.layer = l;
+        a.seqs = seqs;
+        a.positions = positions;
+        a.tok_ok = m->tok_ok;
+        a.kc = kv->k;
+        a.vc = kv->v;
+        a.max_len = kv->max_len;
+        a.cos_t = kv->cos_t;
+        a.sin_t = kv->sin_t;
+        a.q_norm = c.qk_norm ? L.q_norm : nullptr;
+        a.k_norm = c.qk_norm ? L.k_norm : nullptr;
+        a.eps = eps;
+        a.att = m->att_f;
+        a.att_b = gemv ? nullptr : m->att_b;
+        a.part = m->part;
+        a.counters = m->counters;
+        a.splits = splits;
+        a.status = m->status;
+        launch_attn_decode(a, s);
+        if (gemv) {
+            GemvArgs g{};
+            g.W = L.wo;
+            g.N = c.hidden;
+            g.K = m->q;
+            g.x = m->att_f;
+            g.ldx = m->q;
+            g.out = m->x;
+            g.ldo = c.hidden;
+            g.nb = B;
+            g.mode = EPI_RESID;
+            g.status = m->status;
+            launch_gemv(g, s, m->sms);
+            g = GemvArgs{};
+            g.W = L.wgu;
+            g.N = 2 * c.ff;
+            g.K = c.hidden;
+            g.x = m->x;
+            g.ldx = c.hidden;
+            g.norm_w = L.mlp_norm;
+            g.eps = eps;
+            g.out = m->act_f;
+            g.ldo = c.ff;
+            g.nb = B;
+            g.mode = EPI_SWIGLU;
+            g.status = m->status;
+            launch_gemv(g, s, m->sms);
+            g = GemvArgs{};
+            g.W = L.wd;
+            g.N = c.hidden;
+            g.K = c.ff;
+            g.x = m->act_f;
+            g.ldx = c.ff;
+            g.out = m->x;
+            g.ldo = c.hidden;
+            g.nb = B;
+            g.mode = EPI_RESID;
+            g.status = m->status;
+            launch_gemv(g, s, m->sms);
+        } else {
+            // the attention kernel wrote its output as the bf16 GEMM operand att_b
+            GemmEpilogue e{};
+            e.mode = EPI_RESID;
+            e.out_f32 = m->x;
+            e.ldo = c.hidden;
+            launch_gemm(L.p_o, B, e, m->status, s);
+            launch_rmsnorm_bf16(m->x, L.mlp_norm, eps, B, c.hidden, m->xb, s);
+            e = GemmEpilogue{};
+            e.mode = EPI_SWIGLU;
+            e.out_bf16 = m->act_b;
+            e.ldo = c.ff;
+            launch_gemm(L.p_gu, B, e, m->status, s);
+            e = GemmEpilogue{};
+            e.mode = EPI_RESID;
+            e.out_f32 = m->x;
+            e.ldo = c.hidden;
+            launch_gemm(L.p_d, B, e, m->status, s);
+        }
+    }
+    // LM head + argmax, in groups of GEMV_MAX_BATCH tokens
+    for (int b0 = 0; b0 < B; b0 += GEMV_MAX_BATCH) {
+        GemvArgs g{};
+        g.W = m->embed;
+        g.N = c.vocab;
+        g.K = c.hidden;
+        g.x = m->x + (size_t)b0 * c.hidden;
+        g.ldx = c.hidden;
+        g.norm_w = m->final_norm;
+        g.eps = eps;
+        g.out = logits ? logits + (size_t)b0 * c.vocab : nullptr;
+        g.ldo = c.vocab;
+        g.nb = (B - b0) < GEMV_MAX_BATCH ? (B - b0) : GEMV_MAX_BATCH;
+        g.mode = EPI_ARGMAX;
+        g.keys = m->keys + b0;
+        g.status = m->status;
+        launch_gemv(g, s, m->sms);
+    }
+    FinishArgs f{};
+    f.nb = B;
+    f.keys = m->keys;
+    f.argmax = argmax;
+    f.seqs = seqs;
+    f.positions = positions;
+    f.tok_ok = m->tok_ok;
+    f.cursor = kv->cursor;
+    f.pf_seq = -1;
+    launch_finish(f, s);
+}
+
+extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t batch,
+                                          const int32_t* seqs, const int32_t* ids,
+                                          const int32_t* positions, float* logits, int32_t* argmax,
+                                          ember_stream_t stream) {
+    if (!m || !kv || !seqs || !ids || !positions)
+        return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv, seqs, ids or positions");
+    if (kv->m != m) return fail(EMBER_ERR_INVALID_ARG, "kv belongs to another model");
+    if (batch <= 0) return fail(EMBER_ERR_INVALID_ARG, "batch must be > 0");
+    if (batch > MAX_DECODE_BATCH || batch > m->T || batch > kv->max_seqs)
+        return fail(EMBER_ERR_CAPACITY, "batch %d exceeds the decode capacity", batch);
+    std::lock_guard<std::mutex> lock(m->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    CK(cudaStreamIsCapturing(s, &cap));
+    if (!m->use_graphs || s == nullptr || cap != cudaStreamCaptureStatusNone) {
+        decode_enqueue(m, kv, batch, seqs, ids, positions, logits, argmax, s);
+        CK(cudaGetLastError());
+        return EMBER_OK;
+    }
+    for (auto& g : m->graphs) {
+        if (g.batch == batch && g.seqs == seqs && g.ids == ids && g.pos == positions &&
+            g.logits == logits && g.argmax == argmax) {
+            CK(cudaGraphLaunch(g.exec, s));
+            return EMBER_OK;
+        }
+    }
+    cudaGraph_t graph = nullptr;
+    CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    decode_enqueue(m, kv, batch, seqs, ids, positions, logits, argmax, s);
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+    if (m->graphs.size() >= 16) {
+        cudaGraphExecDestroy(m->graphs.front().exec);
+        m->graphs.erase(m->graphs.begin());
+    }
+    m->graphs.push_back({batch, seqs, ids, positions, logits, argmax, exec});
+    CK(cudaGraphLaunch(exec, s));
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_encode(ember_model* m, const int32_t* ids, int32_t B, int32_t T,
+                                     float* out, float* hidden, ember_stream_t stream) {
+    if (!m || !ids) return fail(EMBER_ERR_INVALID_ARG, "NULL model or ids");
+    if (B <= 0 || T <= 0) return fail(EMBER_ERR_INVALID_ARG, "input_ids must not be empty");
+    if ((long long)B * T > m->T) return fail(EMBER_ERR_CAPACITY, "B*T = %lld > max_tokens %d", (long long)B * T, m->T);
+    if (m->c.causal) return fail(EMBER_ERR_UNSUPPORTED, "encode of a causal model is not built yet");
+    if (T > m->c.max_positions) return fail(EMBER_ERR_CAPACITY, "T = %d > max_positions %d", T, m->c.max_positions);
+    std::lock_guard<std::mutex> lock(m->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    const ember_config& c = m->c;
+    const int n = B * T;
+    EmbedArgs ea{};
+    ea.E = m->embed;
+    ea.V = c.vocab;
+    ea.H = c.hidden;
+    ea.ids = ids;
+    ea.n = n;
+    ea.x = m->x;
+    ea.status = m->status;
+    ea.pf_seq = -1;
+    launch_embed(ea, s);
+    for (int l = 0; l < c.layers; ++l) {
+        CacheView cv{};
+        cv.k = m->enc_k;
+        cv.v = m->enc_v;
+        cv.head_stride = (long long)T * c.head_dim;
+        cv.seq_stride = cv.head_stride * c.n_kv_heads;
+        cv.T_per_seq = T;
+        cv.pos0 = 0;
+        cv.causal = c.causal;
+        cv.cos_t = m->enc_cos;
+        cv.sin_t = m->enc_sin;
+        layer_tc(m, l, n, cv, s);
+    }
+    float* h = hidden ? hidden : m->hbuf;
+    launch_rmsnorm_f32(m->x, m->final_norm, (float)c.rms_eps, n, c.hidden, h, s);
+    if (out) {
+        if (c.n_labels > 0) {
+            launch_cls_head(h, n, c.hidden, m->cls_w, m->cls_b, c.n_labels, out, s);
+        } else {
+            return fail(EMBER_ERR_UNSUPPORTED, "encode with the tied vocabulary head is not built yet");
+        }
+    }
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_rope_store(const float* x, int32_t n_tok, int32_t n_heads,
+                                         int32_t head_dim, const float* cos_t, const float* sin_t,
+                                         uint16_t* out, ember_stream_t stream) {
+    if (!x || !cos_t || !sin_t || !out) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (n_tok <= 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2)
+        return fail(EMBER_ERR_INVALID_ARG, "bad sizes");
+    launch_rope_store(x, n_tok, n_heads, head_dim, cos_t, sin_t, out, (cudaStream_t)stream);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_gemm_bf16(const uint16_t* A, const uint16_t* Bm, float* Dm, int32_t M,
+                                        int32_t N, int32_t K, ember_stream_t stream) {
+    if (!A || !Bm || !Dm) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (M <= 0 || N <= 0 || K <= 0 || K % 8 || N % 4)
+        return fail(EMBER_ERR_INVALID_ARG, "M, N, K must be > 0, K %% 8 == 0, N %% 4 == 0");
+    GemmPlan p;
+    if (!make_gemm_plan(p, A, M, K, Bm, N, K, K))
+        return fail(EMBER_ERR_INVALID_ARG, "TMA tensor map rejected (alignment?)");
+    GemmEpilogue e{};
+    e.mode = EPI_STORE;
+    e.out_f32 = Dm;
+    e.ldo = N;
+    launch_gemm(p, M, e, nullptr, (cudaStream_t)stream);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}

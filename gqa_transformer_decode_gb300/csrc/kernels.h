@@ -1,0 +1,174 @@
+// kernels.h -- launch interfaces of the ember kernels (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ember {
+
+// ---------------------------------------------------------------- embedding --
+// x[t] = f32(E[ids[t]]) and the per-token argument checks of a decode step
+// (seq in range, position == cursor, position < max_len, id < vocab) or of a
+// prefill (start position == cursor).
+struct EmbedArgs {
+    const uint16_t* E;
+    int V, H;
+    const int32_t* ids;
+    int n;
+    float* x;                    // [n][H]
+    int* status;
+    // decode-step checks (seqs == nullptr for prefill / encode)
+    const int32_t* seqs;
+    const int32_t* positions;
+    const int32_t* cursor;
+    int max_seqs, max_len;
+    int* tok_ok;                 // [n] 1 = token may touch the cache
+    // prefill check (pf_seq < 0: none)
+    int pf_seq, pf_start;
+};
+void launch_embed(const EmbedArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------------------- GEMV --
+// Batch-1..8 decode projections: y[b][n] = rinv_b * sum_k W[n][k] x[b][k] w_k
+// with the RMSNorm of x fused into the prologue when norm_w != nullptr.
+struct GemvArgs {
+    const uint16_t* W;           // [N][K] bf16
+    int N, K;
+    const float* x;              // [nb][ldx] f32
+    int ldx;
+    const float* norm_w;         // [K] f32 or nullptr
+    float eps;
+    const float* bias;           // [N] f32 or nullptr (EPI_STORE)
+    float* out;                  // mode-dependent, row stride ldo
+    int ldo;
+    int nb;
+    int mode;                    // EpiMode
+    unsigned long long* keys;    // [nb] argmax keys (EPI_ARGMAX)
+    int* status;
+};
+void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms);
+
+// ------------------------------------------------------- decode attention --
+// Split-KV flash decoding: one CTA per (token, kv head, split), all G query
+// heads of the kv head together; the last CTA of a (token, kv head) merges the
+// splits.  Also applies q/k norm + RoPE and writes the token's K/V row.
+struct AttnDecodeArgs {
+    const float* qkv;            // [nb][ld_qkv] pre-RoPE q | k | v (biased)
+    int ld_qkv;
+    int nb, NH, NKV, D, L, layer;
+    const int32_t* seqs;
+    const int32_t* positions;
+    const int* tok_ok;
+    uint16_t* kc;                // K cache base [S][L][NKV][max_len][D]
+    uint16_t* vc;
+    int max_len;
+    const float* cos_t;          // [max_len][D/2]
+    const float* sin_t;
+    const float* q_norm;         // [D] or nullptr
+    const float* k_norm;
+    float eps;
+    float* att;                  // [nb][NH*D] f32 (used when att_b == nullptr)
+    uint16_t* att_b;             // [nb][NH*D] bf16 GEMM operand, or nullptr
+    float* part;                 // split partials
+    unsigned* counters;          // [nb*NKV], zero between launches
+    int splits;
+    int* status;
+};
+void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s);
+
+// Greedy argmax write-back and cursor advance at the end of a step.
+struct FinishArgs {
+    int nb;
+    unsigned long long* keys;    // reset to 0 here
+    int32_t* argmax;             // [nb] or nullptr
+    // decode: cursor[seqs[b]] = positions[b] + 1 for ok tokens
+    const int32_t* seqs;
+    const int32_t* positions;
+    const int* tok_ok;
+    int32_t* cursor;
+    // prefill: cursor[pf_seq] = pf_end (pf_seq >= 0)
+    int pf_seq, pf_end;
+};
+void launch_finish(const FinishArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------- prefill side --
+// xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
+void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+                         cudaStream_t s);
+// h[t] = RMSNorm(x[t]) * w  in f32
+void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
+                        cudaStream_t s);
+
+// q/k norm + RoPE of n tokens; q -> bf16 [n][NH*D]; K, V rows -> bf16 cache.
+// Token t of sequence z = t / T_per_seq goes to position pos0 + t % T_per_seq
+// of cache rows k + z*seq_stride + g*head_stride + pos*D.
+struct RopeKVArgs {
+    const float* qkv;
+    int ld_qkv;
+    int n, NH, NKV, D;
+    int T_per_seq, pos0;
+    const float* cos_t;
+    const float* sin_t;
+    const float* q_norm;
+    const float* k_norm;
+    float eps;
+    uint16_t* q_out;             // [n][NH*D] bf16
+    uint16_t* kc;
+    uint16_t* vc;
+    long long seq_stride, head_stride;
+};
+void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s);
+
+// Whole-prompt attention reading K/V rows from the cache layout above.
+// Query row t of sequence z sits at position pos0 + t; keys [0, pos0+t] are
+// visible when causal, [0, T_per_seq + pos0) otherwise.
+struct AttnPrefillArgs {
+    const uint16_t* q;           // [n][NH*D] bf16, RoPE'd
+    int n, NH, NKV, D;
+    int T_per_seq, pos0, causal;
+    const uint16_t* kc;
+    const uint16_t* vc;
+    long long seq_stride, head_stride;
+    uint16_t* att;               // [n][NH*D] bf16
+};
+void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s);
+
+// out[t][j] = sum_k h[t][k] W[j][k] + b[j]  (label head, f32 h)
+void launch_cls_head(const float* h, int n, int H, const uint16_t* W, const float* b, int labels,
+                     float* out, cudaStream_t s);
+
+// Standalone RoPE + bf16 store (kernel-level parity entry point).
+void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const float* cos_t,
+                       const float* sin_t, uint16_t* out, cudaStream_t s);
+
+// bf16 [n] -> f32 [n] (weight repack of norms / biases)
+void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s);
+
+// ----------------------------------------------------------- tcgen05 GEMM --
+// D[M,N] = A[M,K] . B[N,K]^T (bf16 in, f32 accumulate in TMEM) with a fused
+// epilogue.  A and B are described by TMA tensor maps made by make_gemm_plan.
+struct GemmEpilogue {
+    int mode;                    // EpiMode (EPI_STORE, EPI_RESID, EPI_SWIGLU)
+    float* out_f32;              // EPI_STORE / EPI_RESID: [M][ldo]
+    uint16_t* out_bf16;          // EPI_SWIGLU: [M][ldo] bf16 (N/2 columns)
+    int ldo;
+    const float* bias;           // EPI_STORE, nullable
+};
+
+struct GemmPlan {
+    alignas(64) unsigned char tmA[128];
+    alignas(64) unsigned char tmB[128];
+    int M, N, K;
+    int bn;                      // N tile (64, 128 or 256)
+    bool ok;
+};
+// A rows = M (activations), B rows = N (weights); both row-major with K
+// contiguous and 16-byte aligned rows.  Returns false if the driver rejects
+// the tensor maps.
+bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16_t* B, int N,
+                    int ldb, int K);
+// m_rows: rows of A actually valid (<= p.M); the rest is ignored.
+void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
+                 cudaStream_t s);
+
+}  // namespace ember

@@ -1,0 +1,272 @@
+// prefill.cu -- whole-prompt side of the forward: RMSNorm to the bf16 GEMM
+// operand, q/k-norm + RoPE + KV-cache write for n tokens, whole-sequence GQA
+// attention (causal over the cache, or bidirectional within a sequence), the
+// f32 final norm and the linear label head.
+//
+// Pages: LowLlamaBasic reference.py predict() (whole-sequence form, causal
+// self_attn); PII-Tracer-vLLM serving/reference_forward.py forward() (q/k
+// RMSNorm before RoPE, no mask, token_cls_head with bias).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ember {
+
+// ============================================================ RMSNorm rows ==
+template <bool BF16>
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w, float eps, int H,
+                                                 void* out) {
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const float* xr = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+    ss = block_sum(ss, red);
+    const float ri = rsqrtf(ss / (float)H + eps);
+    if (BF16) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
+        for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
+            o[i] = pack_bf16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
+    } else {
+        float* o = static_cast<float*>(out) + (size_t)t * H;
+        for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = xr[i] * ri * w[i];
+    }
+}
+
+void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+                         cudaStream_t s) {
+    k_rmsnorm<true><<<n, 256, 0, s>>>(x, w, eps, H, xb);
+}
+void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
+                        cudaStream_t s) {
+    k_rmsnorm<false><<<n, 256, 0, s>>>(x, w, eps, H, h);
+}
+
+// =================================================== q/k norm, RoPE, K/V write ==
+__global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
+    extern __shared__ float sm[];   // [(NH + 2*NKV) * D] f32
+    const int t = blockIdx.x;
+    const int D = a.D, H2 = D / 2;
+    const int nq = a.NH * D, nkv = a.NKV * D;
+    const int z = t / a.T_per_seq;
+    const int pos = a.pos0 + t % a.T_per_seq;
+    const float* row = a.qkv + (size_t)t * a.ld_qkv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < nq + 2 * nkv; e += blockDim.x) sm[e] = row[e];
+    __syncthreads();
+    if (a.q_norm) {   // PII-Tracer forward(): per-head RMSNorm of q and k before RoPE
+        for (int h = warp; h < a.NH + a.NKV; h += blockDim.x / 32) {
+            float* v = sm + h * D;
+            const float* w = h < a.NH ? a.q_norm : a.k_norm;
+            float ss = 0.f;
+            for (int d = lane; d < D; d += 32) ss += v[d] * v[d];
+            ss = warp_sum(ss);
+            const float ri = rsqrtf(ss / (float)D + a.eps);
+            for (int d = lane; d < D; d += 32) v[d] = v[d] * ri * w[d];
+        }
+        __syncthreads();
+    }
+    const float* cs = a.cos_t + (size_t)pos * H2;
+    const float* sn = a.sin_t + (size_t)pos * H2;
+    uint16_t* qo = a.q_out + (size_t)t * nq;
+    for (int e = tid; e < (a.NH + a.NKV) * H2; e += blockDim.x) {
+        const int h = e / H2, i = e % H2;
+        const float* v = sm + h * D;
+        float r0, r1;
+        rope_pair(v[i], v[i + H2], cs[i], sn[i], r0, r1);
+        if (h < a.NH) {
+            qo[h * D + i] = f32_to_bf16(r0);
+            qo[h * D + i + H2] = f32_to_bf16(r1);
+        } else {
+            const int g = h - a.NH;
+            uint16_t* kr = a.kc + z * a.seq_stride + g * a.head_stride + (long long)pos * D;
+            kr[i] = f32_to_bf16(r0);
+            kr[i + H2] = f32_to_bf16(r1);
+        }
+    }
+    for (int e = tid; e < nkv; e += blockDim.x) {
+        const int g = e / D, d = e % D;
+        a.vc[z * a.seq_stride + g * a.head_stride + (long long)pos * D + d] =
+            f32_to_bf16(sm[nq + nkv + e]);
+    }
+}
+
+void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s) {
+    const size_t smem = (size_t)(a.NH + 2 * a.NKV) * a.D * sizeof(float);
+    k_rope_kv<<<a.n, 128, smem, s>>>(a);
+}
+
+// ======================================================== prefill attention ==
+// CTA = (query tile of QT rows, kv head g, sequence z), 8 warps.  The QT*G
+// (row, head) items are dealt round-robin to the warps; key tiles of 32 rows
+// are staged in shared memory, lane j scores key j, the warp keeps an online
+// softmax per item and accumulates P.V with lane-owned output columns.
+constexpr int APF_THREADS = 256;
+constexpr int APF_TK = 32;
+
+template <int D, int IPW>
+__global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a, int QT) {
+    constexpr int KP = D + 2;
+    constexpr int DL = D / 32 > 0 ? D / 32 : 1;   // output columns per lane
+    extern __shared__ float smq[];                // [QT*G][D] f32 queries
+    __shared__ __align__(16) uint16_t s_k[APF_TK][KP];
+    __shared__ __align__(16) uint16_t s_v[APF_TK][D];
+    const int G = a.NH / a.NKV;
+    const int g = blockIdx.y, z = blockIdx.z;
+    const int qt0 = blockIdx.x * QT;
+    const int rows = min(QT, a.T_per_seq - qt0);
+    if (rows <= 0) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int items = rows * G;
+    const float qk_scale = 1.4426950408889634f * rsqrtf((float)D);
+
+    // stage this tile's queries (item i = r*G + h -> query head g*G + h of row r)
+    for (int e = tid; e < items * D; e += APF_THREADS) {
+        const int i = e / D, d = e % D, r = i / G, h = i % G;
+        const size_t qrow = (size_t)z * a.T_per_seq + qt0 + r;
+        smq[e] = bf16_to_f32(a.q[qrow * a.NH * D + (size_t)(g * G + h) * D + d]) * qk_scale;
+    }
+    float m[IPW], l[IPW], acc[IPW][DL];
+#pragma unroll
+    for (int k = 0; k < IPW; ++k) {
+        m[k] = -INFINITY;
+        l[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < DL; ++c) acc[k][c] = 0.f;
+    }
+    const int n_all = a.pos0 + a.T_per_seq;                     // keys in the sequence
+    const int kend = a.causal ? min(n_all, a.pos0 + qt0 + rows) : n_all;
+    const uint16_t* kb = a.kc + z * a.seq_stride + g * a.head_stride;
+    const uint16_t* vb = a.vc + z * a.seq_stride + g * a.head_stride;
+
+    for (int t0 = 0; t0 < kend; t0 += APF_TK) {
+        const int nt = min(APF_TK, kend - t0);
+        __syncthreads();
+        constexpr int C8 = D / 8;
+        for (int e = tid; e < nt * C8; e += APF_THREADS) {
+            const int j = e / C8, c = e % C8;
+            const uint4 k4 = *reinterpret_cast<const uint4*>(kb + (size_t)(t0 + j) * D + c * 8);
+            const uint4 v4 = *reinterpret_cast<const uint4*>(vb + (size_t)(t0 + j) * D + c * 8);
+            uint32_t* kd = reinterpret_cast<uint32_t*>(&s_k[j][c * 8]);
+            kd[0] = k4.x; kd[1] = k4.y; kd[2] = k4.z; kd[3] = k4.w;
+            *reinterpret_cast<uint4*>(&s_v[j][c * 8]) = v4;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < IPW; ++k) {
+            const int i = warp + k * (APF_THREADS / 32);
+            if (i >= items) break;
+            const int r = i / G;
+            const int qpos = a.pos0 + qt0 + r;
+            const int kp = t0 + lane;
+            const bool vis = lane < nt && (a.causal ? kp <= qpos : true);
+            float s = -INFINITY;
+            if (vis) {
+                const float* qv = smq + (size_t)i * D;
+                const uint32_t* kr = reinterpret_cast<const uint32_t*>(s_k[lane]);
+                float dot = 0.f;
+#pragma unroll 8
+                for (int d2 = 0; d2 < D / 2; ++d2) {
+                    const uint32_t kk = kr[d2];
+                    dot = fmaf(qv[2 * d2], bf16_lo(kk), dot);
+                    dot = fmaf(qv[2 * d2 + 1], bf16_hi(kk), dot);
+                }
+                s = dot;
+            }
+            const float tm = warp_max(s);
+            if (tm == -INFINITY) continue;   // nothing visible for this item in this tile
+            const float mn = fmaxf(m[k], tm);
+            const float p = exp2f(s - mn);
+            const float sc = exp2f(m[k] - mn);
+            l[k] = l[k] * sc + warp_sum(p);
+            m[k] = mn;
+#pragma unroll
+            for (int c = 0; c < DL; ++c) acc[k][c] *= sc;
+            for (int j = 0; j < nt; ++j) {
+                const float pj = __shfl_sync(FULL_MASK, p, j);
+#pragma unroll
+                for (int c = 0; c < DL; ++c) {
+                    const int d = lane + 32 * c;
+                    if (d < D) acc[k][c] = fmaf(pj, bf16_to_f32(s_v[j][d]), acc[k][c]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < IPW; ++k) {
+        const int i = warp + k * (APF_THREADS / 32);
+        if (i >= items) break;
+        const int r = i / G, h = i % G;
+        const size_t qrow = (size_t)z * a.T_per_seq + qt0 + r;
+        uint16_t* o = a.att + qrow * a.NH * D + (size_t)(g * G + h) * D;
+        const float inv = 1.f / l[k];
+#pragma unroll
+        for (int c = 0; c < DL; ++c) {
+            const int d = lane + 32 * c;
+            if (d < D) o[d] = f32_to_bf16(acc[k][c] * inv);
+        }
+    }
+}
+
+void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s) {
+    const int G = a.NH / a.NKV;
+    // QT rows x G heads = items, at most 16 per warp (128 per CTA) and their
+    // f32 queries within 48 KB of shared memory.
+    const int max_items = 12288 / a.D < 128 ? 12288 / a.D : 128;
+    int QT = 64;
+    while (QT > 1 && QT * G > max_items) QT >>= 1;
+    const int nseq = a.n / a.T_per_seq;
+    dim3 grid((a.T_per_seq + QT - 1) / QT, a.NKV, nseq);
+    const size_t smem = (size_t)QT * G * a.D * sizeof(float);
+    switch (a.D) {
+        case 16: k_attn_prefill<16, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
+        case 32: k_attn_prefill<32, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
+        case 64: k_attn_prefill<64, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
+        case 128: k_attn_prefill<128, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
+        default: break;
+    }
+}
+
+// ================================================================ label head ==
+__global__ void __launch_bounds__(256) k_cls_head(const float* h, int n, int H, const uint16_t* W,
+                                                  const float* b, int labels, float* out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= n) return;
+    const float* hr = h + (size_t)t * H;
+    for (int j = 0; j < labels; ++j) {
+        const uint16_t* w = W + (size_t)j * H;
+        float s = 0.f;
+        for (int k = lane; k < H; k += 32) s = fmaf(hr[k], bf16_to_f32(w[k]), s);
+        s = warp_sum(s);
+        if (lane == 0) out[(size_t)t * labels + j] = s + (b ? b[j] : 0.f);
+    }
+}
+
+void launch_cls_head(const float* h, int n, int H, const uint16_t* W, const float* b, int labels,
+                     float* out, cudaStream_t s) {
+    k_cls_head<<<(n + 7) / 8, 256, 0, s>>>(h, n, H, W, b, labels, out);
+}
+
+// ============================================== standalone RoPE + bf16 store ==
+__global__ void k_rope_store(const float* x, int n_heads, int D, const float* cos_t,
+                             const float* sin_t, uint16_t* out) {
+    const int t = blockIdx.x, H2 = D / 2;
+    const float* xr = x + (size_t)t * n_heads * D;
+    uint16_t* o = out + (size_t)t * n_heads * D;
+    const float* cs = cos_t + (size_t)t * H2;
+    const float* sn = sin_t + (size_t)t * H2;
+    for (int e = threadIdx.x; e < n_heads * H2; e += blockDim.x) {
+        const int h = e / H2, i = e % H2;
+        float r0, r1;
+        rope_pair(xr[h * D + i], xr[h * D + i + H2], cs[i], sn[i], r0, r1);
+        o[h * D + i] = f32_to_bf16(r0);
+        o[h * D + i + H2] = f32_to_bf16(r1);
+    }
+}
+
+void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const float* cos_t,
+                       const float* sin_t, uint16_t* out, cudaStream_t s) {
+    k_rope_store<<<n_tok, 128, 0, s>>>(x, n_heads, D, cos_t, sin_t, out);
+}
+
+}  // namespace ember

@@ -1,0 +1,215 @@
+/*
+ * ember.h -- C ABI of the GB300 (sm_103a) decoder forward library.
+ *
+ * One forward pass of a Llama/Qwen2-style decoder-only transformer: embedding
+ * gather; per layer RMSNorm, q/k/v projections (optional biases, optional
+ * per-head q/k RMSNorm), rotate-half RoPE (plain or llama3-scaled),
+ * grouped-query attention over a causal bf16 KV cache (or unmasked, for the
+ * bidirectional encoder variant), o_proj and a SwiGLU MLP; then a final
+ * RMSNorm, a tied LM head (or a linear label head) and greedy argmax.  It runs
+ * as one prefill followed by one cached decode step per new token.
+ *
+ * Where each operation is defined (page title, section / function):
+ *   ember, scripts/reference_forward.py: forward() -- rmsnorm, q/k/v + bias,
+ *     rope() rotate-half, KV append, per-head GQA loop, o_proj, SwiGLU, tied
+ *     head; main() -- the greedy loop; load_safetensors() -- bf16 decode.
+ *   LowLlamaBasic, reference.py: predict() -- rotary_cos_sin() with llama3
+ *     scaling, self_attn() causal whole-sequence attention.
+ *   PII-Tracer-vLLM, serving/reference_forward.py: forward() -- per-head q/k
+ *     RMSNorm before RoPE, bidirectional attention, token_cls_head (+ bias).
+ *   Falcon-H1-0.5B-Rust, src/lib.rs: Config::validate and logits()/generate()
+ *     -- the argument errors mirrored by EMBER_ERR_INVALID_ARG / _TOKEN.
+ *   ember internals: "ForwardModel trait" -- create_cache(max_seq_len) and
+ *     forward_with_cache(ids, cache, start_pos), the shape of this ABI;
+ *     "kv cache" -- one contiguous block per layer, a cursor that advances once
+ *     per token after all layers, explicit positions (the prefill bug);
+ *     "qk_scratch" -- no allocation on the hot path.
+ *
+ * Conventions for every call:
+ *   - Pointers named ids / seqs / positions / logits / argmax / hidden / out and
+ *     every weight pointer are DEVICE pointers (cudaMalloc'd or equivalent);
+ *     every other pointer is a host pointer.
+ *   - Calls that take a stream are asynchronous on it: the library enqueues
+ *     kernels and returns.  Argument errors detectable on the host return at
+ *     once; errors that depend on device data (a token id >= vocab, a position
+ *     that disagrees with the cache cursor) raise a device-side status that
+ *     ember_sync_status() reports.  The kernels never read or write outside
+ *     their buffers on such errors: the offending token is skipped.
+ *   - Nothing allocates device memory after ember_model_create / ember_kv_alloc
+ *     except the first decode call of a new (batch, pointer) signature, which
+ *     instantiates a CUDA graph for it.
+ *   - ember_last_error() returns a thread-local message for the last failure.
+ *   - Only one stream may use a given model at a time: the model owns one
+ *     activation workspace.
+ */
+#ifndef EMBER_H
+#define EMBER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *ember_stream_t;
+
+typedef enum ember_status {
+    EMBER_OK = 0,
+    EMBER_ERR_INVALID_ARG = 1, /* bad dims, null pointer, n == 0, bad seq index       */
+    EMBER_ERR_CAPACITY = 2,    /* start_pos + n > max_len, n > max_tokens, batch too big */
+    EMBER_ERR_STATE = 3,       /* a position disagrees with the sequence's cursor        */
+    EMBER_ERR_TOKEN = 4,       /* a token id outside [0, vocab) (found on the device)    */
+    EMBER_ERR_TIMEOUT = 5,     /* a bounded device wait gave up                          */
+    EMBER_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed                    */
+    EMBER_ERR_OOM = 7,         /* device allocation failed                               */
+    EMBER_ERR_UNSUPPORTED = 8  /* a valid request this build does not serve              */
+} ember_status;
+
+/* Model hyper-parameters.  Field names follow the HuggingFace config.json
+ * fields the pages read (ember reference_forward.py main(); LowLlamaBasic
+ * predict(); PII-Tracer forward(): head_dim is explicit, not hidden/heads).
+ * Validation (Falcon-H1 Config::validate): every dimension > 0,
+ * n_heads % n_kv_heads == 0, head_dim even; this build additionally needs
+ * hidden, head_dim and ff to be multiples of 8 (16-byte weight rows),
+ * head_dim <= 256 and n_heads/n_kv_heads <= 16. */
+typedef struct ember_config {
+    int32_t vocab, hidden, layers, n_heads, n_kv_heads, head_dim, ff;
+    double rope_theta;       /* RoPE base                                         */
+    double rms_eps;          /* RMSNorm epsilon                                   */
+    int32_t rope_llama3;     /* 1: llama3 frequency scaling (LowLlamaBasic)       */
+    double rs_factor, rs_low, rs_high; /* llama3 factor, low/high freq factors   */
+    int32_t rs_orig_max_pos; /* llama3 original_max_position_embeddings           */
+    int32_t qkv_bias;        /* 1: q/k/v projections carry biases (Qwen2)         */
+    int32_t qk_norm;         /* 1: per-head RMSNorm of q and k before RoPE (Qwen3)*/
+    int32_t causal;          /* 1: causal decoder; 0: bidirectional encoder       */
+    int32_t n_labels;        /* 0: tied LM head over vocab; >0: linear head       */
+    int32_t max_tokens;      /* capacity of one prefill / encode / decode call in
+                                tokens (0 -> 4096); sizes the workspace           */
+    int32_t max_positions;   /* RoPE table length for encode (0 -> max_tokens)    */
+} ember_config;
+
+/* One layer's weights: device pointers to bf16 bit patterns, HuggingFace
+ * [out_features, in_features] row-major.  Biases / q_norm / k_norm may be NULL
+ * when the config disables them. */
+typedef struct ember_layer_weights {
+    const uint16_t *attn_norm;          /* [hidden]                          */
+    const uint16_t *wq, *wk, *wv;       /* [NH*D, hidden], [NKV*D, hidden] x2 */
+    const uint16_t *bq, *bk, *bv;       /* [NH*D], [NKV*D], [NKV*D]          */
+    const uint16_t *q_norm, *k_norm;    /* [head_dim]                        */
+    const uint16_t *wo;                 /* [hidden, NH*D]                    */
+    const uint16_t *mlp_norm;           /* [hidden]                          */
+    const uint16_t *w_gate, *w_up;      /* [ff, hidden]                      */
+    const uint16_t *w_down;             /* [hidden, ff]                      */
+} ember_layer_weights;
+
+typedef struct ember_weights {
+    const uint16_t *embed;              /* [vocab, hidden]; tied LM head     */
+    const uint16_t *final_norm;         /* [hidden]                          */
+    const uint16_t *cls_w, *cls_b;      /* [n_labels, hidden], [n_labels]    */
+    const ember_layer_weights *layers;  /* HOST array of `layers` entries    */
+} ember_weights;
+
+typedef struct ember_model ember_model;
+typedef struct ember_kv ember_kv;
+
+/* Validate the config, repack the weights into the library's device layout
+ * (fused [q;k;v] rows, interleaved gate/up rows, f32 norms and biases) and
+ * allocate the activation workspace for cfg->max_tokens tokens.  The caller
+ * keeps ownership of its weight buffers and may free them once this returns
+ * (the call synchronises the device).  Errors: INVALID_ARG, OOM, CUDA. */
+ember_status ember_model_create(const ember_config *cfg, const ember_weights *w,
+                                ember_model **out);
+void ember_model_destroy(ember_model *m);
+
+/* Bytes of one bf16 KV cache for max_seqs sequences of max_len positions:
+ * layers * 2 (K and V) * n_kv_heads * max_len * head_dim * 2 bytes * max_seqs
+ * (ember internals, "kv cache": one contiguous block per layer). */
+size_t ember_kv_bytes(const ember_config *cfg, int32_t max_seqs, int32_t max_len);
+
+/* Allocate a zeroed bf16 KV cache ([seq][layer][kv_head][pos][head_dim] for
+ * K and for V) and zeroed cursors, plus the RoPE tables for max_len
+ * positions.  Errors: INVALID_ARG (max_seqs or max_len <= 0, encoder model),
+ * OOM, CUDA. */
+ember_status ember_kv_alloc(ember_model *m, int32_t max_seqs, int32_t max_len, ember_kv **out);
+void ember_kv_free(ember_kv *kv);
+
+/* Set sequence seq's cursor to 0 (its rows are left as they are and are
+ * overwritten by the next prefill).  Asynchronous on stream. */
+ember_status ember_kv_reset(ember_kv *kv, int32_t seq, ember_stream_t stream);
+
+/* Read-only view of the cache for inspection: device base pointers of K and
+ * V (bf16 bits) and the element strides of [seq, layer, kv_head, pos]; the
+ * head_dim stride is 1. */
+ember_status ember_kv_layout(const ember_kv *kv, const uint16_t **k_base,
+                             const uint16_t **v_base, int64_t strides[4]);
+
+/* Prefill: run n tokens ids[0..n) of sequence seq at positions
+ * start_pos .. start_pos+n-1 through every layer, appending their K/V rows,
+ * then advance the cursor to start_pos + n (ember internals, ForwardModel
+ * forward_with_cache(ids, cache, start_pos)).
+ *   logits  [vocab]   f32, logits of the last position (nullable)
+ *   argmax  [1]       int32, greedy token of the last position, lowest index
+ *                     among equal maxima (nullable)
+ *   hidden  [n,hidden] f32, final-RMSNorm'd states of every position (nullable)
+ * Host errors: INVALID_ARG (n <= 0, seq out of range, null ids), CAPACITY
+ * (start_pos + n > max_len or n > max_tokens).  Device status: STATE when
+ * start_pos != the cursor, TOKEN for an id >= vocab. */
+ember_status ember_prefill(ember_model *m, ember_kv *kv, int32_t seq, const int32_t *ids,
+                           int32_t n, int32_t start_pos, float *logits, int32_t *argmax,
+                           float *hidden, ember_stream_t stream);
+
+/* One cached decode step for `batch` sequences: token ids[b] of sequence
+ * seqs[b] at position positions[b] (ember reference_forward.py forward(tok,
+ * pos)); afterwards the cursor of seqs[b] is positions[b] + 1.  All arrays are
+ * device arrays of `batch` entries; the sequences must be distinct.
+ *   logits [batch, vocab] f32 (nullable); argmax [batch] int32 (nullable).
+ * argmax may be the next call's ids, so a greedy loop needs no host sync.
+ * Host errors: INVALID_ARG, CAPACITY (batch > max_tokens or > max_seqs).
+ * Device status: STATE (position != cursor), CAPACITY (position >= max_len),
+ * INVALID_ARG (seq out of range), TOKEN. */
+ember_status ember_decode_step(ember_model *m, ember_kv *kv, int32_t batch, const int32_t *seqs,
+                               const int32_t *ids, const int32_t *positions, float *logits,
+                               int32_t *argmax, ember_stream_t stream);
+
+/* Bidirectional (or causal, per the config) forward of B independent
+ * sequences of T tokens each, positions restarting at 0 per sequence, no KV
+ * cache (PII-Tracer forward()).
+ *   out    [B*T, n_labels] f32 label logits (n_labels > 0), or
+ *          [B*T, vocab] f32 tied-head logits (n_labels == 0)   (nullable)
+ *   hidden [B*T, hidden] f32 final-RMSNorm'd states              (nullable)
+ * Host errors: INVALID_ARG, CAPACITY (B*T > max_tokens, T > max_positions). */
+ember_status ember_encode(ember_model *m, const int32_t *ids, int32_t B, int32_t T, float *out,
+                          float *hidden, ember_stream_t stream);
+
+/* Synchronise the stream, read and clear the device status word.  Returns
+ * the first device-side error raised since the last call, else EMBER_OK. */
+ember_status ember_sync_status(ember_model *m, ember_stream_t stream);
+
+const char *ember_last_error(void);
+
+/* ---- kernel-level entry points used by the parity tests ------------------ */
+
+/* The RoPE-and-store step of the K cache write, alone: for each of n_tok rows
+ * of n_heads*head_dim f32 values x (already q/k-normed where the model does
+ * so), rotate-half by the f32 tables cos_t/sin_t [n_tok, head_dim/2] and
+ * round to bf16 (nearest even) into out [n_tok, n_heads*head_dim].  It is the
+ * same device code the fused cache write runs; every product and sum is
+ * rounded separately, so identical f32 inputs give identical bits on any
+ * correct f32 implementation (ember reference_forward.py rope()). */
+ember_status ember_rope_store(const float *x, int32_t n_tok, int32_t n_heads, int32_t head_dim,
+                              const float *cos_t, const float *sin_t, uint16_t *out,
+                              ember_stream_t stream);
+
+/* D[M,N] = A[M,K] . B[N,K]^T with bf16 A, B and f32 D (row-major, K
+ * contiguous), on the tcgen05 tensor-core GEMM the projections use.  K and
+ * the row strides must be multiples of 8 elements.  Errors: INVALID_ARG. */
+ember_status ember_gemm_bf16(const uint16_t *A, const uint16_t *B, float *D, int32_t M,
+                             int32_t N, int32_t K, ember_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EMBER_H */

@@ -1,0 +1,72 @@
+"""The C ABI library builds, loads and exports every symbol include/ember.h
+declares; host-side argument checks run without a GPU (no compute calls)."""
+import ctypes as C
+import json
+import os
+import re
+
+import pytest
+
+from gqa_transformer_decode_gb300 import ember as E
+from gqa_transformer_decode_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "ember.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ember_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = E.load()
+    names = declared_symbols()
+    assert len(names) >= 14, names
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def test_kv_bytes_matches_the_pages_worked_example():
+    """ember internals, "kv cache" layout: GPT-2 small at 2048 context, factors
+    12 layers x 12 heads x 2048 x 64 x 4 bytes x 2 (K and V).  The printed
+    total (~72 MB) is one tensor's share; the factor product is the size of
+    both.  The library stores bf16, so its figure is half the f32 one."""
+    g = json.load(open(os.path.join(GOLDEN, "kv_cache_size_gpt2_small.json")))
+    cfg = E.ember_config(vocab=50257, hidden=768, layers=g["layers"], n_heads=g["heads"],
+                         n_kv_heads=g["heads"], head_dim=g["head_dim"], ff=3072)
+    f32_bytes = E.ember_kv_bytes(cfg, 1, g["max_seq_len"]) * g["dtype_bytes"] // 2
+    assert f32_bytes == g["bytes_f32_product_of_factors"]
+    assert abs(f32_bytes / 2 / 2 ** 20 - g["stated_total_mb"]) < 0.5
+
+
+def _create(shape, **over):
+    d = {**shape.asdict(), **over}
+    cfg = E.make_config(d)
+    w = E.ember_weights()
+    out = C.c_void_p()
+    st = E.load().ember_model_create(C.byref(cfg), C.byref(w), C.byref(out))
+    return st, E.last_error()
+
+
+@pytest.mark.parametrize("over,msg", [
+    (dict(n_kv_heads=3), "GQA"),          # Falcon-H1 Config::validate: heads % kv_heads
+    (dict(head_dim=15), "GQA"),           # odd head_dim
+    (dict(hidden=0), "zero dimension"),
+    (dict(vocab=0), "zero dimension"),
+    (dict(rope_theta=0.0), "rope_theta"),
+])
+def test_invalid_configs_are_rejected_on_the_host(over, msg):
+    st, err = _create(synth.TINY, **over)
+    assert st == 1 and msg in err, (st, err)
+
+
+def test_missing_weights_are_reported():
+    st, err = _create(synth.TINY)
+    assert st == 1 and "missing weight" in err
+
+
+def test_unsupported_shapes_say_so():
+    st, err = _create(synth.TINY, head_dim=24, n_heads=4, n_kv_heads=2)
+    assert st == 8 and "head_dim" in err

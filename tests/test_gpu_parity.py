@@ -1,0 +1,204 @@
+"""Whole-forward parity of the CUDA library against the CPU oracle, through the
+C ABI, on seeded synthetic weights: prefill + greedy decode, token-by-token
+decode, chunked prefill, batched decode on both decode paths, the bf16 KV
+cache contents, device-side argument errors and the encoder."""
+import numpy as np
+import pytest
+import torch
+
+from gqa_transformer_decode_gb300 import runtime as R
+from gqa_transformer_decode_gb300 import synth
+from oracle import oracle as O
+
+from parity_util import assert_close, assert_tokens, first_argmax
+
+pytestmark = pytest.mark.gpu
+
+SMALL_QWEN2 = synth.ModelShape("s-qwen2", vocab=300, hidden=112, layers=3, n_heads=14,
+                               n_kv_heads=2, head_dim=16, ff=160, rope_theta=1e6, qkv_bias=1)
+SMALL_LLAMA = synth.ModelShape("s-llama", vocab=1000, hidden=256, layers=2, n_heads=8,
+                               n_kv_heads=2, head_dim=32, ff=512, rope_theta=5e5,
+                               rope_llama3=1, rs_factor=32.0, rs_low=1.0, rs_high=4.0,
+                               rs_orig_max_pos=64)
+SMALL_ENC = synth.ModelShape("s-enc", vocab=500, hidden=256, layers=2, n_heads=4, n_kv_heads=2,
+                             head_dim=128, ff=384, rope_theta=1e6, qk_norm=1, causal=0,
+                             n_labels=16)
+
+_cache = {}
+
+
+def model_pair(shape, max_tokens=512):
+    key = (shape.name, max_tokens)
+    if key not in _cache:
+        w = synth.weights_bf16(shape)
+        _cache[key] = (w, O.OracleModel(shape, w), R.Model(shape, w, max_tokens=max_tokens))
+    return _cache[key]
+
+
+@pytest.fixture(scope="module")
+def stream():
+    return torch.cuda.Stream()
+
+
+def i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).cuda()
+
+
+def run_greedy_gpu(model, kv, prompt, n_steps, forced, stream, seq=0, pos0=0):
+    """Prefill, then n_steps decode steps fed the given tokens (teacher forcing
+    with the oracle's tokens keeps later steps comparable)."""
+    V, H, n = model.V, model.H, len(prompt)
+    logits = torch.empty((n_steps + 1, V), dtype=torch.float32, device="cuda")
+    hidden = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    amax = torch.empty(n_steps + 1, dtype=torch.int32, device="cuda")
+    ids = i32(prompt)
+    with torch.cuda.stream(stream):
+        model.prefill(kv, seq, ids, pos0, logits=logits[0], argmax=amax[0:1], hidden=hidden,
+                      stream=stream)
+        seqs = i32([seq])
+        for i in range(1, n_steps + 1):
+            tok = i32([forced[i - 1]])
+            pos = i32([pos0 + n + i - 1])
+            model.decode_step(kv, seqs, tok, pos, logits=logits[i], argmax=amax[i:i + 1],
+                              stream=stream)
+    st = model.sync_status(stream)
+    assert st == 0, st
+    return logits.cpu().numpy(), amax.cpu().numpy(), hidden.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape,n_prompt,n_steps", [(synth.TINY, 8, 16), (SMALL_QWEN2, 37, 12),
+                                                    (SMALL_LLAMA, 150, 10)])
+def test_prefill_and_greedy_decode_match_oracle(shape, n_prompt, n_steps, stream):
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, n_prompt)
+    toks, olg, ohd = om.greedy(prompt, n_steps)
+    kv = gm.kv_alloc(2, n_prompt + n_steps + 8)
+    glg, gam, ghd = run_greedy_gpu(gm, kv, prompt, n_steps, toks[:-1], stream)
+    h_full, _, _ = om.forward_full(np.concatenate([prompt, toks[:-1]]), logits=False)
+    assert_close(h_full[:n_prompt], ghd, "prefill hidden")
+    assert_close(olg, glg, "logits")
+    assert_tokens(olg, toks, gam, "greedy tokens")
+    for i in range(n_steps + 1):   # argmax is the first maximum of the GPU's own logits
+        assert gam[i] == first_argmax(glg[i])
+
+
+def test_token_by_token_decode_equals_oracle(stream):
+    """ember reference_forward.py main(): the prompt fed one token at a time."""
+    shape = SMALL_QWEN2
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, 9)
+    _, olg, _ = om.forward_full(prompt)
+    kv = gm.kv_alloc(1, 16)
+    lg = torch.empty((9, shape.vocab), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for t in range(9):
+            gm.decode_step(kv, i32([0]), i32([prompt[t]]), i32([t]), logits=lg[t], stream=stream)
+    assert gm.sync_status(stream) == 0
+    assert_close(olg, lg.cpu().numpy(), "token-by-token logits")
+
+
+def test_chunked_prefill_equals_single_prefill(stream):
+    shape = SMALL_LLAMA
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, 200)
+    _, olg, _ = om.forward_full(prompt)
+    kv = gm.kv_alloc(1, 256)
+    lg = torch.empty((2, shape.vocab), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        gm.prefill(kv, 0, i32(prompt[:130]), 0, logits=lg[0], stream=stream)
+        gm.prefill(kv, 0, i32(prompt[130:]), 130, logits=lg[1], stream=stream)
+    assert gm.sync_status(stream) == 0
+    assert_close(olg[[129, 199]], lg.cpu().numpy(), "chunked prefill logits")
+
+
+def test_kv_cache_rows_match_oracle(stream):
+    shape = SMALL_QWEN2
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, 20)
+    oc = om.new_cache(24)
+    om.forward_cached(oc, prompt)
+    kv = gm.kv_alloc(2, 24)
+    with torch.cuda.stream(stream):
+        gm.prefill(kv, 1, i32(prompt), 0, stream=stream)
+    assert gm.sync_status(stream) == 0
+    K, V = kv.tensors()
+    gk = O.bf16_decode(K[1].cpu().numpy().view(np.uint16))[:, :, :20]
+    gv = O.bf16_decode(V[1].cpu().numpy().view(np.uint16))[:, :, :20]
+    ok, ov = oc.arrays()
+    assert_close(ok[:, :, :20].reshape(-1, shape.head_dim), gk.reshape(-1, shape.head_dim), "K")
+    assert_close(ov[:, :, :20].reshape(-1, shape.head_dim), gv.reshape(-1, shape.head_dim), "V")
+    # nothing written past the prompt, nothing in the other sequence
+    assert not K[0].any() and not K[1][:, :, 20:].any()
+
+
+@pytest.mark.parametrize("B", [3, 8, 13])
+def test_batched_decode_matches_oracle_per_sequence(B, stream):
+    """B sequences with different prompt lengths decoded together (B <= 8 on
+    the GEMV path, larger on the tensor-core path)."""
+    shape = SMALL_QWEN2
+    w, om, gm = model_pair(shape)
+    lens = [5 + 3 * b for b in range(B)]
+    kv = gm.kv_alloc(B, 64)
+    prompts = [synth.prompt_ids(shape, L, seq=b) for b, L in enumerate(lens)]
+    nxt = [synth.uniform_ids(7, f"next.{b}", 3, shape.vocab) for b in range(B)]
+    lg = torch.empty((3, B, shape.vocab), dtype=torch.float32, device="cuda")
+    am = torch.empty((3, B), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            gm.prefill(kv, b, i32(prompts[b]), 0, stream=stream)
+        seqs = i32(list(range(B)))
+        for s in range(3):
+            gm.decode_step(kv, seqs, i32([nxt[b][s] for b in range(B)]),
+                           i32([lens[b] + s for b in range(B)]), logits=lg[s], argmax=am[s],
+                           stream=stream)
+    assert gm.sync_status(stream) == 0
+    glg = lg.cpu().numpy()
+    gam = am.cpu().numpy()
+    for b in range(B):
+        _, olg, _ = om.forward_full(np.concatenate([prompts[b], nxt[b]]))
+        assert_close(olg[lens[b]:lens[b] + 3], glg[:, b], f"seq {b}")
+        for s in range(3):
+            assert gam[s, b] == first_argmax(glg[s, b])
+
+
+def test_device_status_errors(stream):
+    shape = synth.TINY
+    w, om, gm = model_pair(shape)
+    kv = gm.kv_alloc(2, 16)
+    with torch.cuda.stream(stream):
+        gm.prefill(kv, 0, i32([1, 2, 3]), 0, stream=stream)
+    assert gm.sync_status(stream) == 0
+    with torch.cuda.stream(stream):   # position 5 != cursor 3
+        gm.decode_step(kv, i32([0]), i32([4]), i32([5]), stream=stream)
+    assert gm.sync_status(stream) == 3
+    with torch.cuda.stream(stream):   # token outside the vocabulary
+        gm.decode_step(kv, i32([1]), i32([shape.vocab + 5]), i32([0]), stream=stream)
+    assert gm.sync_status(stream) == 4
+    with torch.cuda.stream(stream):   # seq out of range
+        gm.decode_step(kv, i32([7]), i32([1]), i32([0]), stream=stream)
+    assert gm.sync_status(stream) == 1
+    with torch.cuda.stream(stream):   # prefill at the wrong start position
+        gm.prefill(kv, 1, i32([1, 2]), 4, stream=stream)
+    assert gm.sync_status(stream) == 3
+    with pytest.raises(R.E.EmberError) as ei:
+        gm.prefill(kv, 0, i32(list(range(20))), 0, stream=stream)
+    assert ei.value.status == 2   # capacity: 20 > max_len 16
+
+
+@pytest.mark.parametrize("B,T", [(1, 7), (3, 40), (2, 130)])
+def test_encoder_matches_oracle(B, T, stream):
+    """PII-Tracer forward(): bidirectional, q/k norm, positions restart per
+    sequence, 16-label head with bias."""
+    shape = SMALL_ENC
+    w, om, gm = model_pair(shape)
+    ids = np.stack([synth.prompt_ids(shape, T, seq=b) for b in range(B)])
+    out = torch.empty((B * T, shape.n_labels), dtype=torch.float32, device="cuda")
+    hid = torch.empty((B * T, shape.hidden), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        gm.encode(i32(ids.reshape(-1)), B, T, out=out, hidden=hid, stream=stream)
+    assert gm.sync_status(stream) == 0
+    go, gh = out.cpu().numpy(), hid.cpu().numpy()
+    for b in range(B):
+        h, _, cls = om.forward_full(ids[b], logits=False, cls=True)
+        assert_close(h, gh[b * T:(b + 1) * T], f"encoder hidden seq {b}")
+        assert_close(cls, go[b * T:(b + 1) * T], f"encoder labels seq {b}")
