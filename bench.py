@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of the decoder forward on one GB300 (or N replicas).
+
+Default workload (one "step" = one whole generation job on the
+Qwen2.5-0.5B-shaped decoder, random bf16 weights, batch 1): prefill of a
+128-token uniform prompt, then 128 greedy decode steps, each fed the previous
+argmax, through the C ABI (ember_prefill, ember_decode_step).  Weights (988 MB)
+exceed the 129 MB L2, so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ember|reference]
+                    [--workload qwen2.5-0.5b|llama-3.2-1b|qwen2.5-0.5b-b64|qwen3-encoder]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (bounded sample, extrapolated to the same job), since the
+pages hold no runnable reference implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from gqa_transformer_decode_gb300 import synth  # noqa: E402
+
+METRIC = "decode tok/s @B=1,64 + prefill tok/s (0.5B/1B shapes); HBM GB/s vs peak"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained",
+                                                                         d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- distributed --
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------- GPU workloads --
+class DecodeJob:
+    """B sequences: prefill `prompt` tokens each, then `steps` greedy decode
+    steps of the whole batch with argmax fed back as the next ids."""
+
+    def __init__(self, wl: synth.Workload, weights, stream):
+        import torch
+        from gqa_transformer_decode_gb300 import runtime as R
+        self.torch = torch
+        self.wl = wl
+        m = wl.model
+        self.B, self.P, self.S = wl.batch, wl.prompt, wl.steps
+        self.stream = stream
+        self.model = R.Model(m, weights, max_tokens=max(self.P, 64))
+        self.kv = self.model.kv_alloc(self.B, self.P + self.S + 1)
+        self.prompts = [torch.as_tensor(synth.prompt_ids(m, self.P, seq=b)).cuda()
+                        for b in range(self.B)]
+        self.seqs = torch.arange(self.B, dtype=torch.int32, device="cuda")
+        self.cur = torch.zeros(self.B, dtype=torch.int32, device="cuda")
+        self.prefill_in_job = self.B == 1
+        if not self.prefill_in_job:   # batched decode: prompts prefilled once, outside timing
+            with torch.cuda.stream(stream):
+                for b in range(self.B):
+                    self.model.prefill(self.kv, b, self.prompts[b], 0, argmax=self.cur[b:b + 1],
+                                       stream=stream)
+            assert self.model.sync_status(stream) == 0
+
+    def run(self, ev=None, host_ids=None, host_out=None):
+        """One job; ev = (start, after_prefill, end) CUDA events."""
+        torch, s, m, kv = self.torch, self.stream, self.model, self.kv
+        with torch.cuda.stream(s):
+            if ev:
+                ev[0].record(s)
+            if self.prefill_in_job:
+                kv.set_cursor(0, 0, stream=s)
+                ids = self.prompts[0]
+                if host_ids is not None:
+                    ids = self._dev_ids
+                    ids.copy_(host_ids, non_blocking=True)
+                m.prefill(kv, 0, ids, 0, argmax=self.cur[0:1], stream=s)
+            else:
+                for b in range(self.B):
+                    kv.set_cursor(b, self.P, stream=s)
+            if ev:
+                ev[1].record(s)
+            for _ in range(self.S):
+                m.decode_step(kv, self.seqs, self.cur, None, argmax=self.cur, stream=s)
+            if host_out is not None:
+                host_out.copy_(self.cur, non_blocking=True)
+            if ev:
+                ev[2].record(s)
+
+    def prepare_e2e(self):
+        torch = self.torch
+        self._dev_ids = torch.empty(self.P, dtype=torch.int32, device="cuda")
+        host_ids = self.prompts[0].cpu().pin_memory()
+        host_out = torch.empty(self.B, dtype=torch.int32).pin_memory()
+        return host_ids, host_out
+
+    def tokens_per_job(self):
+        return self.B * self.S
+
+    def bytes_per_decode_step(self, ctx_mid):
+        """Algorithmic HBM bytes of one decode step: every bf16 weight once
+        (layers + tied head) plus the KV rows read and the new rows written."""
+        m = self.wl.model
+        weights = 2 * m.params() - 2 * m.hidden   # bf16; final norm not re-read per token
+        kv_tok = m.layers * 2 * m.n_kv_heads * m.head_dim * 2
+        return weights + self.B * kv_tok * (ctx_mid + 1)
+
+
+class EncodeJob:
+    """B sequences of T tokens through the bidirectional encoder and the label
+    head (ember_encode)."""
+
+    def __init__(self, wl: synth.Workload, weights, stream):
+        import torch
+        from gqa_transformer_decode_gb300 import runtime as R
+        self.torch = torch
+        self.wl = wl
+        m = wl.model
+        self.B, self.T = wl.batch, wl.prompt
+        self.stream = stream
+        self.model = R.Model(m, weights, max_tokens=self.B * self.T, max_positions=self.T)
+        ids = np.concatenate([synth.prompt_ids(m, self.T, seq=b) for b in range(self.B)])
+        self.ids = torch.as_tensor(ids).cuda()
+        self.out = torch.empty((self.B * self.T, m.n_labels), dtype=torch.float32, device="cuda")
+        self.prefill_in_job = True
+
+    def run(self, ev=None, host_ids=None, host_out=None):
+        torch, s = self.torch, self.stream
+        with torch.cuda.stream(s):
+            if ev:
+                ev[0].record(s)
+            ids = self.ids
+            if host_ids is not None:
+                ids = self._dev_ids
+                ids.copy_(host_ids, non_blocking=True)
+            if ev:
+                ev[1].record(s)
+            self.model.encode(ids, self.B, self.T, out=self.out, stream=s)
+            if host_out is not None:
+                host_out.copy_(self.out, non_blocking=True)
+            if ev:
+                ev[2].record(s)
+
+    def prepare_e2e(self):
+        torch = self.torch
+        self._dev_ids = torch.empty_like(self.ids)
+        return self.ids.cpu().pin_memory(), torch.empty(tuple(self.out.shape)).pin_memory()
+
+    def tokens_per_job(self):
+        return self.B * self.T
+
+    def flops_per_job(self):
+        m = self.wl.model
+        H, D, F = m.hidden, m.head_dim, m.ff
+        q, kv = m.n_heads * D, m.n_kv_heads * D
+        lin = 2 * self.B * self.T * m.layers * ((q + 2 * kv) * H + q * H + 3 * F * H)
+        att = 4 * self.B * self.T * self.T * D * m.n_heads * m.layers
+        return lin + att
+
+
+def gemv_roofline(stream, hbm_peak, n_launch=30):
+    """Live CUDA-event timing of the split GEMV (the decode projections'
+    kernel) on the LM-head shape of the workload, alone, inputs > L2."""
+    import ctypes
+    import torch
+    from gqa_transformer_decode_gb300 import ember as E
+    N, K = synth.QWEN25_05B.vocab, synth.QWEN25_05B.hidden
+    W = (torch.randn(N, K, device="cuda") * 0.02).to(torch.bfloat16).view(torch.int16)
+    x = torch.randn(K, device="cuda")
+    y = torch.empty(N, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_launch)]
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            E.check(E.ember_gemv_bf16(P(W), N, K, P(x), 1, P(y), sp), "gemv")
+        for a, b in evs:
+            a.record(stream)
+            E.check(E.ember_gemv_bf16(P(W), N, K, P(x), 1, P(y), sp), "gemv")
+            b.record(stream)
+    stream.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = N * K * 2 + K * 4 + N * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "k_gemv (split GEMV, LM-head shape 151936x896, nb=1, alone)",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(gbs / hbm_peak, 4), "traffic": None, "bytes_per_launch": nbytes,
+            "avg_launch_us": round(ms * 1e3, 2)}
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    from gqa_transformer_decode_gb300 import ember as E
+    wl = synth.WORKLOADS[args.workload]
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+    stream = torch.cuda.Stream()
+    weights = synth.weights_bf16(wl.model)
+    encoder = wl.model.causal == 0
+    job = EncodeJob(wl, weights, stream) if encoder else DecodeJob(wl, weights, stream)
+    del weights
+
+    # warm-up (graph capture happens on the first decode call)
+    for _ in range(args.warmup):
+        job.run()
+    assert job.model.sync_status(stream) == 0
+
+    # timed region: K jobs, per-job events on the launching stream
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = E.ember_kernel_launches()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            job.run(ev=evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    launches = E.ember_kernel_launches() - launches0
+    barrier(world)
+    st = job.model.sync_status(stream)
+    assert st == 0, f"device status {st}"
+    job_ms = [a.elapsed_time(c) for a, b, c in evs]
+    pre_ms = [a.elapsed_time(b) for a, b, c in evs]
+    dec_ms = [b.elapsed_time(c) for a, b, c in evs]
+    total_s = max_over_ranks(sum(job_ms) / 1e3, world)
+    tokens = job.tokens_per_job() * args.steps * world
+    value = tokens / total_s
+    if encoder:
+        step_ms = statistics.mean(dec_ms)
+        step_bytes, step_gbs = 0, 0.0
+    else:
+        step_ms = statistics.mean(dec_ms) / wl.steps
+        ctx_mid = wl.prompt + wl.steps // 2
+        step_bytes = job.bytes_per_decode_step(ctx_mid)
+        step_gbs = step_bytes / (step_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers (prompt in, last tokens out)
+    e2e = None
+    if job.prefill_in_job:
+        host_ids, host_out = job.prepare_e2e()
+        e2e_ms = []
+        for i in range(max(1, min(args.steps, 5))):
+            barrier(world)
+            torch.cuda.synchronize()
+            t = time.perf_counter()
+            job.run(host_ids=host_ids, host_out=host_out)
+            stream.synchronize()
+            _ = host_out.numpy().copy()
+            e2e_ms.append((time.perf_counter() - t) * 1e3)
+        e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
+        e2e = {"value": round(job.tokens_per_job() * len(e2e_ms) * world / e2e_s, 2),
+               "unit": "tok/s", "h2d_bytes_per_step": int(host_ids.numel() * 4),
+               "d2h_bytes_per_step": int(host_out.numel() * 4)}
+
+    roof = gemv_roofline(stream, hbm_peak)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(max_over_ranks(statistics.mean(job_ms), world), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random bf16 weights N(0,0.02), norms 1+N(0,0.1); uniform ids)",
+        "config": {"workload": wl.key, "model_shape": wl.model.name, "batch": wl.batch,
+                   "prompt": wl.prompt, "decode_steps": wl.steps,
+                   "step": ("one job: prefill + greedy decode" if job.prefill_in_job
+                            else "one job: greedy decode of the prefilled batch"),
+                   "value": "generated tokens / job time (prefill included when in the job)",
+                   "l2": "weights 2x-20x larger than the 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "decode_tok_s": None if encoder else round(wl.batch / (step_ms * 1e-3), 2),
+        "encode_tflops": (round(job.flops_per_job() / (step_ms * 1e-3) / 1e12, 1)
+                          if encoder else None),
+        "decode_step_us": round(step_ms * 1e3, 2),
+        "prefill_tok_s": (round(wl.prompt / (statistics.mean(pre_ms) * 1e-3), 1)
+                          if job.prefill_in_job and not encoder else None),
+        "step_hbm": {"bytes_per_step": step_bytes, "achieved": round(step_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(step_gbs / hbm_peak, 4),
+                     "peak_source": peak_src},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not encoder:
+        out["cpu_baseline"] = cpu_baseline(wl, sample_steps=8)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(wl: synth.Workload, sample_steps: int):
+    """Oracle on the host cores: prefill + sample_steps decode steps of
+    sequence 0; returns (prefill_s, per_step_s, threads)."""
+    from oracle import oracle as O
+    m = wl.model
+    om = O.OracleModel(m, synth.weights_bf16(m))
+    prompt = synth.prompt_ids(m, wl.prompt)
+    cache = om.new_cache(wl.prompt + sample_steps + 1)
+    t = time.perf_counter()
+    rc, _, lg = om.forward_cached(cache, prompt)
+    pre = time.perf_counter() - t
+    tok = np.array([O.argmax(lg)], dtype=np.int32)
+    t = time.perf_counter()
+    for _ in range(sample_steps):
+        rc, _, lg = om.forward_cached(cache, tok)
+        tok = np.array([O.argmax(lg)], dtype=np.int32)
+    per = (time.perf_counter() - t) / max(1, sample_steps)
+    return pre, per, O.num_threads()
+
+
+def cpu_baseline(wl, sample_steps=8):
+    pre, per, thr = oracle_sample(wl, sample_steps)
+    job = (pre if wl.batch == 1 else 0.0) + wl.steps * per * wl.batch
+    return {"value": round(wl.batch * wl.steps / job, 3), "unit": "tok/s", "cores": thr,
+            "kind": "oracle",
+            "sample": (f"prefill {wl.prompt} + {sample_steps} decode steps of one sequence, "
+                       f"extrapolated to the {wl.steps}-step job"),
+            "prefill_s": round(pre, 3), "decode_step_s": round(per, 4)}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    vals = []
+    for i in range(args.warmup + args.steps):
+        pre, per, thr = oracle_sample(wl, sample_steps=2)
+        if i >= args.warmup:
+            job = (pre if wl.batch == 1 else 0.0) + wl.steps * per * wl.batch
+            vals.append((job, pre, per))
+    job_s = statistics.mean(v[0] for v in vals)
+    value = wl.batch * wl.steps / job_s
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(job_s * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.key, "model_shape": wl.model.name, "batch": wl.batch,
+                      "prompt": wl.prompt, "decode_steps": wl.steps},
+           "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": thr,
+                            "kind": "oracle",
+                            "sample": (f"each step: prefill {wl.prompt} + 2 decode steps, "
+                                       f"extrapolated to the {wl.steps}-step job")},
+           "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ember", choices=["ember", "reference"])
+    ap.add_argument("--workload", default="qwen2.5-0.5b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

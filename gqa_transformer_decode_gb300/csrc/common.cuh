@@ -109,6 +109,17 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, 
     r1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// pdl_trigger: allow the next kernel in the stream to start its prologue;
+// pdl_wait: block until the previous kernel has completed and its writes are
+// visible.  Both are no-ops when the kernel was launched without the
+// programmatic-serialization attribute.  Every read of data produced by an
+// earlier kernel comes after pdl_wait().
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- device side of the model ------------------------------------------------------------
 enum EpiMode : int {
     EPI_STORE = 0,   // out_f32[m][n] = acc (+ bias[n])

@@ -16,6 +16,8 @@ namespace ember {
 __global__ void k_embed(EmbedArgs a) {
     const int t = blockIdx.x;
     __shared__ int s_id;
+    pdl_trigger();
+    pdl_wait();   // x is still read by the previous step's LM head
     if (threadIdx.x == 0) {
         int id = a.ids[t];
         int ok = 1;
@@ -25,17 +27,23 @@ __global__ void k_embed(EmbedArgs a) {
             ok = 0;
         }
         if (a.seqs) {
-            const int seq = a.seqs[t], pos = a.positions[t];
+            const int seq = a.seqs[t];
+            int pos = -1;
             if (seq < 0 || seq >= a.max_seqs) {
                 raise_status(a.status, EMBER_ERR_INVALID_ARG);
                 ok = 0;
-            } else if (pos < 0 || pos >= a.max_len) {
-                raise_status(a.status, EMBER_ERR_CAPACITY);
-                ok = 0;
-            } else if (pos != a.cursor[seq]) {  // ember internals: explicit pos == cursor
-                raise_status(a.status, EMBER_ERR_STATE);
+            } else {
+                // no positions array: the token goes at its sequence's cursor
+                pos = a.positions ? a.positions[t] : a.cursor[seq];
+                if (pos < 0 || pos >= a.max_len) {
+                    raise_status(a.status, EMBER_ERR_CAPACITY);
+                    ok = 0;
+                } else if (pos != a.cursor[seq]) {  // ember internals: explicit pos == cursor
+                    raise_status(a.status, EMBER_ERR_STATE);
+                }
             }
             a.tok_ok[t] = ok;
+            a.tok_pos[t] = pos;
         }
         if (t == 0 && a.pf_seq >= 0 && a.cursor[a.pf_seq] != a.pf_start)
             raise_status(a.status, EMBER_ERR_STATE);
@@ -48,7 +56,7 @@ __global__ void k_embed(EmbedArgs a) {
 }
 
 void launch_embed(const EmbedArgs& a, cudaStream_t s) {
-    k_embed<<<a.n, 256, 0, s>>>(a);
+    launch_k(k_embed, dim3(a.n), dim3(256), 0, s, a);
 }
 
 // =================================================================== GEMV ==
@@ -59,6 +67,22 @@ void launch_embed(const EmbedArgs& a, cudaStream_t s) {
 // statistics of the nb input rows are computed once per CTA.
 constexpr int GEMV_THREADS = 256;
 constexpr int GEMV_MAXJ = 8;
+
+// Issue the weight loads of one row tile (immutable data: may run before
+// the predecessor kernel has finished).
+template <int TPR>
+__device__ __forceinline__ void gemv_load_tile(const GemvArgs& a, int tile, int r, int sub, int K8,
+                                               uint4 (&w)[GEMV_MAXJ]) {
+    constexpr int R = GEMV_THREADS / TPR;
+    const int row = tile * R + r;
+    if (row >= a.N) return;
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.W + (size_t)row * a.K);
+#pragma unroll
+    for (int j = 0; j < GEMV_MAXJ; ++j) {
+        const int c = sub + j * TPR;
+        if (c < K8) w[j] = ld_stream(wrow + c);
+    }
+}
 
 template <int TPR, int NB>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
@@ -74,6 +98,14 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     const int r = tid / TPR, sub = tid % TPR;
     const int K8 = a.K >> 3;
     const int nb = a.nb;
+    const int n_tiles = (a.N + R - 1) / R;
+
+    pdl_trigger();
+    // The first tile's weights stream in while the previous kernel drains.
+    uint4 w[GEMV_MAXJ];
+    int tile = blockIdx.x;
+    if (tile < n_tiles) gemv_load_tile<TPR>(a, tile, r, sub, K8, w);
+    pdl_wait();
 
     // RMSNorm statistics of every input row (ember reference_forward.py rmsnorm()).
     for (int b = 0; b < NB; ++b) {
@@ -94,17 +126,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) best[b] = 0ull;
 
-    const int n_tiles = (a.N + R - 1) / R;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (; tile < n_tiles; tile += gridDim.x) {
         const int row = tile * R + r;
         const bool rv = row < a.N;
-        const uint4* wrow = reinterpret_cast<const uint4*>(a.W + (size_t)(rv ? row : 0) * a.K);
-        uint4 w[GEMV_MAXJ];
-#pragma unroll
-        for (int j = 0; j < GEMV_MAXJ; ++j) {
-            const int c = sub + j * TPR;
-            if (rv && c < K8) w[j] = ld_stream(wrow + c);
-        }
         float acc[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[b] = 0.f;
@@ -136,6 +160,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
                 }
             }
         }
+        // next tile's weights fly during this tile's reduction and epilogue
+        if (tile + (int)gridDim.x < n_tiles) gemv_load_tile<TPR>(a, tile + gridDim.x, r, sub, K8, w);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
 #pragma unroll
@@ -196,10 +222,11 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
 
 template <int TPR>
 static void gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
-    if (a.nb <= 1) k_gemv<TPR, 1><<<grid, GEMV_THREADS, 0, s>>>(a);
-    else if (a.nb <= 2) k_gemv<TPR, 2><<<grid, GEMV_THREADS, 0, s>>>(a);
-    else if (a.nb <= 4) k_gemv<TPR, 4><<<grid, GEMV_THREADS, 0, s>>>(a);
-    else k_gemv<TPR, 8><<<grid, GEMV_THREADS, 0, s>>>(a);
+    const dim3 g(grid), b(GEMV_THREADS);
+    if (a.nb <= 1) launch_k(k_gemv<TPR, 1>, g, b, 0, s, a);
+    else if (a.nb <= 2) launch_k(k_gemv<TPR, 2>, g, b, 0, s, a);
+    else if (a.nb <= 4) launch_k(k_gemv<TPR, 4>, g, b, 0, s, a);
+    else launch_k(k_gemv<TPR, 8>, g, b, 0, s, a);
 }
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
@@ -223,36 +250,46 @@ void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
 }
 
 // ========================================================= decode attention ==
-// CTA (split s, kv head g, token b), 128 threads.  Keys [0, pos] are divided
-// evenly over gridDim.x splits; each split streams its K/V rows through
-// shared memory in tiles of 64 and keeps an online softmax (running max m,
-// sum l, output acc) per query head, in the base-2 domain.
+// CTA (split s, kv head g, token b), 128 threads.  Keys [0, pos] are cut into
+// at most gridDim.x splits of at least ATT_MIN_CHUNK keys (decided on the
+// device from the token's position, so one launch shape serves every
+// context length); each active split streams its K/V rows through shared
+// memory in tiles of 64 and keeps an online softmax (running max m, sum l,
+// output acc) per query head in the base-2 domain.  The last split to finish
+// merges the partials (log-sum-exp rescale).
 constexpr int ATT_THREADS = 128;
 constexpr int ATT_TK = 64;
 constexpr int ATT_MAXG = 16;
+constexpr int ATT_MIN_CHUNK = 64;
+constexpr int ATT_MAX_SPLITS = 32;
 
 template <int D>
 __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
     constexpr int H2 = D / 2;
     constexpr int KP = D + 2;   // padded K row (bf16 elements): conflict-free row reads
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int S = gridDim.x;
     const int G = a.NH / a.NKV;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     __shared__ float s_q[ATT_MAXG][D];
     __shared__ __align__(16) uint16_t s_k[ATT_TK][KP];
     __shared__ __align__(16) uint16_t s_v[ATT_TK][D];
-    __shared__ float s_sc[ATT_MAXG][ATT_TK];
+    __shared__ float s_sc[ATT_MAXG][ATT_TK];   // scores; split statistics at the merge
+    static_assert(ATT_MAXG * ATT_TK >= 2 * ATT_MAX_SPLITS * ATT_MAXG, "merge scratch");
     __shared__ float s_m[ATT_MAXG], s_l[ATT_MAXG], s_scale[ATT_MAXG];
     __shared__ float s_kv[2][D];
     __shared__ int s_last;
 
+    pdl_trigger();
+    pdl_wait();
     if (!a.tok_ok[b]) return;   // the embed kernel flagged this token
     const int pos = a.positions[b];
     const int seq = a.seqs[b];
     const int n_keys = pos + 1;
-    const int per = (n_keys + S - 1) / S;
+    int per = (n_keys + gridDim.x - 1) / gridDim.x;
+    per = per < ATT_MIN_CHUNK ? ATT_MIN_CHUNK : per;
+    const int S = (n_keys + per - 1) / per;   // active splits
+    if (split >= S) return;
     const int lo = split * per;
     const int hi = min(n_keys, lo + per);
     const float* qkv = a.qkv + (size_t)b * a.ld_qkv;
@@ -384,8 +421,22 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
         __syncthreads();
     }
 
+    const size_t out0 = (size_t)b * a.NH * D + (size_t)(g * G) * D;
+    if (S == 1) {   // a single split is already the answer
+#pragma unroll
+        for (int i = 0; i < MAXE; ++i) {
+            const int e = tid + i * ATT_THREADS;
+            if (e < G * D) {
+                const float o = acc[i] / s_l[e / D];
+                if (a.att_b) a.att_b[out0 + e] = f32_to_bf16(o);
+                else a.att[out0 + e] = o;
+            }
+        }
+        return;
+    }
+
     // ---- write this split's partial (m, l, acc) ----
-    float* part = a.part + ((((size_t)b * a.NKV + g) * S + split) * G) * (D + 2);
+    float* part = a.part + ((((size_t)b * a.NKV + g) * ATT_MAX_SPLITS + split) * G) * (D + 2);
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {
         const int e = tid + i * ATT_THREADS;
@@ -405,39 +456,51 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
     if (!s_last) return;
     __threadfence();
 
-    // ---- last split: merge all S partials (log-sum-exp rescale) ----
-    const float* pb = a.part + (((size_t)b * a.NKV + g) * S) * G * (D + 2);
+    // ---- last split: merge the S partials.  All (m, l) pairs are fetched in
+    // one parallel pass, then every output element sums S independent loads.
+    const float* pb = a.part + (((size_t)b * a.NKV + g) * ATT_MAX_SPLITS) * G * (D + 2);
+    float* s_pm = &s_sc[0][0];                       // [S][G] maxima, then weights
+    float* s_pl = &s_sc[0][0] + ATT_MAX_SPLITS * ATT_MAXG;   // [S][G] sums
+    for (int e = tid; e < S * G; e += ATT_THREADS) {
+        const float* ps = pb + (size_t)e * (D + 2);
+        s_pm[e] = __ldcg(ps);
+        s_pl[e] = __ldcg(ps + 1);
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < S; ++s2)
+            if (s_pl[s2 * G + tid] > 0.f) M = fmaxf(M, s_pm[s2 * G + tid]);
+        float L = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+            const float l = s_pl[s2 * G + tid];
+            const float f = l > 0.f ? exp2f(s_pm[s2 * G + tid] - M) : 0.f;   // empty: nothing
+            s_pm[s2 * G + tid] = f;
+            L += l * f;
+        }
+        s_scale[tid] = 1.f / L;
+    }
+    __syncthreads();
     for (int e = tid; e < G * D; e += ATT_THREADS) {
         const int h = e / D, d = e % D;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < S; ++s2) {
-            const volatile float* ps = pb + ((size_t)s2 * G + h) * (D + 2);
-            if (ps[1] > 0.f) M = fmaxf(M, ps[0]);
-        }
-        float L = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < S; ++s2) {
-            const volatile float* ps = pb + ((size_t)s2 * G + h) * (D + 2);
-            const float l = ps[1];
-            if (l > 0.f) {   // empty splits contribute nothing (no NaN)
-                const float f = exp2f(ps[0] - M);
-                L += l * f;
-                O += ps[2 + d] * f;
-            }
-        }
-        const size_t oi = (size_t)b * a.NH * D + (size_t)(g * G + h) * D + d;
-        if (a.att_b) a.att_b[oi] = f32_to_bf16(O / L);
-        else a.att[oi] = O / L;
+        float O = 0.f;
+#pragma unroll 4
+        for (int s2 = 0; s2 < S; ++s2)
+            O = fmaf(__ldcg(pb + ((size_t)s2 * G + h) * (D + 2) + 2 + d), s_pm[s2 * G + h], O);
+        O *= s_scale[h];
+        if (a.att_b) a.att_b[out0 + e] = f32_to_bf16(O);
+        else a.att[out0 + e] = O;
     }
     if (tid == 0) a.counters[b * a.NKV + g] = 0u;
 }
 
 void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s) {
-    dim3 grid(a.splits, a.NKV, a.nb);
+    dim3 grid(a.splits < ATT_MAX_SPLITS ? a.splits : ATT_MAX_SPLITS, a.NKV, a.nb);
     switch (a.D) {
-        case 16: k_attn_decode<16><<<grid, ATT_THREADS, 0, s>>>(a); break;
-        case 32: k_attn_decode<32><<<grid, ATT_THREADS, 0, s>>>(a); break;
-        case 64: k_attn_decode<64><<<grid, ATT_THREADS, 0, s>>>(a); break;
-        case 128: k_attn_decode<128><<<grid, ATT_THREADS, 0, s>>>(a); break;
+        case 16: launch_k(k_attn_decode<16>, grid, dim3(ATT_THREADS), 0, s, a); break;
+        case 32: launch_k(k_attn_decode<32>, grid, dim3(ATT_THREADS), 0, s, a); break;
+        case 64: launch_k(k_attn_decode<64>, grid, dim3(ATT_THREADS), 0, s, a); break;
+        case 128: launch_k(k_attn_decode<128>, grid, dim3(ATT_THREADS), 0, s, a); break;
         default: break;   // rejected by model validation
     }
 }
@@ -445,6 +508,8 @@ void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s) {
 // ================================================================== finish ==
 __global__ void k_finish(FinishArgs a) {
     const int b = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (b < a.nb) {
         if (a.argmax) a.argmax[b] = argmax_key_index(a.keys[b]);
         a.keys[b] = 0ull;
@@ -455,7 +520,15 @@ __global__ void k_finish(FinishArgs a) {
 
 void launch_finish(const FinishArgs& a, cudaStream_t s) {
     const int th = a.nb < 32 ? 32 : ((a.nb + 31) / 32) * 32;
-    k_finish<<<1, th, 0, s>>>(a);
+    launch_k(k_finish, dim3(1), dim3(th), 0, s, a);
+}
+
+// Set one sequence's cursor (value passed by argument: capturable, no host buffer).
+__global__ void k_set_cursor(int32_t* cursor, int seq, int pos) { cursor[seq] = pos; }
+
+void launch_set_cursor(int32_t* cursor, int seq, int pos, cudaStream_t s) {
+    count_launches(1);
+    k_set_cursor<<<1, 1, 0, s>>>(cursor, seq, pos);
 }
 
 // ================================================================ repack ==
@@ -466,6 +539,7 @@ __global__ void k_bf16_to_f32(const uint16_t* in, float* out, long long n) {
 }
 
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s) {
+    count_launches(1);
     if (n <= 0) return;
     long long blocks = (n + 255) / 256;
     k_bf16_to_f32<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(in, out, n);

@@ -175,10 +175,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             "r"((uint32_t)BN));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // barrier init and TMEM allocation overlapped the previous kernel's tail;
+    // activations (A) and the residual stream are its outputs.
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------- TMA producer
@@ -362,7 +366,8 @@ static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int*
     dim3 grid((p.N + BN - 1) / BN, (m_rows + GEMM_BM - 1) / GEMM_BM);
     const CUtensorMap* ta = reinterpret_cast<const CUtensorMap*>(p.tmA);
     const CUtensorMap* tb = reinterpret_cast<const CUtensorMap*>(p.tmB);
-    k_gemm_tc<BN, STAGES><<<grid, GEMM_THREADS, SMEM, s>>>(*ta, *tb, m_rows, p.N, p.K, e, status);
+    launch_k(k_gemm_tc<BN, STAGES>, grid, dim3(GEMM_THREADS), SMEM, s, *ta, *tb, m_rows, p.N, p.K,
+             e, status);
 }
 
 void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,

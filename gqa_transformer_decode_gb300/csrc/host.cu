@@ -7,6 +7,7 @@
 // "kv cache" (one block per layer, cursor advanced after all layers, explicit
 // positions); argument errors after Falcon-H1-0.5B-Rust Config::validate,
 // logits() and generate().
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -109,9 +110,21 @@ struct GraphEntry {
     int batch;
     const void *seqs, *ids, *pos, *logits, *argmax;
     cudaGraphExec_t exec;
+    long long kernels;   // kernel nodes, counted once per replay
 };
 
+std::atomic<long long> g_launches{0};
+
 }  // namespace
+
+namespace ember {
+bool pdl_enabled() {
+    static const bool on = !(getenv("EMBER_NO_PDL") && atoi(getenv("EMBER_NO_PDL")));
+    return on;
+}
+void count_launches(long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+unsigned long long launches_so_far() { return (unsigned long long)g_launches.load(); }
+}  // namespace ember
 
 struct ember_model {
     ember_config c;
@@ -128,6 +141,7 @@ struct ember_model {
     unsigned* counters;
     unsigned long long* keys;
     int *tok_ok, *status;
+    int32_t* tok_pos;
     float *enc_cos = nullptr, *enc_sin = nullptr;
     int enc_positions = 0;
     GemmPlan p_head;   // tied head on bf16 final states (encode without labels)
@@ -248,6 +262,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     aa.add(&m->counters, (size_t)B * NKV);
     aa.add(&m->keys, (size_t)B);
     aa.add(&m->tok_ok, (size_t)B);
+    aa.add(&m->tok_pos, (size_t)B);
     aa.add(&m->status, 1);
     if (!c.causal) {
         aa.add(&m->enc_k, (size_t)T * m->kv);
@@ -401,6 +416,15 @@ ember_status ember_kv_reset(ember_kv* kv, int32_t seq, ember_stream_t stream) {
     if (!kv) return fail(EMBER_ERR_INVALID_ARG, "kv is NULL");
     if (seq < 0 || seq >= kv->max_seqs) return fail(EMBER_ERR_INVALID_ARG, "seq %d out of range", seq);
     CK(cudaMemsetAsync(kv->cursor + seq, 0, 4, (cudaStream_t)stream));
+    return EMBER_OK;
+}
+
+ember_status ember_kv_set_cursor(ember_kv* kv, int32_t seq, int32_t pos, ember_stream_t stream) {
+    if (!kv) return fail(EMBER_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(EMBER_ERR_INVALID_ARG, "seq %d out of range", seq);
+    if (pos < 0 || pos > kv->max_len) return fail(EMBER_ERR_CAPACITY, "pos %d outside [0, %d]", pos, kv->max_len);
+    launch_set_cursor(kv->cursor, seq, pos, (cudaStream_t)stream);
+    CK(cudaGetLastError());
     return EMBER_OK;
 }
 
@@ -593,6 +617,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     ea.max_seqs = kv->max_seqs;
     ea.max_len = kv->max_len;
     ea.tok_ok = m->tok_ok;
+    ea.tok_pos = m->tok_pos;
     ea.pf_seq = -1;
     launch_embed(ea, s);
     const bool gemv = B <= GEMV_MAX_BATCH;
@@ -635,7 +660,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         a.L = c.layers;
         a.layer = l;
         a.seqs = seqs;
-        a.positions = positions;
+        a.positions = m->tok_pos;
         a.tok_ok = m->tok_ok;
         a.kc = kv->k;
         a.vc = kv->v;
@@ -734,7 +759,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     f.keys = m->keys;
     f.argmax = argmax;
     f.seqs = seqs;
-    f.positions = positions;
+    f.positions = m->tok_pos;
     f.tok_ok = m->tok_ok;
     f.cursor = kv->cursor;
     f.pf_seq = -1;
@@ -745,8 +770,8 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
                                           const int32_t* seqs, const int32_t* ids,
                                           const int32_t* positions, float* logits, int32_t* argmax,
                                           ember_stream_t stream) {
-    if (!m || !kv || !seqs || !ids || !positions)
-        return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv, seqs, ids or positions");
+    if (!m || !kv || !seqs || !ids)
+        return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv, seqs or ids");
     if (kv->m != m) return fail(EMBER_ERR_INVALID_ARG, "kv belongs to another model");
     if (batch <= 0) return fail(EMBER_ERR_INVALID_ARG, "batch must be > 0");
     if (batch > MAX_DECODE_BATCH || batch > m->T || batch > kv->max_seqs)
@@ -764,12 +789,16 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
         if (g.batch == batch && g.seqs == seqs && g.ids == ids && g.pos == positions &&
             g.logits == logits && g.argmax == argmax) {
             CK(cudaGraphLaunch(g.exec, s));
+            count_launches(g.kernels);
             return EMBER_OK;
         }
     }
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    const long long before = (long long)launches_so_far();
     decode_enqueue(m, kv, batch, seqs, ids, positions, logits, argmax, s);
+    const long long kernels = (long long)launches_so_far() - before;
+    count_launches(-kernels);   // captured, not run
     cudaError_t e = cudaStreamEndCapture(s, &graph);
     if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
     cudaGraphExec_t exec = nullptr;
@@ -780,8 +809,9 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
         cudaGraphExecDestroy(m->graphs.front().exec);
         m->graphs.erase(m->graphs.begin());
     }
-    m->graphs.push_back({batch, seqs, ids, positions, logits, argmax, exec});
+    m->graphs.push_back({batch, seqs, ids, positions, logits, argmax, exec, kernels});
     CK(cudaGraphLaunch(exec, s));
+    count_launches(kernels);
     return EMBER_OK;
 }
 
@@ -859,3 +889,30 @@ extern "C" ember_status ember_gemm_bf16(const uint16_t* A, const uint16_t* Bm, f
     CK(cudaGetLastError());
     return EMBER_OK;
 }
+
+extern "C" ember_status ember_gemv_bf16(const uint16_t* W, int32_t N, int32_t K, const float* x,
+                                        int32_t nb, float* y, ember_stream_t stream) {
+    if (!W || !x || !y) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (N <= 0 || K <= 0 || K % 8 || K > 16384 || nb <= 0 || nb > GEMV_MAX_BATCH)
+        return fail(EMBER_ERR_INVALID_ARG, "N, K > 0, K %% 8 == 0, K <= 16384, 1 <= nb <= 8");
+    if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(x)) & 15)
+        return fail(EMBER_ERR_INVALID_ARG, "W and x must be 16-byte aligned");
+    int dev = 0, sms = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    GemvArgs g{};
+    g.W = W;
+    g.N = N;
+    g.K = K;
+    g.x = x;
+    g.ldx = K;
+    g.out = y;
+    g.ldo = N;
+    g.nb = nb;
+    g.mode = EPI_STORE;
+    launch_gemv(g, (cudaStream_t)stream, sms);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" uint64_t ember_kernel_launches(void) { return (uint64_t)launches_so_far(); }

@@ -6,6 +6,31 @@
 
 namespace ember {
 
+// Host-side count of kernel launches (every launch_* call adds its kernels).
+void count_launches(long long n);
+unsigned long long launches_so_far();
+
+// Launch with the programmatic-stream-serialization attribute (PDL) unless
+// disabled (EMBER_NO_PDL=1): the kernel may start while its predecessor in
+// the stream finishes, and must pdl_wait() before reading its outputs.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+    count_launches(1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- embedding --
 // x[t] = f32(E[ids[t]]) and the per-token argument checks of a decode step
 // (seq in range, position == cursor, position < max_len, id < vocab) or of a
@@ -23,6 +48,7 @@ struct EmbedArgs {
     const int32_t* cursor;
     int max_seqs, max_len;
     int* tok_ok;                 // [n] 1 = token may touch the cache
+    int32_t* tok_pos;            // [n] resolved position (positions[t] or the cursor)
     // prefill check (pf_seq < 0: none)
     int pf_seq, pf_start;
 };
@@ -57,7 +83,7 @@ struct AttnDecodeArgs {
     int ld_qkv;
     int nb, NH, NKV, D, L, layer;
     const int32_t* seqs;
-    const int32_t* positions;
+    const int32_t* positions;    // resolved positions (the embed kernel's tok_pos)
     const int* tok_ok;
     uint16_t* kc;                // K cache base [S][L][NKV][max_len][D]
     uint16_t* vc;
@@ -90,6 +116,7 @@ struct FinishArgs {
     int pf_seq, pf_end;
 };
 void launch_finish(const FinishArgs& a, cudaStream_t s);
+void launch_set_cursor(int32_t* cursor, int seq, int pos, cudaStream_t s);
 
 // ------------------------------------------------------------- prefill side --
 // xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)

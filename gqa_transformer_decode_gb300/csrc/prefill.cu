@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
                                                  void* out) {
     __shared__ float red[32];
     const int t = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const float* xr = x + (size_t)t * H;
     float ss = 0.f;
     for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
@@ -34,11 +36,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
 
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
-    k_rmsnorm<true><<<n, 256, 0, s>>>(x, w, eps, H, xb);
+    launch_k(k_rmsnorm<true>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
 }
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
                         cudaStream_t s) {
-    k_rmsnorm<false><<<n, 256, 0, s>>>(x, w, eps, H, h);
+    launch_k(k_rmsnorm<false>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h);
 }
 
 // =================================================== q/k norm, RoPE, K/V write ==
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
     const int pos = a.pos0 + t % a.T_per_seq;
     const float* row = a.qkv + (size_t)t * a.ld_qkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();
     for (int e = tid; e < nq + 2 * nkv; e += blockDim.x) sm[e] = row[e];
     __syncthreads();
     if (a.q_norm) {   // PII-Tracer forward(): per-head RMSNorm of q and k before RoPE
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
 
 void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s) {
     const size_t smem = (size_t)(a.NH + 2 * a.NKV) * a.D * sizeof(float);
-    k_rope_kv<<<a.n, 128, smem, s>>>(a);
+    launch_k(k_rope_kv, dim3(a.n), dim3(128), smem, s, a);
 }
 
 // ======================================================== prefill attention ==
@@ -116,6 +120,8 @@ __global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a,
     const int rows = min(QT, a.T_per_seq - qt0);
     if (rows <= 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();
     const int items = rows * G;
     const float qk_scale = 1.4426950408889634f * rsqrtf((float)D);
 
@@ -207,6 +213,17 @@ __global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a,
     }
 }
 
+template <int D>
+static void launch_apf(const AttnPrefillArgs& a, int QT, dim3 grid, size_t smem, cudaStream_t s) {
+    static bool attr = false;   // static K/V tiles + dynamic queries may exceed 48 KB
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_prefill<D, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             64 * 1024);
+        attr = true;
+    }
+    launch_k(k_attn_prefill<D, 16>, grid, dim3(APF_THREADS), smem, s, a, QT);
+}
+
 void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s) {
     const int G = a.NH / a.NKV;
     // QT rows x G heads = items, at most 16 per warp (128 per CTA) and their
@@ -218,10 +235,10 @@ void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s) {
     dim3 grid((a.T_per_seq + QT - 1) / QT, a.NKV, nseq);
     const size_t smem = (size_t)QT * G * a.D * sizeof(float);
     switch (a.D) {
-        case 16: k_attn_prefill<16, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
-        case 32: k_attn_prefill<32, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
-        case 64: k_attn_prefill<64, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
-        case 128: k_attn_prefill<128, 16><<<grid, APF_THREADS, smem, s>>>(a, QT); break;
+        case 16: launch_apf<16>(a, QT, grid, smem, s); break;
+        case 32: launch_apf<32>(a, QT, grid, smem, s); break;
+        case 64: launch_apf<64>(a, QT, grid, smem, s); break;
+        case 128: launch_apf<128>(a, QT, grid, smem, s); break;
         default: break;
     }
 }
@@ -231,6 +248,8 @@ __global__ void __launch_bounds__(256) k_cls_head(const float* h, int n, int H, 
                                                   const float* b, int labels, float* out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
+    pdl_trigger();
+    pdl_wait();
     if (t >= n) return;
     const float* hr = h + (size_t)t * H;
     for (int j = 0; j < labels; ++j) {
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(256) k_cls_head(const float* h, int n, int H, 
 
 void launch_cls_head(const float* h, int n, int H, const uint16_t* W, const float* b, int labels,
                      float* out, cudaStream_t s) {
-    k_cls_head<<<(n + 7) / 8, 256, 0, s>>>(h, n, H, W, b, labels, out);
+    launch_k(k_cls_head, dim3((n + 7) / 8), dim3(256), 0, s, h, n, H, W, b, labels, out);
 }
 
 // ============================================== standalone RoPE + bf16 store ==
@@ -266,6 +285,7 @@ __global__ void k_rope_store(const float* x, int n_heads, int D, const float* co
 
 void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const float* cos_t,
                        const float* sin_t, uint16_t* out, cudaStream_t s) {
+    count_launches(1);
     k_rope_store<<<n_tok, 128, 0, s>>>(x, n_heads, D, cos_t, sin_t, out);
 }
 

@@ -73,6 +73,7 @@ def load():
         "ember_kv_alloc": (st, [P, C.c_int32, C.c_int32, C.POINTER(P)]),
         "ember_kv_free": (None, [P]),
         "ember_kv_reset": (st, [P, C.c_int32, P]),
+        "ember_kv_set_cursor": (st, [P, C.c_int32, C.c_int32, P]),
         "ember_kv_layout": (st, [P, C.POINTER(P), C.POINTER(P), C.POINTER(C.c_int64)]),
         "ember_prefill": (st, [P, P, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_decode_step": (st, [P, P, C.c_int32, P, P, P, P, P, P]),
@@ -81,6 +82,8 @@ def load():
         "ember_last_error": (C.c_char_p, []),
         "ember_rope_store": (st, [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_gemm_bf16": (st, [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]),
+        "ember_gemv_bf16": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P]),
+        "ember_kernel_launches": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -140,6 +143,10 @@ def ember_kv_reset(kv, seq, stream=None):
     check(load().ember_kv_reset(kv, seq, stream), "ember_kv_reset")
 
 
+def ember_kv_set_cursor(kv, seq, pos, stream=None):
+    check(load().ember_kv_set_cursor(kv, seq, pos, stream), "ember_kv_set_cursor")
+
+
 def ember_kv_layout(kv):
     k, v = P(), P()
     strides = (C.c_int64 * 4)()
@@ -169,3 +176,11 @@ def ember_rope_store(x, n_tok, n_heads, head_dim, cos_t, sin_t, out, stream):
 
 def ember_gemm_bf16(A, B, D, M, N, K, stream):
     return load().ember_gemm_bf16(A, B, D, M, N, K, stream)
+
+
+def ember_gemv_bf16(W, N, K, x, nb, y, stream):
+    return load().ember_gemv_bf16(W, N, K, x, nb, y, stream)
+
+
+def ember_kernel_launches() -> int:
+    return int(load().ember_kernel_launches())

@@ -78,6 +78,7 @@ class Model:
     def decode_step(self, kv, seqs, ids, positions, logits=None, argmax=None, stream=None):
         st = E.ember_decode_step(self.handle, kv.handle, ids.numel(), _ptr(seqs), _ptr(ids),
                                  _ptr(positions), _ptr(logits), _ptr(argmax), _stream_ptr(stream))
+
         E.check(st, "ember_decode_step")
 
     def encode(self, ids, B, T, out=None, hidden=None, stream=None):
@@ -97,6 +98,9 @@ class KVCache:
 
     def reset(self, seq, stream=None):
         E.ember_kv_reset(self.handle, seq, _stream_ptr(stream))
+
+    def set_cursor(self, seq, pos, stream=None):
+        E.ember_kv_set_cursor(self.handle, seq, pos, _stream_ptr(stream))
 
     def tensors(self):
         """(K, V) int16 tensors [S, L, NKV, max_len, D] aliasing the cache (read only)."""

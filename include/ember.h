@@ -73,8 +73,8 @@ typedef enum ember_status {
  * predict(); PII-Tracer forward(): head_dim is explicit, not hidden/heads).
  * Validation (Falcon-H1 Config::validate): every dimension > 0,
  * n_heads % n_kv_heads == 0, head_dim even; this build additionally needs
- * hidden, head_dim and ff to be multiples of 8 (16-byte weight rows),
- * head_dim <= 256 and n_heads/n_kv_heads <= 16. */
+ * hidden and ff to be multiples of 8 (16-byte weight rows), head_dim one of
+ * 16, 32, 64, 128, n_heads/n_kv_heads <= 16, hidden <= 8192, ff <= 16384. */
 typedef struct ember_config {
     int32_t vocab, hidden, layers, n_heads, n_kv_heads, head_dim, ff;
     double rope_theta;       /* RoPE base                                         */
@@ -140,6 +140,11 @@ void ember_kv_free(ember_kv *kv);
  * overwritten by the next prefill).  Asynchronous on stream. */
 ember_status ember_kv_reset(ember_kv *kv, int32_t seq, ember_stream_t stream);
 
+/* Set sequence seq's cursor to pos (0 <= pos <= max_len): rewinds a sequence
+ * to an earlier length, keeping rows [0, pos).  Asynchronous on stream.
+ * Errors: INVALID_ARG (seq out of range), CAPACITY (pos out of range). */
+ember_status ember_kv_set_cursor(ember_kv *kv, int32_t seq, int32_t pos, ember_stream_t stream);
+
 /* Read-only view of the cache for inspection: device base pointers of K and
  * V (bf16 bits) and the element strides of [seq, layer, kv_head, pos]; the
  * head_dim stride is 1. */
@@ -165,6 +170,9 @@ ember_status ember_prefill(ember_model *m, ember_kv *kv, int32_t seq, const int3
  * seqs[b] at position positions[b] (ember reference_forward.py forward(tok,
  * pos)); afterwards the cursor of seqs[b] is positions[b] + 1.  All arrays are
  * device arrays of `batch` entries; the sequences must be distinct.
+ * positions may be NULL: each token then goes at its sequence's cursor, so
+ * repeated calls with the same buffers (argmax fed back as ids) replay one
+ * CUDA graph.
  *   logits [batch, vocab] f32 (nullable); argmax [batch] int32 (nullable).
  * argmax may be the next call's ids, so a greedy loop needs no host sync.
  * Host errors: INVALID_ARG, CAPACITY (batch > max_tokens or > max_seqs).
@@ -208,6 +216,18 @@ ember_status ember_rope_store(const float *x, int32_t n_tok, int32_t n_heads, in
  * the row strides must be multiples of 8 elements.  Errors: INVALID_ARG. */
 ember_status ember_gemm_bf16(const uint16_t *A, const uint16_t *B, float *D, int32_t M,
                              int32_t N, int32_t K, ember_stream_t stream);
+
+/* y[b][n] = sum_k W[n][k] * x[b][k] for b < nb (nb <= 8), on the split GEMV
+ * the batch-1..8 decode projections run (W bf16 [N][K], x and y f32, row
+ * strides K and N; K a multiple of 8, K <= 16384).  The projections of
+ * ember reference_forward.py forward() (q = Wq xb, ...) without their fused
+ * prologue / epilogue.  Errors: INVALID_ARG. */
+ember_status ember_gemv_bf16(const uint16_t *W, int32_t N, int32_t K, const float *x, int32_t nb,
+                             float *y, ember_stream_t stream);
+
+/* Number of kernels this library has launched in this process so far (a
+ * CUDA-graph replay counts each kernel node it runs).  For accounting. */
+uint64_t ember_kernel_launches(void);
 
 #ifdef __cplusplus
 }

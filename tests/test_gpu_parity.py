@@ -202,3 +202,31 @@ def test_encoder_matches_oracle(B, T, stream):
         h, _, cls = om.forward_full(ids[b], logits=False, cls=True)
         assert_close(h, gh[b * T:(b + 1) * T], f"encoder hidden seq {b}")
         assert_close(cls, go[b * T:(b + 1) * T], f"encoder labels seq {b}")
+
+
+def test_graph_replayed_greedy_loop_with_cursor_positions(stream):
+    """positions = NULL (each token at its sequence's cursor) and argmax fed
+    back as the next ids: one CUDA graph replayed every step; then the cursor
+    is rewound and the same continuation is produced again."""
+    shape = SMALL_QWEN2
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, 11)
+    toks, olg, _ = om.greedy(prompt, 8)
+    kv = gm.kv_alloc(1, 32)
+    cur = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seqs = i32([0])
+    lg = torch.empty((9, shape.vocab), dtype=torch.float32, device="cuda")
+    got = []
+    for rep in range(2):
+        out = torch.empty(9, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            kv.set_cursor(0, 0, stream=stream)
+            gm.prefill(kv, 0, i32(prompt), 0, argmax=cur, logits=lg[0], stream=stream)
+            out[0:1].copy_(cur)
+            for i in range(1, 9):
+                gm.decode_step(kv, seqs, cur, None, argmax=cur, stream=stream)
+                out[i:i + 1].copy_(cur)
+        assert gm.sync_status(stream) == 0
+        got.append(out.cpu().numpy())
+    assert np.array_equal(got[0], got[1])
+    assert_tokens(olg, toks, got[0], "graph greedy")
