@@ -287,6 +287,9 @@ def run_gpu(args):
         dist.init_process_group("gloo")
     from gqa_transformer_decode_gb300 import ember as E
     wl = synth.WORKLOADS[args.workload]
+    if args.decode_steps is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, steps=args.decode_steps)
     hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
     stream = torch.cuda.Stream()
     weights = synth.weights_bf16(wl.model)
@@ -452,11 +455,19 @@ def main():
     ap.add_argument("--impl", default="ember", choices=["ember", "reference"])
     ap.add_argument("--workload", default="qwen2.5-0.5b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="override the workload's decode steps per job (short profiling runs)")
+    ap.add_argument("--gemv-only", action="store_true",
+                    help="only the standalone GEMV roofline launches (for counter captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.gemv_only:
+        import torch
+        hbm_peak = peaks()[0]
+        print(json.dumps(gemv_roofline(torch.cuda.Stream(), hbm_peak, n_launch=args.steps)))
     else:
         run_gpu(args)
 

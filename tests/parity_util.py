@@ -2,7 +2,7 @@
 
 The metrics follow PII-Tracer-vLLM serving/reference_forward.py main(): max
 and mean absolute delta, minimum per-row cosine and argmax agreement.  The
-bar (spec tolerance): every position's hidden state and logits within
+bar: every position's hidden state and logits within
 max-abs 2e-2 and cosine >= 0.9999; greedy tokens identical wherever the
 oracle's top-2 logit gap exceeds 1e-2.
 """
