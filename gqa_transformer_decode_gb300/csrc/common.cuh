@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ember.h"
+#include "ember.h"
 
 namespace ember {
 

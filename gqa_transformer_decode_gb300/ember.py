@@ -60,11 +60,14 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    if not _build.up_to_date():
-        _build.build()
-    if not os.path.exists(_build.LIB):
-        raise ImportError("libember.so is missing and could not be built")
-    L = C.CDLL(_build.LIB)
+    path = os.environ.get("EMBER_LIB")   # an alternative build of the same sources
+    if not path:
+        if not _build.up_to_date():
+            _build.build()
+        path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing and could not be built")
+    L = C.CDLL(path)
     st = C.c_int
     sig = {
         "ember_model_create": (st, [C.POINTER(ember_config), C.POINTER(ember_weights), C.POINTER(P)]),
