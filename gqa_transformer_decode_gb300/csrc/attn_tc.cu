@@ -1,0 +1,339 @@
+// attn_tc.cu -- whole-prompt GQA attention on the tcgen05 tensor cores.
+//
+// One CTA = 128 query rows of one query head h (kv head g = h / G: ember
+// internals "grouped-query attention").  Per key tile of 128 keys:
+//   S = Q . K^T                  tcgen05.mma M=128, N=128, K=D  -> TMEM
+//   softmax rows (online)        4 warps, thread r owns query row r (tcgen05.ld)
+//   P -> shared memory           f16, the 128-byte-swizzled K-major A operand
+//   O_t = P . V                  tcgen05.mma (f16) M=128, N=D, K=128 -> TMEM
+//   O = O * exp2(m_old - m_new) + O_t   in registers of the row's thread
+// Causal rows see keys at positions <= their own (LowLlamaBasic reference.py
+// self_attn()); the bidirectional encoder sees every key of its sequence
+// (PII-Tracer-vLLM forward()).  Q rows come from the RoPE'd bf16 queries, K
+// rows from the bf16 cache (or the encoder's K buffer), V through a
+// transposed f16 copy Vt [kv head][D][keys] so that it is K-major for the MMA
+// (bf16 -> f16 is exact for these magnitudes; P in [0, 1] keeps 11 bits
+// instead of bf16's 8).
+// Warp 0: TMA producer (Q once, K and Vt double-buffered); warp 1: TMEM
+// allocation and the MMA issuer; warps 2-5: softmax and output.  Every
+// mbarrier wait is bounded; a timeout raises EMBER_ERR_TIMEOUT and the CTA
+// drains its copies and frees TMEM.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ember {
+
+constexpr int AT_THREADS = 192;
+constexpr int AT_BQ = 128;   // query rows per CTA
+constexpr int AT_BK = 128;   // keys per tile
+
+template <int D>
+struct AtSmem {
+    static constexpr int KB = D / 64;                    // 64-element K blocks of Q / K rows
+    static constexpr int Q_BYTES = KB * AT_BQ * 128;
+    static constexpr int K_BYTES = KB * AT_BK * 128;     // one stage
+    static constexpr int V_BLOCK = D * 128;              // [D rows][64 keys] f16
+    static constexpr int V_BYTES = 2 * V_BLOCK;          // one stage: 128 keys
+    static constexpr int P_BYTES = 2 * AT_BQ * 128;      // [128 rows][128 keys] f16
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
+    static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
+    static constexpr int OFF_BAR = OFF_P + P_BYTES;
+    static constexpr int TOTAL = OFF_BAR + 256 + 1024;   // + barriers, + alignment slack
+    static constexpr uint32_t TMEM_COLS = (128 + D) <= 256 ? 256 : 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, AttnTcArgs a) {
+    using L = AtSmem<D>;
+    extern __shared__ uint8_t at_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* q_full = bar + 0;
+    uint64_t* kv_full = bar + 1;    // [2]
+    uint64_t* kv_empty = bar + 3;   // [2]
+    uint64_t* s_full = bar + 5;
+    uint64_t* p_full = bar + 6;
+    uint64_t* o_full = bar + 7;
+    uint64_t* o_empty = bar + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+    int* sflag = reinterpret_cast<int*>(bar + 10);   // [0] failed, [1] issued, [2] consumed
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x;        // heaviest (last) query tiles first
+    const int h = blockIdx.y, z = blockIdx.z;
+    const int g = h / a.G;
+    const int kz = a.kv_z_base + z * a.NKV + g;       // K rows of this kv head
+    const int vz = z * a.NKV + g;                     // Vt rows of this kv head
+    const int q_first = qt * AT_BQ;                    // first query row within the sequence
+    const int q_last = min(a.T_per_seq, q_first + AT_BQ) - 1;
+    const int nkt = a.causal ? (a.pos0 + q_last) / AT_BK + 1 : (a.n_keys + AT_BK - 1) / AT_BK;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, 128);
+        sflag[0] = 0;
+        sflag[1] = 0;
+        sflag[2] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(L::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+    pdl_wait();   // Q, K and Vt are the previous kernels' outputs
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------ TMA producer
+            const int qrow0 = z * a.T_per_seq + q_first;
+            mbar_expect_tx(q_full, L::Q_BYTES);
+            for (int kb = 0; kb < L::KB; ++kb)
+                tma_load_2d(sm + L::OFF_Q + kb * AT_BQ * 128, &tmQ, h * D + kb * 64, qrow0, q_full);
+            int j = 0;
+            for (; j < nkt; ++j) {
+                const int s = j & 1;
+                const uint32_t u = (uint32_t)(j >> 1);
+                if (!mbar_wait(&kv_empty[s], (u & 1u) ^ 1u)) {
+                    sflag[0] = 1;
+                    break;
+                }
+                mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
+                                j * AT_BK, kz, &kv_full[s]);
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
+                                j * AT_BK + kb * 64, 0, vz, &kv_full[s]);
+            }
+            sflag[1] = j;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------ MMA issuer
+            constexpr uint32_t idS = idesc_bf16(AT_BQ, AT_BK);
+            constexpr uint32_t idO = idesc_f16(AT_BQ, D);
+            bool ok = mbar_wait(q_full, 0);
+            int j = 0;
+            for (; ok && j < nkt; ++j) {
+                const int s = j & 1;
+                const uint32_t u = (uint32_t)(j >> 1);
+                if (!mbar_wait(&kv_full[s], u & 1u)) break;
+                tc_fence_after();
+                const uint32_t q0 = smem_u32(sm + L::OFF_Q);
+                const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);
+#pragma unroll
+                for (int kb = 0; kb < L::KB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(tS, sdesc_sw128(q0 + kb * AT_BQ * 128 + k * 32),
+                                  sdesc_sw128(k0 + kb * AT_BK * 128 + k * 32), idS,
+                                  (kb | k) ? 1u : 0u);
+                umma_commit(s_full);
+                // P . V once the softmax warps have written P and read O_t(j-1)
+                if (!mbar_wait(p_full, (uint32_t)j & 1u)) break;
+                if (!mbar_wait(o_empty, ((uint32_t)j & 1u) ^ 1u)) break;
+                tc_fence_after();
+                const uint32_t p0 = smem_u32(sm + L::OFF_P);
+                const uint32_t v0 = smem_u32(sm + L::OFF_V + s * L::V_BYTES);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(tO, sdesc_sw128(p0 + kb * AT_BQ * 128 + k * 32),
+                                  sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO,
+                                  (kb | k) ? 1u : 0u);
+                umma_commit(o_full);
+                umma_commit(&kv_empty[s]);
+            }
+            if (j < nkt) sflag[0] = 1;
+            sflag[2] = j;
+        }
+    } else {   // ------------------------------------------------ softmax warps
+        const int qw = warp & 3;
+        const int r = qw * 32 + lane;                 // query row within the tile
+        const int qp = a.pos0 + q_first + r;          // its position
+        const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const float sc_log2 = 1.4426950408889634f * rsqrtf((float)D);
+        float m = -INFINITY, l = 0.f;
+        float o[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] = 0.f;
+        uint8_t* sP = sm + L::OFF_P;
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            if (!mbar_wait(s_full, (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int key0 = j * AT_BK;
+            // pass 1: row maximum of the visible scaled scores
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < AT_BK; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tS + lane_off + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int kp = key0 + c0 + i;
+                    const bool vis = kp < a.n_keys && (!a.causal || kp <= qp);
+                    if (vis) mt = fmaxf(mt, __uint_as_float(v[i]) * sc_log2);
+                }
+            }
+            const float mn = fmaxf(m, mt);
+            const float corr = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+            // pass 2: p = exp2(s - m), row sum, P -> shared (swizzled K-major)
+            float rs = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < AT_BK; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tS + lane_off + c0, v);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int kp = key0 + c0 + i;
+                    const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
+                    const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
+                    const float p0 = v0 ? exp2f(__uint_as_float(v[i]) * sc_log2 - mn) : 0.f;
+                    const float p1 = v1 ? exp2f(__uint_as_float(v[i + 1]) * sc_log2 - mn) : 0.f;
+                    rs += p0 + p1;
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    pk[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                }
+                const int kb = c0 / 64;
+                uint8_t* rowp = sP + kb * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int chunk = ((c0 % 64) / 8) + t;
+                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
+                        make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(p_full);
+            l = l * corr + rs;
+            m = mn;
+            if (!mbar_wait(o_full, (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tO + lane_off + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c0 + i] = o[c0 + i] * corr + __uint_as_float(v[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(o_empty);
+        }
+        if (!ok) sflag[0] = 1;
+        if (ok && q_first + r < a.T_per_seq) {
+            const float inv = 1.f / l;
+            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + q_first + r) * a.ld_att + h * D;
+#pragma unroll
+            for (int d = 0; d < D; d += 8) {
+                uint4 w;
+                w.x = pack_f16x2(o[d] * inv, o[d + 1] * inv);
+                w.y = pack_f16x2(o[d + 2] * inv, o[d + 3] * inv);
+                w.z = pack_f16x2(o[d + 4] * inv, o[d + 5] * inv);
+                w.w = pack_f16x2(o[d + 6] * inv, o[d + 7] * inv);
+                *reinterpret_cast<uint4*>(out + d) = w;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && sflag[0]) raise_status(a.status, EMBER_ERR_TIMEOUT);
+    if (warp == 0 && lane == 0 && sflag[0]) {
+        // drain K/V copies issued but never consumed
+        for (int j = sflag[2]; j < sflag[1]; ++j)
+            (void)mbar_wait(&kv_full[j & 1], (uint32_t)(j >> 1) & 1u);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(L::TMEM_COLS));
+    }
+}
+
+// Vt[z][d][key] = f16(V[z][key][d]); zero past n_keys.
+__global__ void __launch_bounds__(256) k_vt(VtArgs a) {
+    __shared__ uint16_t tile[64][129];   // [key][d], padded
+    const int z = blockIdx.y;
+    const int key0 = blockIdx.x * 64;
+    const int D = a.D;
+    pdl_trigger();
+    pdl_wait();
+    const uint16_t* src =
+        a.v + (size_t)(z / a.nkv) * a.v_z_stride + (size_t)(z % a.nkv) * a.v_h_stride;
+    for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
+        const int k = e / D, d = e % D;
+        tile[k][d] = (key0 + k < a.n_keys) ? src[(size_t)(key0 + k) * D + d] : (uint16_t)0;
+    }
+    __syncthreads();
+    uint16_t* dst = a.vt + (size_t)z * D * a.keys_pad;
+    for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
+        const int d = e / 64, k = e % 64;
+        if (key0 + k < a.keys_pad)
+            dst[(size_t)d * a.keys_pad + key0 + k] =
+                __half_as_ushort(__float2half_rn(bf16_to_f32(tile[k][d])));
+    }
+}
+
+void launch_vt(const VtArgs& a, int zs, cudaStream_t s) {
+    launch_k(k_vt, dim3((a.keys_pad + 63) / 64, zs), dim3(256), 0, s, a);
+}
+
+template <int D>
+static void launch_at(const void* mq, const void* mk, const void* mv, const AttnTcArgs& a, int nseq,
+                      cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AtSmem<D>::TOTAL);
+        attr = true;
+    }
+    dim3 grid((a.T_per_seq + AT_BQ - 1) / AT_BQ, a.NH, nseq);
+    launch_k(k_attn_tc<D>, grid, dim3(AT_THREADS), AtSmem<D>::TOTAL, s,
+             *reinterpret_cast<const CUtensorMap*>(mq), *reinterpret_cast<const CUtensorMap*>(mk),
+             *reinterpret_cast<const CUtensorMap*>(mv), a);
+}
+
+bool attn_tc_supported(int D) { return D == 64 || D == 128; }
+
+void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
+                    int nseq, int D, cudaStream_t s) {
+    if (D == 64) launch_at<64>(map_q, map_k, map_vt, a, nseq, s);
+    else if (D == 128) launch_at<128>(map_q, map_k, map_vt, a, nseq, s);
+}
+
+}  // namespace ember

@@ -1,6 +1,7 @@
 // common.cuh -- device helpers shared by the ember kernels (sm_103a).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,6 +41,30 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* f) {
     f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
     f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
     f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+}
+
+// f16 side: the layer weights and the activations fed to the tensor-core
+// GEMMs are IEEE half (11 significant bits; the bf16 weights convert exactly
+// above 6.1e-5 in magnitude, below it to the f16 subnormal grid, <= 3e-8 off).
+__device__ __forceinline__ uint16_t f32_to_f16(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void unpack8_f16(const uint4& w, float* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+// bf16 or f16 weights (F16 is a compile-time choice of the caller)
+template <bool F16>
+__device__ __forceinline__ void unpack8w(const uint4& w, float* f) {
+    if (F16) unpack8_f16(w, f);
+    else unpack8(w, f);
 }
 
 // Streaming 128-bit load that does not allocate in L1 (weights are read once).

@@ -84,7 +84,7 @@ __device__ __forceinline__ void gemv_load_tile(const GemvArgs& a, int tile, int 
     }
 }
 
-template <int TPR, int NB>
+template <int TPR, int NB, bool WF16>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     constexpr int R = GEMV_THREADS / TPR;
     constexpr int GL = TPR < 32 ? TPR : 32;       // lanes reduced by shuffles
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
             const int c = sub + j * TPR;
             if (rv && c < K8) {
                 float wf[8];
-                unpack8(w[j], wf);
+                unpack8w<WF16>(w[j], wf);
                 if (a.norm_w) {
                     const float4 n0 = reinterpret_cast<const float4*>(a.norm_w)[2 * c];
                     const float4 n1 = reinterpret_cast<const float4*>(a.norm_w)[2 * c + 1];
@@ -223,10 +223,17 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
 template <int TPR>
 static void gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
     const dim3 g(grid), b(GEMV_THREADS);
-    if (a.nb <= 1) launch_k(k_gemv<TPR, 1>, g, b, 0, s, a);
-    else if (a.nb <= 2) launch_k(k_gemv<TPR, 2>, g, b, 0, s, a);
-    else if (a.nb <= 4) launch_k(k_gemv<TPR, 4>, g, b, 0, s, a);
-    else launch_k(k_gemv<TPR, 8>, g, b, 0, s, a);
+    if (a.w_f16) {
+        if (a.nb <= 1) launch_k(k_gemv<TPR, 1, true>, g, b, 0, s, a);
+        else if (a.nb <= 2) launch_k(k_gemv<TPR, 2, true>, g, b, 0, s, a);
+        else if (a.nb <= 4) launch_k(k_gemv<TPR, 4, true>, g, b, 0, s, a);
+        else launch_k(k_gemv<TPR, 8, true>, g, b, 0, s, a);
+    } else {
+        if (a.nb <= 1) launch_k(k_gemv<TPR, 1, false>, g, b, 0, s, a);
+        else if (a.nb <= 2) launch_k(k_gemv<TPR, 2, false>, g, b, 0, s, a);
+        else if (a.nb <= 4) launch_k(k_gemv<TPR, 4, false>, g, b, 0, s, a);
+        else launch_k(k_gemv<TPR, 8, false>, g, b, 0, s, a);
+    }
 }
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
             const int e = tid + i * ATT_THREADS;
             if (e < G * D) {
                 const float o = acc[i] / s_l[e / D];
-                if (a.att_b) a.att_b[out0 + e] = f32_to_bf16(o);
+                if (a.att_b) a.att_b[out0 + e] = f32_to_f16(o);
                 else a.att[out0 + e] = o;
             }
         }
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
         for (int s2 = 0; s2 < S; ++s2)
             O = fmaf(__ldcg(pb + ((size_t)s2 * G + h) * (D + 2) + 2 + d), s_pm[s2 * G + h], O);
         O *= s_scale[h];
-        if (a.att_b) a.att_b[out0 + e] = f32_to_bf16(O);
+        if (a.att_b) a.att_b[out0 + e] = f32_to_f16(O);
         else a.att[out0 + e] = O;
     }
     if (tid == 0) a.counters[b * a.NKV + g] = 0u;
@@ -536,6 +543,19 @@ __global__ void k_bf16_to_f32(const uint16_t* in, float* out, long long n) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x)
         out[i] = bf16_to_f32(in[i]);
+}
+
+__global__ void k_bf16_to_f16(uint16_t* p, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        p[i] = f32_to_f16(bf16_to_f32(p[i]));
+}
+
+void launch_bf16_to_f16_inplace(uint16_t* p, long long n, cudaStream_t s) {
+    if (n <= 0) return;
+    count_launches(1);
+    long long blocks = (n + 255) / 256;
+    k_bf16_to_f16<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(p, n);
 }
 
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s) {

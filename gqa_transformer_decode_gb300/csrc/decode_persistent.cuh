@@ -257,7 +257,8 @@ __device__ __forceinline__ const uint4* pk_row_ptr(const PkCtx& c, int row, int 
 // dropped; per-warp sums meet in red_rows[warp][R].
 template <int R>
 __device__ __forceinline__ void pk_split_pass(const PkCtx& c, int rows, int wr0, uint32_t n0,
-                                              int rc, int K, const float4* xs4, float* red_rows) {
+                                              int rc, int K, const float4* xs4, float* red_rows,
+                                              bool f16) {
     const int K8 = K >> 3;
     const uint4* wq[R];
 #pragma unroll
@@ -271,7 +272,7 @@ __device__ __forceinline__ void pk_split_pass(const PkCtx& c, int rows, int wr0,
 #pragma unroll
         for (int q = 0; q < R; ++q) {
             float wf[8];
-            unpack8(wq[q][p], wf);
+            if (f16) unpack8_f16(wq[q][p], wf); else unpack8(wq[q][p], wf);
             float s = acc[q];
             s = fmaf(wf[0], x0.x, s); s = fmaf(wf[1], x0.y, s);
             s = fmaf(wf[2], x0.z, s); s = fmaf(wf[3], x0.w, s);
@@ -306,6 +307,7 @@ __device__ __forceinline__ void pk_consume(PkCtx& c, int kind, int l, float* red
     const int rc = pk_chunk_rows(a, m.K);
     const int K8 = m.K >> 3;
     const bool pairs = (kind == PH_GU);
+    const bool f16 = (kind != PH_HEAD);   // layer matrices are f16, the tied head bf16
     const float4* xs4 = reinterpret_cast<const float4*>(c.xs);
     const int nchunks = (r1 - r0 + rc - 1) / rc;
     const int W = a.ring_slots > 2 ? a.ring_slots - 2 : 1;
@@ -338,7 +340,7 @@ __device__ __forceinline__ void pk_consume(PkCtx& c, int kind, int l, float* red
 #pragma unroll
                     for (int q = 0; q < PK_RB; ++q) {
                         float wf[8];
-                        unpack8(wq[q][p], wf);
+                        if (f16) unpack8_f16(wq[q][p], wf); else unpack8(wq[q][p], wf);
                         float s = acc[q];
                         s = fmaf(wf[0], x0.x, s); s = fmaf(wf[1], x0.y, s);
                         s = fmaf(wf[2], x0.z, s); s = fmaf(wf[3], x0.w, s);
@@ -364,10 +366,10 @@ __device__ __forceinline__ void pk_consume(PkCtx& c, int kind, int l, float* red
         } else {
             // ---- split-K mode; the barriers run whatever c.ok says
             if (c.ok) {
-                if (wrows <= 2) pk_split_pass<2>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows);
-                else if (wrows <= 4) pk_split_pass<4>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows);
-                else if (wrows <= 8) pk_split_pass<8>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows);
-                else pk_split_pass<PK_SPLIT_ROWS>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows);
+                if (wrows <= 2) pk_split_pass<2>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows, f16);
+                else if (wrows <= 4) pk_split_pass<4>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows, f16);
+                else if (wrows <= 8) pk_split_pass<8>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows, f16);
+                else pk_split_pass<PK_SPLIT_ROWS>(c, wrows, wr0, n0, rc, m.K, xs4, red_rows, f16);
             }
             consumer_sync();
             const int step = pairs ? 2 : 1;

@@ -20,126 +20,20 @@
 // The projections this serves: q/k/v (+bias), o_proj (+residual), gate/up
 // (SwiGLU) and down (+residual) of ember scripts/reference_forward.py
 // forward(), in the whole-sequence form of LowLlamaBasic reference.py.
-#include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace ember {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
 constexpr int GEMM_THREADS = 192;
-constexpr long long WAIT_CYCLES = 1ll << 31;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(addr, parity)) {
-        if (clock64() - t0 > WAIT_CYCLES) return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(tm), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride
-// byte offset), descriptor version 1, layout SWIZZLE_128B.  The leading byte
-// offset is unused for this layout.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3ffffu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              int M, int N, int K, GemmEpilogue e, int* status) {
+              int M, int N, int K, uint32_t idesc, GemmEpilogue e, int* status) {
     constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
     constexpr int B_BYTES = BN * GEMM_BK * 2;
     constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -203,7 +97,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16(GEMM_BM, BN);
             int kb = 0;
             for (; kb < nk; ++kb) {
                 const int s = kb % STAGES;
@@ -246,14 +139,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const bool fullc = (n + 32 <= N);
                 if (e.mode == EPI_SWIGLU) {
                     // columns 2i / 2i+1 = gate_i / up_i -> output column n/2 + i
-                    uint16_t* o = e.out_bf16 + (size_t)row * e.ldo + (n >> 1);
+                    uint16_t* o = e.out_h + (size_t)row * e.ldo + (n >> 1);
                     if (fullc) {
                         uint32_t pk[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float g0 = v[4 * i], u0 = v[4 * i + 1];
                             const float g1 = v[4 * i + 2], u1 = v[4 * i + 3];
-                            pk[i] = pack_bf16x2(g0 / (1.f + __expf(-g0)) * u0,
+                            pk[i] = pack_f16x2(g0 / (1.f + __expf(-g0)) * u0,
                                                 g1 / (1.f + __expf(-g1)) * u1);
                         }
                         uint4* o4 = reinterpret_cast<uint4*>(o);
@@ -262,7 +155,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     } else {
                         for (int i = 0; i < 16 && n + 2 * i + 1 < N; ++i) {
                             const float g = v[2 * i], u = v[2 * i + 1];
-                            o[i] = f32_to_bf16(g / (1.f + __expf(-g)) * u);
+                            o[i] = f32_to_f16(g / (1.f + __expf(-g)) * u);
                         }
                     }
                 } else {
@@ -320,19 +213,35 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-static bool make_map(void* out, const uint16_t* ptr, int rows, int ld, int K, int box_rows) {
+bool encode_map_bf16(void* out, const void* ptr, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
     auto enc = encode_fn();
-    if (!enc) return false;
-    if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld % 8) || (K % 8)) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {(cuuint32_t)GEMM_BK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                     const_cast<uint16_t*>(ptr), dims, strides, box, estr,
+    if (!enc || rank < 2 || rank > 5) return false;
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) {
+            if (strides[i] % 16) return false;
+            st[i] = strides[i];
+        }
+    }
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     (cuuint32_t)rank, const_cast<void*>(ptr), d, st, bx, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+static bool make_map(void* out, const uint16_t* ptr, int rows, int ld, int K, int box_rows) {
+    if ((ld % 8) || (K % 8)) return false;
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)ld * 2};
+    const uint32_t box[2] = {(uint32_t)GEMM_BK, (uint32_t)box_rows};
+    return encode_map_bf16(out, ptr, 2, dims, strides, box);
 }
 
 static int pick_bn(int N) {
@@ -342,7 +251,8 @@ static int pick_bn(int N) {
 }
 
 bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16_t* B, int N,
-                    int ldb, int K) {
+                    int ldb, int K, bool f16) {
+    p.f16 = f16;
     static_assert(sizeof(CUtensorMap) <= sizeof(p.tmA), "tensor map size");
     p.M = M;
     p.N = N;
@@ -366,8 +276,9 @@ static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int*
     dim3 grid((p.N + BN - 1) / BN, (m_rows + GEMM_BM - 1) / GEMM_BM);
     const CUtensorMap* ta = reinterpret_cast<const CUtensorMap*>(p.tmA);
     const CUtensorMap* tb = reinterpret_cast<const CUtensorMap*>(p.tmB);
+    const uint32_t idesc = p.f16 ? idesc_f16(GEMM_BM, BN) : idesc_bf16(GEMM_BM, BN);
     launch_k(k_gemm_tc<BN, STAGES>, grid, dim3(GEMM_THREADS), SMEM, s, *ta, *tb, m_rows, p.N, p.K,
-             e, status);
+             idesc, e, status);
 }
 
 void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,

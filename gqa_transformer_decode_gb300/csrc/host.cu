@@ -143,6 +143,9 @@ struct ember_model {
     int *tok_ok, *status;
     int32_t* tok_pos;
     float *enc_cos = nullptr, *enc_sin = nullptr;
+    uint16_t* enc_vt = nullptr;          // transposed V of the encoder batch
+    alignas(64) unsigned char q_map[128];   // TMA map over the RoPE'd bf16 queries
+    bool q_map_ok = false;
     int enc_positions = 0;
     GemmPlan p_head;   // tied head on bf16 final states (encode without labels)
     // persistent batch-1 decode kernel
@@ -162,6 +165,9 @@ struct ember_kv {
     uint16_t *k = nullptr, *v = nullptr;
     int32_t* cursor = nullptr;
     float *cos_t = nullptr, *sin_t = nullptr;
+    uint16_t* vt = nullptr;              // transposed V of one layer's kv heads (prefill)
+    alignas(64) unsigned char k_map[128];   // TMA map over the whole K cache, 3-D
+    bool k_map_ok = false;
 };
 
 static ember_status validate(const ember_config* c) {
@@ -275,6 +281,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     if (!c.causal) {
         aa.add(&m->enc_k, (size_t)T * m->kv);
         aa.add(&m->enc_v, (size_t)T * m->kv);
+        aa.add(&m->enc_vt, (size_t)8 * T * m->kv);   // B * round8(T) <= 8 * B * T keys
         aa.add(&m->enc_cos, (size_t)m->c.max_positions * (D / 2));
         aa.add(&m->enc_sin, (size_t)m->c.max_positions * (D / 2));
     }
@@ -323,6 +330,14 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
             e = cudaMemcpy2DAsync(L.wgu + H, (size_t)4 * H, W.w_up, (size_t)2 * H, (size_t)2 * H, F,
                                   D2D, s);
         cp(L.wd, W.w_down, (size_t)H * F * 2);
+        // the layer matrices run as f16 (more mantissa for the f16 activations
+        // they meet in the tensor-core GEMMs); embedding / head stay bf16
+        if (e == cudaSuccess) {
+            launch_bf16_to_f16_inplace(L.wqkv, (long long)m->qkv_n * H, s);
+            launch_bf16_to_f16_inplace(L.wo, (long long)H * m->q, s);
+            launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, s);
+            launch_bf16_to_f16_inplace(L.wd, (long long)H * F, s);
+        }
         launch_bf16_to_f32(W.attn_norm, L.attn_norm, H, s);
         launch_bf16_to_f32(W.mlp_norm, L.mlp_norm, H, s);
         if (c.qkv_bias) {
@@ -337,14 +352,21 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
             launch_bf16_to_f32(W.k_norm, L.k_norm, D, s);
         }
         // tensor-core plans of the whole-prompt projections
-        bool ok = make_gemm_plan(L.p_qkv, m->xb, T, H, L.wqkv, m->qkv_n, H, H) &&
-                  make_gemm_plan(L.p_o, m->att_b, T, m->q, L.wo, H, m->q, m->q) &&
-                  make_gemm_plan(L.p_gu, m->xb, T, H, L.wgu, 2 * F, H, H) &&
-                  make_gemm_plan(L.p_d, m->act_b, T, F, L.wd, H, F, F);
+        bool ok = make_gemm_plan(L.p_qkv, m->xb, T, H, L.wqkv, m->qkv_n, H, H, true) &&
+                  make_gemm_plan(L.p_o, m->att_b, T, m->q, L.wo, H, m->q, m->q, true) &&
+                  make_gemm_plan(L.p_gu, m->xb, T, H, L.wgu, 2 * F, H, H, true) &&
+                  make_gemm_plan(L.p_d, m->act_b, T, F, L.wd, H, F, F, true);
         if (!ok) return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (layer %d)", l));
     }
-    if (!make_gemm_plan(m->p_head, m->hb, T, H, m->embed, V, H, H))
+    if (!make_gemm_plan(m->p_head, m->hb, T, H, m->embed, V, H, H, false))
         return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (head)"));
+    if (attn_tc_supported(D)) {
+        const uint64_t qd[2] = {(uint64_t)m->q, (uint64_t)T};
+        const uint64_t qs[1] = {(uint64_t)m->q * 2};
+        const uint32_t qb[2] = {64, 128};
+        m->q_map_ok = encode_map_bf16(m->q_map, m->qr, 2, qd, qs, qb);
+        if (!m->q_map_ok) return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (q)"));
+    }
     if (e == cudaSuccess) e = cudaMemsetAsync(m->counters, 0, (size_t)B * NKV * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->keys, 0, (size_t)B * 8, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, 4, s);
@@ -426,6 +448,9 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
     if (e == cudaSuccess) e = cudaMalloc(&kv->cursor, (size_t)max_seqs * 4);
     if (e == cudaSuccess) e = cudaMalloc(&kv->cos_t, (size_t)max_len * h2 * 4);
     if (e == cudaSuccess) e = cudaMalloc(&kv->sin_t, (size_t)max_len * h2 * 4);
+    const int keys_cap = (max_len + 7) / 8 * 8;
+    if (e == cudaSuccess && attn_tc_supported(m->c.head_dim))
+        e = cudaMalloc(&kv->vt, (size_t)m->c.n_kv_heads * m->c.head_dim * keys_cap * 2);
     if (e != cudaSuccess) {
         cudaGetLastError();
         ember_kv_free(kv);
@@ -443,6 +468,19 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
         ember_kv_free(kv);
         return fail(EMBER_ERR_CUDA, "KV cache init failed: %s", cudaGetErrorString(e));
     }
+    if (attn_tc_supported(m->c.head_dim)) {
+        // K cache [seq][layer][kv head][pos][D] as one 3-D tensor: (D, pos, seq*layer*head)
+        const ember_config& c = m->c;
+        const uint64_t kd[3] = {(uint64_t)c.head_dim, (uint64_t)max_len,
+                                (uint64_t)max_seqs * c.layers * c.n_kv_heads};
+        const uint64_t ks[2] = {(uint64_t)c.head_dim * 2, (uint64_t)max_len * c.head_dim * 2};
+        const uint32_t kb[3] = {64, 128, 1};
+        kv->k_map_ok = encode_map_bf16(kv->k_map, kv->k, 3, kd, ks, kb);
+        if (!kv->k_map_ok) {
+            ember_kv_free(kv);
+            return fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (K cache)");
+        }
+    }
     *out = kv;
     return EMBER_OK;
 }
@@ -455,6 +493,7 @@ void ember_kv_free(ember_kv* kv) {
     cudaFree(kv->cursor);
     cudaFree(kv->cos_t);
     cudaFree(kv->sin_t);
+    cudaFree(kv->vt);
     delete kv;
 }
 
@@ -509,13 +548,28 @@ struct CacheView {
     long long seq_stride, head_stride;
     int T_per_seq, pos0, causal;
     const float *cos_t, *sin_t;
+    // tensor-core attention (head_dim 64 / 128): K map, its z index of (z=0, g=0),
+    // the transposed-V buffer and its map (keys_pad keys per row)
+    const void* k_map = nullptr;
+    int kv_z_base = 0;
+    uint16_t* vt = nullptr;
+    const void* vt_map = nullptr;
+    int keys_pad = 0;
 };
+
+// Map over a transposed-V buffer [zs][D][keys_pad].
+static bool make_vt_map(void* out, const uint16_t* vt, int keys_pad, int D, int zs) {
+    const uint64_t d[3] = {(uint64_t)keys_pad, (uint64_t)D, (uint64_t)zs};
+    const uint64_t st[2] = {(uint64_t)keys_pad * 2, (uint64_t)keys_pad * D * 2};
+    const uint32_t b[3] = {64, (uint32_t)D, 1};
+    return encode_map_bf16(out, vt, 3, d, st, b);
+}
 
 static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStream_t s) {
     const ember_config& c = m->c;
     LayerDev& L = m->layers[l];
     const float eps = (float)c.rms_eps;
-    launch_rmsnorm_bf16(m->x, L.attn_norm, eps, n, c.hidden, m->xb, s);
+    launch_rmsnorm_h(m->x, L.attn_norm, eps, n, c.hidden, m->xb, s);
     GemmEpilogue e{};
     e.mode = EPI_STORE;
     e.out_f32 = m->qkv;
@@ -542,6 +596,33 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     r.seq_stride = cv.seq_stride;
     r.head_stride = cv.head_stride;
     launch_rope_kv(r, s);
+    if (cv.k_map && cv.vt_map) {   // tensor-core attention
+        const int nseq = n / cv.T_per_seq;
+        const int n_keys = cv.pos0 + cv.T_per_seq;
+        VtArgs va{};
+        va.v = cv.v;
+        va.v_z_stride = cv.seq_stride;
+        va.v_h_stride = cv.head_stride;
+        va.nkv = c.n_kv_heads;
+        va.D = c.head_dim;
+        va.n_keys = n_keys;
+        va.keys_pad = cv.keys_pad;
+        va.vt = cv.vt;
+        launch_vt(va, nseq * c.n_kv_heads, s);
+        AttnTcArgs ta{};
+        ta.T_per_seq = cv.T_per_seq;
+        ta.pos0 = cv.pos0;
+        ta.causal = cv.causal;
+        ta.n_keys = n_keys;
+        ta.NH = c.n_heads;
+        ta.NKV = c.n_kv_heads;
+        ta.G = c.n_heads / c.n_kv_heads;
+        ta.kv_z_base = cv.kv_z_base;
+        ta.att = m->att_b;
+        ta.ld_att = m->q;
+        ta.status = m->status;
+        launch_attn_tc(m->q_map, cv.k_map, cv.vt_map, ta, nseq, c.head_dim, s);
+    } else {
     AttnPrefillArgs a{};
     a.q = m->qr;
     a.n = n;
@@ -557,15 +638,16 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     a.head_stride = cv.head_stride;
     a.att = m->att_b;
     launch_attn_prefill(a, s);
+    }
     e = GemmEpilogue{};
     e.mode = EPI_RESID;
     e.out_f32 = m->x;
     e.ldo = c.hidden;
     launch_gemm(L.p_o, n, e, m->status, s);
-    launch_rmsnorm_bf16(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, s);
+    launch_rmsnorm_h(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, s);
     e = GemmEpilogue{};
     e.mode = EPI_SWIGLU;
-    e.out_bf16 = m->act_b;
+    e.out_h = m->act_b;
     e.ldo = c.ff;
     launch_gemm(L.p_gu, n, e, m->status, s);
     e = GemmEpilogue{};
@@ -602,8 +684,19 @@ extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq,
     ea.cursor = kv->cursor;
     launch_embed(ea, s);
     const long long head_stride = (long long)kv->max_len * c.head_dim;
+    alignas(64) unsigned char vt_map[128];
+    const int keys_pad = (start_pos + n + 7) / 8 * 8;
+    const bool tc = m->q_map_ok && kv->k_map_ok &&
+                    make_vt_map(vt_map, kv->vt, keys_pad, c.head_dim, c.n_kv_heads);
     for (int l = 0; l < c.layers; ++l) {
         CacheView cv{};
+        if (tc) {
+            cv.k_map = kv->k_map;
+            cv.kv_z_base = (seq * c.layers + l) * c.n_kv_heads;
+            cv.vt = kv->vt;
+            cv.vt_map = vt_map;
+            cv.keys_pad = keys_pad;
+        }
         const long long off = (((long long)seq * c.layers + l) * c.n_kv_heads) * head_stride;
         cv.k = kv->k + off;
         cv.v = kv->v + off;
@@ -691,7 +784,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         LayerDev& L = m->layers[l];
         if (gemv) {
             GemvArgs g{};
-            g.W = L.wqkv;
+            g.W = L.wqkv; g.w_f16 = 1;
             g.N = m->qkv_n;
             g.K = c.hidden;
             g.x = m->x;
@@ -706,7 +799,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
         } else {
-            launch_rmsnorm_bf16(m->x, L.attn_norm, eps, B, c.hidden, m->xb, s);
+            launch_rmsnorm_h(m->x, L.attn_norm, eps, B, c.hidden, m->xb, s);
             GemmEpilogue e{};
             e.mode = EPI_STORE;
             e.out_f32 = m->qkv;
@@ -743,7 +836,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         launch_attn_decode(a, s);
         if (gemv) {
             GemvArgs g{};
-            g.W = L.wo;
+            g.W = L.wo; g.w_f16 = 1;
             g.N = c.hidden;
             g.K = m->q;
             g.x = m->att_f;
@@ -755,7 +848,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
             g = GemvArgs{};
-            g.W = L.wgu;
+            g.W = L.wgu; g.w_f16 = 1;
             g.N = 2 * c.ff;
             g.K = c.hidden;
             g.x = m->x;
@@ -769,7 +862,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
             g = GemvArgs{};
-            g.W = L.wd;
+            g.W = L.wd; g.w_f16 = 1;
             g.N = c.hidden;
             g.K = c.ff;
             g.x = m->act_f;
@@ -781,16 +874,16 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
         } else {
-            // the attention kernel wrote its output as the bf16 GEMM operand att_b
+            // the attention kernel wrote its output as the f16 GEMM operand att_b
             GemmEpilogue e{};
             e.mode = EPI_RESID;
             e.out_f32 = m->x;
             e.ldo = c.hidden;
             launch_gemm(L.p_o, B, e, m->status, s);
-            launch_rmsnorm_bf16(m->x, L.mlp_norm, eps, B, c.hidden, m->xb, s);
+            launch_rmsnorm_h(m->x, L.mlp_norm, eps, B, c.hidden, m->xb, s);
             e = GemmEpilogue{};
             e.mode = EPI_SWIGLU;
-            e.out_bf16 = m->act_b;
+            e.out_h = m->act_b;
             e.ldo = c.ff;
             launch_gemm(L.p_gu, B, e, m->status, s);
             e = GemmEpilogue{};
@@ -900,8 +993,25 @@ extern "C" ember_status ember_encode(ember_model* m, const int32_t* ids, int32_t
     ea.status = m->status;
     ea.pf_seq = -1;
     launch_embed(ea, s);
+    alignas(64) unsigned char k_map[128], vt_map[128];
+    const int keys_pad = (T + 7) / 8 * 8;
+    bool tc = m->q_map_ok;
+    if (tc) {
+        const uint64_t kd[3] = {(uint64_t)c.head_dim, (uint64_t)T, (uint64_t)B * c.n_kv_heads};
+        const uint64_t ks[2] = {(uint64_t)c.head_dim * 2, (uint64_t)T * c.head_dim * 2};
+        const uint32_t kb[3] = {64, 128, 1};
+        tc = encode_map_bf16(k_map, m->enc_k, 3, kd, ks, kb) &&
+             make_vt_map(vt_map, m->enc_vt, keys_pad, c.head_dim, B * c.n_kv_heads);
+    }
     for (int l = 0; l < c.layers; ++l) {
         CacheView cv{};
+        if (tc) {
+            cv.k_map = k_map;
+            cv.kv_z_base = 0;
+            cv.vt = m->enc_vt;
+            cv.vt_map = vt_map;
+            cv.keys_pad = keys_pad;
+        }
         cv.k = m->enc_k;
         cv.v = m->enc_v;
         cv.head_stride = (long long)T * c.head_dim;
@@ -943,7 +1053,7 @@ extern "C" ember_status ember_gemm_bf16(const uint16_t* A, const uint16_t* Bm, f
     if (M <= 0 || N <= 0 || K <= 0 || K % 8 || N % 4)
         return fail(EMBER_ERR_INVALID_ARG, "M, N, K must be > 0, K %% 8 == 0, N %% 4 == 0");
     GemmPlan p;
-    if (!make_gemm_plan(p, A, M, K, Bm, N, K, K))
+    if (!make_gemm_plan(p, A, M, K, Bm, N, K, K, false))
         return fail(EMBER_ERR_INVALID_ARG, "TMA tensor map rejected (alignment?)");
     GemmEpilogue e{};
     e.mode = EPI_STORE;

@@ -58,8 +58,9 @@ void launch_embed(const EmbedArgs& a, cudaStream_t s);
 // Batch-1..8 decode projections: y[b][n] = rinv_b * sum_k W[n][k] x[b][k] w_k
 // with the RMSNorm of x fused into the prologue when norm_w != nullptr.
 struct GemvArgs {
-    const uint16_t* W;           // [N][K] bf16
+    const uint16_t* W;           // [N][K] bf16, or f16 when w_f16
     int N, K;
+    int w_f16;
     const float* x;              // [nb][ldx] f32
     int ldx;
     const float* norm_w;         // [K] f32 or nullptr
@@ -94,7 +95,7 @@ struct AttnDecodeArgs {
     const float* k_norm;
     float eps;
     float* att;                  // [nb][NH*D] f32 (used when att_b == nullptr)
-    uint16_t* att_b;             // [nb][NH*D] bf16 GEMM operand, or nullptr
+    uint16_t* att_b;             // [nb][NH*D] f16 GEMM operand, or nullptr
     float* part;                 // split partials
     unsigned* counters;          // [nb*NKV], zero between launches
     int splits;
@@ -156,8 +157,8 @@ bool persist_prepare(PersistArgs& a, int& grid, int& smem);
 cudaError_t launch_persist(const PersistArgs& a, int grid, int smem, cudaStream_t s);
 
 // ------------------------------------------------------------- prefill side --
-// xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
-void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+// xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
+void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s);
 // h[t] = RMSNorm(x[t]) * w  in f32
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
@@ -193,7 +194,7 @@ struct AttnPrefillArgs {
     const uint16_t* kc;
     const uint16_t* vc;
     long long seq_stride, head_stride;
-    uint16_t* att;               // [n][NH*D] bf16
+    uint16_t* att;               // [n][NH*D] f16 (GEMM operand)
 };
 void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s);
 
@@ -207,6 +208,8 @@ void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const floa
 
 // bf16 [n] -> f32 [n] (weight repack of norms / biases)
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s);
+// bf16 bits -> f16 bits in place (weight repack of the layer matrices)
+void launch_bf16_to_f16_inplace(uint16_t* p, long long n, cudaStream_t s);
 
 // ----------------------------------------------------------- tcgen05 GEMM --
 // D[M,N] = A[M,K] . B[N,K]^T (bf16 in, f32 accumulate in TMEM) with a fused
@@ -214,7 +217,7 @@ void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_
 struct GemmEpilogue {
     int mode;                    // EpiMode (EPI_STORE, EPI_RESID, EPI_SWIGLU)
     float* out_f32;              // EPI_STORE / EPI_RESID: [M][ldo]
-    uint16_t* out_bf16;          // EPI_SWIGLU: [M][ldo] bf16 (N/2 columns)
+    uint16_t* out_h;             // EPI_SWIGLU: [M][ldo] f16 (N/2 columns)
     int ldo;
     const float* bias;           // EPI_STORE, nullable
 };
@@ -224,15 +227,50 @@ struct GemmPlan {
     alignas(64) unsigned char tmB[128];
     int M, N, K;
     int bn;                      // N tile (64, 128 or 256)
+    bool f16;                    // operands f16 (else bf16)
     bool ok;
 };
 // A rows = M (activations), B rows = N (weights); both row-major with K
 // contiguous and 16-byte aligned rows.  Returns false if the driver rejects
 // the tensor maps.
 bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16_t* B, int N,
-                    int ldb, int K);
+                    int ldb, int K, bool f16);
+// Encode a bf16 TMA tensor map (rank 2..4, 128-byte swizzle, zero fill out
+// of bounds).  dims[0] is the contiguous dimension; strides (rank-1 entries)
+// are in bytes.  False if the driver rejects it.
+bool encode_map_bf16(void* out, const void* ptr, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
+
 // m_rows: rows of A actually valid (<= p.M); the rest is ignored.
 void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
                  cudaStream_t s);
+
+// ------------------------------------------------ tensor-core attention --
+// Whole-prompt GQA attention on tcgen05 (head_dim 64 or 128).  Maps: Q over
+// the bf16 queries [rows][NH*D] (box 64 x 128); K over K rows [z][key][D]
+// (3-D, box 64 x 128 x 1); Vt over transposed f16 V [z][D][keys_pad] (3-D, box
+// 64 x D x 1).  Query row t of sequence z (t < T_per_seq) sits at position
+// pos0 + t; it reads K at z index kv_z_base + z*NKV + g and Vt at z*NKV + g.
+struct AttnTcArgs {
+    int T_per_seq, pos0, causal, n_keys;
+    int NH, NKV, G;
+    int kv_z_base;
+    uint16_t* att;               // [rows][ld_att] f16 (GEMM operand)
+    int ld_att;
+    int* status;
+};
+bool attn_tc_supported(int D);
+void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
+                    int nseq, int D, cudaStream_t s);
+
+// Vt[z][d][key] = f16(V[z][key][d]) for keys < n_keys, 0 for keys in [n_keys, keys_pad):
+// V rows of index z = (z / nkv, z % nkv) start at v + (z/nkv)*v_z_stride + (z%nkv)*v_h_stride.
+struct VtArgs {
+    const uint16_t* v;
+    long long v_z_stride, v_h_stride;
+    int nkv, D, n_keys, keys_pad;
+    uint16_t* vt;
+};
+void launch_vt(const VtArgs& a, int zs, cudaStream_t s);
 
 }  // namespace ember

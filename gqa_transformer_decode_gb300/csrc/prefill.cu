@@ -1,4 +1,4 @@
-// prefill.cu -- whole-prompt side of the forward: RMSNorm to the bf16 GEMM
+// prefill.cu -- whole-prompt side of the forward: RMSNorm to the f16 GEMM
 // operand, q/k-norm + RoPE + KV-cache write for n tokens, whole-sequence GQA
 // attention (causal over the cache, or bidirectional within a sequence), the
 // f32 final norm and the linear label head.
@@ -27,14 +27,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     if (BF16) {
         uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
         for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
-            o[i] = pack_bf16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
+            o[i] = pack_f16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
     } else {
         float* o = static_cast<float*>(out) + (size_t)t * H;
         for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = xr[i] * ri * w[i];
     }
 }
 
-void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
     launch_k(k_rmsnorm<true>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
 }
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a,
 #pragma unroll
         for (int c = 0; c < DL; ++c) {
             const int d = lane + 32 * c;
-            if (d < D) o[d] = f32_to_bf16(acc[k][c] * inv);
+            if (d < D) o[d] = f32_to_f16(acc[k][c] * inv);
         }
     }
 }

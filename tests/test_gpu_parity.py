@@ -230,3 +230,45 @@ def test_graph_replayed_greedy_loop_with_cursor_positions(stream):
         got.append(out.cpu().numpy())
     assert np.array_equal(got[0], got[1])
     assert_tokens(olg, toks, got[0], "graph greedy")
+
+
+# head_dim 64 / 128 decoders: prompts run through the tensor-core attention
+MID_QWEN2 = synth.ModelShape("m-qwen2", vocab=2000, hidden=448, layers=2, n_heads=7,
+                             n_kv_heads=1, head_dim=64, ff=640, rope_theta=1e6, qkv_bias=1)
+MID_LLAMA = synth.ModelShape("m-llama", vocab=1500, hidden=256, layers=2, n_heads=8,
+                             n_kv_heads=2, head_dim=64, ff=512, rope_theta=5e5, rope_llama3=1,
+                             rs_factor=32.0, rs_low=1.0, rs_high=4.0, rs_orig_max_pos=256)
+MID_D128 = synth.ModelShape("m-d128", vocab=900, hidden=256, layers=2, n_heads=4, n_kv_heads=2,
+                            head_dim=128, ff=384, rope_theta=1e6, qk_norm=1)
+
+
+@pytest.mark.parametrize("shape,n_prompt", [(MID_QWEN2, 1), (MID_QWEN2, 150), (MID_LLAMA, 128),
+                                            (MID_LLAMA, 300), (MID_D128, 77), (MID_D128, 257)])
+def test_tensor_core_prefill_matches_oracle(shape, n_prompt, stream):
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, n_prompt)
+    toks, olg, _ = om.greedy(prompt, 3)
+    kv = gm.kv_alloc(1, n_prompt + 8)
+    glg, gam, ghd = run_greedy_gpu(gm, kv, prompt, 3, toks[:-1], stream)
+    h_full, _, _ = om.forward_full(prompt, logits=False)
+    assert_close(h_full, ghd, "prefill hidden")
+    assert_close(olg, glg, "logits")
+    assert_tokens(olg, toks, gam, "greedy tokens")
+
+
+def test_tensor_core_chunked_prefill(stream):
+    """Second chunk starts at position 200 (not a key-tile boundary)."""
+    shape = MID_LLAMA
+    w, om, gm = model_pair(shape)
+    prompt = synth.prompt_ids(shape, 420)
+    _, olg, _ = om.forward_full(prompt)
+    kv = gm.kv_alloc(2, 448)
+    lg = torch.empty((3, shape.vocab), dtype=torch.float32, device="cuda")
+    hid = torch.empty((220, shape.hidden), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        gm.prefill(kv, 1, i32(prompt[:200]), 0, logits=lg[0], stream=stream)
+        gm.prefill(kv, 1, i32(prompt[200:]), 200, logits=lg[1], hidden=hid, stream=stream)
+    assert gm.sync_status(stream) == 0
+    assert_close(olg[[199, 419]], lg[:2].cpu().numpy(), "chunked prefill logits")
+    h_full, _, _ = om.forward_full(prompt, logits=False)
+    assert_close(h_full[200:], hid.cpu().numpy(), "second chunk hidden")
