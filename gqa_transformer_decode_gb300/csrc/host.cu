@@ -1090,3 +1090,103 @@ extern "C" ember_status ember_gemv_bf16(const uint16_t* W, int32_t N, int32_t K,
 }
 
 extern "C" uint64_t ember_kernel_launches(void) { return (uint64_t)launches_so_far(); }
+
+// ====================================== greedy LM head without allocation ==
+// ember_gemv_argmax_noalloc: the split GEMV with its argmax epilogue, for a
+// caller that may not allocate device memory (its whole budget is already
+// handed out, e.g. to a KV pool, or it cannot afford the device-wide stall a
+// cudaMalloc / cudaFree can cause on its latency path).  The per-row argmax
+// keys live in a fixed file-scope device array instead of a caller buffer.
+
+namespace {
+
+// One u64 key per input row: (order-preserving logit bits << 32 | ~index).
+// The GEMV CTAs atomicMax into it, so it must hold zero when a call starts;
+// the set-up zeroes it once and every call's finishing kernel zeroes it again
+// after reading it.  64 bytes per device.
+static __device__ __align__(256) unsigned long long g_noalloc_keys[EMBER_NOALLOC_MAX_ROWS];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+unsigned long long* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+int g_noalloc_sms[NOALLOC_MAX_DEVICES] = {};
+
+// keys -> int32 argmax, then clear the keys for the next call
+__global__ void k_noalloc_finish(unsigned long long* keys, int nb, int32_t* argmax) {
+    pdl_wait();
+    const int b = threadIdx.x;
+    if (b < nb) {
+        argmax[b] = argmax_key_index(keys[b]);
+        keys[b] = 0ull;
+    }
+}
+
+// First call on a device (that device current): resolve the scratch address
+// and clear it, ordered on the caller's stream.  Returns nullptr on failure.
+unsigned long long* noalloc_scratch(int dev, cudaStream_t s, int* sms, ember_status* st) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev]) {
+        *sms = g_noalloc_sms[dev];
+        return g_noalloc_ptr[dev];
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_keys);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g_noalloc_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(g_noalloc_keys), s);
+    if (e != cudaSuccess) {
+        *st = fail(EMBER_ERR_CUDA, "no-alloc set-up on device %d failed: %s", dev,
+                   cudaGetErrorString(e));
+        return nullptr;
+    }
+    g_noalloc_ptr[dev] = static_cast<unsigned long long*>(p);
+    *sms = g_noalloc_sms[dev];
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" ember_status ember_gemv_argmax_noalloc(const uint16_t* W, int32_t N, int32_t K,
+                                                  const float* x, int32_t nb, float* y,
+                                                  int32_t* argmax, ember_stream_t stream) {
+    if (!W || !x || !argmax) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (nb > EMBER_NOALLOC_MAX_ROWS)
+        return fail(EMBER_ERR_CAPACITY,
+                    "nb = %d rows exceeds the fixed scratch of EMBER_NOALLOC_MAX_ROWS = %d rows",
+                    nb, EMBER_NOALLOC_MAX_ROWS);
+    if (N <= 0 || K <= 0 || K % 8 || K > 16384 || nb <= 0)
+        return fail(EMBER_ERR_INVALID_ARG, "N, K > 0, K %% 8 == 0, K <= 16384, nb >= 1");
+    if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(x)) & 15)
+        return fail(EMBER_ERR_INVALID_ARG, "W and x must be 16-byte aligned");
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+        return fail(EMBER_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, NOALLOC_MAX_DEVICES);
+    const cudaStream_t s = (cudaStream_t)stream;
+    int sms = 0;
+    ember_status st = EMBER_OK;
+    unsigned long long* keys = noalloc_scratch(dev, s, &sms, &st);
+    if (!keys) return st;
+
+    GemvArgs g{};
+    g.W = W;
+    g.N = N;
+    g.K = K;
+    g.x = x;
+    g.ldx = K;
+    g.out = y;   // logits too, when the caller wants them
+    g.ldo = N;
+    g.nb = nb;
+    g.mode = EPI_ARGMAX;
+    g.keys = keys;
+    launch_gemv(g, s, sms);
+    CK(cudaGetLastError());
+    cudaError_t e = launch_k(k_noalloc_finish, dim3(1), dim3(32), 0, s, keys, (int)nb, argmax);
+    if (e != cudaSuccess) {
+        // the GEMV ran but nothing will clear its keys: redo the set-up next time
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        g_noalloc_ptr[dev] = nullptr;
+        return fail(EMBER_ERR_CUDA, "argmax finish launch failed: %s", cudaGetErrorString(e));
+    }
+    return EMBER_OK;
+}

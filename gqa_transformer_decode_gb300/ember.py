@@ -86,6 +86,7 @@ def load():
         "ember_rope_store": (st, [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_gemm_bf16": (st, [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]),
         "ember_gemv_bf16": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P]),
+        "ember_gemv_argmax_noalloc": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P, P]),
         "ember_kernel_launches": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():
@@ -183,6 +184,10 @@ def ember_gemm_bf16(A, B, D, M, N, K, stream):
 
 def ember_gemv_bf16(W, N, K, x, nb, y, stream):
     return load().ember_gemv_bf16(W, N, K, x, nb, y, stream)
+
+
+def ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream):
+    return load().ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream)
 
 
 def ember_kernel_launches() -> int:

@@ -225,6 +225,44 @@ ember_status ember_gemm_bf16(const uint16_t *A, const uint16_t *B, float *D, int
 ember_status ember_gemv_bf16(const uint16_t *W, int32_t N, int32_t K, const float *x, int32_t nb,
                              float *y, ember_stream_t stream);
 
+/* ---- greedy LM head with no allocation ----------------------------------- */
+
+/* The method this library implements has no counterpart to this entry point;
+ * it serves callers that may not allocate device memory at all -- a serving
+ * loop whose HBM is already handed out (to a KV pool, say), or a latency path
+ * that cannot take the device-wide stall a cudaMalloc / cudaFree can cause.
+ *
+ * argmax[b] = the first index n of the largest y[b][n] = sum_k W[n][k] x[b][k]
+ * for b < nb: the split GEMV of ember_gemv_bf16 (same arguments, same
+ * arithmetic, bf16 W [N][K], f32 x [nb][K]; K a multiple of 8, K <= 16384, W
+ * and x 16-byte aligned) with its argmax epilogue, the greedy step of the tied
+ * LM head.  y (f32 [nb][N]) receives the logits when non-NULL.  argmax is a
+ * device int32 [nb].  All pointers are the caller's; nothing is kept.
+ *
+ * Scratch: the per-row argmax keys sit in a fixed device array inside the
+ * library (EMBER_NOALLOC_MAX_ROWS u64 keys, 64 bytes per device); no call
+ * allocates, frees or calls an allocating library routine.  The keys must be
+ * zero when a call starts: the set-up clears them once and each call clears
+ * them again after use, in its second kernel.
+ *
+ * Set-up: the first call on each device (with that device current) resolves
+ * the array's address and clears it on the given stream.  Make that first
+ * call before any stream capture begins on the device.
+ *
+ * Concurrency: every call on one device shares that one array.  Two calls
+ * whose kernels may overlap (different streams without an ordering between
+ * them, or different host threads) race on it and may return wrong indices:
+ * order them on one stream or with events.
+ *
+ * Errors: CAPACITY when nb > EMBER_NOALLOC_MAX_ROWS; INVALID_ARG for NULL or
+ * misaligned pointers and bad sizes; UNSUPPORTED for device ordinals >= 64;
+ * CUDA for a failed set-up or launch.  Returns once the two kernels are
+ * queued on `stream`. */
+#define EMBER_NOALLOC_MAX_ROWS 8
+ember_status ember_gemv_argmax_noalloc(const uint16_t *W, int32_t N, int32_t K, const float *x,
+                                       int32_t nb, float *y, int32_t *argmax,
+                                       ember_stream_t stream);
+
 /* Number of kernels this library has launched in this process so far (a
  * CUDA-graph replay counts each kernel node it runs).  For accounting. */
 uint64_t ember_kernel_launches(void);
