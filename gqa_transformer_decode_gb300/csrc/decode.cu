@@ -53,6 +53,11 @@ __global__ void k_embed(EmbedArgs a) {
     const uint16_t* row = a.E + (size_t)s_id * a.H;
     float* out = a.x + (size_t)t * a.H;
     for (int i = threadIdx.x; i < a.H; i += blockDim.x) out[i] = bf16_to_f32(row[i]);
+    if (a.zero0)
+        for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
+            a.zero0[(size_t)t * a.H + i] = 0.f;
+            a.zero1[(size_t)t * a.H + i] = 0.f;
+        }
 }
 
 void launch_embed(const EmbedArgs& a, cudaStream_t s) {
@@ -84,7 +89,7 @@ __device__ __forceinline__ void gemv_load_tile(const GemvArgs& a, int tile, int 
     }
 }
 
-template <int TPR, int NB, bool WF16>
+template <int TPR, int NB, bool WF16, bool XA = false>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     constexpr int R = GEMV_THREADS / TPR;
     constexpr int GL = TPR < 32 ? TPR : 32;       // lanes reduced by shuffles
@@ -106,12 +111,22 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     int tile = blockIdx.x;
     if (tile < n_tiles) gemv_load_tile<TPR>(a, tile, r, sub, K8, w);
     pdl_wait();
+    // XA (one row): x + x_add staged once in shared memory
+    extern __shared__ float s_xa[];
+    if (XA) {
+        for (int i = tid * 4; i < a.K; i += GEMV_THREADS * 4) {
+            const float4 u = __ldcg(reinterpret_cast<const float4*>(a.x + i));
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x_add + i));
+            *reinterpret_cast<float4*>(s_xa + i) = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+        }
+        __syncthreads();
+    }
 
     // RMSNorm statistics of every input row (ember reference_forward.py rmsnorm()).
     for (int b = 0; b < NB; ++b) {
         float rinv = 1.f;
         if (a.norm_w && b < nb) {
-            const float* xb = a.x + (size_t)b * a.ldx;
+            const float* xb = XA ? s_xa : a.x + (size_t)b * a.ldx;
             float ss = 0.f;
             for (int i = tid; i < a.K; i += GEMV_THREADS) ss += xb[i] * xb[i];
             ss = block_sum(ss, s_red);
@@ -148,7 +163,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
                 for (int b = 0; b < NB; ++b) {
                     if (b < nb) {
                         const float4* xp =
-                            reinterpret_cast<const float4*>(a.x + (size_t)b * a.ldx) + 2 * c;
+                            reinterpret_cast<const float4*>(XA ? s_xa : a.x + (size_t)b * a.ldx) + 2 * c;
                         const float4 x0 = xp[0], x1 = xp[1];
                         float s = acc[b];
                         s = fmaf(wf[0], x0.x, s); s = fmaf(wf[1], x0.y, s);
@@ -223,6 +238,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
 template <int TPR>
 static void gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
     const dim3 g(grid), b(GEMV_THREADS);
+    if (a.x_add) {   // batch-1 head over a residual held as two buffers (K <= 12288)
+        launch_k(k_gemv<TPR, 1, false, true>, g, b, (size_t)a.K * 4, s, a);
+        return;
+    }
     if (a.w_f16) {
         if (a.nb <= 1) launch_k(k_gemv<TPR, 1, true>, g, b, 0, s, a);
         else if (a.nb <= 2) launch_k(k_gemv<TPR, 2, true>, g, b, 0, s, a);

@@ -1,0 +1,772 @@
+// decode_fused.cu -- batch-1 decode as two kernels per decoder layer.
+//
+// D1 (k_fused_attn): one thread-block cluster of C CTAs per kv head g.  Each
+//   CTA RMS-normalises x, computes its share of the group's q/k/v rows
+//   (weights bulk-loaded into shared memory before the programmatic-launch
+//   wait), broadcasts them through distributed shared memory, applies the
+//   optional q/k RMSNorm and RoPE, writes the new K/V row (the CTA whose key
+//   range holds the position), runs flash attention over its key range for
+//   all G query heads of the group, merges the C partial softmaxes through
+//   distributed shared memory, and multiplies the merged heads by its rows of
+//   the group's o_proj column block, adding the result into the residual.
+// D2 (k_fused_mlp): every CTA owns chunks of FC intermediate features:
+//   RMSNorm, the gate/up rows of those features, SwiGLU, and their columns of
+//   down_proj (a transposed f16 copy, so each chunk is 4 contiguous rows),
+//   adding its partial down_proj output into the residual.
+//
+// The split-K additions use red.global.add into a zeroed accumulator, so the
+// residual stream of kernel n is x_n = X[n-1] + Z[n-1]: kernel n reads
+// X[(n-1)%2] and Z[(n-1)%3], writes X[n%2] = x_n, zeroes Z[(n-2)%3] and
+// accumulates into Z[n%3] -- no kernel writes a buffer that one of its own
+// CTAs may still read.  (Llama / Qwen2 decoder layer: x += o_proj(attn(
+// rmsnorm(x))); x += down(silu(gate(rmsnorm(x))) * up(rmsnorm(x))).)
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ember {
+
+namespace {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of shared variable p in CTA `cta` of this cluster
+__device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+    return r;
+}
+__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void red_add(float* p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// RMSNorm of the residual x = x_in + z_in (H floats, H % 4 == 0, H <= 4096
+// for 256 threads).  The weights are loaded into registers before the
+// programmatic-launch wait (load_w); apply() issues all of its 16-byte loads
+// at once, writes this CTA's slice of x_out (= x) and of z_zero (= 0) from
+// the values it holds, and leaves f16(x * rsqrt(mean(x^2) + eps) * w) in s_xh
+// (the projections' input, at the precision of the tensor-core GEMM operands).
+struct ResidualNorm {
+    static constexpr int MAXV = 4;
+    float4 w[MAXV];
+    __device__ __forceinline__ void load_w(const float* wp, int H) {
+        const int H4 = H >> 2;
+#pragma unroll
+        for (int q = 0; q < MAXV; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            w[q] = i < H4 ? __ldg(reinterpret_cast<const float4*>(wp) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __device__ __forceinline__ void apply(const float* x_in, const float* z_in, float* x_out, float* z_zero,
+                                          float eps, int H, int cta, int ncta, uint16_t* s_xh, float* s_red) {
+        const int H4 = H >> 2;
+        const int per = (H4 + ncta - 1) / ncta;
+        const int e0 = cta * per, e1 = e0 + per;
+        float4 v[MAXV];
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < MAXV; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            if (i < H4) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(x_in) + i);
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(z_in) + i);
+                v[q] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < MAXV; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            if (i < H4) {
+                ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+                if (i >= e0 && i < e1) {
+                    reinterpret_cast<float4*>(x_out)[i] = v[q];
+                    reinterpret_cast<float4*>(z_zero)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        for (int k = 0; k < (int)(blockDim.x >> 5); ++k) tot += s_red[k];
+        const float ri = rsqrtf(tot / (float)H + eps);
+#pragma unroll
+        for (int q = 0; q < MAXV; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            if (i < H4)
+                reinterpret_cast<uint2*>(s_xh)[i] =
+                    make_uint2(pack_f16x2(v[q].x * ri * w[q].x, v[q].y * ri * w[q].y),
+                               pack_f16x2(v[q].z * ri * w[q].z, v[q].w * ri * w[q].w));
+        }
+        __syncthreads();
+    }
+};
+
+// Row dot products by whole warps with the input vector held in registers:
+// lane l keeps chunks c = l + 32*i (8 f16 values each) of the input, so
+// shared memory only streams the weights.  Eight partial sums per lane, then
+// a 5-step butterfly (every lane gets the row's value).
+constexpr int XR_MAX = 8;          // chunks per lane: input length <= 8 * 32 * 8 = 2048
+struct XRegs {
+    uint4 v[XR_MAX];
+    __device__ __forceinline__ void load(const uint16_t* xh, int n8) {   // f16 input
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int i = 0; i < XR_MAX; ++i) {
+            const int c = lane + 32 * i;
+            v[i] = c < n8 ? reinterpret_cast<const uint4*>(xh)[c] : make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ void load_f32(const float* x, int n8) {  // f32 input, rounded to f16
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int i = 0; i < XR_MAX; ++i) {
+            const int c = lane + 32 * i;
+            if (c < n8) {
+                const float4 a = reinterpret_cast<const float4*>(x)[2 * c];
+                const float4 b = reinterpret_cast<const float4*>(x)[2 * c + 1];
+                v[i] = make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(b.x, b.y),
+                                  pack_f16x2(b.z, b.w));
+            } else {
+                v[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+};
+__device__ __forceinline__ float wdot_f16(const uint4* row, const XRegs& x, int n8) {
+    const int lane = threadIdx.x & 31;
+    float s[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s[u] = 0.f;
+#pragma unroll
+    for (int i = 0; i < XR_MAX; ++i) {
+        const int c = lane + 32 * i;
+        if (c < n8) {
+            float w[8], xf[8];
+            unpack8_f16(row[c], w);
+            unpack8_f16(x.v[i], xf);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s[u] = fmaf(w[u], xf[u], s[u]);
+        }
+    }
+    float t = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL_MASK, t, o);
+    return t;
+}
+
+}  // namespace
+
+// ================================================================== D1 ==
+constexpr int FA_THREADS = 256;
+constexpr int FA_KT = 128;     // keys per K/V tile (the TMA box height)
+constexpr int FA_C = 16;       // CTAs per cluster (one cluster per kv head)
+
+// Shared-memory plan of D1 (host and device compute it the same way).
+struct FaLayout {
+    int k, v, w, x, qkv, part, att, sc, red, bar, total;
+};
+__host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int no) {
+    FaLayout L;
+    const int tile = FA_KT * D * 2;              // one K (or V) tile, bf16
+    int o = 0;
+    L.k = o; o += tile;
+    L.v = o; o += tile;
+    L.w = o;
+    const int wb = 2 * (nr * H > no * G * D ? nr * H : no * G * D);
+    o += (wb + 1023) / 1024 * 1024;
+    L.x = o; o += ((H * 4 + 15) / 16) * 16;
+    L.qkv = o; o += (((G + 2) * D * 4 + 15) / 16) * 16;
+    L.part = o; o += ((G * (D + 2) * 4 + 15) / 16) * 16;
+    L.att = o; o += ((G * D * 4 + 15) / 16) * 16;
+    L.sc = o; o += G * FA_KT * 4;
+    L.red = o; o += 32 * 4;
+    L.bar = o; o += 4 * 8;
+    L.total = o + 1024;                           // room to align the base to 1024
+    return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_constant__ CUtensorMap k_map,
+                                                           const __grid_constant__ CUtensorMap v_map,
+                                                           FusedAttnArgs a) {
+    constexpr int H2 = D / 2;
+    constexpr int NSUB = D / 64;               // 64-column TMA sub-tiles per row
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int H = a.H, G = a.NH / a.NKV;
+    constexpr int C = FA_C;
+    const int Rg = (G + 2) * D;
+    const FaLayout Lo = fa_layout(D, G, H, a.nr, a.no);
+    uint8_t* sK = sm + Lo.k;
+    uint8_t* sV = sm + Lo.v;
+    uint16_t* sW = reinterpret_cast<uint16_t*>(sm + Lo.w);
+    uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + Lo.x);  // normed input, f16
+    float* s_qkv = reinterpret_cast<float*>(sm + Lo.qkv);    // [G*D q | D k | D v]
+    float* s_part = reinterpret_cast<float*>(sm + Lo.part);  // [G][m, l, acc[D]]
+    float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads
+    float* s_sc = reinterpret_cast<float*>(sm + Lo.sc);      // [G][FA_KT]
+    float* s_red = reinterpret_cast<float*>(sm + Lo.red);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);  // 0: qkv W, 1: K/V, 2: o W
+    __shared__ float s_scale[16], s_m[16], s_l[16];
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = (int)cluster_rank();
+    const int g = blockIdx.y;
+    const int r0 = r * a.nr, r1 = min(Rg, r0 + a.nr);     // this CTA's rows of the group
+    const int o0 = r * a.no, o1 = min(H, o0 + a.no);      // this CTA's o_proj rows
+    const int GD = G * D;
+    const size_t rowb = (size_t)H * 2;
+
+    // ---- before the wait: immutable weights only ----
+    if (tid == 0) {
+        s_err = 0;
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (r1 > r0) {
+            mbar_expect_tx(&bar[0], (uint32_t)((r1 - r0) * rowb));
+            // the group's rows are three runs of the fused [q; k; v] matrix
+            int i = r0;
+            while (i < r1) {
+                int src, run_end;
+                if (i < GD) { src = g * GD + i; run_end = GD; }
+                else if (i < GD + D) { src = a.NH * D + g * D + (i - GD); run_end = GD + D; }
+                else { src = a.NH * D + a.NKV * D + g * D + (i - GD - D); run_end = Rg; }
+                const int n = min(r1, run_end) - i;
+                bulk_g2s(sW + (size_t)(i - r0) * H, a.wqkv + (size_t)src * H, (uint32_t)(n * rowb), &bar[0]);
+                i += n;
+            }
+        }
+    }
+    // o_proj rows of this CTA (columns of group g): into L2 now, shared memory later
+    for (int row = o0 + tid; row < o1; row += FA_THREADS)
+        prefetch_l2(a.wo + (size_t)row * a.NH * D + (size_t)g * GD, (uint32_t)(GD * 2));
+    ResidualNorm rn;
+    rn.load_w(a.norm_w, H);
+    float* s_bias = s_part;   // the biases of this CTA's rows, until the partials are written
+    if (a.bqkv && tid < r1 - r0) {
+        const int i = r0 + tid;
+        int src;
+        if (i < GD) src = g * GD + i;
+        else if (i < GD + D) src = a.NH * D + g * D + (i - GD);
+        else src = a.NH * D + a.NKV * D + g * D + (i - GD - D);
+        s_bias[tid] = a.bqkv[src];
+    }
+    __syncthreads();
+    pdl_trigger();
+    pdl_wait();
+
+    const int ok = __ldcg(a.tok_ok);
+    const int pos = ok ? __ldcg(a.tok_pos) : 0;
+    float* s_cs = s_att;      // RoPE row of pos (cos | sin), until the merged heads arrive
+    if (ok && tid < D) s_cs[tid] = tid < H2 ? a.cos_t[(size_t)pos * H2 + tid]
+                                            : a.sin_t[(size_t)pos * H2 + tid - H2];
+    const int n_keys = ok ? pos + 1 : 0;
+    const int per = (n_keys + C - 1) / C;
+    const int lo = min(n_keys, r * per), hi = min(n_keys, lo + per);
+    const int seq = ok ? a.seqs[0] : 0;
+    const int kz = (seq * a.L + a.layer) * a.NKV + g;     // (seq, layer, kv head) plane
+    const bool owner = ok && pos >= lo && pos < hi;
+    uint32_t kv_phase = 0;
+    auto issue_tile = [&](int t0) {
+        const uint32_t bytes = (uint32_t)(2 * NSUB * FA_KT * 128);
+        mbar_expect_tx(&bar[1], bytes);
+        for (int sb = 0; sb < NSUB; ++sb) {
+            tma_load_3d(sK + sb * FA_KT * 128, &k_map, sb * 64, t0, kz, &bar[1]);
+            tma_load_3d(sV + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, &bar[1]);
+        }
+    };
+    if (tid == 0 && hi > lo) issue_tile(lo);
+
+    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
+
+    // ---- this CTA's q/k/v rows (a warp a row), broadcast to every CTA of the cluster ----
+    if (r1 > r0 && !mbar_wait(&bar[0], 0)) s_err = 1;
+    {
+        XRegs xr;
+        xr.load(s_xh, H / 8);
+        for (int ri = warp; ri < r1 - r0; ri += FA_THREADS / 32) {
+            float v = wdot_f16(reinterpret_cast<const uint4*>(sW + (size_t)ri * H), xr, H / 8);
+            if (a.bqkv) v += s_bias[ri];
+            if (lane < C) st_dsmem(dsmem(&s_qkv[r0 + ri], lane), v);
+        }
+    }
+    cluster_sync_all();
+
+    // o_proj rows into the (now free) weight buffer, while attention runs
+    if (warp == 0 && o1 > o0) {   // one bulk copy per row, spread over the warp's lanes
+        if (lane == 0) mbar_expect_tx(&bar[2], (uint32_t)((o1 - o0) * GD * 2));
+        __syncwarp();
+        for (int row = o0 + lane; row < o1; row += 32)
+            bulk_g2s(sW + (size_t)(row - o0) * GD, a.wo + (size_t)row * a.NH * D + (size_t)g * GD,
+                     (uint32_t)(GD * 2), &bar[2]);
+    }
+
+    // ---- optional per-head q/k RMSNorm, then RoPE (q pre-scaled, base 2) ----
+    if (a.q_norm) {
+        for (int h = warp; h < G + 1; h += FA_THREADS / 32) {
+            float* v = h < G ? s_qkv + h * D : s_qkv + GD;
+            const float* w = h < G ? a.q_norm : a.k_norm;
+            float ss = 0.f;
+            for (int d = lane; d < D; d += 32) ss += v[d] * v[d];
+            ss = warp_sum(ss);
+            const float ri = rsqrtf(ss / (float)D + a.eps);
+            __syncwarp();
+            for (int d = lane; d < D; d += 32) v[d] = v[d] * ri * w[d];
+        }
+        __syncthreads();
+    }
+    const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+    if (ok) {
+        const float* cs = s_cs;
+        const float* sn = s_cs + H2;
+        for (int e = tid; e < (G + 1) * H2; e += FA_THREADS) {
+            const int h = e / H2, i = e % H2;
+            float* v = h < G ? s_qkv + h * D : s_qkv + GD;
+            float r0v, r1v;
+            rope_pair(v[i], v[i + H2], cs[i], sn[i], r0v, r1v);
+            if (h < G) {
+                v[i] = r0v * qscale;
+                v[i + H2] = r1v * qscale;
+            } else {
+                v[i] = r0v;
+                v[i + H2] = r1v;
+            }
+        }
+    }
+    __syncthreads();
+    if (owner) {   // the new K/V row: to the cache (bf16) and, below, into the tile
+        const size_t off = ((size_t)kz * a.max_len + pos) * D;
+        for (int d = tid; d < D; d += FA_THREADS) {
+            a.kc[off + d] = f32_to_bf16(s_qkv[GD + d]);
+            a.vc[off + d] = f32_to_bf16(s_qkv[GD + D + d]);
+        }
+    }
+
+    // ---- flash attention over keys [lo, hi) for the G heads ----
+    if (tid < G) {
+        s_m[tid] = -INFINITY;
+        s_l[tid] = 0.f;
+    }
+    constexpr int MAXE = (16 * D + FA_THREADS - 1) / FA_THREADS;
+    float acc[MAXE];
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) acc[i] = 0.f;
+    for (int t0 = lo; t0 < hi; t0 += FA_KT) {
+        const int nt = min(FA_KT, hi - t0);
+        if (!mbar_wait(&bar[1], kv_phase)) s_err = 1;
+        kv_phase ^= 1;
+        if (owner && pos >= t0 && pos < t0 + nt) {   // patch the row the TMA read stale
+            const int j = pos - t0;
+            for (int d = tid; d < D; d += FA_THREADS) {
+                const int sb = d >> 6, c = (d & 63) >> 3;
+                const int off = sb * FA_KT * 128 + j * 128 + ((c ^ (j & 7)) << 4) + (d & 7) * 2;
+                *reinterpret_cast<uint16_t*>(sK + off) = f32_to_bf16(s_qkv[GD + d]);
+                *reinterpret_cast<uint16_t*>(sV + off) = f32_to_bf16(s_qkv[GD + D + d]);
+            }
+        }
+        __syncthreads();
+        // scores: thread -> key j = tid % 128, heads tid / 128, +2, ...
+        {
+            const int j = tid % FA_KT;
+            for (int h = tid / FA_KT; h < G; h += FA_THREADS / FA_KT) {
+                float sc = -INFINITY;
+                if (j < nt) {
+                    const float* q = s_qkv + h * D;
+                    float dot = 0.f;
+#pragma unroll
+                    for (int c8 = 0; c8 < D / 8; ++c8) {
+                        const int sb = c8 >> 3, c = c8 & 7;
+                        const uint4 kk = *reinterpret_cast<const uint4*>(
+                            sK + sb * FA_KT * 128 + j * 128 + ((c ^ (j & 7)) << 4));
+                        float kf[8];
+                        unpack8(kk, kf);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) dot = fmaf(q[c8 * 8 + u], kf[u], dot);
+                    }
+                    sc = dot;
+                }
+                s_sc[h * FA_KT + j] = sc;
+            }
+        }
+        __syncthreads();
+        // online softmax, one warp per head
+        for (int h = warp; h < G; h += FA_THREADS / 32) {
+            float v[FA_KT / 32];
+            float tm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < FA_KT / 32; ++u) {
+                v[u] = s_sc[h * FA_KT + lane + 32 * u];
+                tm = fmaxf(tm, v[u]);
+            }
+            tm = warp_max(tm);
+            const float mo = s_m[h];
+            const float mn = fmaxf(mo, tm);
+            float ps = 0.f;
+#pragma unroll
+            for (int u = 0; u < FA_KT / 32; ++u) {
+                const float p = exp2f(v[u] - mn);
+                s_sc[h * FA_KT + lane + 32 * u] = p;
+                ps += p;
+            }
+            ps = warp_sum(ps);
+            if (lane == 0) {
+                const float sc = exp2f(mo - mn);   // 0 when mo == -inf
+                s_scale[h] = sc;
+                s_l[h] = s_l[h] * sc + ps;
+                s_m[h] = mn;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < MAXE; ++i) {
+            const int e = tid + i * FA_THREADS;
+            if (e < GD) {
+                const int h = e / D, d = e % D;
+                const int sb = d >> 6, c = (d & 63) >> 3;
+                const uint8_t* vb = sV + sb * FA_KT * 128 + (d & 7) * 2;
+                const float* p = s_sc + h * FA_KT;
+                float s = acc[i] * s_scale[h];
+                for (int j = 0; j < nt; ++j)
+                    s = fmaf(p[j], bf16_to_f32(*reinterpret_cast<const uint16_t*>(
+                                       vb + j * 128 + ((c ^ (j & 7)) << 4))),
+                             s);
+                acc[i] = s;
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && t0 + FA_KT < hi) issue_tile(t0 + FA_KT);
+    }
+    // partial (m, l, acc) of this CTA's keys
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+        const int e = tid + i * FA_THREADS;
+        if (e < GD) s_part[(e / D) * (D + 2) + 2 + (e % D)] = acc[i];
+    }
+    if (tid < G) {
+        s_part[tid * (D + 2)] = s_m[tid];
+        s_part[tid * (D + 2) + 1] = s_l[tid];
+    }
+    cluster_sync_all();
+
+    // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
+    {
+        const int ne = (GD + C - 1) / C;
+        const int e = r * ne + tid;
+        if (tid < ne && e < GD) {
+            const int h = e / D, d = e % D;
+            // log-sum-exp merge of the C partials (empty ranges have l = 0); all
+            // 3*C remote loads are issued before the first is used
+            float mc[C], lc[C], oc[C];
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc) {
+                mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
+                lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
+                oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc)
+                if (lc[cc] > 0.f) M = fmaxf(M, mc[cc]);
+            float Ls = 0.f, O = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc) {
+                if (lc[cc] > 0.f) {
+                    const float f = exp2f(mc[cc] - M);
+                    Ls = fmaf(lc[cc], f, Ls);
+                    O = fmaf(oc[cc], f, O);
+                }
+            }
+            O = Ls > 0.f ? O / Ls : 0.f;
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc) st_dsmem(dsmem(&s_att[e], cc), O);
+        }
+    }
+    cluster_sync_all();
+
+    // ---- o_proj: this CTA's rows of the group's column block, into the residual ----
+    if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
+    {
+        XRegs xr;
+        xr.load_f32(s_att, GD / 8);
+        for (int ri = warp; ri < o1 - o0; ri += FA_THREADS / 32) {
+            const float v = wdot_f16(reinterpret_cast<const uint4*>(sW + (size_t)ri * GD), xr, GD / 8);
+            if (lane == 0) red_add(a.z_acc + o0 + ri, v);
+        }
+    }
+    if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
+}
+
+// ================================================================== D2 ==
+constexpr int FM_THREADS = 256;
+
+// Chunk = FC intermediate features: 2*FC gate/up rows then FC down_proj^T
+// rows, 6*FC*H bytes.  Phase 1 gives each gate/up row one warp.
+template <int FC>
+__global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
+    constexpr int MAXHG = 2;                      // h-groups of 8 per thread: H <= 4096
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int H = a.H, ns = a.ns, H8 = H / 8;
+    const uint32_t stage_bytes = (uint32_t)(6 * FC * H);
+    uint8_t* ring = sm;
+    uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + (size_t)ns * stage_bytes);   // normed input
+    __shared__ float s_red[32];
+    __shared__ float s_g[2][2 * FC];
+    __shared__ __align__(8) uint64_t bar[8];
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_chunks = a.F / FC;
+    const int my_n = (int)blockIdx.x < n_chunks ? (n_chunks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto issue = [&](int k) {   // chunk k of this CTA into stage k % ns
+        const int ch = blockIdx.x + k * gridDim.x;
+        uint8_t* st = ring + (size_t)(k % ns) * stage_bytes;
+        mbar_expect_tx(&bar[k % ns], stage_bytes);
+        bulk_g2s(st, a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H), &bar[k % ns]);
+        bulk_g2s(st + 4 * FC * H, a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H), &bar[k % ns]);
+    };
+    if (tid == 0) {
+        s_err = 0;
+        for (int s = 0; s < ns; ++s) mbar_init(&bar[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int k = 0; k < my_n && k < ns; ++k) issue(k);
+    }
+    for (int k = ns + tid; k < my_n; k += FM_THREADS) {   // the rest: into L2 now
+        const int ch = blockIdx.x + k * gridDim.x;
+        prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
+        prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
+    }
+    ResidualNorm rn;
+    rn.load_w(a.norm_w, H);
+    __syncthreads();
+    pdl_trigger();
+    pdl_wait();
+
+    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
+    XRegs xr;
+    xr.load(s_xh, H8);
+
+    float y[MAXHG][8];
+#pragma unroll
+    for (int q = 0; q < MAXHG; ++q)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) y[q][u] = 0.f;
+
+    for (int k = 0; k < my_n; ++k) {
+        const int s = k % ns;
+        if (!mbar_wait(&bar[s], (uint32_t)((k / ns) & 1))) s_err = 1;
+        const uint8_t* st = ring + (size_t)s * stage_bytes;
+        // gate / up rows: a warp a row
+#pragma unroll
+        for (int rr = warp; rr < 2 * FC; rr += FM_THREADS / 32) {
+            const float v = wdot_f16(reinterpret_cast<const uint4*>(st + (size_t)rr * H * 2), xr, H8);
+            if (lane == 0) s_g[k & 1][rr] = v;
+        }
+        __syncthreads();   // s_g[k & 1] complete; chunk k - 1 fully consumed
+        if (tid == 0 && k >= 1 && k - 1 + ns < my_n) issue(k - 1 + ns);
+        float act[FC];
+#pragma unroll
+        for (int j = 0; j < FC; ++j) {
+            const float gt = s_g[k & 1][2 * j], up = s_g[k & 1][2 * j + 1];
+            act[j] = gt / (1.f + __expf(-gt)) * up;
+        }
+        const uint4* wd = reinterpret_cast<const uint4*>(st + (size_t)4 * FC * H);
+#pragma unroll
+        for (int q = 0; q < MAXHG; ++q) {
+            const int hg = tid + q * FM_THREADS;
+            if (hg < H8) {
+#pragma unroll
+                for (int j = 0; j < FC; ++j) {
+                    float w[8];
+                    unpack8_f16(wd[(size_t)j * H8 + hg], w);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) y[q][u] = fmaf(w[u], act[j], y[q][u]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < MAXHG; ++q) {
+        const int hg = tid + q * FM_THREADS;
+        if (hg < H8 && my_n > 0) {
+            red_add4(a.z_acc + 8 * hg, y[q][0], y[q][1], y[q][2], y[q][3]);
+            red_add4(a.z_acc + 8 * hg + 4, y[q][4], y[q][5], y[q][6], y[q][7]);
+        }
+    }
+    if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
+}
+
+// ================================================================ host ==
+bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int num_sms) {
+    p = FusedPlan{};
+    auto no = [&](const char* why) {
+        p.why = why;
+        cudaGetLastError();
+        return false;
+    };
+    if (D != 64 && D != 128) return no("head_dim is not 64 or 128");
+    if (NH % NKV) return no("n_heads % n_kv_heads != 0");
+    const int G = NH / NKV;
+    if (G > 16 || H % 8 || H > XR_MAX * 256 || F % 4 || (G * D) % 8)
+        return no("group > 16 heads, hidden % 8, hidden > 2048 or ff % 4");
+    const int C = FA_C;
+    p.C = C;
+    p.nr = ((G + 2) * D + C - 1) / C;
+    p.no = (H + C - 1) / C;
+    p.smem_attn = fa_layout(D, G, H, p.nr, p.no).total;
+    if (p.smem_attn > 200 * 1024) return no("attention block needs > 200 KB of shared memory");
+    // MLP chunk size: the largest FC in {16, 8, 4} (dividing F) whose two-stage
+    // ring still fits beside the attention kernel on one SM; else FC = 4.
+    const int fixed = H * 4 + 256;
+    const int budget = 227 * 1024 - p.smem_attn - 2 * 1024;
+    p.fc = 0;
+    for (int fc : {16, 8, 4})
+        if (F % fc == 0 && 2 * 6 * fc * H + fixed <= budget) {
+            p.fc = fc;
+            break;
+        }
+    const bool coresident = p.fc != 0;
+    if (!coresident) p.fc = 4;
+    const int stage = 6 * p.fc * H;
+    const int n_chunks = F / p.fc;
+    p.mlp_grid = n_chunks < num_sms ? n_chunks : num_sms;
+    const int per_cta = (n_chunks + p.mlp_grid - 1) / p.mlp_grid;
+    int ns = ((coresident ? budget : 200 * 1024) - fixed) / stage;
+    if (ns > per_cta) ns = per_cta;
+    if (ns > 8) ns = 8;
+    if (ns < 2) ns = 2;
+    p.ns = ns;
+    p.smem_mlp = ns * stage + fixed;
+    if (p.smem_mlp > 227 * 1024) return no("MLP ring does not fit shared memory");
+    // The limit is a property of the function, shared by every model in the
+    // process: raise it to the device maximum so that no model lowers it
+    // below what another one launches with.
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess && (p.smem_attn > optin - 1024 || p.smem_mlp > optin - 1024))
+        return no("shared memory above the device limit");
+    auto setup = [&](auto kern, int) {   // the limit covers static + dynamic shared memory
+        cudaFuncAttributes fa{};
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - (int)fa.sharedSizeBytes);
+    };
+    if (D == 64) setup(k_fused_attn<64>, p.smem_attn);
+    else setup(k_fused_attn<128>, p.smem_attn);
+    if (e == cudaSuccess) {
+        e = D == 64 ? cudaFuncSetAttribute(k_fused_attn<64>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)
+                    : cudaFuncSetAttribute(k_fused_attn<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
+    setup(k_fused_mlp<4>, p.smem_mlp);
+    setup(k_fused_mlp<8>, p.smem_mlp);
+    setup(k_fused_mlp<16>, p.smem_mlp);
+    if (e != cudaSuccess) return no("kernel attributes rejected");
+    // one cluster of C CTAs must fit somewhere on the chip
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, NKV);
+    cfg.blockDim = dim3(FA_THREADS);
+    cfg.dynamicSmemBytes = p.smem_attn;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = D == 64 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64>, &cfg)
+                : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128>, &cfg);
+    if (e != cudaSuccess) return no("cluster occupancy query failed");
+    if (n < 1) return no("a cluster of 16 CTAs does not fit");
+    p.ok = true;
+    p.why = "";
+    return true;
+}
+
+void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int smem,
+                       cudaStream_t s) {
+    count_launches(1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.C, a.NKV);
+    cfg.blockDim = dim3(FA_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = a.C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    const CUtensorMap& km = *reinterpret_cast<const CUtensorMap*>(k_map);
+    const CUtensorMap& vm = *reinterpret_cast<const CUtensorMap*>(v_map);
+    if (a.D == 64) cudaLaunchKernelEx(&cfg, k_fused_attn<64>, km, vm, a);
+    else cudaLaunchKernelEx(&cfg, k_fused_attn<128>, km, vm, a);
+}
+
+void launch_fused_mlp(const FusedMlpArgs& a, int fc, int grid, int smem, cudaStream_t s) {
+    const dim3 g(grid), b(FM_THREADS);
+    if (fc == 16) launch_k(k_fused_mlp<16>, g, b, (size_t)smem, s, a);
+    else if (fc == 8) launch_k(k_fused_mlp<8>, g, b, (size_t)smem, s, a);
+    else launch_k(k_fused_mlp<4>, g, b, (size_t)smem, s, a);
+}
+
+// wdT[f][h] = wd[h][f] (16-bit elements), 32x32 tiles through shared memory
+__global__ void k_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols) {
+    __shared__ uint16_t t[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int rr = r0 + i, cc = c0 + threadIdx.x;
+        if (rr < rows && cc < cols) t[i][threadIdx.x] = in[(size_t)rr * cols + cc];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int cc = c0 + i, rr = r0 + threadIdx.x;
+        if (rr < rows && cc < cols) out[(size_t)cc * rows + rr] = t[threadIdx.x][i];
+    }
+}
+
+void launch_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols, cudaStream_t s) {
+    count_launches(1);
+    k_transpose16<<<dim3((cols + 31) / 32, (rows + 31) / 32), dim3(32, 8), 0, s>>>(in, out, rows, cols);
+}
+
+}  // namespace ember

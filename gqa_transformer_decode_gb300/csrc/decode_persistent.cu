@@ -64,7 +64,14 @@ static PkKernel pk_kernel(const PersistArgs& a) {
 bool persist_prepare(PersistArgs& a, int& grid, int& smem) {
     PkKernel k = pk_kernel(a);
     if (!k || !pk_config(a, smem)) return false;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    // a per-function limit shared by all models: set it to the device maximum
+    int cur_dev = 0, optin = 0;
+    cudaFuncAttributes fa{};
+    if (cudaGetDevice(&cur_dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, cur_dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, k) != cudaSuccess || smem > optin - (int)fa.sharedSizeBytes ||
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }

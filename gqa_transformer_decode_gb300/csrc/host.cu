@@ -102,11 +102,13 @@ void rope_tables(const ember_config& c, int npos, std::vector<float>& cs, std::v
 
 struct LayerDev {
     uint16_t *wqkv, *wo, *wgu, *wd;
+    uint16_t* wdT = nullptr;   // f16 [F][H] down_proj transposed (fused batch-1 decode)
     float *attn_norm, *mlp_norm, *bqkv, *q_norm, *k_norm;
     GemmPlan p_qkv, p_o, p_gu, p_d;
 };
 
 struct GraphEntry {
+    unsigned long long kv_gen;   // the KV cache the graph was captured against
     int batch;
     const void *seqs, *ids, *pos, *logits, *argmax;
     cudaGraphExec_t exec;
@@ -114,6 +116,7 @@ struct GraphEntry {
 };
 
 std::atomic<long long> g_launches{0};
+std::atomic<unsigned long long> g_kv_gen{0};   // a unique id per KV cache ever allocated
 
 }  // namespace
 
@@ -154,7 +157,12 @@ struct ember_model {
     PersistArgs pk{};
     int pk_grid = 0, pk_smem = 0;
     bool pk_ok = false;
+    // fused batch-1 decode (two kernels per layer)
+    FusedPlan fp;
+    float* fx[2] = {nullptr, nullptr};             // residual stream copies [H]
+    float* fz[3] = {nullptr, nullptr, nullptr};    // split-K accumulators [H]
     std::vector<GraphEntry> graphs;
+    std::vector<ember_kv*> kvs;   // live caches (detached when the model goes first)
     bool use_graphs = true;
     std::mutex mu;
 };
@@ -168,6 +176,9 @@ struct ember_kv {
     uint16_t* vt = nullptr;              // transposed V of one layer's kv heads (prefill)
     alignas(64) unsigned char k_map[128];   // TMA map over the whole K cache, 3-D
     bool k_map_ok = false;
+    alignas(64) unsigned char v_map[128];   // the same over the V cache
+    bool v_map_ok = false;
+    unsigned long long gen = 0;             // never reused, unlike the host address
 };
 
 static ember_status validate(const ember_config* c) {
@@ -237,6 +248,11 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
     m->layers.resize(c.layers);
+    if (c.causal && !(getenv("EMBER_NO_FUSED") && atoi(getenv("EMBER_NO_FUSED"))))
+        fused_decode_plan(m->fp, H, c.n_heads, NKV, D, F, m->sms);
+    if (getenv("EMBER_VERBOSE") && atoi(getenv("EMBER_VERBOSE")))
+        fprintf(stderr, "ember: fused batch-1 decode %s%s\n", m->fp.ok ? "on" : "off: ",
+                m->fp.ok ? "" : m->fp.why);
 
     // ---- weights ----
     Arena wa;
@@ -251,6 +267,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
         wa.add(&L.wo, (size_t)H * m->q);
         wa.add(&L.wgu, (size_t)2 * F * H);
         wa.add(&L.wd, (size_t)H * F);
+        if (m->fp.ok) wa.add(&L.wdT, (size_t)F * H);
         wa.add(&L.attn_norm, H);
         wa.add(&L.mlp_norm, H);
         wa.add(&L.bqkv, m->qkv_n);
@@ -278,6 +295,10 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     aa.add(&m->status, 1);
     aa.add(&m->pk_layers, (size_t)c.layers);
     aa.add(&m->pk_bar, 32 + 1024);
+    if (m->fp.ok) {
+        for (auto& p : m->fx) aa.add(&p, (size_t)H);
+        for (auto& p : m->fz) aa.add(&p, (size_t)H);
+    }
     if (!c.causal) {
         aa.add(&m->enc_k, (size_t)T * m->kv);
         aa.add(&m->enc_v, (size_t)T * m->kv);
@@ -337,6 +358,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
             launch_bf16_to_f16_inplace(L.wo, (long long)H * m->q, s);
             launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, s);
             launch_bf16_to_f16_inplace(L.wd, (long long)H * F, s);
+            if (L.wdT) launch_transpose16(L.wd, L.wdT, H, F, s);
         }
         launch_bf16_to_f32(W.attn_norm, L.attn_norm, H, s);
         launch_bf16_to_f32(W.mlp_norm, L.mlp_norm, H, s);
@@ -427,6 +449,7 @@ void ember_model_destroy(ember_model* m) {
     if (!m) return;
     cudaDeviceSynchronize();
     for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
+    for (ember_kv* kv : m->kvs) kv->m = nullptr;
     if (m->wblock) cudaFree(m->wblock);
     if (m->ablock) cudaFree(m->ablock);
     delete m;
@@ -439,6 +462,7 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
     if (!m->c.causal) return fail(EMBER_ERR_INVALID_ARG, "a bidirectional encoder has no KV cache");
     const size_t half = ember_kv_bytes(&m->c, max_seqs, max_len) / 2;
     ember_kv* kv = new ember_kv();
+    kv->gen = ++g_kv_gen;
     kv->m = m;
     kv->max_seqs = max_seqs;
     kv->max_len = max_len;
@@ -476,10 +500,15 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
         const uint64_t ks[2] = {(uint64_t)c.head_dim * 2, (uint64_t)max_len * c.head_dim * 2};
         const uint32_t kb[3] = {64, 128, 1};
         kv->k_map_ok = encode_map_bf16(kv->k_map, kv->k, 3, kd, ks, kb);
-        if (!kv->k_map_ok) {
+        kv->v_map_ok = encode_map_bf16(kv->v_map, kv->v, 3, kd, ks, kb);
+        if (!kv->k_map_ok || !kv->v_map_ok) {
             ember_kv_free(kv);
-            return fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (K cache)");
+            return fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (KV cache)");
         }
+    }
+    {
+        std::lock_guard<std::mutex> lk(m->mu);
+        m->kvs.push_back(kv);
     }
     *out = kv;
     return EMBER_OK;
@@ -488,6 +517,24 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
 void ember_kv_free(ember_kv* kv) {
     if (!kv) return;
     cudaDeviceSynchronize();
+    if (kv->m) {   // decode graphs captured against this cache point at its memory
+        std::lock_guard<std::mutex> lk(kv->m->mu);
+        auto& ks = kv->m->kvs;
+        for (auto it = ks.begin(); it != ks.end(); ++it)
+            if (*it == kv) {
+                ks.erase(it);
+                break;
+            }
+        auto& gs = kv->m->graphs;
+        for (auto it = gs.begin(); it != gs.end();) {
+            if (it->kv_gen == kv->gen) {
+                cudaGraphExecDestroy(it->exec);
+                it = gs.erase(it);
+            } else {
+                ++it;
+            }
+        }
+    }
     cudaFree(kv->k);
     cudaFree(kv->v);
     cudaFree(kv->cursor);
@@ -516,6 +563,7 @@ ember_status ember_kv_set_cursor(ember_kv* kv, int32_t seq, int32_t pos, ember_s
 ember_status ember_kv_layout(const ember_kv* kv, const uint16_t** k_base, const uint16_t** v_base,
                              int64_t strides[4]) {
     if (!kv || !k_base || !v_base || !strides) return fail(EMBER_ERR_INVALID_ARG, "NULL argument");
+    if (!kv->m) return fail(EMBER_ERR_STATE, "the model of this cache was destroyed");
     const ember_config& c = kv->m->c;
     *k_base = kv->k;
     *v_base = kv->v;
@@ -776,6 +824,93 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         launch_persist(a, m->pk_grid, m->pk_smem, s);
         return;
     }
+    if (B == 1 && m->fp.ok && kv->k_map_ok && kv->v_map_ok) {
+        // two kernels per layer; kernel n reads fx[(n-1)%2] + fz[(n-1)%3], writes
+        // fx[n%2], zeroes fz[(n-2)%3] and accumulates into fz[n%3] (embed: n = 0)
+        ea.x = m->fx[0];
+        ea.zero0 = m->fz[0];
+        ea.zero1 = m->fz[1];
+        launch_embed(ea, s);
+        const FusedPlan& fp = m->fp;
+        int n = 1;
+        auto io = [&](const float*& xi, const float*& zi, float*& xo, float*& zz, float*& za) {
+            xi = m->fx[(n - 1) % 2];
+            zi = m->fz[(n - 1) % 3];
+            xo = m->fx[n % 2];
+            zz = m->fz[(n + 1) % 3];   // (n - 2) mod 3
+            za = m->fz[n % 3];
+            ++n;
+        };
+        for (int l = 0; l < c.layers; ++l) {
+            LayerDev& L = m->layers[l];
+            FusedAttnArgs a{};
+            a.wqkv = L.wqkv;
+            a.bqkv = c.qkv_bias ? L.bqkv : nullptr;
+            a.norm_w = L.attn_norm;
+            a.eps = eps;
+            a.q_norm = c.qk_norm ? L.q_norm : nullptr;
+            a.k_norm = c.qk_norm ? L.k_norm : nullptr;
+            a.wo = L.wo;
+            a.H = c.hidden;
+            a.NH = c.n_heads;
+            a.NKV = c.n_kv_heads;
+            a.D = c.head_dim;
+            a.L = c.layers;
+            a.layer = l;
+            io(a.x_in, a.z_in, a.x_out, a.z_zero, a.z_acc);
+            a.kc = kv->k;
+            a.vc = kv->v;
+            a.max_len = kv->max_len;
+            a.seqs = seqs;
+            a.tok_pos = m->tok_pos;
+            a.tok_ok = m->tok_ok;
+            a.cos_t = kv->cos_t;
+            a.sin_t = kv->sin_t;
+            a.status = m->status;
+            a.C = fp.C;
+            a.nr = fp.nr;
+            a.no = fp.no;
+            launch_fused_attn(kv->k_map, kv->v_map, a, fp.smem_attn, s);
+            FusedMlpArgs f{};
+            f.wgu = L.wgu;
+            f.wdT = L.wdT;
+            f.norm_w = L.mlp_norm;
+            f.eps = eps;
+            f.H = c.hidden;
+            f.F = c.ff;
+            io(f.x_in, f.z_in, f.x_out, f.z_zero, f.z_acc);
+            f.status = m->status;
+            f.ns = fp.ns;
+            launch_fused_mlp(f, fp.fc, fp.mlp_grid, fp.smem_mlp, s);
+        }
+        GemvArgs g{};
+        g.W = m->embed;
+        g.N = c.vocab;
+        g.K = c.hidden;
+        g.x = m->fx[(n - 1) % 2];
+        g.x_add = m->fz[(n - 1) % 3];
+        g.ldx = c.hidden;
+        g.norm_w = m->final_norm;
+        g.eps = eps;
+        g.out = logits;
+        g.ldo = c.vocab;
+        g.nb = 1;
+        g.mode = EPI_ARGMAX;
+        g.keys = m->keys;
+        g.status = m->status;
+        launch_gemv(g, s, m->sms);
+        FinishArgs f{};
+        f.nb = 1;
+        f.keys = m->keys;
+        f.argmax = argmax;
+        f.seqs = seqs;
+        f.positions = m->tok_pos;
+        f.tok_ok = m->tok_ok;
+        f.cursor = kv->cursor;
+        f.pf_seq = -1;
+        launch_finish(f, s);
+        return;
+    }
     launch_embed(ea, s);
     const bool gemv = B <= GEMV_MAX_BATCH;
     int splits = (2 * m->sms + B * c.n_kv_heads - 1) / (B * c.n_kv_heads);
@@ -943,7 +1078,7 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
         return EMBER_OK;
     }
     for (auto& g : m->graphs) {
-        if (g.batch == batch && g.seqs == seqs && g.ids == ids && g.pos == positions &&
+        if (g.kv_gen == kv->gen && g.batch == batch && g.seqs == seqs && g.ids == ids && g.pos == positions &&
             g.logits == logits && g.argmax == argmax) {
             CK(cudaGraphLaunch(g.exec, s));
             count_launches(g.kernels);
@@ -956,8 +1091,11 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
     decode_enqueue(m, kv, batch, seqs, ids, positions, logits, argmax, s);
     const long long kernels = (long long)launches_so_far() - before;
     count_launches(-kernels);   // captured, not run
+    const cudaError_t le = cudaGetLastError();   // a launch the capture rejected
     cudaError_t e = cudaStreamEndCapture(s, &graph);
-    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess)
+        return fail(EMBER_ERR_CUDA, "graph capture failed: %s (launch error: %s)", cudaGetErrorString(e),
+                    cudaGetErrorString(le));
     cudaGraphExec_t exec = nullptr;
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
@@ -966,7 +1104,7 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
         cudaGraphExecDestroy(m->graphs.front().exec);
         m->graphs.erase(m->graphs.begin());
     }
-    m->graphs.push_back({batch, seqs, ids, positions, logits, argmax, exec, kernels});
+    m->graphs.push_back({kv->gen, batch, seqs, ids, positions, logits, argmax, exec, kernels});
     CK(cudaGraphLaunch(exec, s));
     count_launches(kernels);
     return EMBER_OK;

@@ -51,6 +51,8 @@ struct EmbedArgs {
     int32_t* tok_pos;            // [n] resolved position (positions[t] or the cursor)
     // prefill check (pf_seq < 0: none)
     int pf_seq, pf_start;
+    float* zero0;                // [n][H] set to 0 when non-null (residual accumulators)
+    float* zero1;
 };
 void launch_embed(const EmbedArgs& a, cudaStream_t s);
 
@@ -72,6 +74,7 @@ struct GemvArgs {
     int mode;                    // EpiMode
     unsigned long long* keys;    // [nb] argmax keys (EPI_ARGMAX)
     int* status;
+    const float* x_add;          // [ldx] added to x (residual accumulator; nb == 1, bf16 W), or nullptr
 };
 void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms);
 
@@ -272,5 +275,69 @@ struct VtArgs {
     uint16_t* vt;
 };
 void launch_vt(const VtArgs& a, int zs, cudaStream_t s);
+
+// ------------------------------------------- fused batch-1 decode layer --
+// Two kernels per decoder layer (decode_fused.cu).  Residual stream of kernel
+// n: x_n = x_in + z_in; the kernel writes x_out = x_n, zeroes z_zero and adds
+// its output into z_acc (three rotating accumulators, two x buffers).
+struct FusedPlan {
+    int C = 0;           // CTAs per cluster (one cluster per kv head)
+    int nr = 0, no = 0;  // q/k/v rows and o_proj rows per CTA
+    int smem_attn = 0, smem_mlp = 0;
+    int ns = 0;          // weight ring stages of the MLP kernel
+    int fc = 0;          // intermediate features per MLP chunk (4, 8 or 16)
+    int mlp_grid = 0;
+    bool ok = false;
+    const char* why = "not planned";   // reason when !ok
+};
+bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int num_sms);
+
+struct FusedAttnArgs {
+    const uint16_t* wqkv;        // f16 [q rows | k rows | v rows][H]
+    const float* bqkv;           // or nullptr
+    const float* norm_w;
+    float eps;
+    const float* q_norm;         // [D] or nullptr (then k_norm unused)
+    const float* k_norm;
+    const uint16_t* wo;          // f16 [H][NH*D]
+    int H, NH, NKV, D, L, layer;
+    const float* x_in;
+    const float* z_in;
+    float* x_out;
+    float* z_zero;
+    float* z_acc;
+    uint16_t* kc;                // K / V cache [seq][layer][kv head][max_len][D] bf16
+    uint16_t* vc;
+    int max_len;
+    const int32_t* seqs;
+    const int32_t* tok_pos;
+    const int* tok_ok;
+    const float* cos_t;
+    const float* sin_t;
+    int* status;
+    int C, nr, no;
+};
+// k_map / v_map: 3-D TMA maps (D, max_len, seqs*layers*kv heads), box 64 x 128 x 1
+void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int smem,
+                       cudaStream_t s);
+
+struct FusedMlpArgs {
+    const uint16_t* wgu;         // f16 [2F][H], row 2f gate_f, row 2f+1 up_f
+    const uint16_t* wdT;         // f16 [F][H] (down_proj transposed)
+    const float* norm_w;
+    float eps;
+    int H, F;
+    const float* x_in;
+    const float* z_in;
+    float* x_out;
+    float* z_zero;
+    float* z_acc;
+    int* status;
+    int ns;
+};
+void launch_fused_mlp(const FusedMlpArgs& a, int fc, int grid, int smem, cudaStream_t s);
+
+// out[c][r] = in[r][c] for 16-bit elements
+void launch_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols, cudaStream_t s);
 
 }  // namespace ember

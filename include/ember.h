@@ -134,6 +134,9 @@ size_t ember_kv_bytes(const ember_config *cfg, int32_t max_seqs, int32_t max_len
  * positions.  Errors: INVALID_ARG (max_seqs or max_len <= 0, encoder model),
  * OOM, CUDA. */
 ember_status ember_kv_alloc(ember_model *m, int32_t max_seqs, int32_t max_len, ember_kv **out);
+/* Synchronises the device, frees the cache and drops the decode graphs
+ * captured against it.  A cache may outlive its model (it is then only good
+ * for ember_kv_free; ember_kv_layout returns STATE). */
 void ember_kv_free(ember_kv *kv);
 
 /* Set sequence seq's cursor to 0 (its rows are left as they are and are

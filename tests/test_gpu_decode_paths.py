@@ -1,6 +1,8 @@
-"""Parity of the persistent weight-streaming batch-1 decode kernel (opt-in
-with EMBER_PERSIST=1), run in a child process so the switch is read at model
-creation: same greedy continuation and logits as the oracle."""
+"""Parity of the alternative batch-1 decode paths, each run in a child process
+so its switch is read at model creation: the persistent weight-streaming
+kernel (opt-in, EMBER_PERSIST=1) and the chained per-projection kernels
+(EMBER_NO_FUSED=1, the path batch 2..8 takes): same greedy continuation and
+logits as the oracle."""
 import os
 import subprocess
 import sys
@@ -24,7 +26,11 @@ shapes = [synth.TINY,
                            head_dim=32, ff=512, rope_theta=5e5, rope_llama3=1, rs_factor=32.0,
                            rs_low=1.0, rs_high=4.0, rs_orig_max_pos=64),
           synth.ModelShape("s-qk", vocab=400, hidden=256, layers=2, n_heads=4, n_kv_heads=2,
-                           head_dim=128, ff=384, rope_theta=1e6, qk_norm=1)]
+                           head_dim=128, ff=384, rope_theta=1e6, qk_norm=1),
+          synth.ModelShape("s-d64", vocab=700, hidden=192, layers=2, n_heads=6, n_kv_heads=2,
+                           head_dim=64, ff=256, rope_theta=1e6, qkv_bias=1)]
+from gqa_transformer_decode_gb300 import ember as E
+persist = %(persist)r
 s = torch.cuda.Stream()
 for shape in shapes:
     w = synth.weights_bf16(shape)
@@ -40,20 +46,28 @@ for shape in shapes:
         m.prefill(kv, 0, torch.as_tensor(prompt).cuda(), 0, logits=lg[0], argmax=am[0:1], stream=s)
         seqs = torch.zeros(1, dtype=torch.int32, device="cuda")
         for i in range(1, n + 1):
+            if i == n:
+                s.synchronize()
+                l0 = E.ember_kernel_launches()
             m.decode_step(kv, seqs, torch.tensor([toks[i - 1]], dtype=torch.int32, device="cuda"),
                           None, logits=lg[i], argmax=am[i:i + 1], stream=s)
     assert m.sync_status(s) == 0
+    # which path ran: one persistent kernel, or embed + 5 per layer + head + finish
+    launches = E.ember_kernel_launches() - l0
+    assert launches == (1 if persist else 5 * shape.layers + 3), (shape.name, launches)
     glg, gam = lg.cpu().numpy(), am.cpu().numpy()
     assert_close(olg, glg, shape.name + " logits")
     assert_tokens(olg, toks, gam, shape.name + " tokens")
     assert all(gam[i] == first_argmax(glg[i]) for i in range(n + 1))
-print("persistent ok")
+print("decode path ok")
 """
 
 
-def test_persistent_decode_kernel_matches_oracle():
-    env = dict(os.environ, EMBER_PERSIST="1")
-    code = CHILD % {"root": ROOT, "tests": os.path.join(ROOT, "tests")}
+@pytest.mark.parametrize("switch", ["EMBER_PERSIST", "EMBER_NO_FUSED"])
+def test_alternative_decode_path_matches_oracle(switch):
+    env = dict(os.environ, **{switch: "1"})
+    code = CHILD % {"root": ROOT, "tests": os.path.join(ROOT, "tests"),
+                    "persist": switch == "EMBER_PERSIST"}
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
-    assert r.returncode == 0 and "persistent ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+    assert r.returncode == 0 and "decode path ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]

@@ -272,3 +272,53 @@ def test_tensor_core_chunked_prefill(stream):
     assert_close(olg[[199, 419]], lg[:2].cpu().numpy(), "chunked prefill logits")
     h_full, _, _ = om.forward_full(prompt, logits=False)
     assert_close(h_full[200:], hid.cpu().numpy(), "second chunk hidden")
+
+
+@pytest.mark.parametrize("shape,n_prompt,n_steps,seq", [(MID_QWEN2, 1, 20, 0),
+                                                        (MID_LLAMA, 2100, 6, 1),
+                                                        (MID_D128, 300, 8, 1)])
+def test_fused_batch1_decode_matches_oracle(shape, n_prompt, n_steps, seq, stream):
+    """Batch-1 decode on the two-kernels-per-layer path (head_dim 64 / 128): one
+    key, a context of more than 16 tiles of 128 keys (every CTA of a cluster
+    loops over two tiles), q/k norm with head_dim 128; second cache slot."""
+    w, om, gm = model_pair(shape, max_tokens=max(512, n_prompt + 16))
+    prompt = synth.prompt_ids(shape, n_prompt)
+    toks, olg, _ = om.greedy(prompt, n_steps)
+    kv = gm.kv_alloc(2, n_prompt + n_steps + 8)
+    glg, gam, _ = run_greedy_gpu(gm, kv, prompt, n_steps, toks[:-1], stream, seq=seq)
+    assert_close(olg, glg, "logits")
+    assert_tokens(olg, toks, gam, "greedy tokens")
+    for i in range(n_steps + 1):
+        assert gam[i] == first_argmax(glg[i])
+    # the step ran as embed + two kernels per layer + LM head + finish
+    from gqa_transformer_decode_gb300 import ember as E
+    pos = n_prompt + n_steps
+    l0 = E.ember_kernel_launches()
+    with torch.cuda.stream(stream):
+        gm.decode_step(kv, i32([seq]), i32([toks[-1]]), i32([pos]), stream=stream)
+    assert gm.sync_status(stream) == 0
+    assert E.ember_kernel_launches() - l0 == 2 * shape.layers + 3
+
+
+@pytest.mark.parametrize("shape", [SMALL_QWEN2, MID_QWEN2])
+def test_decode_graph_follows_a_new_cache_with_the_same_buffers(shape, stream):
+    """A decode graph is bound to the KV cache it was captured against: the same
+    seqs / ids / argmax tensors used with a second cache (after the first one
+    is freed) must read and write the second cache."""
+    w, om, gm = model_pair(shape)
+    seqs, cur = i32([0]), i32([0])
+    got = []
+    for k, n_prompt in enumerate((11, 23)):
+        prompt = synth.prompt_ids(shape, n_prompt, seq=k)
+        kv = gm.kv_alloc(1, 64 + 40 * k)   # another row stride: a stale graph misreads it
+        out = torch.empty(5, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            gm.prefill(kv, 0, i32(prompt), 0, argmax=cur, stream=stream)
+            out[0:1].copy_(cur)
+            for i in range(1, 5):
+                gm.decode_step(kv, seqs, cur, None, argmax=cur, stream=stream)
+                out[i:i + 1].copy_(cur)
+        assert gm.sync_status(stream) == 0
+        toks, olg, _ = om.greedy(prompt, 4)
+        assert_tokens(olg, toks, out.cpu().numpy(), f"cache {k} greedy")
+        kv.close()
