@@ -61,6 +61,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+// 16-byte shared-memory load (explicit state space: short-scoreboard path)
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
 __device__ __forceinline__ void red_add(float* p, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -173,7 +181,7 @@ __device__ __forceinline__ float wdot_f16(const uint4* row, const XRegs& x, int 
         const int c = lane + 32 * i;
         if (c < n8) {
             float w[8], xf[8];
-            unpack8_f16(row[c], w);
+            unpack8_f16(lds128(row + c), w);
             unpack8_f16(x.v[i], xf);
 #pragma unroll
             for (int u = 0; u < 8; ++u) s[u] = fmaf(w[u], xf[u], s[u]);
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
 #pragma unroll
         for (int j = 0; j < FC; ++j) {
             const float gt = s_g[k & 1][2 * j], up = s_g[k & 1][2 * j + 1];
-            act[j] = gt / (1.f + __expf(-gt)) * up;
+            act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
         }
         const uint4* wd = reinterpret_cast<const uint4*>(st + (size_t)4 * FC * H);
 #pragma unroll
@@ -612,7 +620,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
 #pragma unroll
                 for (int j = 0; j < FC; ++j) {
                     float w[8];
-                    unpack8_f16(wd[(size_t)j * H8 + hg], w);
+                    unpack8_f16(lds128(wd + (size_t)j * H8 + hg), w);
 #pragma unroll
                     for (int u = 0; u < 8; ++u) y[q][u] = fmaf(w[u], act[j], y[q][u]);
                 }

@@ -48,7 +48,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * GEMM_BM;
-    const int nk = (K + GEMM_BK - 1) / GEMM_BK;
+    // this CTA's k-blocks [kb0, kb0 + nk) (split-K over grid.z)
+    const int nk_all = (K + GEMM_BK - 1) / GEMM_BK;
+    const int per = (nk_all + (int)gridDim.z - 1) / (int)gridDim.z;
+    const int kb0 = (int)blockIdx.z * per;
+    const int nk = max(0, min(nk_all, kb0 + per) - kb0);
+    const bool split = gridDim.z > 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -90,8 +95,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 uint8_t* sa = smem + s * STAGE_BYTES;
                 mbar_expect_tx(&full[s], STAGE_BYTES);
-                tma_load_2d(sa, &tmA, kb * GEMM_BK, m0, &full[s]);
-                tma_load_2d(sa + A_BYTES, &tmB, kb * GEMM_BK, n0, &full[s]);
+                tma_load_2d(sa, &tmA, (kb0 + kb) * GEMM_BK, m0, &full[s]);
+                tma_load_2d(sa + A_BYTES, &tmB, (kb0 + kb) * GEMM_BK, n0, &full[s]);
             }
             sflag[1] = kb;
         }
@@ -121,6 +126,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else {   // ---------------- epilogue warps 2..5
         const int q = warp & 3;
         const int row = m0 + q * 32 + lane;
+        unsigned long long best = 0ull;   // EPI_ARGMAX
         if (!mbar_wait(tfull, 0)) {
             sflag[0] = 1;
         } else {
@@ -132,12 +138,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tmem_ld16(tbase + c + 16, r + 16);
                 tmem_ld_wait();
                 const int n = n0 + c;
-                if (row >= M || n >= N) continue;
+                if (row >= M || n >= N || nk == 0) continue;
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                 const bool fullc = (n + 32 <= N);
-                if (e.mode == EPI_SWIGLU) {
+                if (e.mode == EPI_ARGMAX) {   // logits (optional) and the row's best key
+                    if (e.out_f32) {
+                        float* o = e.out_f32 + (size_t)row * e.ldo + n;
+                        for (int i = 0; i < 32 && n + i < N; ++i) o[i] = v[i];
+                    }
+                    for (int i = 0; i < 32 && n + i < N; ++i) {
+                        const unsigned long long kk = argmax_key(v[i], (uint32_t)(n + i));
+                        best = kk > best ? kk : best;
+                    }
+                } else if (split) {   // partial sums of a K split: add into the output
+                    float* o = e.out_f32 + (size_t)row * e.ldo + n;
+                    if (e.mode == EPI_STORE && e.bias && blockIdx.z == 0) {
+                        for (int i = 0; i < 32; ++i)
+                            if (n + i < N) v[i] += e.bias[n + i];
+                    }
+                    if (fullc) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(o + 4 * i),
+                                         "f"(v[4 * i]), "f"(v[4 * i + 1]), "f"(v[4 * i + 2]),
+                                         "f"(v[4 * i + 3])
+                                         : "memory");
+                    } else {
+                        for (int i = 0; i < 32 && n + i < N; ++i) atomicAdd(o + i, v[i]);
+                    }
+                } else if (e.mode == EPI_SWIGLU) {
                     // columns 2i / 2i+1 = gate_i / up_i -> output column n/2 + i
                     uint16_t* o = e.out_h + (size_t)row * e.ldo + (n >> 1);
                     if (fullc) {
@@ -181,6 +212,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
+            if (e.mode == EPI_ARGMAX && row < M && best) atomicMax(e.keys + row, best);
         }
     }
 
@@ -258,13 +290,29 @@ bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16
     p.N = N;
     p.K = K;
     p.bn = pick_bn(N);
-    p.ok = make_map(p.tmA, A, M, lda, K, GEMM_BM) && make_map(p.tmB, B, N, ldb, K, p.bn);
+    int dev = 0;
+    p.sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev);
+    p.ok = make_map(p.tmA, A, M, lda, K, GEMM_BM) && make_map(p.tmB, B, N, ldb, K, p.bn) &&
+           make_map(p.tmB64, B, N, ldb, K, 64);
     return p.ok;
+}
+
+int gemm_splits(const GemmPlan& p, int m_rows, int mode) {
+    if (m_rows > GEMM_BM || (mode != EPI_STORE && mode != EPI_RESID)) return 1;
+    const int tiles = (p.N + 63) / 64;
+    const int nk = (p.K + GEMM_BK - 1) / GEMM_BK;
+    int ks = p.sms / tiles;
+    if (ks > nk) ks = nk;
+    if (ks <= 1) return 1;
+    const int per = (nk + ks - 1) / ks;
+    return (nk + per - 1) / per;   // no empty split
 }
 
 template <int BN, int STAGES>
 static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
-                      cudaStream_t s) {
+                      cudaStream_t s, int ksplit = 1) {
     constexpr int STAGE_BYTES = (GEMM_BM + BN) * GEMM_BK * 2;
     constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
     static bool attr = false;
@@ -273,9 +321,9 @@ static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int*
                              SMEM);
         attr = true;
     }
-    dim3 grid((p.N + BN - 1) / BN, (m_rows + GEMM_BM - 1) / GEMM_BM);
+    dim3 grid((p.N + BN - 1) / BN, (m_rows + GEMM_BM - 1) / GEMM_BM, ksplit);
     const CUtensorMap* ta = reinterpret_cast<const CUtensorMap*>(p.tmA);
-    const CUtensorMap* tb = reinterpret_cast<const CUtensorMap*>(p.tmB);
+    const CUtensorMap* tb = reinterpret_cast<const CUtensorMap*>(BN == p.bn ? p.tmB : p.tmB64);
     const uint32_t idesc = p.f16 ? idesc_f16(GEMM_BM, BN) : idesc_bf16(GEMM_BM, BN);
     launch_k(k_gemm_tc<BN, STAGES>, grid, dim3(GEMM_THREADS), SMEM, s, *ta, *tb, m_rows, p.N, p.K,
              idesc, e, status);
@@ -284,6 +332,14 @@ static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int*
 void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
                  cudaStream_t s) {
     if (m_rows <= 0) return;
+    if (m_rows <= GEMM_BM) {   // one row tile: narrow tiles, K split for the additive epilogues
+        GemmEpilogue e2 = e;
+        int ks = gemm_splits(p, m_rows, e.mode);
+        if (e.mode == EPI_STORE && !e.zeroed) ks = 1;
+        e2.ksplit = ks;
+        launch_bn<64, 8>(p, m_rows, e2, status, s, ks);
+        return;
+    }
     switch (p.bn) {
         case 64: launch_bn<64, 8>(p, m_rows, e, status, s); break;
         case 128: launch_bn<128, 6>(p, m_rows, e, status, s); break;

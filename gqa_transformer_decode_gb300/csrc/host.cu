@@ -913,7 +913,8 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     }
     launch_embed(ea, s);
     const bool gemv = B <= GEMV_MAX_BATCH;
-    int splits = (2 * m->sms + B * c.n_kv_heads - 1) / (B * c.n_kv_heads);
+    // enough (token, kv head, split) CTAs for ~8 per SM streaming the cache
+    int splits = (8 * m->sms + B * c.n_kv_heads - 1) / (B * c.n_kv_heads);
     splits = splits < 1 ? 1 : (splits > MAX_SPLITS ? MAX_SPLITS : splits);
     for (int l = 0; l < c.layers; ++l) {
         LayerDev& L = m->layers[l];
@@ -940,6 +941,10 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             e.out_f32 = m->qkv;
             e.ldo = m->qkv_n;
             e.bias = c.qkv_bias ? L.bqkv : nullptr;
+            if (gemm_splits(L.p_qkv, B, EPI_STORE) > 1) {   // split K adds into a zeroed output
+                cudaMemsetAsync(m->qkv, 0, (size_t)B * m->qkv_n * 4, s);
+                e.zeroed = 1;
+            }
             launch_gemm(L.p_qkv, B, e, m->status, s);
         }
         AttnDecodeArgs a{};
@@ -1028,8 +1033,18 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             launch_gemm(L.p_d, B, e, m->status, s);
         }
     }
-    // LM head + argmax, in groups of GEMV_MAX_BATCH tokens
-    for (int b0 = 0; b0 < B; b0 += GEMV_MAX_BATCH) {
+    // LM head + argmax: the split GEMV for up to GEMV_MAX_BATCH tokens, else one
+    // tensor-core GEMM over the bf16 final states (the vocabulary is read once)
+    if (!gemv) {
+        launch_rmsnorm_bf16(m->x, m->final_norm, eps, B, c.hidden, m->hb, s);
+        GemmEpilogue e{};
+        e.mode = EPI_ARGMAX;
+        e.out_f32 = logits;
+        e.ldo = c.vocab;
+        e.keys = m->keys;
+        launch_gemm(m->p_head, B, e, m->status, s);
+    }
+    for (int b0 = 0; gemv && b0 < B; b0 += GEMV_MAX_BATCH) {
         GemvArgs g{};
         g.W = m->embed;
         g.N = c.vocab;

@@ -163,6 +163,9 @@ cudaError_t launch_persist(const PersistArgs& a, int grid, int smem, cudaStream_
 // xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s);
+// xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tied-head GEMM)
+void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+                         cudaStream_t s);
 // h[t] = RMSNorm(x[t]) * w  in f32
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
                         cudaStream_t s);
@@ -218,18 +221,23 @@ void launch_bf16_to_f16_inplace(uint16_t* p, long long n, cudaStream_t s);
 // D[M,N] = A[M,K] . B[N,K]^T (bf16 in, f32 accumulate in TMEM) with a fused
 // epilogue.  A and B are described by TMA tensor maps made by make_gemm_plan.
 struct GemmEpilogue {
-    int mode;                    // EpiMode (EPI_STORE, EPI_RESID, EPI_SWIGLU)
-    float* out_f32;              // EPI_STORE / EPI_RESID: [M][ldo]
+    int mode;                    // EpiMode (EPI_STORE, EPI_RESID, EPI_SWIGLU, EPI_ARGMAX)
+    float* out_f32;              // EPI_STORE / EPI_RESID: [M][ldo]; EPI_ARGMAX: logits or nullptr
     uint16_t* out_h;             // EPI_SWIGLU: [M][ldo] f16 (N/2 columns)
     int ldo;
     const float* bias;           // EPI_STORE, nullable
+    unsigned long long* keys;    // EPI_ARGMAX: [M] argmax keys (start at 0)
+    int ksplit;                  // set by launch_gemm: K split over grid.z (red.add outputs)
+    int zeroed;                  // EPI_STORE: out_f32 is zero, so K may be split
 };
 
 struct GemmPlan {
     alignas(64) unsigned char tmA[128];
     alignas(64) unsigned char tmB[128];
+    alignas(64) unsigned char tmB64[128];   // B with a 64-row box (few-row A, split-K)
     int M, N, K;
     int bn;                      // N tile (64, 128 or 256)
+    int sms;                     // SMs of the device the plan was made on
     bool f16;                    // operands f16 (else bf16)
     bool ok;
 };
@@ -238,6 +246,11 @@ struct GemmPlan {
 // the tensor maps.
 bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16_t* B, int N,
                     int ldb, int K, bool f16);
+// For m_rows <= 128 (one row tile) the GEMM runs with 64-column tiles and,
+// for EPI_STORE / EPI_RESID, splits K across CTAs until about one CTA per SM;
+// the partial sums are added with red.global.add, so EPI_STORE then needs a
+// zeroed output.  gemm_splits() returns the split launch_gemm will use.
+int gemm_splits(const GemmPlan& p, int m_rows, int mode);
 // Encode a bf16 TMA tensor map (rank 2..4, 128-byte swizzle, zero fill out
 // of bounds).  dims[0] is the contiguous dimension; strides (rank-1 entries)
 // are in bytes.  False if the driver rejects it.

@@ -12,7 +12,8 @@
 namespace ember {
 
 // ============================================================ RMSNorm rows ==
-template <bool BF16>
+// OUT: 0 = f32, 1 = f16 (projection GEMM operand), 2 = bf16 (tied-head GEMM operand)
+template <int OUT>
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w, float eps, int H,
                                                  void* out) {
     __shared__ float red[32];
@@ -24,10 +25,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
     ss = block_sum(ss, red);
     const float ri = rsqrtf(ss / (float)H + eps);
-    if (BF16) {
+    if (OUT == 1) {
         uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
         for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
             o[i] = pack_f16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
+    } else if (OUT == 2) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
+        for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
+            o[i] = pack_bf16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
     } else {
         float* o = static_cast<float*>(out) + (size_t)t * H;
         for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = xr[i] * ri * w[i];
@@ -36,11 +41,15 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
 
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
-    launch_k(k_rmsnorm<true>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
+    launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
+}
+void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
+                         cudaStream_t s) {
+    launch_k(k_rmsnorm<2>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
 }
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
                         cudaStream_t s) {
-    launch_k(k_rmsnorm<false>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h);
+    launch_k(k_rmsnorm<0>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h);
 }
 
 // =================================================== q/k norm, RoPE, K/V write ==
