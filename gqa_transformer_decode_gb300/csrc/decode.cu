@@ -381,19 +381,40 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) acc[i] = 0.f;
 
+    // K/V tiles are loaded into registers one tile ahead (all of a tile's
+    // 16-byte loads in flight together) and stored to shared memory when
+    // the tile's turn comes.
+    constexpr int C8 = D / 8;
+    constexpr int PER = (ATT_TK * C8 + ATT_THREADS - 1) / ATT_THREADS;
+    uint4 kr[PER], vr[PER];
+    auto load_tile = [&](int t0) {
+        const int nt = min(ATT_TK, hi - t0);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = tid + u * ATT_THREADS;
+            if (e < nt * C8) {
+                const int j = e / C8, cc = e % C8;
+                kr[u] = __ldcg(reinterpret_cast<const uint4*>(kc + (size_t)(t0 + j) * D + cc * 8));
+                vr[u] = __ldcg(reinterpret_cast<const uint4*>(vc + (size_t)(t0 + j) * D + cc * 8));
+            }
+        }
+    };
+    if (lo < hi) load_tile(lo);
     for (int t0 = lo; t0 < hi; t0 += ATT_TK) {
         const int nt = min(ATT_TK, hi - t0);
-        // stage K (padded rows) and V
-        constexpr int C8 = D / 8;
-        for (int e = tid; e < nt * C8; e += ATT_THREADS) {
-            const int j = e / C8, c = e % C8;
-            const uint4 kv4 = *reinterpret_cast<const uint4*>(kc + (size_t)(t0 + j) * D + c * 8);
-            const uint4 vv4 = *reinterpret_cast<const uint4*>(vc + (size_t)(t0 + j) * D + c * 8);
-            uint32_t* kd = reinterpret_cast<uint32_t*>(&s_k[j][c * 8]);
-            kd[0] = kv4.x; kd[1] = kv4.y; kd[2] = kv4.z; kd[3] = kv4.w;
-            *reinterpret_cast<uint4*>(&s_v[j][c * 8]) = vv4;
+        // stage K (padded rows) and V from the registers, then fetch the next tile
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = tid + u * ATT_THREADS;
+            if (e < nt * C8) {
+                const int j = e / C8, cc = e % C8;
+                uint32_t* kd = reinterpret_cast<uint32_t*>(&s_k[j][cc * 8]);
+                kd[0] = kr[u].x; kd[1] = kr[u].y; kd[2] = kr[u].z; kd[3] = kr[u].w;
+                *reinterpret_cast<uint4*>(&s_v[j][cc * 8]) = vr[u];
+            }
         }
         __syncthreads();
+        if (t0 + ATT_TK < hi) load_tile(t0 + ATT_TK);
         // scores: thread -> key j = tid % 64, heads h = tid/64, +2, ...
         {
             const int j = tid % ATT_TK;
@@ -521,6 +542,10 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
 }
 
 void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s) {
+    if (attn_decode_mma_supported(a.D, a.NH / a.NKV)) {
+        launch_attn_decode_mma(a, s);
+        return;
+    }
     dim3 grid(a.splits < ATT_MAX_SPLITS ? a.splits : ATT_MAX_SPLITS, a.NKV, a.nb);
     switch (a.D) {
         case 16: launch_k(k_attn_decode<16>, grid, dim3(ATT_THREADS), 0, s, a); break;

@@ -105,6 +105,10 @@ struct AttnDecodeArgs {
     int* status;
 };
 void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s);
+// The same on the warp tensor cores (decode_attn_mma.cu): head_dim 64 / 128,
+// at most 16 query heads per kv head.  launch_attn_decode picks it.
+bool attn_decode_mma_supported(int D, int G);
+void launch_attn_decode_mma(const AttnDecodeArgs& a, cudaStream_t s);
 
 // Greedy argmax write-back and cursor advance at the end of a step.
 struct FinishArgs {
