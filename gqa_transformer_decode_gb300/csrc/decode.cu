@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
 }
 
 void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s) {
-    if (attn_decode_mma_supported(a.D, a.NH / a.NKV)) {
+    if (a.k_map && a.v_map && attn_decode_mma_supported(a.D, a.NH / a.NKV)) {
         launch_attn_decode_mma(a, s);
         return;
     }

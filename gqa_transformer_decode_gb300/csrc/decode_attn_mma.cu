@@ -2,17 +2,20 @@
 // (head_dim 64 / 128, up to 16 query heads per kv head).
 //
 // One CTA = (token b, kv head g, key split); 4 warps.  The G query heads of
-// the group are the 16-row A operand (rows >= G are zero): per 64-key tile,
-// warp w takes keys 16w..16w+15 and computes S = Q K^T with mma.m16n8k16
+// the group are the 16-row A operand (rows >= G are zero): per 128-key tile,
+// warp w takes keys 32w..32w+31 in two blocks of 16 and computes S = Q K^T with mma.m16n8k16
 // (f16 operands, f32 accumulators; K fragments by ldmatrix from a swizzled
 // shared tile), keeps an online softmax per row in the base-2 domain, packs P
 // to f16 in registers as the A operand of O += P V (V fragments by
 // ldmatrix.trans).  The four warps' states are merged in shared memory; the
 // split partials are merged by the last CTA of the (token, kv head) as in
-// the SIMT kernel.  K/V tiles are loaded one tile ahead into registers and
-// converted from the bf16 cache to f16 when stored.  The prologue (optional
+// the SIMT kernel.  K/V tiles of 128 keys stream through a 2-3 stage ring of
+// bulk tensor copies (bf16, 128-byte swizzle) issued as soon as the position
+// is known; fragments are converted to f16 in registers.  The prologue (optional
 // q/k RMSNorm, RoPE, the new K/V row written as bf16 by the split holding the
 // position) is that of grouped-query attention in the Llama / Qwen2 decoder.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -21,9 +24,10 @@ namespace ember {
 namespace {
 
 constexpr int AM_THREADS = 128;
-constexpr int AM_TK = 64;               // keys per tile, 16 per warp
+constexpr int AM_TK = 128;              // keys per tile (the TMA box height)
 constexpr int AM_MIN_CHUNK = 64;        // keys per split at least
 constexpr int AM_MAX_SPLITS = 32;       // partial buffer layout (same as the SIMT kernel)
+constexpr long long AM_WAIT = 1ll << 31;
 
 __device__ __forceinline__ uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -45,49 +49,78 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// a bf16 pair -> the same pair as f16 (round to nearest)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) { return pack_f16x2(bf16_lo(u), bf16_hi(u)); }
 
-// Byte offset of 16-byte chunk c of row r in a [rows][D] f16 tile whose
-// chunks are XOR-swizzled by (r & 7): ldmatrix reads 8 rows at one logical
-// chunk without bank conflicts.
+// Q tile: [16][D] f16, 16-byte chunk c of row r XOR-swizzled by (r & 7).
 template <int D>
-__device__ __forceinline__ int tile_off(int r, int c) {
+__device__ __forceinline__ int q_off(int r, int c) {
     return r * (D * 2) + ((c ^ (r & 7)) << 4);
 }
+// K / V tile as written by the 128-byte-swizzled TMA box (64 elements x 128
+// keys per box; D / 64 boxes side by side): element chunk c (8 values) of key r.
+__device__ __forceinline__ int kv_off(int r, int c) {
+    return (c >> 3) * (AM_TK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
-// 8 bf16 (one uint4) -> 8 f16 (one uint4)
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& u) {
-    uint4 o;
-    o.x = pack_f16x2(bf16_lo(u.x), bf16_hi(u.x));
-    o.y = pack_f16x2(bf16_lo(u.y), bf16_hi(u.y));
-    o.z = pack_f16x2(bf16_lo(u.z), bf16_hi(u.z));
-    o.w = pack_f16x2(bf16_lo(u.w), bf16_hi(u.w));
-    return o;
+__device__ __forceinline__ void mbar_expect_tx_(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                     uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sa(dst)),
+        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(sa(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool am_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = sa(bar);
+    uint32_t ok;
+    const long long t0 = clock64();
+    do {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    } while (clock64() - t0 < AM_WAIT);
+    return false;
 }
 
 template <int D>
 struct AmSmem {
-    static constexpr int TILE = AM_TK * D * 2;          // one f16 K (or V) tile
-    static constexpr int Q = 0;                          // [16][D] f16, swizzled
-    static constexpr int K0 = 16 * D * 2;                // 2 stages of K then V
-    static constexpr int V0 = K0 + 2 * TILE;
-    static constexpr int END = V0 + 2 * TILE;
-    // after the key loop the K/V area holds the warps' states [4][16][D + 2] f32
-    static_assert(4 * 16 * (D + 2) * 4 <= 4 * TILE, "merge scratch");
+    static constexpr int NS = D == 64 ? 3 : 2;           // ring stages
+    static constexpr int TILE = AM_TK * D * 2;           // one bf16 K (or V) tile
+    static constexpr int Q = 0;                          // [16][D] f16
+    static constexpr int R0 = 4096;                      // ring (1024-aligned)
+    static constexpr int BAR = R0 + NS * 2 * TILE;
+    static constexpr int END = BAR + 64;
+    // after the key loop the ring holds the warps' states [4][16][D + 2] f32
+    static_assert(4 * 16 * (D + 2) * 4 <= NS * 2 * TILE, "merge scratch");
+    static_assert(16 * D * 2 <= R0, "q tile");
     static constexpr int TOTAL = END + 1024;
 };
 
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a) {
-    constexpr int H2 = D / 2, C8 = D / 8, NT = D / 8, KS = D / 16;
-    constexpr int PER = AM_TK * C8 / AM_THREADS;     // 16-byte K (and V) chunks per thread and tile
+__global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_constant__ CUtensorMap k_map,
+                                                              const __grid_constant__ CUtensorMap v_map,
+                                                              AttnDecodeArgs a) {
+    constexpr int H2 = D / 2, C8 = D / 8, NT = D / 8, KS = D / 16, NSUB = D / 64;
     using L = AmSmem<D>;
+    constexpr int NS = L::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
     __shared__ float s_q[16][D];
     __shared__ float s_kv[2][D];
-    __shared__ int s_last;
+    __shared__ float s_cs[D];            // RoPE row of pos: cos | sin
+    __shared__ int s_last, s_err;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = a.NH / a.NKV;
@@ -95,8 +128,9 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
 
     pdl_trigger();
     pdl_wait();
-    if (!__ldcg(a.tok_ok + b)) return;   // the embed kernel flagged this token
-    const int pos = __ldcg(a.positions + b);
+    const int tok_ok = __ldcg(a.tok_ok + b);
+    const int pos = __ldcg(a.positions + b);   // both loads in flight together
+    if (!tok_ok) return;   // the embed kernel flagged this token
     const int seq = a.seqs[b];
     const int n_keys = pos + 1;
     int per = (n_keys + gridDim.x - 1) / gridDim.x;
@@ -105,10 +139,29 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
     if (split >= S) return;
     const int lo = split * per;
     const int hi = min(n_keys, lo + per);
+    const int n_tiles = (hi - lo + AM_TK - 1) / AM_TK;
+    const int kz = (seq * a.L + a.layer) * a.NKV + g;   // (seq, layer, kv head) plane of the maps
+    auto issue = [&](int it) {   // tile it -> stage it % NS
+        const int st = it % NS;
+        uint8_t* kt = sm + L::R0 + st * 2 * L::TILE;
+        mbar_expect_tx_(&full[st], (uint32_t)(2 * L::TILE));
+#pragma unroll
+        for (int sb = 0; sb < NSUB; ++sb) {
+            tma3(kt + sb * AM_TK * 128, &k_map, sb * 64, lo + it * AM_TK, kz, &full[st]);
+            tma3(kt + L::TILE + sb * AM_TK * 128, &v_map, sb * 64, lo + it * AM_TK, kz, &full[st]);
+        }
+    };
+    if (tid == 0) {
+        s_err = 0;
+        for (int st = 0; st < NS; ++st)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&full[st])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int it = 0; it < NS && it < n_tiles; ++it) issue(it);
+    }
     const float* qkv = a.qkv + (size_t)b * a.ld_qkv;
     const float* cs = a.cos_t + (size_t)pos * H2;
     const float* sn = a.sin_t + (size_t)pos * H2;
-    const size_t head_off = (((size_t)seq * a.L + a.layer) * a.NKV + g) * (size_t)a.max_len * D;
+    const size_t head_off = (size_t)kz * a.max_len * D;
     uint16_t* kc = a.kc + head_off;
     uint16_t* vc = a.vc + head_off;
     const float qscale = 1.4426950408889634f * rsqrtf((float)D);   // scores in base 2
@@ -122,6 +175,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
         const int which = e / D, d = e % D;   // 0: k, 1: v
         s_kv[which][d] = __ldcg(qkv + (size_t)a.NH * D + (size_t)which * a.NKV * D + (size_t)g * D + d);
     }
+    for (int e = tid; e < D; e += AM_THREADS) s_cs[e] = e < H2 ? cs[e] : sn[e - H2];
     __syncthreads();
     if (a.q_norm) {
         for (int h = warp; h < G + 1; h += AM_THREADS / 32) {
@@ -140,7 +194,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
         const int h = e / H2, i = e % H2;
         float* v = h < G ? s_q[h] : s_kv[0];
         float r0, r1;
-        rope_pair(v[i], v[i + H2], cs[i], sn[i], r0, r1);
+        rope_pair(v[i], v[i + H2], s_cs[i], s_cs[H2 + i], r0, r1);
         if (h < G) {
             v[i] = r0 * qscale;
             v[i + H2] = r1 * qscale;
@@ -150,7 +204,8 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
         }
     }
     __syncthreads();
-    if (pos >= lo && pos < hi) {   // the split holding pos writes the new K/V row (bf16)
+    const bool owner = pos >= lo && pos < hi;
+    if (owner) {   // the split holding pos writes the new K/V row (bf16)
         for (int d = tid; d < D; d += AM_THREADS) {
             kc[(size_t)pos * D + d] = f32_to_bf16(s_kv[0][d]);
             vc[(size_t)pos * D + d] = f32_to_bf16(s_kv[1][d]);
@@ -159,70 +214,59 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
     for (int e = tid; e < 16 * C8; e += AM_THREADS) {   // q as the f16 A tile
         const int r = e / C8, c = e % C8;
         const float* q = &s_q[r][c * 8];
-        *reinterpret_cast<uint4*>(sm + L::Q + tile_off<D>(r, c)) =
+        *reinterpret_cast<uint4*>(sm + L::Q + q_off<D>(r, c)) =
             make_uint4(pack_f16x2(q[0], q[1]), pack_f16x2(q[2], q[3]), pack_f16x2(q[4], q[5]),
                        pack_f16x2(q[6], q[7]));
     }
-    __syncthreads();   // also orders the K/V row write before the tile loads below
+    __syncthreads();
     uint32_t qa[KS][4];
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
         const int mi = lane >> 3;
         const int r = (mi & 1) * 8 + (lane & 7), c = 2 * kk + (mi >> 1);
-        ldsm4(sa(sm + L::Q + tile_off<D>(r, c)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        ldsm4(sa(sm + L::Q + q_off<D>(r, c)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
 
-    // ---- keys [lo, hi) in tiles of 64, one tile ahead in registers ----
-    uint4 kr[PER], vr[PER];
-    auto load_tile = [&](int t0) {
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int e = tid + u * AM_THREADS;
-            const int j = e / C8, c = e % C8;
-            if (t0 + j < hi) {
-                kr[u] = __ldcg(reinterpret_cast<const uint4*>(kc + (size_t)(t0 + j) * D + c * 8));
-                vr[u] = __ldcg(reinterpret_cast<const uint4*>(vc + (size_t)(t0 + j) * D + c * 8));
-            } else {
-                kr[u] = make_uint4(0, 0, 0, 0);
-                vr[u] = make_uint4(0, 0, 0, 0);
-            }
-        }
-    };
-    auto store_tile = [&](int st) {
-#pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int e = tid + u * AM_THREADS;
-            const int j = e / C8, c = e % C8;
-            *reinterpret_cast<uint4*>(sm + L::K0 + st * L::TILE + tile_off<D>(j, c)) = bf16x8_to_f16x8(kr[u]);
-            *reinterpret_cast<uint4*>(sm + L::V0 + st * L::TILE + tile_off<D>(j, c)) = bf16x8_to_f16x8(vr[u]);
-        }
-    };
+    // ---- keys [lo, hi): tiles of 128 from the ring; warp w takes keys 32w..32w+31 ----
     float o[NT][4];
 #pragma unroll
     for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4 and lane/4 + 8
     const int g4 = lane >> 2, q4 = lane & 3;
-    int stg = 0;
-    if (lo < hi) load_tile(lo);
-    for (int t0 = lo; t0 < hi; t0 += AM_TK, stg ^= 1) {
-        store_tile(stg);
+    for (int it = 0; it < n_tiles; ++it) {
+        const int st = it % NS;
+        const int t0 = lo + it * AM_TK;
+        if (!am_wait(&full[st], (uint32_t)((it / NS) & 1))) s_err = 1;
+        uint8_t* kt = sm + L::R0 + st * 2 * L::TILE;
+        uint8_t* vt = kt + L::TILE;
+        if (owner && pos >= t0 && pos < t0 + AM_TK && tid < C8) {   // the row the copy read stale
+            const int r = pos - t0, c = tid;
+            const float* kk8 = &s_kv[0][c * 8];
+            const float* vv8 = &s_kv[1][c * 8];
+            *reinterpret_cast<uint4*>(kt + kv_off(r, c)) =
+                make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
+                           pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
+            *reinterpret_cast<uint4*>(vt + kv_off(r, c)) =
+                make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
+                           pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
+        }
         __syncthreads();
-        if (t0 + AM_TK < hi) load_tile(t0 + AM_TK);
-        const int kw = t0 + warp * 16;   // this warp's first key (valid when < hi)
-        if (kw < hi) {
-            const uint8_t* kt = sm + L::K0 + stg * L::TILE;
-            const uint8_t* vt = sm + L::V0 + stg * L::TILE;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            const int r0k = warp * 32 + blk * 16;       // first key row of this block in the tile
+            const int kw = t0 + r0k;
+            if (kw >= hi) continue;                     // warp-uniform
             float s[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {   // S = Q K^T over the warp's 16 keys
+            for (int kk = 0; kk < KS; ++kk) {   // S = Q K^T over 16 keys
                 const int mi = lane >> 3;
-                const int row = warp * 16 + (mi >> 1) * 8 + (lane & 7), c = 2 * kk + (mi & 1);
+                const int row = r0k + (mi >> 1) * 8 + (lane & 7), c = 2 * kk + (mi & 1);
                 uint32_t b0, b1, b2, b3;
-                ldsm4(sa(kt + tile_off<D>(row, c)), b0, b1, b2, b3);
-                mma16816(s[0], qa[kk], b0, b1);
-                mma16816(s[1], qa[kk], b2, b3);
+                ldsm4(sa(kt + kv_off(row, c)), b0, b1, b2, b3);
+                mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
+                mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
             }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -259,22 +303,24 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(AttnDecodeArgs a
 #pragma unroll
             for (int dn = 0; dn < NT; dn += 2) {   // O += P V
                 const int mi = lane >> 3;
-                const int row = warp * 16 + (mi & 1) * 8 + (lane & 7), c = dn + (mi >> 1);
+                const int row = r0k + (mi & 1) * 8 + (lane & 7), c = dn + (mi >> 1);
                 uint32_t r0, r1, r2, r3;
-                ldsm4t(sa(vt + tile_off<D>(row, c)), r0, r1, r2, r3);
-                mma16816(o[dn], pa, r0, r1);
-                mma16816(o[dn + 1], pa, r2, r3);
+                ldsm4t(sa(vt + kv_off(row, c)), r0, r1, r2, r3);
+                mma16816(o[dn], pa, bf2_to_h2(r0), bf2_to_h2(r1));
+                mma16816(o[dn + 1], pa, bf2_to_h2(r2), bf2_to_h2(r3));
             }
         }
-        __syncthreads();
+        __syncthreads();   // stage st fully read
+        if (tid == 0 && it + NS < n_tiles) issue(it + NS);
     }
+    if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
 
     // ---- merge the four warps: [4][16][D + 2] f32 = (m, l, O) per warp and row ----
     l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
     l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
     l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
     l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
-    float* ws = reinterpret_cast<float*>(sm + L::K0);   // the K/V tiles are no longer read
+    float* ws = reinterpret_cast<float*>(sm + L::R0);   // the ring is no longer read
     {
         float* w0 = ws + ((size_t)warp * 16 + g4) * (D + 2);
         float* w1 = ws + ((size_t)warp * 16 + g4 + 8) * (D + 2);
@@ -376,6 +422,8 @@ bool attn_decode_mma_supported(int D, int G) { return (D == 64 || D == 128) && G
 
 void launch_attn_decode_mma(const AttnDecodeArgs& a, cudaStream_t s) {
     dim3 grid(a.splits < AM_MAX_SPLITS ? a.splits : AM_MAX_SPLITS, a.NKV, a.nb);
+    const CUtensorMap& km = *reinterpret_cast<const CUtensorMap*>(a.k_map);
+    const CUtensorMap& vm = *reinterpret_cast<const CUtensorMap*>(a.v_map);
     if (a.D == 64) {
         static bool attr = false;
         if (!attr) {
@@ -383,7 +431,7 @@ void launch_attn_decode_mma(const AttnDecodeArgs& a, cudaStream_t s) {
                                  AmSmem<64>::TOTAL);
             attr = true;
         }
-        launch_k(k_attn_decode_mma<64>, grid, dim3(AM_THREADS), AmSmem<64>::TOTAL, s, a);
+        launch_k(k_attn_decode_mma<64>, grid, dim3(AM_THREADS), AmSmem<64>::TOTAL, s, km, vm, a);
     } else {
         static bool attr = false;
         if (!attr) {
@@ -391,7 +439,7 @@ void launch_attn_decode_mma(const AttnDecodeArgs& a, cudaStream_t s) {
                                  AmSmem<128>::TOTAL);
             attr = true;
         }
-        launch_k(k_attn_decode_mma<128>, grid, dim3(AM_THREADS), AmSmem<128>::TOTAL, s, a);
+        launch_k(k_attn_decode_mma<128>, grid, dim3(AM_THREADS), AmSmem<128>::TOTAL, s, km, vm, a);
     }
 }
 

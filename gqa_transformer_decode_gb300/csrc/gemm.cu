@@ -66,6 +66,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         sflag[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the weights (B) of the first stages do not depend on the previous
+        // kernel: start them now, under its tail
+        for (int kb = 0; kb < nk && kb < STAGES; ++kb) {
+            uint8_t* sa = smem + kb * STAGE_BYTES;
+            mbar_expect_tx(&full[kb], STAGE_BYTES);
+            tma_load_2d(sa + A_BYTES, &tmB, (kb0 + kb) * GEMM_BK, n0, &full[kb]);
+        }
     }
     if (warp == 1) {
         asm volatile(
@@ -89,14 +96,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (; kb < nk; ++kb) {
                 const int s = kb % STAGES;
                 const uint32_t it = (uint32_t)(kb / STAGES);
-                if (!mbar_wait(&empty[s], (it & 1u) ^ 1u)) {
-                    sflag[0] = 1;
-                    break;
-                }
                 uint8_t* sa = smem + s * STAGE_BYTES;
-                mbar_expect_tx(&full[s], STAGE_BYTES);
+                if (kb >= STAGES) {   // the first STAGES got their weights before the wait
+                    if (!mbar_wait(&empty[s], (it & 1u) ^ 1u)) {
+                        sflag[0] = 1;
+                        break;
+                    }
+                    mbar_expect_tx(&full[s], STAGE_BYTES);
+                    tma_load_2d(sa + A_BYTES, &tmB, (kb0 + kb) * GEMM_BK, n0, &full[s]);
+                }
                 tma_load_2d(sa, &tmA, (kb0 + kb) * GEMM_BK, m0, &full[s]);
-                tma_load_2d(sa + A_BYTES, &tmB, (kb0 + kb) * GEMM_BK, n0, &full[s]);
             }
             sflag[1] = kb;
         }

@@ -913,8 +913,14 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     }
     launch_embed(ea, s);
     const bool gemv = B <= GEMV_MAX_BATCH;
-    // enough (token, kv head, split) CTAs for ~8 per SM streaming the cache
-    int splits = (8 * m->sms + B * c.n_kv_heads - 1) / (B * c.n_kv_heads);
+    // key splits per (token, kv head): the SIMT kernel wants ~8 CTAs per SM;
+    // the tensor-core kernel streams best as one wave of long-lived CTAs at
+    // 2 per SM (each with a deep copy ring), so it takes the most splits
+    // that still fit in that wave
+    const bool mma_attn = kv->k_map_ok && kv->v_map_ok &&
+                          attn_decode_mma_supported(c.head_dim, c.n_heads / c.n_kv_heads);
+    const int units = B * c.n_kv_heads;
+    int splits = mma_attn ? (2 * m->sms) / units : (8 * m->sms + units - 1) / units;
     splits = splits < 1 ? 1 : (splits > MAX_SPLITS ? MAX_SPLITS : splits);
     for (int l = 0; l < c.layers; ++l) {
         LayerDev& L = m->layers[l];
@@ -973,6 +979,8 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         a.counters = m->counters;
         a.splits = splits;
         a.status = m->status;
+        a.k_map = mma_attn ? kv->k_map : nullptr;
+        a.v_map = mma_attn ? kv->v_map : nullptr;
         launch_attn_decode(a, s);
         if (gemv) {
             GemvArgs g{};

@@ -103,10 +103,13 @@ struct AttnDecodeArgs {
     unsigned* counters;          // [nb*NKV], zero between launches
     int splits;
     int* status;
+    const void* k_map;           // host copies of the caches' 3-D TMA maps, or nullptr
+    const void* v_map;           // (read by the launcher only)
 };
 void launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t s);
 // The same on the warp tensor cores (decode_attn_mma.cu): head_dim 64 / 128,
-// at most 16 query heads per kv head.  launch_attn_decode picks it.
+// at most 16 query heads per kv head, K/V through the TMA maps.
+// launch_attn_decode picks it when the maps are given.
 bool attn_decode_mma_supported(int D, int G);
 void launch_attn_decode_mma(const AttnDecodeArgs& a, cudaStream_t s);
 

@@ -16,26 +16,47 @@ namespace ember {
 template <int OUT>
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w, float eps, int H,
                                                  void* out) {
+    // one row per CTA; H % 4 == 0 and H <= 8192 (the weights are loaded into
+    // registers before the wait, the row in one batch of 16-byte loads)
+    constexpr int MAXV = 8;
     __shared__ float red[32];
-    const int t = blockIdx.x;
+    const int t = blockIdx.x, H4 = H >> 2;
+    float4 wv[MAXV], xv[MAXV];
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+        const int i = threadIdx.x + q * 256;
+        wv[q] = i < H4 ? __ldg(reinterpret_cast<const float4*>(w) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     pdl_trigger();
     pdl_wait();
-    const float* xr = x + (size_t)t * H;
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
-    ss = block_sum(ss, red);
-    const float ri = rsqrtf(ss / (float)H + eps);
-    if (OUT == 1) {
-        uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
-        for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
-            o[i] = pack_f16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
-    } else if (OUT == 2) {
-        uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(out) + (size_t)t * H);
-        for (int i = threadIdx.x; i < H / 2; i += blockDim.x)
-            o[i] = pack_bf16x2(xr[2 * i] * ri * w[2 * i], xr[2 * i + 1] * ri * w[2 * i + 1]);
-    } else {
-        float* o = static_cast<float*>(out) + (size_t)t * H;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = xr[i] * ri * w[i];
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+        const int i = threadIdx.x + q * 256;
+        xv[q] = i < H4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += xv[q].x * xv[q].x + xv[q].y * xv[q].y + xv[q].z * xv[q].z + xv[q].w * xv[q].w;
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tot += red[k];
+    const float ri = rsqrtf(tot / (float)H + eps);
+#pragma unroll
+    for (int q = 0; q < MAXV; ++q) {
+        const int i = threadIdx.x + q * 256;
+        if (i >= H4) continue;
+        const float a0 = xv[q].x * ri * wv[q].x, a1 = xv[q].y * ri * wv[q].y;
+        const float a2 = xv[q].z * ri * wv[q].z, a3 = xv[q].w * ri * wv[q].w;
+        if (OUT == 0) {
+            reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H)[i] = make_float4(a0, a1, a2, a3);
+        } else {
+            uint2* o = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + (size_t)t * H);
+            o[i] = OUT == 1 ? make_uint2(pack_f16x2(a0, a1), pack_f16x2(a2, a3))
+                            : make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+        }
     }
 }
 
