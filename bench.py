@@ -157,20 +157,25 @@ class DecodeJob:
         with torch.cuda.stream(s):
             if ev:
                 ev[0].record(s)
+            # NVTX ranges name the phases for profilers (ncu --nvtx-include prefill/ | decode/)
             if self.prefill_in_job:
                 kv.set_cursor(0, 0, stream=s)
                 ids = self.prompts[0]
                 if host_ids is not None:
                     ids = self._dev_ids
                     ids.copy_(host_ids, non_blocking=True)
+                torch.cuda.nvtx.range_push("prefill")
                 m.prefill(kv, 0, ids, 0, argmax=self.cur[0:1], stream=s)
+                torch.cuda.nvtx.range_pop()
             else:
                 for b in range(self.B):
                     kv.set_cursor(b, self.P, stream=s)
             if ev:
                 ev[1].record(s)
+            torch.cuda.nvtx.range_push("decode")
             for _ in range(self.S):
                 m.decode_step(kv, self.seqs, self.cur, None, argmax=self.cur, stream=s)
+            torch.cuda.nvtx.range_pop()
             if host_out is not None:
                 host_out.copy_(self.cur, non_blocking=True)
             if ev:
@@ -224,7 +229,9 @@ class EncodeJob:
                 ids.copy_(host_ids, non_blocking=True)
             if ev:
                 ev[1].record(s)
+            torch.cuda.nvtx.range_push("encode")
             self.model.encode(ids, self.B, self.T, out=self.out, stream=s)
+            torch.cuda.nvtx.range_pop()
             if host_out is not None:
                 host_out.copy_(self.out, non_blocking=True)
             if ev:
