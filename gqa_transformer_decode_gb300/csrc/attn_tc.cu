@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int qw = warp & 3;
         const int r = qw * 32 + lane;                 // query row within the tile
         const int qp = a.pos0 + q_first + r;          // its position
+        const int qmin = a.pos0 + q_first;            // the tile's first position
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
         const float sc_log2 = 1.4426950408889634f * rsqrtf((float)D);
         float m = -INFINITY, l = 0.f;
@@ -189,20 +190,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             }
             tc_fence_after();
             const int key0 = j * AT_BK;
-            // pass 1: row maximum of the visible scaled scores
+            // every key of the tile visible to every row of the query tile: no masking
+            const bool full = key0 + AT_BK <= a.n_keys && (!a.causal || key0 + AT_BK - 1 <= qmin);
+            // pass 1: row maximum of the visible scores (the scale is positive)
             float mt = -INFINITY;
 #pragma unroll
             for (int c0 = 0; c0 < AT_BK; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tS + lane_off + c0, v);
                 tmem_ld_wait();
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kp = key0 + c0 + i;
-                    const bool vis = kp < a.n_keys && (!a.causal || kp <= qp);
-                    if (vis) mt = fmaxf(mt, __uint_as_float(v[i]) * sc_log2);
+                    for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(v[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int kp = key0 + c0 + i;
+                        const bool vis = kp < a.n_keys && (!a.causal || kp <= qp);
+                        if (vis) mt = fmaxf(mt, __uint_as_float(v[i]));
+                    }
                 }
             }
+            mt *= sc_log2;
             const float mn = fmaxf(m, mt);
             const float corr = (m == -INFINITY) ? 0.f : exp2f(m - mn);
             // pass 2: p = exp2(s - m), row sum, P -> shared (swizzled K-major)
@@ -213,16 +222,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 tmem_ld32(tS + lane_off + c0, v);
                 tmem_ld_wait();
                 uint32_t pk[16];
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int kp = key0 + c0 + i;
-                    const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
-                    const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
-                    const float p0 = v0 ? exp2f(__uint_as_float(v[i]) * sc_log2 - mn) : 0.f;
-                    const float p1 = v1 ? exp2f(__uint_as_float(v[i + 1]) * sc_log2 - mn) : 0.f;
-                    rs += p0 + p1;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    pk[i / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(v[i]), sc_log2, -mn));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[i + 1]), sc_log2, -mn));
+                        rs += p0 + p1;
+                        pk[i / 2] = pack_f16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int kp = key0 + c0 + i;
+                        const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
+                        const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
+                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(v[i]), sc_log2, -mn)) : 0.f;
+                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(v[i + 1]), sc_log2, -mn)) : 0.f;
+                        rs += p0 + p1;
+                        pk[i / 2] = pack_f16x2(p0, p1);
+                    }
                 }
                 const int kb = c0 / 64;
                 uint8_t* rowp = sP + kb * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;

@@ -76,6 +76,13 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return r;
 }
 
+// 2^x by the hardware approximation (relative error ~2^-22; ftz)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- reductions --------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
