@@ -85,6 +85,42 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     pdl_wait();
+    if (!a.q_norm) {   // no per-head norm: four rotate-half pairs per item, in registers
+        const int Q4 = H2 / 4;                       // items per head
+        const int n_rope = (a.NH + a.NKV) * Q4, n_v = nkv / 4;
+        const float* cs = a.cos_t + (size_t)pos * H2;
+        const float* sn = a.sin_t + (size_t)pos * H2;
+        for (int e = tid; e < n_rope + n_v; e += blockDim.x) {
+            if (e < n_rope) {
+                const int h = e / Q4, i0 = (e % Q4) * 4;
+                const float4 x0 = *reinterpret_cast<const float4*>(row + h * D + i0);
+                const float4 x1 = *reinterpret_cast<const float4*>(row + h * D + H2 + i0);
+                const float4 cv = *reinterpret_cast<const float4*>(cs + i0);
+                const float4 sv = *reinterpret_cast<const float4*>(sn + i0);
+                float r0[4], r1[4];
+                rope_pair(x0.x, x1.x, cv.x, sv.x, r0[0], r1[0]);
+                rope_pair(x0.y, x1.y, cv.y, sv.y, r0[1], r1[1]);
+                rope_pair(x0.z, x1.z, cv.z, sv.z, r0[2], r1[2]);
+                rope_pair(x0.w, x1.w, cv.w, sv.w, r0[3], r1[3]);
+                const uint2 lo = make_uint2(pack_bf16x2(r0[0], r0[1]), pack_bf16x2(r0[2], r0[3]));
+                const uint2 hi = make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
+                uint16_t* dst;
+                if (h < a.NH) {
+                    dst = a.q_out + (size_t)t * nq + h * D;
+                } else {
+                    dst = a.kc + z * a.seq_stride + (h - a.NH) * a.head_stride + (long long)pos * D;
+                }
+                *reinterpret_cast<uint2*>(dst + i0) = lo;
+                *reinterpret_cast<uint2*>(dst + H2 + i0) = hi;
+            } else {
+                const int f = (e - n_rope) * 4, g = f / D, d = f % D;
+                const float4 v = *reinterpret_cast<const float4*>(row + nq + nkv + f);
+                *reinterpret_cast<uint2*>(a.vc + z * a.seq_stride + g * a.head_stride + (long long)pos * D + d) =
+                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            }
+        }
+        return;
+    }
     for (int e = tid; e < nq + 2 * nkv; e += blockDim.x) sm[e] = row[e];
     __syncthreads();
     if (a.q_norm) {   // PII-Tracer forward(): per-head RMSNorm of q and k before RoPE
