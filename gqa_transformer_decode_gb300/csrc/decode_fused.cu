@@ -193,6 +193,49 @@ __device__ __forceinline__ float wdot_f16(const uint4* row, const XRegs& x, int 
     return t;
 }
 
+// Four rows at once: the same per-lane chunks for rows r[0..3] (four
+// independent streams of loads and FMAs), then a transposing butterfly that
+// leaves row ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1) summed in every lane of
+// its group of 8 (6 shuffles instead of 20).  Rows may repeat (padding).
+__device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, const uint4* r2,
+                                           const uint4* r3, const XRegs& x, int n8) {
+    const int lane = threadIdx.x & 31;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < XR_MAX; ++i) {
+        const int c = lane + 32 * i;
+        if (c < n8) {
+            float xf[8], w0[8], w1[8], w2[8], w3[8];
+            unpack8_f16(x.v[i], xf);
+            unpack8_f16(lds128(r0 + c), w0);
+            unpack8_f16(lds128(r1 + c), w1);
+            unpack8_f16(lds128(r2 + c), w2);
+            unpack8_f16(lds128(r3 + c), w3);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                a0 = fmaf(w0[u], xf[u], a0);
+                a1 = fmaf(w1[u], xf[u], a1);
+                a2 = fmaf(w2[u], xf[u], a2);
+                a3 = fmaf(w3[u], xf[u], a3);
+            }
+            s0 += a0; s1 += a1; s2 += a2; s3 += a3;
+        }
+    }
+    // lanes 0-15 keep rows 0,1 and lanes 16-31 rows 2,3
+    const bool lo16 = lane < 16;
+    const float v1 = __shfl_xor_sync(FULL_MASK, lo16 ? s2 : s0, 16);
+    const float v2 = __shfl_xor_sync(FULL_MASK, lo16 ? s3 : s1, 16);
+    const float a = (lo16 ? s0 : s2) + v1, b = (lo16 ? s1 : s3) + v2;
+    // lanes with bit 3 clear keep the first of their two rows
+    const bool lo8 = (lane & 8) == 0;
+    float t = (lo8 ? a : b) + __shfl_xor_sync(FULL_MASK, lo8 ? b : a, 8);
+    t += __shfl_xor_sync(FULL_MASK, t, 4);
+    t += __shfl_xor_sync(FULL_MASK, t, 2);
+    t += __shfl_xor_sync(FULL_MASK, t, 1);
+    return t;
+}
+
 }  // namespace
 
 // ================================================================== D1 ==
@@ -326,10 +369,20 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     {
         XRegs xr;
         xr.load(s_xh, H / 8);
-        for (int ri = warp; ri < r1 - r0; ri += FA_THREADS / 32) {
-            float v = wdot_f16(reinterpret_cast<const uint4*>(sW + (size_t)ri * H), xr, H / 8);
-            if (a.bqkv) v += s_bias[ri];
-            if (lane < C) st_dsmem(dsmem(&s_qkv[r0 + ri], lane), v);
+        const int nrow = r1 - r0;
+        const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1), l8 = lane & 7;
+        for (int base = warp * 4; base < nrow; base += FA_THREADS / 8) {   // 4 rows per warp
+            const uint4* rp[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                rp[k] = reinterpret_cast<const uint4*>(sW + (size_t)min(base + k, nrow - 1) * H);
+            float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, H / 8);
+            const int ri = base + my;
+            if (ri < nrow) {
+                if (a.bqkv) v += s_bias[ri];
+                st_dsmem(dsmem(&s_qkv[r0 + ri], l8), v);
+                st_dsmem(dsmem(&s_qkv[r0 + ri], l8 + 8), v);
+            }
         }
     }
     cluster_sync_all();
@@ -530,9 +583,16 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     {
         XRegs xr;
         xr.load_f32(s_att, GD / 8);
-        for (int ri = warp; ri < o1 - o0; ri += FA_THREADS / 32) {
-            const float v = wdot_f16(reinterpret_cast<const uint4*>(sW + (size_t)ri * GD), xr, GD / 8);
-            if (lane == 0) red_add(a.z_acc + o0 + ri, v);
+        const int nrow = o1 - o0;
+        const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+        for (int base = warp * 4; base < nrow; base += FA_THREADS / 8) {   // 4 rows per warp
+            const uint4* rp[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                rp[k] = reinterpret_cast<const uint4*>(sW + (size_t)min(base + k, nrow - 1) * GD);
+            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, GD / 8);
+            const int ri = base + my;
+            if (ri < nrow && (lane & 7) == 0) red_add(a.z_acc + o0 + ri, v);
         }
     }
     if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
@@ -598,11 +658,15 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
         const int s = k % ns;
         if (!mbar_wait(&bar[s], (uint32_t)((k / ns) & 1))) s_err = 1;
         const uint8_t* st = ring + (size_t)s * stage_bytes;
-        // gate / up rows: a warp a row
+        // gate / up rows: four per warp (2 * FC <= 32 rows over 8 warps)
+        if (warp * 4 < 2 * FC) {
+            const uint4* rp[4];
 #pragma unroll
-        for (int rr = warp; rr < 2 * FC; rr += FM_THREADS / 32) {
-            const float v = wdot_f16(reinterpret_cast<const uint4*>(st + (size_t)rr * H * 2), xr, H8);
-            if (lane == 0) s_g[k & 1][rr] = v;
+            for (int q = 0; q < 4; ++q)
+                rp[q] = reinterpret_cast<const uint4*>(st + (size_t)min(warp * 4 + q, 2 * FC - 1) * H * 2);
+            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, H8);
+            const int rr = warp * 4 + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            if ((lane & 7) == 0 && rr < 2 * FC) s_g[k & 1][rr] = v;
         }
         __syncthreads();   // s_g[k & 1] complete; chunk k - 1 fully consumed
         if (tid == 0 && k >= 1 && k - 1 + ns < my_n) issue(k - 1 + ns);
@@ -655,7 +719,10 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     p.C = C;
     p.nr = ((G + 2) * D + C - 1) / C;
     p.no = (H + C - 1) / C;
+    // more than half an SM's shared memory: one attention CTA per SM, so a
+    // cluster spreads over 16 SMs instead of packing two CTAs onto each
     p.smem_attn = fa_layout(D, G, H, p.nr, p.no).total;
+    if (p.smem_attn < 116 * 1024) p.smem_attn = 116 * 1024;
     if (p.smem_attn > 200 * 1024) return no("attention block needs > 200 KB of shared memory");
     // MLP chunk size: the largest FC in {16, 8, 4} (dividing F) whose two-stage
     // ring still fits beside the attention kernel on one SM; else FC = 4.
