@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "mma_common.cuh"
 
 namespace ember {
 
@@ -29,54 +30,20 @@ constexpr int AM_MIN_CHUNK = 64;        // keys per split at least
 constexpr int AM_MAX_SPLITS = 32;       // partial buffer layout (same as the SIMT kernel)
 constexpr long long AM_WAIT = 1ll << 31;
 
-__device__ __forceinline__ uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-// c += a (16x16, f16) * b (16x8, f16), f32 accumulators
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// a bf16 pair -> the same pair as f16 (round to nearest)
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t u) { return pack_f16x2(bf16_lo(u), bf16_hi(u)); }
-
-// Q tile: [16][D] f16, 16-byte chunk c of row r XOR-swizzled by (r & 7).
-template <int D>
-__device__ __forceinline__ int q_off(int r, int c) {
-    return r * (D * 2) + ((c ^ (r & 7)) << 4);
-}
-// K / V tile as written by the 128-byte-swizzled TMA box (64 elements x 128
-// keys per box; D / 64 boxes side by side): element chunk c (8 values) of key r.
-__device__ __forceinline__ int kv_off(int r, int c) {
-    return (c >> 3) * (AM_TK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
 __device__ __forceinline__ void mbar_expect_tx_(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(bar)), "r"(bytes)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa_u32(bar)), "r"(bytes)
                  : "memory");
 }
 __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
                                      uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sa(dst)),
-        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(sa(bar))
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sa_u32(dst)),
+        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(sa_u32(bar))
         : "memory");
 }
 __device__ __forceinline__ bool am_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t addr = sa(bar);
+    const uint32_t addr = sa_u32(bar);
     uint32_t ok;
     const long long t0 = clock64();
     do {
@@ -154,7 +121,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
     if (tid == 0) {
         s_err = 0;
         for (int st = 0; st < NS; ++st)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&full[st])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa_u32(&full[st])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int it = 0; it < NS && it < n_tiles; ++it) issue(it);
     }
@@ -224,7 +191,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
     for (int kk = 0; kk < KS; ++kk) {
         const int mi = lane >> 3;
         const int r = (mi & 1) * 8 + (lane & 7), c = 2 * kk + (mi >> 1);
-        ldsm4(sa(sm + L::Q + q_off<D>(r, c)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        ldsm4(sa_u32(sm + L::Q + q_off<D>(r, c)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
 
     // ---- keys [lo, hi): tiles of 128 from the ring; warp w takes keys 32w..32w+31 ----
@@ -264,7 +231,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
                 const int mi = lane >> 3;
                 const int row = r0k + (mi >> 1) * 8 + (lane & 7), c = 2 * kk + (mi & 1);
                 uint32_t b0, b1, b2, b3;
-                ldsm4(sa(kt + kv_off(row, c)), b0, b1, b2, b3);
+                ldsm4(sa_u32(kt + kv_off(row, c)), b0, b1, b2, b3);
                 mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
                 mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
             }
@@ -305,7 +272,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
                 const int mi = lane >> 3;
                 const int row = r0k + (mi & 1) * 8 + (lane & 7), c = dn + (mi >> 1);
                 uint32_t r0, r1, r2, r3;
-                ldsm4t(sa(vt + kv_off(row, c)), r0, r1, r2, r3);
+                ldsm4t(sa_u32(vt + kv_off(row, c)), r0, r1, r2, r3);
                 mma16816(o[dn], pa, bf2_to_h2(r0), bf2_to_h2(r1));
                 mma16816(o[dn + 1], pa, bf2_to_h2(r2), bf2_to_h2(r3));
             }

@@ -23,6 +23,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
+#include "mma_common.cuh"
 
 namespace ember {
 
@@ -245,7 +246,7 @@ constexpr int FA_C = 16;       // CTAs per cluster (one cluster per kv head)
 
 // Shared-memory plan of D1 (host and device compute it the same way).
 struct FaLayout {
-    int k, v, w, x, qkv, part, att, sc, red, bar, total;
+    int k, v, w, x, qkv, part, att, qh, wm, red, bar, total;
 };
 __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int no) {
     FaLayout L;
@@ -260,7 +261,8 @@ __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int n
     L.qkv = o; o += (((G + 2) * D * 4 + 15) / 16) * 16;
     L.part = o; o += ((G * (D + 2) * 4 + 15) / 16) * 16;
     L.att = o; o += ((G * D * 4 + 15) / 16) * 16;
-    L.sc = o; o += G * FA_KT * 4;
+    L.qh = o; o += 16 * D * 2;                    // q as the f16 A tile of the key mma
+    L.wm = o; o += 8 * G * (D + 2) * 4;           // the 8 warps' (m, l, O) per head
     L.red = o; o += 32 * 4;
     L.bar = o; o += 4 * 8;
     L.total = o + 1024;                           // room to align the base to 1024
@@ -286,10 +288,10 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     float* s_qkv = reinterpret_cast<float*>(sm + Lo.qkv);    // [G*D q | D k | D v]
     float* s_part = reinterpret_cast<float*>(sm + Lo.part);  // [G][m, l, acc[D]]
     float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads
-    float* s_sc = reinterpret_cast<float*>(sm + Lo.sc);      // [G][FA_KT]
+    uint8_t* sQh = sm + Lo.qh;                                 // [16][D] f16, swizzled
+    float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [8][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);  // 0: qkv W, 1: K/V, 2: o W
-    __shared__ float s_scale[16], s_m[16], s_l[16];
     __shared__ int s_err;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -437,109 +439,143 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         }
     }
 
-    // ---- flash attention over keys [lo, hi) for the G heads ----
-    if (tid < G) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
+    // ---- flash attention over keys [lo, hi): the G heads are the 16-row A
+    // operand of mma.m16n8k16 (rows >= G zero), warp w takes keys 16w..16w+15
+    // of each 128-key tile; online softmax per row in registers; P (f16) is
+    // the A operand of O += P V ----
+    constexpr int KS = D / 16, NT = D / 8;
+    for (int e = tid; e < 16 * (D / 8); e += FA_THREADS) {
+        const int rq = e / (D / 8), cq = e % (D / 8);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (rq < G) {
+            const float* q = s_qkv + rq * D + cq * 8;
+            val = make_uint4(pack_f16x2(q[0], q[1]), pack_f16x2(q[2], q[3]), pack_f16x2(q[4], q[5]),
+                             pack_f16x2(q[6], q[7]));
+        }
+        *reinterpret_cast<uint4*>(sQh + q_off<D>(rq, cq)) = val;
     }
-    constexpr int MAXE = (16 * D + FA_THREADS - 1) / FA_THREADS;
-    float acc[MAXE];
+    __syncthreads();
+    uint32_t qa[KS][4];
 #pragma unroll
-    for (int i = 0; i < MAXE; ++i) acc[i] = 0.f;
+    for (int kk = 0; kk < KS; ++kk) {
+        const int mi = lane >> 3;
+        ldsm4(sa_u32(sQh + q_off<D>((mi & 1) * 8 + (lane & 7), 2 * kk + (mi >> 1))), qa[kk][0],
+              qa[kk][1], qa[kk][2], qa[kk][3]);
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4, lane/4 + 8
+    const int g4 = lane >> 2, q4 = lane & 3;
     for (int t0 = lo; t0 < hi; t0 += FA_KT) {
         const int nt = min(FA_KT, hi - t0);
         if (!mbar_wait(&bar[1], kv_phase)) s_err = 1;
         kv_phase ^= 1;
-        if (owner && pos >= t0 && pos < t0 + nt) {   // patch the row the TMA read stale
-            const int j = pos - t0;
-            for (int d = tid; d < D; d += FA_THREADS) {
-                const int sb = d >> 6, c = (d & 63) >> 3;
-                const int off = sb * FA_KT * 128 + j * 128 + ((c ^ (j & 7)) << 4) + (d & 7) * 2;
-                *reinterpret_cast<uint16_t*>(sK + off) = f32_to_bf16(s_qkv[GD + d]);
-                *reinterpret_cast<uint16_t*>(sV + off) = f32_to_bf16(s_qkv[GD + D + d]);
-            }
+        if (owner && pos >= t0 && pos < t0 + nt && tid < D / 8) {   // the row the TMA read stale
+            const int j = pos - t0, cq = tid;
+            const float* kk8 = s_qkv + GD + cq * 8;
+            const float* vv8 = s_qkv + GD + D + cq * 8;
+            *reinterpret_cast<uint4*>(sK + kv_off(j, cq)) =
+                make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
+                           pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
+            *reinterpret_cast<uint4*>(sV + kv_off(j, cq)) =
+                make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
+                           pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
         }
         __syncthreads();
-        // scores: thread -> key j = tid % 128, heads tid / 128, +2, ...
-        {
-            const int j = tid % FA_KT;
-            for (int h = tid / FA_KT; h < G; h += FA_THREADS / FA_KT) {
-                float sc = -INFINITY;
-                if (j < nt) {
-                    const float* q = s_qkv + h * D;
-                    float dot = 0.f;
+        const int r0k = warp * 16;
+        if (r0k < nt) {   // warp-uniform
+            float s[2][4];
 #pragma unroll
-                    for (int c8 = 0; c8 < D / 8; ++c8) {
-                        const int sb = c8 >> 3, c = c8 & 7;
-                        const uint4 kk = *reinterpret_cast<const uint4*>(
-                            sK + sb * FA_KT * 128 + j * 128 + ((c ^ (j & 7)) << 4));
-                        float kf[8];
-                        unpack8(kk, kf);
+            for (int n8 = 0; n8 < 2; ++n8) s[n8][0] = s[n8][1] = s[n8][2] = s[n8][3] = 0.f;
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) dot = fmaf(q[c8 * 8 + u], kf[u], dot);
-                    }
-                    sc = dot;
+            for (int kk = 0; kk < KS; ++kk) {
+                const int mi = lane >> 3;
+                uint32_t b0, b1, b2, b3;
+                ldsm4(sa_u32(sK + kv_off(r0k + (mi >> 1) * 8 + (lane & 7), 2 * kk + (mi & 1))), b0, b1, b2, b3);
+                mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
+                mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int n8 = 0; n8 < 2; ++n8)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (r0k + n8 * 8 + 2 * q4 + (i & 1) >= nt) s[n8][i] = -INFINITY;
+                    if (i < 2) mx0 = fmaxf(mx0, s[n8][i]);
+                    else mx1 = fmaxf(mx1, s[n8][i]);
                 }
-                s_sc[h * FA_KT + j] = sc;
-            }
-        }
-        __syncthreads();
-        // online softmax, one warp per head
-        for (int h = warp; h < G; h += FA_THREADS / 32) {
-            float v[FA_KT / 32];
-            float tm = -INFINITY;
+            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: key r0k is valid
+            const float sc0 = exp2f(m0 - mn0), sc1 = exp2f(m1 - mn1);
+            float p[2][4];
 #pragma unroll
-            for (int u = 0; u < FA_KT / 32; ++u) {
-                v[u] = s_sc[h * FA_KT + lane + 32 * u];
-                tm = fmaxf(tm, v[u]);
-            }
-            tm = warp_max(tm);
-            const float mo = s_m[h];
-            const float mn = fmaxf(mo, tm);
-            float ps = 0.f;
+            for (int n8 = 0; n8 < 2; ++n8)
 #pragma unroll
-            for (int u = 0; u < FA_KT / 32; ++u) {
-                const float p = exp2f(v[u] - mn);
-                s_sc[h * FA_KT + lane + 32 * u] = p;
-                ps += p;
-            }
-            ps = warp_sum(ps);
-            if (lane == 0) {
-                const float sc = exp2f(mo - mn);   // 0 when mo == -inf
-                s_scale[h] = sc;
-                s_l[h] = s_l[h] * sc + ps;
-                s_m[h] = mn;
-            }
-        }
-        __syncthreads();
+                for (int i = 0; i < 4; ++i) p[n8][i] = exp2f(s[n8][i] - (i < 2 ? mn0 : mn1));
+            l0 = l0 * sc0 + ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
+            l1 = l1 * sc1 + ((p[0][2] + p[0][3]) + (p[1][2] + p[1][3]));
+            m0 = mn0;
+            m1 = mn1;
 #pragma unroll
-        for (int i = 0; i < MAXE; ++i) {
-            const int e = tid + i * FA_THREADS;
-            if (e < GD) {
-                const int h = e / D, d = e % D;
-                const int sb = d >> 6, c = (d & 63) >> 3;
-                const uint8_t* vb = sV + sb * FA_KT * 128 + (d & 7) * 2;
-                const float* p = s_sc + h * FA_KT;
-                float s = acc[i] * s_scale[h];
-                for (int j = 0; j < nt; ++j)
-                    s = fmaf(p[j], bf16_to_f32(*reinterpret_cast<const uint16_t*>(
-                                       vb + j * 128 + ((c ^ (j & 7)) << 4))),
-                             s);
-                acc[i] = s;
+            for (int dn = 0; dn < NT; ++dn) {
+                o[dn][0] *= sc0; o[dn][1] *= sc0;
+                o[dn][2] *= sc1; o[dn][3] *= sc1;
+            }
+            const uint32_t pa[4] = {pack_f16x2(p[0][0], p[0][1]), pack_f16x2(p[0][2], p[0][3]),
+                                    pack_f16x2(p[1][0], p[1][1]), pack_f16x2(p[1][2], p[1][3])};
+#pragma unroll
+            for (int dn = 0; dn < NT; dn += 2) {
+                const int mi = lane >> 3;
+                uint32_t v0, v1, v2, v3;
+                ldsm4t(sa_u32(sV + kv_off(r0k + (mi & 1) * 8 + (lane & 7), dn + (mi >> 1))), v0, v1, v2, v3);
+                mma16816(o[dn], pa, bf2_to_h2(v0), bf2_to_h2(v1));
+                mma16816(o[dn + 1], pa, bf2_to_h2(v2), bf2_to_h2(v3));
             }
         }
         __syncthreads();
         if (tid == 0 && t0 + FA_KT < hi) issue_tile(t0 + FA_KT);
     }
-    // partial (m, l, acc) of this CTA's keys
+    // the 8 warps' states -> this CTA's partial (m, l, acc) per head
+    l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
+    l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
+    l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
+    l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
 #pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
-        const int e = tid + i * FA_THREADS;
-        if (e < GD) s_part[(e / D) * (D + 2) + 2 + (e % D)] = acc[i];
+    for (int half = 0; half < 2; ++half) {
+        const int row = g4 + 8 * half;
+        if (row < G) {
+            float* w = s_wm + ((size_t)warp * G + row) * (D + 2);
+            if (q4 == 0) {
+                w[0] = half ? m1 : m0;
+                w[1] = half ? l1 : l0;
+            }
+#pragma unroll
+            for (int dn = 0; dn < NT; ++dn) {
+                w[2 + dn * 8 + 2 * q4] = o[dn][2 * half];
+                w[3 + dn * 8 + 2 * q4] = o[dn][2 * half + 1];
+            }
+        }
     }
-    if (tid < G) {
-        s_part[tid * (D + 2)] = s_m[tid];
-        s_part[tid * (D + 2) + 1] = s_l[tid];
+    __syncthreads();
+    for (int e = tid; e < G * (D + 2); e += FA_THREADS) {
+        const int hh = e / (D + 2), k = e % (D + 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
+            if (st[1] > 0.f) M = fmaxf(M, st[0]);
+        }
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
+            if (st[1] > 0.f) v = fmaf(st[k], exp2f(st[0] - M), v);
+        }
+        s_part[e] = k == 0 ? M : v;
     }
     cluster_sync_all();
 
