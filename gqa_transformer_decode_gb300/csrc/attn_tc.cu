@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint64_t* o_full = bar + 7;
     uint64_t* o_empty = bar + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+    uint64_t* kconv = bar + 12;     // [2] K tile of the stage converted to f16
     int* sflag = reinterpret_cast<int*>(bar + 10);   // [0] failed, [1] issued, [2] consumed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             mbar_init(&kv_empty[s], 1);
         }
         mbar_init(s_full, 1);
+        mbar_init(&kconv[0], 1);
+        mbar_init(&kconv[1], 1);
         mbar_init(p_full, 128);
         mbar_init(o_full, 1);
         mbar_init(o_empty, 128);
@@ -106,40 +109,71 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t tS = tmem, tO = tmem + 128;
     pdl_wait();   // Q, K and Vt are the previous kernels' outputs
 
-    if (warp == 0) {
-        if (lane == 0) {   // ------------------------------------------ TMA producer
+    if (warp == 0) {   // ------------------------------- TMA producer + K converter
+        // Tiles j and j + 1 are in flight; K arrives as bf16 from the cache and
+        // the whole warp rewrites it in place as f16 (the queries are f16) before
+        // releasing it to the MMA warp; tile j + 1 is issued once the MMAs of
+        // tile j - 1 have freed its stage.
+        auto issue = [&](int j) {
+            const int s = j & 1;
+            mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
+            for (int kb = 0; kb < L::KB; ++kb)
+                tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
+                            j * AT_BK, kz, &kv_full[s]);
+            for (int kb = 0; kb < 2; ++kb)
+                tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
+                            j * AT_BK + kb * 64, 0, vz, &kv_full[s]);
+        };
+        int issued = 0;
+        if (lane == 0) {
             const int qrow0 = z * a.T_per_seq + q_first;
             mbar_expect_tx(q_full, L::Q_BYTES);
             for (int kb = 0; kb < L::KB; ++kb)
                 tma_load_2d(sm + L::OFF_Q + kb * AT_BQ * 128, &tmQ, h * D + kb * 64, qrow0, q_full);
-            int j = 0;
-            for (; j < nkt; ++j) {
-                const int s = j & 1;
-                const uint32_t u = (uint32_t)(j >> 1);
-                if (!mbar_wait(&kv_empty[s], (u & 1u) ^ 1u)) {
-                    sflag[0] = 1;
-                    break;
-                }
-                mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
-                for (int kb = 0; kb < L::KB; ++kb)
-                    tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
-                                j * AT_BK, kz, &kv_full[s]);
-                for (int kb = 0; kb < 2; ++kb)
-                    tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
-                                j * AT_BK + kb * 64, 0, vz, &kv_full[s]);
+            for (; issued < 2 && issued < nkt; ++issued) issue(issued);
+        }
+        issued = __shfl_sync(FULL_MASK, issued, 0);
+        bool fail = false;
+        for (int j = 0; j < nkt && !fail; ++j) {
+            const int s = j & 1;
+            if (!mbar_wait(&kv_full[s], (uint32_t)(j >> 1) & 1u)) {
+                fail = true;
+                break;
             }
-            sflag[1] = j;
+            uint4* kt = reinterpret_cast<uint4*>(sm + L::OFF_K + s * L::K_BYTES);
+            for (int i = lane; i < L::K_BYTES / 16; i += 32) {
+                const uint4 u = kt[i];
+                kt[i] = make_uint4(pack_f16x2(bf16_lo(u.x), bf16_hi(u.x)), pack_f16x2(bf16_lo(u.y), bf16_hi(u.y)),
+                                   pack_f16x2(bf16_lo(u.z), bf16_hi(u.z)), pack_f16x2(bf16_lo(u.w), bf16_hi(u.w)));
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&kconv[s]);
+                if (j >= 1 && j + 1 < nkt) {   // stage of tile j - 1 -> tile j + 1
+                    if (!mbar_wait(&kv_empty[(j + 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) fail = true;
+                    else {
+                        issue(j + 1);
+                        ++issued;
+                    }
+                }
+            }
+            fail = __shfl_sync(FULL_MASK, (int)fail, 0) != 0;
+        }
+        if (lane == 0) {
+            if (fail) sflag[0] = 1;
+            sflag[1] = issued;
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ------------------------------------------ MMA issuer
-            constexpr uint32_t idS = idesc_bf16(AT_BQ, AT_BK);
+            constexpr uint32_t idS = idesc_f16(AT_BQ, AT_BK);   // f16 queries, K converted to f16
             constexpr uint32_t idO = idesc_f16(AT_BQ, D);
             bool ok = mbar_wait(q_full, 0);
             int j = 0;
             for (; ok && j < nkt; ++j) {
                 const int s = j & 1;
                 const uint32_t u = (uint32_t)(j >> 1);
-                if (!mbar_wait(&kv_full[s], u & 1u)) break;
+                if (!mbar_wait(&kconv[s], u & 1u)) break;
                 tc_fence_after();
                 const uint32_t q0 = smem_u32(sm + L::OFF_Q);
                 const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);

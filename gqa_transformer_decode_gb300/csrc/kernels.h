@@ -190,7 +190,7 @@ struct RopeKVArgs {
     const float* q_norm;
     const float* k_norm;
     float eps;
-    uint16_t* q_out;             // [n][NH*D] bf16
+    uint16_t* q_out;             // [n][NH*D] f16 (the attention MMA operand)
     uint16_t* kc;
     uint16_t* vc;
     long long seq_stride, head_stride;
@@ -201,7 +201,7 @@ void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s);
 // Query row t of sequence z sits at position pos0 + t; keys [0, pos0+t] are
 // visible when causal, [0, T_per_seq + pos0) otherwise.
 struct AttnPrefillArgs {
-    const uint16_t* q;           // [n][NH*D] bf16, RoPE'd
+    const uint16_t* q;           // [n][NH*D] f16, RoPE'd
     int n, NH, NKV, D;
     int T_per_seq, pos0, causal;
     const uint16_t* kc;

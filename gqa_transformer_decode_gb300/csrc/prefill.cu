@@ -102,10 +102,14 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
                 rope_pair(x0.y, x1.y, cv.y, sv.y, r0[1], r1[1]);
                 rope_pair(x0.z, x1.z, cv.z, sv.z, r0[2], r1[2]);
                 rope_pair(x0.w, x1.w, cv.w, sv.w, r0[3], r1[3]);
-                const uint2 lo = make_uint2(pack_bf16x2(r0[0], r0[1]), pack_bf16x2(r0[2], r0[3]));
-                const uint2 hi = make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
+                // queries in f16 (the attention MMA's operand), keys in bf16 (the cache)
+                const bool isq = h < a.NH;
+                const uint2 lo = isq ? make_uint2(pack_f16x2(r0[0], r0[1]), pack_f16x2(r0[2], r0[3]))
+                                     : make_uint2(pack_bf16x2(r0[0], r0[1]), pack_bf16x2(r0[2], r0[3]));
+                const uint2 hi = isq ? make_uint2(pack_f16x2(r1[0], r1[1]), pack_f16x2(r1[2], r1[3]))
+                                     : make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
                 uint16_t* dst;
-                if (h < a.NH) {
+                if (isq) {
                     dst = a.q_out + (size_t)t * nq + h * D;
                 } else {
                     dst = a.kc + z * a.seq_stride + (h - a.NH) * a.head_stride + (long long)pos * D;
@@ -144,8 +148,8 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
         float r0, r1;
         rope_pair(v[i], v[i + H2], cs[i], sn[i], r0, r1);
         if (h < a.NH) {
-            qo[h * D + i] = f32_to_bf16(r0);
-            qo[h * D + i + H2] = f32_to_bf16(r1);
+            qo[h * D + i] = f32_to_f16(r0);
+            qo[h * D + i + H2] = f32_to_f16(r1);
         } else {
             const int g = h - a.NH;
             uint16_t* kr = a.kc + z * a.seq_stride + g * a.head_stride + (long long)pos * D;
@@ -195,7 +199,8 @@ __global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a,
     for (int e = tid; e < items * D; e += APF_THREADS) {
         const int i = e / D, d = e % D, r = i / G, h = i % G;
         const size_t qrow = (size_t)z * a.T_per_seq + qt0 + r;
-        smq[e] = bf16_to_f32(a.q[qrow * a.NH * D + (size_t)(g * G + h) * D + d]) * qk_scale;
+        smq[e] = __half2float(__ushort_as_half(a.q[qrow * a.NH * D + (size_t)(g * G + h) * D + d])) *
+                 qk_scale;
     }
     float m[IPW], l[IPW], acc[IPW][DL];
 #pragma unroll

@@ -1,0 +1,199 @@
+"""Parity at the full model sizes of the benchmark workloads, in the launch
+configuration bench.py times (CUDA graphs; the fused batch-1 decode; the
+batched tensor-core path): against the f64 oracle where it finishes in
+seconds, on sampled outputs where the whole run would not, and through
+properties that hold at any size (a prefix's rows do not depend on later
+tokens; a batched step equals the batch-1 step of the same cache; a prompt
+split into chunks equals the prompt in one piece).  The method keeps its KV
+cache in bf16, so the oracle rounds K and V to bf16 (RNE) at write time."""
+import numpy as np
+import pytest
+import torch
+
+from gqa_transformer_decode_gb300 import runtime as R
+from gqa_transformer_decode_gb300 import synth
+from oracle import oracle as O
+
+from parity_util import assert_close, assert_tokens, first_argmax
+
+pytestmark = pytest.mark.gpu
+
+_weights = {}
+
+
+def weights(name):
+    if name not in _weights:
+        _weights[name] = synth.weights_bf16(synth.WORKLOADS[name].model)
+    return _weights[name]
+
+
+def i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).cuda()
+
+
+@pytest.fixture(scope="module")
+def stream():
+    return torch.cuda.Stream()
+
+
+def greedy_gpu(model, kv, prompt, forced, stream, seq=0):
+    """Prefill, then one decode step per forced token through the graph path
+    (positions from the device cursor, ids from one fixed buffer)."""
+    n = len(forced)
+    lg = torch.empty((n + 1, model.V), dtype=torch.float32, device="cuda")
+    am = torch.empty(n + 1, dtype=torch.int32, device="cuda")
+    hid = torch.empty((len(prompt), model.H), dtype=torch.float32, device="cuda")
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seqs = i32([seq])
+    with torch.cuda.stream(stream):
+        kv.set_cursor(seq, 0, stream=stream)
+        model.prefill(kv, seq, i32(prompt), 0, logits=lg[0], argmax=am[0:1], hidden=hid,
+                      stream=stream)
+        for i in range(n):
+            ids.copy_(i32([forced[i]]), non_blocking=True)
+            model.decode_step(kv, seqs, ids, None, logits=lg[i + 1], argmax=am[i + 1:i + 2],
+                              stream=stream)
+    assert model.sync_status(stream) == 0
+    return lg.cpu().numpy(), am.cpu().numpy(), hid.cpu().numpy()
+
+
+def test_qwen25_05b_prefill_and_decode(stream):
+    """Qwen2.5-0.5B shape, batch 1: the benchmark's 128-token prompt and 8
+    greedy steps (fused decode path) against the oracle."""
+    name = "qwen2.5-0.5b"
+    shape = synth.WORKLOADS[name].model
+    w = weights(name)
+    prompt = synth.prompt_ids(shape, 128)
+    toks, olg, _ = O.OracleModel(shape, w).greedy(prompt, 8, kv_bf16=True)
+    m = R.Model(shape, w, max_tokens=128)
+    kv = m.kv_alloc(1, 128 + 16)
+    glg, gam, _ = greedy_gpu(m, kv, prompt, toks[:-1], stream)
+    assert_close(olg, glg, "logits")
+    assert_tokens(olg, toks, gam, "greedy tokens")
+    assert all(gam[i] == first_argmax(glg[i]) for i in range(len(gam)))
+
+
+def test_llama32_1b_prefix_and_full_prompt(stream):
+    """Llama-3.2-1B shape: a 128-token prefix and 4 steps against the oracle;
+    the benchmark's 2048-token prefill then reproduces the prefix's hidden
+    states (causality), equals the same prompt prefilled in two chunks, and
+    greedy-decodes like the chunked cache."""
+    name = "llama-3.2-1b"
+    shape = synth.WORKLOADS[name].model
+    w = weights(name)
+    full = synth.prompt_ids(shape, 2048)
+    prefix = full[:128]
+    toks, olg, _ = O.OracleModel(shape, w).greedy(prefix, 4, kv_bf16=True)
+    m = R.Model(shape, w, max_tokens=2048)
+    kv = m.kv_alloc(2, 2048 + 8)
+    glg, gam, ghd = greedy_gpu(m, kv, prefix, toks[:-1], stream)
+    assert_close(olg, glg, "prefix logits")
+    assert_tokens(olg, toks, gam, "prefix greedy tokens")
+
+    # the full prompt in one piece (slot 0) and in two chunks (slot 1)
+    H, V = shape.hidden, shape.vocab
+    hid = torch.empty((2048, H), dtype=torch.float32, device="cuda")
+    lg = torch.empty((2, V), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        kv.set_cursor(0, 0, stream=stream)
+        m.prefill(kv, 0, i32(full), 0, logits=lg[0], hidden=hid, stream=stream)
+        kv.set_cursor(1, 0, stream=stream)
+        m.prefill(kv, 1, i32(full[:1000]), 0, stream=stream)
+        m.prefill(kv, 1, i32(full[1000:]), 1000, logits=lg[1], stream=stream)
+    assert m.sync_status(stream) == 0
+    assert_close(ghd, hid[:128].cpu().numpy(), "prefix rows of the 2048-token prefill")
+    lgn = lg.cpu().numpy()
+    assert_close(lgn[0:1], lgn[1:2], "2048-token prefill vs two chunks")
+    # four decode steps of both caches in one batch, both fed slot 0's argmax
+    # (teacher forcing keeps the histories equal): the rows must agree
+    ids = i32([first_argmax(lgn[0])] * 2)
+    seqs2 = i32([0, 1])
+    step_lg = torch.empty((4, 2, V), dtype=torch.float32, device="cuda")
+    am = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            m.decode_step(kv, seqs2, ids, None, logits=step_lg[i], argmax=am, stream=stream)
+            ids.copy_(am[0:1].expand(2))
+    assert m.sync_status(stream) == 0
+    sl = step_lg.cpu().numpy()
+    assert_close(sl[:, 0], sl[:, 1], "decode after the full vs the chunked prompt")
+
+
+def test_batch64_decode_sampled_sequences(stream):
+    """Qwen2.5-0.5B shape, 64 sequences: ragged short prompts with two
+    sampled sequences against the oracle; then the benchmark's 4096-token
+    caches, where a batched step's logits for sampled sequences equal the
+    batch-1 (fused) step on the same cache."""
+    name = "qwen2.5-0.5b"
+    shape = synth.WORKLOADS[name].model
+    w = weights(name)
+    B = 64
+    m = R.Model(shape, w, max_tokens=4096)
+    V = shape.vocab
+
+    # ragged short prompts, oracle on sequences 5 and 50
+    lens = [24 + (7 * b) % 41 for b in range(B)]
+    kv = m.kv_alloc(B, 80)
+    prompts = [synth.prompt_ids(shape, lens[b], seq=b) for b in range(B)]
+    cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            m.prefill(kv, b, i32(prompts[b]), 0, argmax=cur[b:b + 1], stream=stream)
+    lg = torch.empty((2, B, V), dtype=torch.float32, device="cuda")
+    seqs = torch.arange(B, dtype=torch.int32, device="cuda")
+    toks = [cur.clone()]
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            m.decode_step(kv, seqs, cur, None, logits=lg[i], argmax=cur, stream=stream)
+            toks.append(cur.clone())
+    assert m.sync_status(stream) == 0
+    glg = lg.cpu().numpy()
+    gt = np.stack([t.cpu().numpy() for t in toks])   # [3][B]: prefill argmax, step 1, step 2
+    om = O.OracleModel(shape, w)
+    for b in (5, 50):
+        otoks, olg, _ = om.greedy(prompts[b], 2, forced=gt[:2, b], kv_bf16=True)
+        assert_close(olg[1:], glg[:, b], f"seq {b} batched decode logits")
+        assert_tokens(olg[1:], otoks[1:], gt[1:, b], f"seq {b} batched greedy")
+    del kv
+
+    # the benchmark's 4096-token caches: batched step vs the batch-1 step
+    P = 4096
+    kv = m.kv_alloc(B, P + 2)
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            m.prefill(kv, b, i32(synth.prompt_ids(shape, P, seq=b)), 0, argmax=cur[b:b + 1],
+                      stream=stream)
+    ids0 = cur.clone()
+    lgb = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        m.decode_step(kv, seqs, ids0, None, logits=lgb, stream=stream)
+    assert m.sync_status(stream) == 0
+    for b in (0, 37, 63):
+        lg1 = torch.empty((1, V), dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            kv.set_cursor(b, P, stream=stream)   # the same position again
+            m.decode_step(kv, i32([b]), ids0[b:b + 1].clone(), None, logits=lg1, stream=stream)
+        assert m.sync_status(stream) == 0
+        assert_close(lgb[b:b + 1].cpu().numpy(), lg1.cpu().numpy(),
+                     f"seq {b}: batched vs batch-1 step at 4096 keys")
+
+
+def test_encoder_8x512_sampled_sequence(stream):
+    """Qwen3 encoder shape, 8 x 512: the label logits and final hidden states
+    of a sampled sequence against the oracle (sequences are independent)."""
+    name = "qwen3-encoder"
+    wl = synth.WORKLOADS[name]
+    shape = wl.model
+    w = weights(name)
+    B, T = wl.batch, wl.prompt
+    m = R.Model(shape, w, max_tokens=B * T, max_positions=T)
+    ids = np.concatenate([synth.prompt_ids(shape, T, seq=b) for b in range(B)])
+    out = torch.empty((B * T, shape.n_labels), dtype=torch.float32, device="cuda")
+    hid = torch.empty((B * T, shape.hidden), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        m.encode(i32(ids), B, T, out=out, hidden=hid, stream=stream)
+    assert m.sync_status(stream) == 0
+    b = 5
+    ohd, _, ocl = O.OracleModel(shape, w).forward_full(ids[b * T:(b + 1) * T], logits=False, cls=True)
+    assert_close(ocl, out[b * T:(b + 1) * T].cpu().numpy(), "label logits")
+    assert_close(ohd, hid[b * T:(b + 1) * T].cpu().numpy(), "final hidden states")
