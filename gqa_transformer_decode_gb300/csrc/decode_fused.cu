@@ -243,10 +243,11 @@ __device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, con
 constexpr int FA_THREADS = 256;
 constexpr int FA_KT = 128;     // keys per K/V tile (the TMA box height)
 constexpr int FA_C = 16;       // CTAs per cluster (one cluster per kv head)
+constexpr int FA_SOLO = 384;   // up to this many keys one CTA of the cluster does the attention
 
 // Shared-memory plan of D1 (host and device compute it the same way).
 struct FaLayout {
-    int k, v, w, x, qkv, part, att, qh, wm, red, bar, total;
+    int k, v, w, x, qkv, part, att, qh, wm, cs, red, bar, total;
 };
 __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int no) {
     FaLayout L;
@@ -263,6 +264,7 @@ __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int n
     L.att = o; o += ((G * D * 4 + 15) / 16) * 16;
     L.qh = o; o += 16 * D * 2;                    // q as the f16 A tile of the key mma
     L.wm = o; o += 8 * G * (D + 2) * 4;           // the 8 warps' (m, l, O) per head
+    L.cs = o; o += D * 4;                         // RoPE row of the position: cos | sin
     L.red = o; o += 32 * 4;
     L.bar = o; o += 4 * 8;
     L.total = o + 1024;                           // room to align the base to 1024
@@ -324,9 +326,11 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             }
         }
     }
-    // o_proj rows of this CTA (columns of group g): into L2 now, shared memory later
-    for (int row = o0 + tid; row < o1; row += FA_THREADS)
-        prefetch_l2(a.wo + (size_t)row * a.NH * D + (size_t)g * GD, (uint32_t)(GD * 2));
+    // o_proj rows of this CTA (group g's block, contiguous): into L2 now, shared memory later
+    const uint16_t* wo_cta = a.wo + ((size_t)g * H + o0) * GD;
+    const uint32_t wo_bytes = o1 > o0 ? (uint32_t)((o1 - o0) * GD * 2) : 0u;
+    for (uint32_t off = (uint32_t)tid * 16384u; off < wo_bytes; off += FA_THREADS * 16384u)
+        prefetch_l2(reinterpret_cast<const uint8_t*>(wo_cta) + off, min(16384u, wo_bytes - off));
     ResidualNorm rn;
     rn.load_w(a.norm_w, H);
     float* s_bias = s_part;   // the biases of this CTA's rows, until the partials are written
@@ -344,12 +348,15 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
 
     const int ok = __ldcg(a.tok_ok);
     const int pos = ok ? __ldcg(a.tok_pos) : 0;
-    float* s_cs = s_att;      // RoPE row of pos (cos | sin), until the merged heads arrive
+    float* s_cs = reinterpret_cast<float*>(sm + Lo.cs);   // RoPE row of pos (cos | sin)
     if (ok && tid < D) s_cs[tid] = tid < H2 ? a.cos_t[(size_t)pos * H2 + tid]
                                             : a.sin_t[(size_t)pos * H2 + tid - H2];
     const int n_keys = ok ? pos + 1 : 0;
-    const int per = (n_keys + C - 1) / C;
-    const int lo = min(n_keys, r * per), hi = min(n_keys, lo + per);
+    // short contexts: CTA 0 takes every key and no partials need merging
+    const bool solo = n_keys <= FA_SOLO;
+    const int per = solo ? n_keys : (n_keys + C - 1) / C;
+    const int lo = solo ? (r == 0 ? 0 : n_keys) : min(n_keys, r * per);
+    const int hi = solo ? n_keys : min(n_keys, lo + per);
     const int seq = ok ? a.seqs[0] : 0;
     const int kz = (seq * a.L + a.layer) * a.NKV + g;     // (seq, layer, kv head) plane
     const bool owner = ok && pos >= lo && pos < hi;
@@ -390,12 +397,9 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     cluster_sync_all();
 
     // o_proj rows into the (now free) weight buffer, while attention runs
-    if (warp == 0 && o1 > o0) {   // one bulk copy per row, spread over the warp's lanes
-        if (lane == 0) mbar_expect_tx(&bar[2], (uint32_t)((o1 - o0) * GD * 2));
-        __syncwarp();
-        for (int row = o0 + lane; row < o1; row += 32)
-            bulk_g2s(sW + (size_t)(row - o0) * GD, a.wo + (size_t)row * a.NH * D + (size_t)g * GD,
-                     (uint32_t)(GD * 2), &bar[2]);
+    if (tid == 0 && o1 > o0) {   // one bulk copy: the slice is contiguous
+        mbar_expect_tx(&bar[2], wo_bytes);
+        bulk_g2s(sW, wo_cta, wo_bytes, &bar[2]);
     }
 
     // ---- optional per-head q/k RMSNorm, then RoPE (q pre-scaled, base 2) ----
@@ -577,6 +581,18 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         }
         s_part[e] = k == 0 ? M : v;
     }
+    if (solo) {   // CTA 0 holds the whole softmax: normalise and broadcast the heads
+        __syncthreads();
+        if (r == 0) {
+            for (int e = tid; e < GD; e += FA_THREADS) {
+                const int h = e / D;
+                const float l = s_part[h * (D + 2) + 1];
+                const float O = l > 0.f ? s_part[h * (D + 2) + 2 + e % D] / l : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) st_dsmem(dsmem(&s_att[e], cc), O);
+            }
+        }
+    } else {
     cluster_sync_all();
 
     // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
@@ -612,6 +628,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             for (int cc = 0; cc < C; ++cc) st_dsmem(dsmem(&s_att[e], cc), O);
         }
     }
+    }   // !solo
     cluster_sync_all();
 
     // ---- o_proj: this CTA's rows of the group's column block, into the residual ----

@@ -103,6 +103,7 @@ void rope_tables(const ember_config& c, int npos, std::vector<float>& cs, std::v
 struct LayerDev {
     uint16_t *wqkv, *wo, *wgu, *wd;
     uint16_t* wdT = nullptr;   // f16 [F][H] down_proj transposed (fused batch-1 decode)
+    uint16_t* woG = nullptr;   // f16 [NKV][H][G*D] o_proj grouped by kv head (fused decode)
     float *attn_norm, *mlp_norm, *bqkv, *q_norm, *k_norm;
     GemmPlan p_qkv, p_o, p_gu, p_d;
 };
@@ -267,7 +268,10 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
         wa.add(&L.wo, (size_t)H * m->q);
         wa.add(&L.wgu, (size_t)2 * F * H);
         wa.add(&L.wd, (size_t)H * F);
-        if (m->fp.ok) wa.add(&L.wdT, (size_t)F * H);
+        if (m->fp.ok) {
+            wa.add(&L.wdT, (size_t)F * H);
+            wa.add(&L.woG, (size_t)H * m->q);
+        }
         wa.add(&L.attn_norm, H);
         wa.add(&L.mlp_norm, H);
         wa.add(&L.bqkv, m->qkv_n);
@@ -359,6 +363,12 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
             launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, s);
             launch_bf16_to_f16_inplace(L.wd, (long long)H * F, s);
             if (L.wdT) launch_transpose16(L.wd, L.wdT, H, F, s);
+            if (L.woG) {   // group g's o_proj columns as one [H][G*D] block
+                const size_t gd = (size_t)m->G * D;
+                for (int g = 0; g < NKV && e == cudaSuccess; ++g)
+                    e = cudaMemcpy2DAsync(L.woG + (size_t)g * H * gd, gd * 2, L.wo + (size_t)g * gd,
+                                          (size_t)m->q * 2, gd * 2, H, D2D, s);
+            }
         }
         launch_bf16_to_f32(W.attn_norm, L.attn_norm, H, s);
         launch_bf16_to_f32(W.mlp_norm, L.mlp_norm, H, s);
@@ -850,7 +860,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.eps = eps;
             a.q_norm = c.qk_norm ? L.q_norm : nullptr;
             a.k_norm = c.qk_norm ? L.k_norm : nullptr;
-            a.wo = L.wo;
+            a.wo = L.woG;
             a.H = c.hidden;
             a.NH = c.n_heads;
             a.NKV = c.n_kv_heads;

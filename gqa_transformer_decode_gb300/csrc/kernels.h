@@ -319,7 +319,7 @@ struct FusedAttnArgs {
     float eps;
     const float* q_norm;         // [D] or nullptr (then k_norm unused)
     const float* k_norm;
-    const uint16_t* wo;          // f16 [H][NH*D]
+    const uint16_t* wo;          // f16 o_proj grouped by kv head: [NKV][H][G*D]
     int H, NH, NKV, D, L, layer;
     const float* x_in;
     const float* z_in;
