@@ -22,6 +22,8 @@
 // forward(), in the whole-sequence form of LowLlamaBasic reference.py.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -347,6 +349,14 @@ void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* stat
         if (e.mode == EPI_STORE && !e.zeroed) ks = 1;
         e2.ksplit = ks;
         launch_bn<64, 8>(p, m_rows, e2, status, s, ks);
+        return;
+    }
+    // persistent tiles with a double-buffered accumulator (EMBER_GEMM_TILED=1: one CTA per tile)
+    static const bool tiled = getenv("EMBER_GEMM_TILED") && atoi(getenv("EMBER_GEMM_TILED"));
+    if (!tiled) {
+        const uint32_t idesc = p.f16 ? (p.bn == 64 ? idesc_f16(GEMM_BM, 64) : p.bn == 128 ? idesc_f16(GEMM_BM, 128) : idesc_f16(GEMM_BM, 256))
+                                     : (p.bn == 64 ? idesc_bf16(GEMM_BM, 64) : p.bn == 128 ? idesc_bf16(GEMM_BM, 128) : idesc_bf16(GEMM_BM, 256));
+        launch_gemm_persistent(p.tmA, p.tmB, p.bn, m_rows, p.N, p.K, idesc, e, status, p.sms, s);
         return;
     }
     switch (p.bn) {

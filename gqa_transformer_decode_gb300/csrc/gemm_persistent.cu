@@ -1,0 +1,293 @@
+// gemm_persistent.cu -- persistent tcgen05 GEMM for many-row operands
+// (prefill and encoder projections, M > 128).
+//
+//   D[M,N] = A[M,K] . B[N,K]^T      (f16 or bf16 operands, f32 accumulation)
+//
+// One CTA per SM walks the 128 x BN output tiles (row tiles fastest, so the
+// CTAs running at the same time share weight tiles in L2).  Warp 0 streams A
+// and B k-blocks through a STAGES-deep shared-memory ring across tile
+// boundaries; warp 1 issues tcgen05.mma into one of two TMEM accumulators
+// (2 x BN columns), so the epilogue warps 2-5 drain tile i while tile i + 1
+// accumulates.  Accumulator hand-off: acc_full[b] (MMA commit -> epilogue),
+// acc_empty[b] (128 epilogue arrivals -> MMA).  Every wait is bounded; a
+// timeout raises EMBER_ERR_TIMEOUT, drains the copies in flight and frees
+// TMEM.  Epilogues: bias store, residual add, SwiGLU (f16 out), argmax.
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ember {
+
+namespace {
+
+constexpr int GP_BM = 128;
+constexpr int GP_BK = 64;
+constexpr int GP_THREADS = 192;
+
+// Epilogue of one accumulator tile: this thread's row `row`, columns
+// [n0, n0 + BN), read from TMEM at tbase (lane quadrant already applied).
+template <int BN>
+__device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tbase, int row, int n0,
+                                              int M, int N, unsigned long long& best) {
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld16(tbase + c, r);
+        tmem_ld16(tbase + c + 16, r + 16);
+        tmem_ld_wait();
+        const int n = n0 + c;
+        if (row >= M || n >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        const bool fullc = (n + 32 <= N);
+        if (e.mode == EPI_ARGMAX) {
+            if (e.out_f32) {
+                float* o = e.out_f32 + (size_t)row * e.ldo + n;
+                for (int i = 0; i < 32 && n + i < N; ++i) o[i] = v[i];
+            }
+            for (int i = 0; i < 32 && n + i < N; ++i) {
+                const unsigned long long kk = argmax_key(v[i], (uint32_t)(n + i));
+                best = kk > best ? kk : best;
+            }
+        } else if (e.mode == EPI_SWIGLU) {
+            // columns 2i / 2i+1 = gate_i / up_i -> output column n/2 + i
+            uint16_t* o = e.out_h + (size_t)row * e.ldo + (n >> 1);
+            if (fullc) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float g0 = v[4 * i], u0 = v[4 * i + 1];
+                    const float g1 = v[4 * i + 2], u1 = v[4 * i + 3];
+                    pk[i] = pack_f16x2(__fdividef(g0, 1.f + __expf(-g0)) * u0,
+                                       __fdividef(g1, 1.f + __expf(-g1)) * u1);
+                }
+                uint4* o4 = reinterpret_cast<uint4*>(o);
+                o4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                o4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+                for (int i = 0; i < 16 && n + 2 * i + 1 < N; ++i) {
+                    const float g = v[2 * i], u = v[2 * i + 1];
+                    o[i] = f32_to_f16(__fdividef(g, 1.f + __expf(-g)) * u);
+                }
+            }
+        } else {
+            float* o = e.out_f32 + (size_t)row * e.ldo + n;
+            if (e.mode == EPI_STORE && e.bias) {
+                for (int i = 0; i < 32; ++i)
+                    if (n + i < N) v[i] += e.bias[n + i];
+            }
+            if (fullc) {
+                float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float4 t = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    if (e.mode == EPI_RESID) {
+                        const float4 x = o4[i];
+                        t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
+                    }
+                    o4[i] = t;
+                }
+            } else {
+                for (int i = 0; i < 32 && n + i < N; ++i)
+                    o[i] = (e.mode == EPI_RESID) ? o[i] + v[i] : v[i];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(GP_THREADS, 1)
+    k_gemm_tcp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               int M, int N, int K, uint32_t idesc, GemmEpilogue e, int* status) {
+    constexpr int A_BYTES = GP_BM * GP_BK * 2;
+    constexpr int B_BYTES = BN * GP_BK * 2;
+    constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;     // [2]
+    uint64_t* acc_empty = acc_full + 2;      // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    int* sflag = reinterpret_cast<int*>(tmem_slot + 1);   // [0] failed, [1] issued, [2] consumed
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = (K + GP_BK - 1) / GP_BK;
+    const int n_mt = (M + GP_BM - 1) / GP_BM, n_nt = (N + BN - 1) / BN;
+    const int n_tiles = n_mt * n_nt;
+    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int pre = nk < STAGES ? nk : STAGES;   // weight blocks of the first tile issued early
+    auto tile_mn = [&](int li, int& m0, int& n0) {
+        const int t = (int)blockIdx.x + li * (int)gridDim.x;
+        m0 = (t % n_mt) * GP_BM;
+        n0 = (t / n_mt) * BN;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        sflag[0] = 0;
+        sflag[1] = 0;
+        sflag[2] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (my_tiles > 0) {   // the first tile's weights do not depend on the previous kernel
+            int m0, n0;
+            tile_mn(0, m0, n0);
+            for (int kb = 0; kb < pre; ++kb) {
+                mbar_expect_tx(&full[kb], STAGE_BYTES);
+                tma_load_2d(smem + kb * STAGE_BYTES + A_BYTES, &tmB, kb * GP_BK, n0, &full[kb]);
+            }
+        }
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_u32(tmem_slot)),
+            "r"((uint32_t)(2 * BN)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // activations and the residual stream are the previous kernels' outputs
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer, k-blocks of all my tiles
+            int g = 0;     // global k-block count
+            bool fail = false;
+            for (int li = 0; li < my_tiles && !fail; ++li) {
+                int m0, n0;
+                tile_mn(li, m0, n0);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    uint8_t* sa = smem + s * STAGE_BYTES;
+                    if (g >= pre) {
+                        if (g >= STAGES &&
+                            !mbar_wait(&empty[s], ((uint32_t)(g / STAGES) & 1u) ^ 1u)) {
+                            fail = true;
+                            break;
+                        }
+                        mbar_expect_tx(&full[s], STAGE_BYTES);
+                        tma_load_2d(sa + A_BYTES, &tmB, kb * GP_BK, n0, &full[s]);
+                    }
+                    tma_load_2d(sa, &tmA, kb * GP_BK, m0, &full[s]);
+                }
+            }
+            if (fail) sflag[0] = 1;
+            sflag[1] = g;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------- MMA issuer
+            int g = 0;
+            bool fail = false;
+            for (int li = 0; li < my_tiles && !fail; ++li) {
+                const int b = li & 1;
+                if (!mbar_wait(&acc_empty[b], ((uint32_t)(li >> 1) & 1u) ^ 1u)) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    if (!mbar_wait(&full[s], (uint32_t)(g / STAGES) & 1u)) {
+                        fail = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < GP_BK / 16; ++k)
+                        umma_bf16(acc, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                                  (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(&empty[s]);   // the stage is free once these MMAs read it
+                }
+                if (!fail) umma_commit(&acc_full[b]);
+            }
+            if (fail) sflag[0] = 1;
+            sflag[2] = g;
+        }
+    } else {   // ---------------- epilogue warps 2..5
+        const int q = warp & 3;
+        unsigned long long best = 0ull;
+        int best_row = -1;
+        for (int li = 0; li < my_tiles; ++li) {
+            const int b = li & 1;
+            int m0, n0;
+            tile_mn(li, m0, n0);
+            const int row = m0 + q * 32 + lane;
+            if (!mbar_wait(&acc_full[b], (uint32_t)(li >> 1) & 1u)) {
+                sflag[0] = 1;
+                break;
+            }
+            tc_fence_after();
+            if (e.mode == EPI_ARGMAX && row != best_row) {   // a new row tile: flush the last key
+                if (best && best_row >= 0 && best_row < M) atomicMax(e.keys + best_row, best);
+                best = 0ull;
+                best_row = row;
+            }
+            tile_epilogue<BN>(e, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), row, n0, M, N,
+                              best);
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+        }
+        if (e.mode == EPI_ARGMAX && best && best_row >= 0 && best_row < M)
+            atomicMax(e.keys + best_row, best);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && sflag[0]) raise_status(status, EMBER_ERR_TIMEOUT);
+    if (warp == 0 && lane == 0 && sflag[0]) {   // copies issued but never consumed
+        for (int g = sflag[2]; g < sflag[1]; ++g)
+            (void)mbar_wait(&full[g % STAGES], (uint32_t)(g / STAGES) & 1u);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)(2 * BN)));
+    }
+}
+
+template <int BN, int STAGES>
+static void launch_p(const void* tmA, const void* tmB, int m_rows, int N, int K, uint32_t idesc,
+                     const GemmEpilogue& e, int* status, int sms, cudaStream_t s) {
+    constexpr int STAGE_BYTES = (GP_BM + BN) * GP_BK * 2;
+    constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_gemm_tcp<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        attr = true;
+    }
+    const int tiles = ((m_rows + GP_BM - 1) / GP_BM) * ((N + BN - 1) / BN);
+    const int grid = tiles < sms ? tiles : sms;
+    launch_k(k_gemm_tcp<BN, STAGES>, dim3(grid), dim3(GP_THREADS), SMEM, s,
+             *reinterpret_cast<const CUtensorMap*>(tmA), *reinterpret_cast<const CUtensorMap*>(tmB),
+             m_rows, N, K, idesc, e, status);
+}
+
+void launch_gemm_persistent(const void* tmA, const void* tmB, int bn, int m_rows, int N, int K,
+                            uint32_t idesc, const GemmEpilogue& e, int* status, int sms,
+                            cudaStream_t s) {
+    switch (bn) {
+        case 64: launch_p<64, 8>(tmA, tmB, m_rows, N, K, idesc, e, status, sms, s); break;
+        case 128: launch_p<128, 6>(tmA, tmB, m_rows, N, K, idesc, e, status, sms, s); break;
+        default: launch_p<256, 4>(tmA, tmB, m_rows, N, K, idesc, e, status, sms, s); break;
+    }
+}
+
+}  // namespace ember

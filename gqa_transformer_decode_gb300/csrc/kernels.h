@@ -258,6 +258,10 @@ bool make_gemm_plan(GemmPlan& p, const uint16_t* A, int M, int lda, const uint16
 // the partial sums are added with red.global.add, so EPI_STORE then needs a
 // zeroed output.  gemm_splits() returns the split launch_gemm will use.
 int gemm_splits(const GemmPlan& p, int m_rows, int mode);
+// Persistent tiles for m_rows > 128 (gemm_persistent.cu); launch_gemm picks it.
+void launch_gemm_persistent(const void* tmA, const void* tmB, int bn, int m_rows, int N, int K,
+                            uint32_t idesc, const GemmEpilogue& e, int* status, int sms,
+                            cudaStream_t s);
 // Encode a bf16 TMA tensor map (rank 2..4, 128-byte swizzle, zero fill out
 // of bounds).  dims[0] is the contiguous dimension; strides (rank-1 entries)
 // are in bytes.  False if the driver rejects it.
