@@ -5,8 +5,13 @@
 //   S = Q . K^T                  tcgen05.mma M=128, N=128, K=D  -> TMEM
 //   softmax rows (online)        4 warps, thread r owns query row r (tcgen05.ld)
 //   P -> shared memory           f16, the 128-byte-swizzled K-major A operand
-//   O_t = P . V                  tcgen05.mma (f16) M=128, N=D, K=128 -> TMEM
-//   O = O * exp2(m_old - m_new) + O_t   in registers of the row's thread
+//   O += P . V                   tcgen05.mma (f16) M=128, N=D, K=128, accumulating
+//                                in TMEM across all key tiles
+// The running row maximum m only moves when a tile's maximum exceeds it by
+// more than 2^8 (lazy rescaling): the row's thread then multiplies its O
+// columns in TMEM by exp2(m_old - m_new) after the previous P . V is done,
+// and l with it.  Every term stays <= 2^8 before the final O / l, far from
+// f32 overflow, and the result is the same softmax.
 // Causal rows see keys at positions <= their own (LowLlamaBasic reference.py
 // self_attn()); the bidirectional encoder sees every key of its sequence
 // (PII-Tracer-vLLM forward()).  Q rows come from the RoPE'd bf16 queries, K
@@ -62,7 +67,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint64_t* s_full = bar + 5;
     uint64_t* p_full = bar + 6;
     uint64_t* o_full = bar + 7;
-    uint64_t* o_empty = bar + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
     uint64_t* kconv = bar + 12;     // [2] K tile of the stage converted to f16
     int* sflag = reinterpret_cast<int*>(bar + 10);   // [0] failed, [1] issued, [2] consumed
@@ -88,7 +92,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_init(&kconv[1], 1);
         mbar_init(p_full, 128);
         mbar_init(o_full, 1);
-        mbar_init(o_empty, 128);
         sflag[0] = 0;
         sflag[1] = 0;
         sflag[2] = 0;
@@ -185,9 +188,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                                   sdesc_sw128(k0 + kb * AT_BK * 128 + k * 32), idS,
                                   (kb | k) ? 1u : 0u);
                 umma_commit(s_full);
-                // P . V once the softmax warps have written P and read O_t(j-1)
+                // O += P . V once the softmax warps have written P (and rescaled O)
                 if (!mbar_wait(p_full, (uint32_t)j & 1u)) break;
-                if (!mbar_wait(o_empty, ((uint32_t)j & 1u) ^ 1u)) break;
                 tc_fence_after();
                 const uint32_t p0 = smem_u32(sm + L::OFF_P);
                 const uint32_t v0 = smem_u32(sm + L::OFF_V + s * L::V_BYTES);
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     for (int k = 0; k < 4; ++k)
                         umma_bf16(tO, sdesc_sw128(p0 + kb * AT_BQ * 128 + k * 32),
                                   sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO,
-                                  (kb | k) ? 1u : 0u);
+                                  (j | kb | k) ? 1u : 0u);
                 umma_commit(o_full);
                 umma_commit(&kv_empty[s]);
             }
@@ -205,6 +207,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             sflag[2] = j;
         }
     } else {   // ------------------------------------------------ softmax warps
+        // Thread = query row.  O accumulates in TMEM across key tiles; the row
+        // keeps a reference maximum m and rescales O (and l) only when a tile's
+        // maximum exceeds m by more than RESCALE (log2 units), so p = 2^(s - m)
+        // stays <= 2^RESCALE (f16-safe).  The rescale is a TMEM read-scale-write
+        // by the whole warp after the previous P.V has completed.
+        constexpr float RESCALE = 8.f;
         const int qw = warp & 3;
         const int r = qw * 32 + lane;                 // query row within the tile
         const int qp = a.pos0 + q_first + r;          // its position
@@ -212,9 +220,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
         const float sc_log2 = 1.4426950408889634f * rsqrtf((float)D);
         float m = -INFINITY, l = 0.f;
-        float o[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.f;
         uint8_t* sP = sm + L::OFF_P;
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
@@ -224,100 +229,123 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             }
             tc_fence_after();
             const int key0 = j * AT_BK;
-            // every key of the tile visible to every row of the query tile: no masking
             const bool full = key0 + AT_BK <= a.n_keys && (!a.causal || key0 + AT_BK - 1 <= qmin);
-            // pass 1: row maximum of the visible scores (the scale is positive)
+            // pass 1: row maximum of the visible scores (64 columns per TMEM wait)
             float mt = -INFINITY;
 #pragma unroll
-            for (int c0 = 0; c0 < AT_BK; c0 += 32) {
-                uint32_t v[32];
+            for (int c0 = 0; c0 < AT_BK; c0 += 64) {
+                uint32_t v[64];
                 tmem_ld32(tS + lane_off + c0, v);
+                tmem_ld32(tS + lane_off + c0 + 32, v + 32);
                 tmem_ld_wait();
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(v[i]));
+                    for (int i = 0; i < 64; ++i) mt = fmaxf(mt, __uint_as_float(v[i]));
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 64; ++i) {
                         const int kp = key0 + c0 + i;
-                        const bool vis = kp < a.n_keys && (!a.causal || kp <= qp);
-                        if (vis) mt = fmaxf(mt, __uint_as_float(v[i]));
+                        if (kp < a.n_keys && (!a.causal || kp <= qp)) mt = fmaxf(mt, __uint_as_float(v[i]));
                     }
                 }
             }
             mt *= sc_log2;
-            const float mn = fmaxf(m, mt);
-            const float corr = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-            // pass 2: p = exp2(s - m), row sum, P -> shared (swizzled K-major)
+            // reference maximum: move it (and rescale O, l) only when it falls behind
+            const bool move = mt > m + RESCALE;
+            const float mref = move ? mt : m;
+            const float corr = (m == -INFINITY) ? 0.f : exp2f(m - mref);   // 1 when not moving
+            if (j > 0) {   // PV(j-1) must be complete before O is touched or P is rewritten
+                if (!mbar_wait(o_full, (uint32_t)(j - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(FULL_MASK, move)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + lane_off + c0, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+                        tmem_st16(tO + lane_off + c0, v);
+                        tmem_st16(tO + lane_off + c0 + 16, v + 16);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            l *= corr;
+            m = mref;
+            // pass 2: p = 2^(s - m), row sum, P -> shared (swizzled K-major)
             float rs = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < AT_BK; c0 += 32) {
-                uint32_t v[32];
+            for (int c0 = 0; c0 < AT_BK; c0 += 64) {
+                uint32_t v[64];
                 tmem_ld32(tS + lane_off + c0, v);
+                tmem_ld32(tS + lane_off + c0 + 32, v + 32);
                 tmem_ld_wait();
-                uint32_t pk[16];
-                if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(v[i]), sc_log2, -mn));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[i + 1]), sc_log2, -mn));
-                        rs += p0 + p1;
-                        pk[i / 2] = pack_f16x2(p0, p1);
+                for (int h32 = 0; h32 < 64; h32 += 32) {
+                    uint32_t pk[16];
+                    if (full) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float p0 = ex2(fmaf(__uint_as_float(v[h32 + i]), sc_log2, -m));
+                            const float p1 = ex2(fmaf(__uint_as_float(v[h32 + i + 1]), sc_log2, -m));
+                            rs += p0 + p1;
+                            pk[i / 2] = pack_f16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const int kp = key0 + c0 + h32 + i;
+                            const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
+                            const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
+                            const float p0 = v0 ? ex2(fmaf(__uint_as_float(v[h32 + i]), sc_log2, -m)) : 0.f;
+                            const float p1 = v1 ? ex2(fmaf(__uint_as_float(v[h32 + i + 1]), sc_log2, -m)) : 0.f;
+                            rs += p0 + p1;
+                            pk[i / 2] = pack_f16x2(p0, p1);
+                        }
                     }
-                } else {
+                    const int cc = c0 + h32;
+                    const int kb = cc / 64;
+                    uint8_t* rowp = sP + kb * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const int kp = key0 + c0 + i;
-                        const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
-                        const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
-                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(v[i]), sc_log2, -mn)) : 0.f;
-                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(v[i + 1]), sc_log2, -mn)) : 0.f;
-                        rs += p0 + p1;
-                        pk[i / 2] = pack_f16x2(p0, p1);
+                    for (int t = 0; t < 4; ++t) {
+                        const int chunk = ((cc % 64) / 8) + t;
+                        *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
+                            make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
                     }
-                }
-                const int kb = c0 / 64;
-                uint8_t* rowp = sP + kb * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int chunk = ((c0 % 64) / 8) + t;
-                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
-                        make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive(p_full);
-            l = l * corr + rs;
-            m = mn;
-            if (!mbar_wait(o_full, (uint32_t)j & 1u)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+            l += rs;
+        }
+        if (ok && nkt > 0 && !mbar_wait(o_full, (uint32_t)(nkt - 1) & 1u)) ok = false;
+        if (!ok) sflag[0] = 1;
+        tc_fence_after();
+        if (ok) {
+            const float inv = 1.f / l;
+            const bool live = q_first + r < a.T_per_seq;
+            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + q_first + r) * a.ld_att + h * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tO + lane_off + c0, v);
                 tmem_ld_wait();
+                if (live) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c0 + i] = o[c0 + i] * corr + __uint_as_float(v[i]);
-            }
-            tc_fence_before();
-            mbar_arrive(o_empty);
-        }
-        if (!ok) sflag[0] = 1;
-        if (ok && q_first + r < a.T_per_seq) {
-            const float inv = 1.f / l;
-            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + q_first + r) * a.ld_att + h * D;
-#pragma unroll
-            for (int d = 0; d < D; d += 8) {
-                uint4 w;
-                w.x = pack_f16x2(o[d] * inv, o[d + 1] * inv);
-                w.y = pack_f16x2(o[d + 2] * inv, o[d + 3] * inv);
-                w.z = pack_f16x2(o[d + 4] * inv, o[d + 5] * inv);
-                w.w = pack_f16x2(o[d + 6] * inv, o[d + 7] * inv);
-                *reinterpret_cast<uint4*>(out + d) = w;
+                    for (int d = 0; d < 32; d += 8) {
+                        uint4 w;
+                        w.x = pack_f16x2(__uint_as_float(v[d]) * inv, __uint_as_float(v[d + 1]) * inv);
+                        w.y = pack_f16x2(__uint_as_float(v[d + 2]) * inv, __uint_as_float(v[d + 3]) * inv);
+                        w.z = pack_f16x2(__uint_as_float(v[d + 4]) * inv, __uint_as_float(v[d + 5]) * inv);
+                        w.w = pack_f16x2(__uint_as_float(v[d + 6]) * inv, __uint_as_float(v[d + 7]) * inv);
+                        *reinterpret_cast<uint4*>(out + c0 + d) = w;
+                    }
+                }
             }
         }
     }
