@@ -3,12 +3,16 @@
 // D1 (k_fused_attn): one thread-block cluster of C CTAs per kv head g.  Each
 //   CTA RMS-normalises x, computes its share of the group's q/k/v rows
 //   (weights bulk-loaded into shared memory before the programmatic-launch
-//   wait), broadcasts them through distributed shared memory, applies the
-//   optional q/k RMSNorm and RoPE, writes the new K/V row (the CTA whose key
-//   range holds the position), runs flash attention over its key range for
-//   all G query heads of the group, merges the C partial softmaxes through
-//   distributed shared memory, and multiplies the merged heads by its rows of
-//   the group's o_proj column block, adding the result into the residual.
+//   wait), and sends them with st.async into the shared memory of the CTAs
+//   that run attention (all C, or CTA 0 alone for contexts up to FA_SOLO
+//   keys), where an mbarrier counts the bytes.  Those apply the optional q/k
+//   RMSNorm and RoPE, write the new K/V row (the CTA whose key range holds
+//   the position), run flash attention over their key ranges for all G query
+//   heads of the group and merge the partial softmaxes through distributed
+//   shared memory; the merged heads reach every CTA the same way, and each
+//   multiplies them by its rows of the group's o_proj column block, adding
+//   the result into the residual.  A CTA leaves only after every store aimed
+//   at its shared memory has been counted on its own barrier.
 // D2 (k_fused_mlp): every CTA owns chunks of FC intermediate features:
 //   RMSNorm, the gate/up rows of those features, SwiGLU, and their columns of
 //   down_proj (a transposed f16 copy, so each chunk is 4 contiguous rows),
@@ -38,19 +42,54 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// split cluster barrier: arrive (relaxed) early, wait (acquire) later
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // address of shared variable p in CTA `cta` of this cluster
 __device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t cta) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
     return r;
 }
-__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+// 16-byte store into the shared memory of a CTA of this cluster whose
+// completion counts 16 bytes on that CTA's mbarrier (both addresses from mapa)
+__device__ __forceinline__ void st_async4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+                 "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async1(uint32_t addr, float a, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(a)), "r"(bar)
+                 : "memory");
+}
+// mbarrier wait whose completion orders the stores of other CTAs of the
+// cluster (st.async complete_tx releases at cluster scope); false after ~1 s
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > TC_WAIT_CYCLES) return false;
+    }
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -172,26 +211,24 @@ struct XRegs {
         }
     }
 };
-__device__ __forceinline__ float wdot_f16(const uint4* row, const XRegs& x, int n8) {
-    const int lane = threadIdx.x & 31;
-    float s[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) s[u] = 0.f;
-#pragma unroll
-    for (int i = 0; i < XR_MAX; ++i) {
-        const int c = lane + 32 * i;
-        if (c < n8) {
-            float w[8], xf[8];
-            unpack8_f16(lds128(row + c), w);
-            unpack8_f16(x.v[i], xf);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) s[u] = fmaf(w[u], xf[u], s[u]);
-        }
-    }
-    float t = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL_MASK, t, o);
-    return t;
+// Two f16 products accumulated in f32 (fma.rn.f32.f16 takes f16 operands,
+// which are exact in f32, so this rounds exactly like fmaf on the converted
+// values while skipping the separate conversions).
+__device__ __forceinline__ float fma2_h(uint32_t w, uint32_t x, float acc) {
+    float d;
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t.reg .f32 t;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.f16 t, wl, xl, %3;\n\tfma.rn.f32.f16 %0, wh, xh, t;\n\t}"
+        : "=f"(d)
+        : "r"(w), "r"(x), "f"(acc));
+    return d;
+}
+// dot product of eight f16 pairs, accumulated in order from 0
+__device__ __forceinline__ float fma8_h(const uint4& w, const uint4& x) {
+    float a = fma2_h(w.x, x.x, 0.f);
+    a = fma2_h(w.y, x.y, a);
+    a = fma2_h(w.z, x.z, a);
+    return fma2_h(w.w, x.w, a);
 }
 
 // Four rows at once: the same per-lane chunks for rows r[0..3] (four
@@ -206,21 +243,12 @@ __device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, con
     for (int i = 0; i < XR_MAX; ++i) {
         const int c = lane + 32 * i;
         if (c < n8) {
-            float xf[8], w0[8], w1[8], w2[8], w3[8];
-            unpack8_f16(x.v[i], xf);
-            unpack8_f16(lds128(r0 + c), w0);
-            unpack8_f16(lds128(r1 + c), w1);
-            unpack8_f16(lds128(r2 + c), w2);
-            unpack8_f16(lds128(r3 + c), w3);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                a0 = fmaf(w0[u], xf[u], a0);
-                a1 = fmaf(w1[u], xf[u], a1);
-                a2 = fmaf(w2[u], xf[u], a2);
-                a3 = fmaf(w3[u], xf[u], a3);
-            }
-            s0 += a0; s1 += a1; s2 += a2; s3 += a3;
+            const uint4 xv = x.v[i];
+            const uint4 u0 = lds128(r0 + c), u1 = lds128(r1 + c), u2 = lds128(r2 + c), u3 = lds128(r3 + c);
+            s0 += fma8_h(u0, xv);
+            s1 += fma8_h(u1, xv);
+            s2 += fma8_h(u2, xv);
+            s3 += fma8_h(u3, xv);
         }
     }
     // lanes 0-15 keep rows 0,1 and lanes 16-31 rows 2,3
@@ -266,7 +294,7 @@ __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int n
     L.wm = o; o += 8 * G * (D + 2) * 4;           // the 8 warps' (m, l, O) per head
     L.cs = o; o += D * 4;                         // RoPE row of the position: cos | sin
     L.red = o; o += 32 * 4;
-    L.bar = o; o += 4 * 8;
+    L.bar = o; o += 8 * 8;
     L.total = o + 1024;                           // room to align the base to 1024
     return L;
 }
@@ -293,7 +321,9 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     uint8_t* sQh = sm + Lo.qh;                                 // [16][D] f16, swizzled
     float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [8][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);  // 0: qkv W, 1: K/V, 2: o W
+    // mbarriers: 0 q/k/v weights, 1 K/V tile, 2 o_proj weights, 3 q/k/v rows
+    // received from the cluster, 4 attention output received from the cluster
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);
     __shared__ int s_err;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -307,9 +337,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     // ---- before the wait: immutable weights only ----
     if (tid == 0) {
         s_err = 0;
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        mbar_init(&bar[2], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (r1 > r0) {
             mbar_expect_tx(&bar[0], (uint32_t)((r1 - r0) * rowb));
@@ -343,14 +371,17 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         s_bias[tid] = a.bqkv[src];
     }
     __syncthreads();
+    cluster_arrive_relaxed();   // barriers initialised; matched by cluster_wait() before the first remote store
     pdl_trigger();
     pdl_wait();
 
-    const int ok = __ldcg(a.tok_ok);
-    const int pos = ok ? __ldcg(a.tok_pos) : 0;
-    float* s_cs = reinterpret_cast<float*>(sm + Lo.cs);   // RoPE row of pos (cos | sin)
-    if (ok && tid < D) s_cs[tid] = tid < H2 ? a.cos_t[(size_t)pos * H2 + tid]
-                                            : a.sin_t[(size_t)pos * H2 + tid - H2];
+    // the step's token state, loaded beside the residual (used after the norm)
+    const int ok_raw = __ldcg(a.tok_ok);
+    const int pos_raw = __ldcg(a.tok_pos);
+    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
+
+    const int ok = ok_raw;
+    const int pos = ok ? pos_raw : 0;
     const int n_keys = ok ? pos + 1 : 0;
     // short contexts: CTA 0 takes every key and no partials need merging
     const bool solo = n_keys <= FA_SOLO;
@@ -360,6 +391,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     const int seq = ok ? a.seqs[0] : 0;
     const int kz = (seq * a.L + a.layer) * a.NKV + g;     // (seq, layer, kv head) plane
     const bool owner = ok && pos >= lo && pos < hi;
+    const bool attn_cta = !solo || r == 0;                // receives q/k/v and runs attention
     uint32_t kv_phase = 0;
     auto issue_tile = [&](int t0) {
         const uint32_t bytes = (uint32_t)(2 * NSUB * FA_KT * 128);
@@ -369,12 +401,21 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             tma_load_3d(sV + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, &bar[1]);
         }
     };
-    if (tid == 0 && hi > lo) issue_tile(lo);
+    if (tid == 0) {
+        if (hi > lo) issue_tile(lo);
+        if (attn_cta) mbar_expect_tx(&bar[3], (uint32_t)(Rg * 4));
+        mbar_expect_tx(&bar[4], (uint32_t)(GD * 4));
+    }
+    float cs_v = 0.f;   // RoPE row of pos (cos | sin), stored to shared memory after the rows
+    if (attn_cta && ok && tid < D)
+        cs_v = tid < H2 ? __ldg(a.cos_t + (size_t)pos * H2 + tid) : __ldg(a.sin_t + (size_t)pos * H2 + tid - H2);
+    float* s_cs = reinterpret_cast<float*>(sm + Lo.cs);
 
-    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
-
-    // ---- this CTA's q/k/v rows (a warp a row), broadcast to every CTA of the cluster ----
+    // ---- this CTA's q/k/v rows (a warp a row quad), sent to the CTAs that
+    // run attention: st.async into their shared memory, counted on their
+    // barrier 3 ----
     if (r1 > r0 && !mbar_wait(&bar[0], 0)) s_err = 1;
+    cluster_wait();
     {
         XRegs xr;
         xr.load(s_xh, H / 8);
@@ -389,12 +430,17 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             const int ri = base + my;
             if (ri < nrow) {
                 if (a.bqkv) v += s_bias[ri];
-                st_dsmem(dsmem(&s_qkv[r0 + ri], l8), v);
-                st_dsmem(dsmem(&s_qkv[r0 + ri], l8 + 8), v);
+                if (solo) {
+                    if (l8 == 0) st_async1(dsmem(&s_qkv[r0 + ri], 0), v, dsmem(&bar[3], 0));
+                } else {
+                    st_async1(dsmem(&s_qkv[r0 + ri], l8), v, dsmem(&bar[3], l8));
+                    st_async1(dsmem(&s_qkv[r0 + ri], l8 + 8), v, dsmem(&bar[3], l8 + 8));
+                }
             }
         }
     }
-    cluster_sync_all();
+    if (attn_cta && ok && tid < D) s_cs[tid] = cs_v;
+    __syncthreads();   // the q/k/v weights are consumed; s_cs is complete
 
     // o_proj rows into the (now free) weight buffer, while attention runs
     if (tid == 0 && o1 > o0) {   // one bulk copy: the slice is contiguous
@@ -402,234 +448,239 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         bulk_g2s(sW, wo_cta, wo_bytes, &bar[2]);
     }
 
-    // ---- optional per-head q/k RMSNorm, then RoPE (q pre-scaled, base 2) ----
-    if (a.q_norm) {
-        for (int h = warp; h < G + 1; h += FA_THREADS / 32) {
-            float* v = h < G ? s_qkv + h * D : s_qkv + GD;
-            const float* w = h < G ? a.q_norm : a.k_norm;
-            float ss = 0.f;
-            for (int d = lane; d < D; d += 32) ss += v[d] * v[d];
-            ss = warp_sum(ss);
-            const float ri = rsqrtf(ss / (float)D + a.eps);
-            __syncwarp();
-            for (int d = lane; d < D; d += 32) v[d] = v[d] * ri * w[d];
-        }
-        __syncthreads();
-    }
-    const float qscale = 1.4426950408889634f * rsqrtf((float)D);
-    if (ok) {
-        const float* cs = s_cs;
-        const float* sn = s_cs + H2;
-        for (int e = tid; e < (G + 1) * H2; e += FA_THREADS) {
-            const int h = e / H2, i = e % H2;
-            float* v = h < G ? s_qkv + h * D : s_qkv + GD;
-            float r0v, r1v;
-            rope_pair(v[i], v[i + H2], cs[i], sn[i], r0v, r1v);
-            if (h < G) {
-                v[i] = r0v * qscale;
-                v[i + H2] = r1v * qscale;
-            } else {
-                v[i] = r0v;
-                v[i + H2] = r1v;
+    if (attn_cta) {
+        if (!mbar_wait_cluster(&bar[3], 0)) s_err = 1;
+        // ---- optional per-head q/k RMSNorm, then RoPE (q pre-scaled, base 2) ----
+        if (a.q_norm) {
+            for (int h = warp; h < G + 1; h += FA_THREADS / 32) {
+                float* v = h < G ? s_qkv + h * D : s_qkv + GD;
+                const float* w = h < G ? a.q_norm : a.k_norm;
+                float ss = 0.f;
+                for (int d = lane; d < D; d += 32) ss += v[d] * v[d];
+                ss = warp_sum(ss);
+                const float ri = rsqrtf(ss / (float)D + a.eps);
+                __syncwarp();
+                for (int d = lane; d < D; d += 32) v[d] = v[d] * ri * w[d];
             }
+            __syncthreads();
         }
-    }
-    __syncthreads();
-    if (owner) {   // the new K/V row: to the cache (bf16) and, below, into the tile
-        const size_t off = ((size_t)kz * a.max_len + pos) * D;
-        for (int d = tid; d < D; d += FA_THREADS) {
-            a.kc[off + d] = f32_to_bf16(s_qkv[GD + d]);
-            a.vc[off + d] = f32_to_bf16(s_qkv[GD + D + d]);
-        }
-    }
-
-    // ---- flash attention over keys [lo, hi): the G heads are the 16-row A
-    // operand of mma.m16n8k16 (rows >= G zero), warp w takes keys 16w..16w+15
-    // of each 128-key tile; online softmax per row in registers; P (f16) is
-    // the A operand of O += P V ----
-    constexpr int KS = D / 16, NT = D / 8;
-    for (int e = tid; e < 16 * (D / 8); e += FA_THREADS) {
-        const int rq = e / (D / 8), cq = e % (D / 8);
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (rq < G) {
-            const float* q = s_qkv + rq * D + cq * 8;
-            val = make_uint4(pack_f16x2(q[0], q[1]), pack_f16x2(q[2], q[3]), pack_f16x2(q[4], q[5]),
-                             pack_f16x2(q[6], q[7]));
-        }
-        *reinterpret_cast<uint4*>(sQh + q_off<D>(rq, cq)) = val;
-    }
-    __syncthreads();
-    uint32_t qa[KS][4];
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-        const int mi = lane >> 3;
-        ldsm4(sa_u32(sQh + q_off<D>((mi & 1) * 8 + (lane & 7), 2 * kk + (mi >> 1))), qa[kk][0],
-              qa[kk][1], qa[kk][2], qa[kk][3]);
-    }
-    float o[NT][4];
-#pragma unroll
-    for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4, lane/4 + 8
-    const int g4 = lane >> 2, q4 = lane & 3;
-    for (int t0 = lo; t0 < hi; t0 += FA_KT) {
-        const int nt = min(FA_KT, hi - t0);
-        if (!mbar_wait(&bar[1], kv_phase)) s_err = 1;
-        kv_phase ^= 1;
-        if (owner && pos >= t0 && pos < t0 + nt && tid < D / 8) {   // the row the TMA read stale
-            const int j = pos - t0, cq = tid;
-            const float* kk8 = s_qkv + GD + cq * 8;
-            const float* vv8 = s_qkv + GD + D + cq * 8;
-            *reinterpret_cast<uint4*>(sK + kv_off(j, cq)) =
-                make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
-                           pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
-            *reinterpret_cast<uint4*>(sV + kv_off(j, cq)) =
-                make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
-                           pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
-        }
-        __syncthreads();
-        const int r0k = warp * 16;
-        if (r0k < nt) {   // warp-uniform
-            float s[2][4];
-#pragma unroll
-            for (int n8 = 0; n8 < 2; ++n8) s[n8][0] = s[n8][1] = s[n8][2] = s[n8][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                const int mi = lane >> 3;
-                uint32_t b0, b1, b2, b3;
-                ldsm4(sa_u32(sK + kv_off(r0k + (mi >> 1) * 8 + (lane & 7), 2 * kk + (mi & 1))), b0, b1, b2, b3);
-                mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
-                mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int n8 = 0; n8 < 2; ++n8)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (r0k + n8 * 8 + 2 * q4 + (i & 1) >= nt) s[n8][i] = -INFINITY;
-                    if (i < 2) mx0 = fmaxf(mx0, s[n8][i]);
-                    else mx1 = fmaxf(mx1, s[n8][i]);
+        const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+        if (ok) {
+            const float* cs = s_cs;
+            const float* sn = s_cs + H2;
+            for (int e = tid; e < (G + 1) * H2; e += FA_THREADS) {
+                const int h = e / H2, i = e % H2;
+                float* v = h < G ? s_qkv + h * D : s_qkv + GD;
+                float r0v, r1v;
+                rope_pair(v[i], v[i + H2], cs[i], sn[i], r0v, r1v);
+                if (h < G) {
+                    v[i] = r0v * qscale;
+                    v[i + H2] = r1v * qscale;
+                } else {
+                    v[i] = r0v;
+                    v[i + H2] = r1v;
                 }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: key r0k is valid
-            const float sc0 = exp2f(m0 - mn0), sc1 = exp2f(m1 - mn1);
-            float p[2][4];
-#pragma unroll
-            for (int n8 = 0; n8 < 2; ++n8)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) p[n8][i] = exp2f(s[n8][i] - (i < 2 ? mn0 : mn1));
-            l0 = l0 * sc0 + ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
-            l1 = l1 * sc1 + ((p[0][2] + p[0][3]) + (p[1][2] + p[1][3]));
-            m0 = mn0;
-            m1 = mn1;
-#pragma unroll
-            for (int dn = 0; dn < NT; ++dn) {
-                o[dn][0] *= sc0; o[dn][1] *= sc0;
-                o[dn][2] *= sc1; o[dn][3] *= sc1;
-            }
-            const uint32_t pa[4] = {pack_f16x2(p[0][0], p[0][1]), pack_f16x2(p[0][2], p[0][3]),
-                                    pack_f16x2(p[1][0], p[1][1]), pack_f16x2(p[1][2], p[1][3])};
-#pragma unroll
-            for (int dn = 0; dn < NT; dn += 2) {
-                const int mi = lane >> 3;
-                uint32_t v0, v1, v2, v3;
-                ldsm4t(sa_u32(sV + kv_off(r0k + (mi & 1) * 8 + (lane & 7), dn + (mi >> 1))), v0, v1, v2, v3);
-                mma16816(o[dn], pa, bf2_to_h2(v0), bf2_to_h2(v1));
-                mma16816(o[dn + 1], pa, bf2_to_h2(v2), bf2_to_h2(v3));
             }
         }
         __syncthreads();
-        if (tid == 0 && t0 + FA_KT < hi) issue_tile(t0 + FA_KT);
-    }
-    // the 8 warps' states -> this CTA's partial (m, l, acc) per head
-    l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
-    l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
-    l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
-    l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int row = g4 + 8 * half;
-        if (row < G) {
-            float* w = s_wm + ((size_t)warp * G + row) * (D + 2);
-            if (q4 == 0) {
-                w[0] = half ? m1 : m0;
-                w[1] = half ? l1 : l0;
-            }
-#pragma unroll
-            for (int dn = 0; dn < NT; ++dn) {
-                w[2 + dn * 8 + 2 * q4] = o[dn][2 * half];
-                w[3 + dn * 8 + 2 * q4] = o[dn][2 * half + 1];
+        if (owner) {   // the new K/V row: to the cache (bf16) and, below, into the tile
+            const size_t off = ((size_t)kz * a.max_len + pos) * D;
+            for (int d = tid; d < D; d += FA_THREADS) {
+                a.kc[off + d] = f32_to_bf16(s_qkv[GD + d]);
+                a.vc[off + d] = f32_to_bf16(s_qkv[GD + D + d]);
             }
         }
-    }
-    __syncthreads();
-    for (int e = tid; e < G * (D + 2); e += FA_THREADS) {
-        const int hh = e / (D + 2), k = e % (D + 2);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
-            if (st[1] > 0.f) M = fmaxf(M, st[0]);
-        }
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
-            if (st[1] > 0.f) v = fmaf(st[k], exp2f(st[0] - M), v);
-        }
-        s_part[e] = k == 0 ? M : v;
-    }
-    if (solo) {   // CTA 0 holds the whole softmax: normalise and broadcast the heads
-        __syncthreads();
-        if (r == 0) {
-            for (int e = tid; e < GD; e += FA_THREADS) {
-                const int h = e / D;
-                const float l = s_part[h * (D + 2) + 1];
-                const float O = l > 0.f ? s_part[h * (D + 2) + 2 + e % D] / l : 0.f;
-#pragma unroll
-                for (int cc = 0; cc < C; ++cc) st_dsmem(dsmem(&s_att[e], cc), O);
-            }
-        }
-    } else {
-    cluster_sync_all();
 
-    // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
-    {
-        const int ne = (GD + C - 1) / C;
-        const int e = r * ne + tid;
-        if (tid < ne && e < GD) {
-            const int h = e / D, d = e % D;
-            // log-sum-exp merge of the C partials (empty ranges have l = 0); all
-            // 3*C remote loads are issued before the first is used
-            float mc[C], lc[C], oc[C];
-#pragma unroll
-            for (int cc = 0; cc < C; ++cc) {
-                mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
-                lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
-                oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+        // ---- flash attention over keys [lo, hi): the G heads are the 16-row A
+        // operand of mma.m16n8k16 (rows >= G zero), warp w takes keys 16w..16w+15
+        // of each 128-key tile; online softmax per row in registers; P (f16) is
+        // the A operand of O += P V ----
+        constexpr int KS = D / 16, NT = D / 8;
+        for (int e = tid; e < 16 * (D / 8); e += FA_THREADS) {
+            const int rq = e / (D / 8), cq = e % (D / 8);
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (rq < G) {
+                const float* q = s_qkv + rq * D + cq * 8;
+                val = make_uint4(pack_f16x2(q[0], q[1]), pack_f16x2(q[2], q[3]), pack_f16x2(q[4], q[5]),
+                                 pack_f16x2(q[6], q[7]));
             }
+            *reinterpret_cast<uint4*>(sQh + q_off<D>(rq, cq)) = val;
+        }
+        __syncthreads();
+        uint32_t qa[KS][4];
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const int mi = lane >> 3;
+            ldsm4(sa_u32(sQh + q_off<D>((mi & 1) * 8 + (lane & 7), 2 * kk + (mi >> 1))), qa[kk][0],
+                  qa[kk][1], qa[kk][2], qa[kk][3]);
+        }
+        float o[NT][4];
+#pragma unroll
+        for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4, lane/4 + 8
+        const int g4 = lane >> 2, q4 = lane & 3;
+        for (int t0 = lo; t0 < hi; t0 += FA_KT) {
+            const int nt = min(FA_KT, hi - t0);
+            if (!mbar_wait(&bar[1], kv_phase)) s_err = 1;
+            kv_phase ^= 1;
+            if (owner && pos >= t0 && pos < t0 + nt && tid < D / 8) {   // the row the TMA read stale
+                const int j = pos - t0, cq = tid;
+                const float* kk8 = s_qkv + GD + cq * 8;
+                const float* vv8 = s_qkv + GD + D + cq * 8;
+                *reinterpret_cast<uint4*>(sK + kv_off(j, cq)) =
+                    make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
+                               pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
+                *reinterpret_cast<uint4*>(sV + kv_off(j, cq)) =
+                    make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
+                               pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
+            }
+            __syncthreads();
+            const int r0k = warp * 16;
+            if (r0k < nt) {   // warp-uniform
+                float s[2][4];
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8) s[n8][0] = s[n8][1] = s[n8][2] = s[n8][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const int mi = lane >> 3;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm4(sa_u32(sK + kv_off(r0k + (mi >> 1) * 8 + (lane & 7), 2 * kk + (mi & 1))), b0, b1, b2, b3);
+                    mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
+                    mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (r0k + n8 * 8 + 2 * q4 + (i & 1) >= nt) s[n8][i] = -INFINITY;
+                        if (i < 2) mx0 = fmaxf(mx0, s[n8][i]);
+                        else mx1 = fmaxf(mx1, s[n8][i]);
+                    }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: key r0k is valid
+                const float sc0 = exp2f(m0 - mn0), sc1 = exp2f(m1 - mn1);
+                float p[2][4];
+#pragma unroll
+                for (int n8 = 0; n8 < 2; ++n8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) p[n8][i] = exp2f(s[n8][i] - (i < 2 ? mn0 : mn1));
+                l0 = l0 * sc0 + ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1]));
+                l1 = l1 * sc1 + ((p[0][2] + p[0][3]) + (p[1][2] + p[1][3]));
+                m0 = mn0;
+                m1 = mn1;
+#pragma unroll
+                for (int dn = 0; dn < NT; ++dn) {
+                    o[dn][0] *= sc0; o[dn][1] *= sc0;
+                    o[dn][2] *= sc1; o[dn][3] *= sc1;
+                }
+                const uint32_t pa[4] = {pack_f16x2(p[0][0], p[0][1]), pack_f16x2(p[0][2], p[0][3]),
+                                        pack_f16x2(p[1][0], p[1][1]), pack_f16x2(p[1][2], p[1][3])};
+#pragma unroll
+                for (int dn = 0; dn < NT; dn += 2) {
+                    const int mi = lane >> 3;
+                    uint32_t v0, v1, v2, v3;
+                    ldsm4t(sa_u32(sV + kv_off(r0k + (mi & 1) * 8 + (lane & 7), dn + (mi >> 1))), v0, v1, v2, v3);
+                    mma16816(o[dn], pa, bf2_to_h2(v0), bf2_to_h2(v1));
+                    mma16816(o[dn + 1], pa, bf2_to_h2(v2), bf2_to_h2(v3));
+                }
+            }
+            __syncthreads();
+            if (tid == 0 && t0 + FA_KT < hi) issue_tile(t0 + FA_KT);
+        }
+        // the 8 warps' states -> this CTA's partial (m, l, acc) per head
+        l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
+        l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
+        l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
+        l1 += __shfl_xor_sync(FULL_MASK, l1, 2);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int row = g4 + 8 * half;
+            if (row < G) {
+                float* w = s_wm + ((size_t)warp * G + row) * (D + 2);
+                if (q4 == 0) {
+                    w[0] = half ? m1 : m0;
+                    w[1] = half ? l1 : l0;
+                }
+#pragma unroll
+                for (int dn = 0; dn < NT; ++dn) {
+                    w[2 + dn * 8 + 2 * q4] = o[dn][2 * half];
+                    w[3 + dn * 8 + 2 * q4] = o[dn][2 * half + 1];
+                }
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < G * (D + 2); e += FA_THREADS) {
+            const int hh = e / (D + 2), k = e % (D + 2);
             float M = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < C; ++cc)
-                if (lc[cc] > 0.f) M = fmaxf(M, mc[cc]);
-            float Ls = 0.f, O = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < C; ++cc) {
-                if (lc[cc] > 0.f) {
-                    const float f = exp2f(mc[cc] - M);
-                    Ls = fmaf(lc[cc], f, Ls);
-                    O = fmaf(oc[cc], f, O);
-                }
+            for (int w = 0; w < 8; ++w) {
+                const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
+                if (st[1] > 0.f) M = fmaxf(M, st[0]);
             }
-            O = Ls > 0.f ? O / Ls : 0.f;
+            float v = 0.f;
 #pragma unroll
-            for (int cc = 0; cc < C; ++cc) st_dsmem(dsmem(&s_att[e], cc), O);
+            for (int w = 0; w < 8; ++w) {
+                const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
+                if (st[1] > 0.f) v = fmaf(st[k], exp2f(st[0] - M), v);
+            }
+            s_part[e] = k == 0 ? M : v;
         }
-    }
-    }   // !solo
-    cluster_sync_all();
+        if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA
+            __syncthreads();
+            for (int e = 4 * tid; e < GD; e += 4 * FA_THREADS) {   // D % 4 == 0: one head per quad
+                const float* ph = s_part + (e / D) * (D + 2);
+                const float l = ph[1];
+                const float* acc = ph + 2 + e % D;
+                const float O0 = l > 0.f ? acc[0] / l : 0.f, O1 = l > 0.f ? acc[1] / l : 0.f;
+                const float O2 = l > 0.f ? acc[2] / l : 0.f, O3 = l > 0.f ? acc[3] / l : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) st_async4(dsmem(&s_att[e], cc), O0, O1, O2, O3, dsmem(&bar[4], cc));
+            }
+        } else {
+        cluster_sync_all();   // every CTA's partial is in its shared memory
+
+        // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
+        {
+            const int ne = (GD + C - 1) / C;
+            const int e = r * ne + tid;
+            if (tid < ne && e < GD) {
+                const int h = e / D, d = e % D;
+                // log-sum-exp merge of the C partials (empty ranges have l = 0); all
+                // 3*C remote loads are issued before the first is used
+                float mc[C], lc[C], oc[C];
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) {
+                    mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
+                    lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
+                    oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc)
+                    if (lc[cc] > 0.f) M = fmaxf(M, mc[cc]);
+                float Ls = 0.f, O = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) {
+                    if (lc[cc] > 0.f) {
+                        const float f = exp2f(mc[cc] - M);
+                        Ls = fmaf(lc[cc], f, Ls);
+                        O = fmaf(oc[cc], f, O);
+                    }
+                }
+                O = Ls > 0.f ? O / Ls : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) st_async1(dsmem(&s_att[e], cc), O, dsmem(&bar[4], cc));
+            }
+        }
+        }   // !solo
+    }   // attn_cta
+    // the merged heads, GD floats from the cluster; a CTA leaves only after
+    // every store aimed at its shared memory has landed
+    if (!mbar_wait_cluster(&bar[4], 0)) s_err = 1;
 
     // ---- o_proj: this CTA's rows of the group's column block, into the residual ----
     if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
@@ -655,18 +706,26 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
 constexpr int FM_THREADS = 256;
 
 // Chunk = FC intermediate features: 2*FC gate/up rows then FC down_proj^T
-// rows, 6*FC*H bytes.  Phase 1 gives each gate/up row one warp.
+// rows, 6*FC*H bytes.  Phase 1 keeps all eight warps on the chunk's gate/up
+// rows: a warp takes a quad of rows over one of 16/FC slices of the hidden
+// dimension, and the slices' partial sums meet in shared memory.  Phase 2
+// (down_proj) gives each thread 8 outputs; when the hidden size leaves half
+// of the threads idle, the two halves take the two halves of the chunk's
+// features and their sums are added once at the end.
 template <int FC>
 __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     constexpr int MAXHG = 2;                      // h-groups of 8 per thread: H <= 4096
+    constexpr int QUADS = FC / 2;                 // row quads of a chunk's 2*FC gate/up rows
+    constexpr int KSL = (FM_THREADS / 32) / QUADS;   // hidden-dimension slices per quad
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int H = a.H, ns = a.ns, H8 = H / 8;
     const uint32_t stage_bytes = (uint32_t)(6 * FC * H);
     uint8_t* ring = sm;
-    uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + (size_t)ns * stage_bytes);   // normed input
+    uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + (size_t)ns * stage_bytes);       // normed input
+    float* s_y = reinterpret_cast<float*>(sm + (size_t)ns * stage_bytes + ((H * 2 + 15) / 16) * 16);  // [H]
     __shared__ float s_red[32];
-    __shared__ float s_g[2][2 * FC];
+    __shared__ float s_g[2][KSL][2 * FC];
     __shared__ __align__(8) uint64_t bar[8];
     __shared__ int s_err;
 
@@ -693,13 +752,21 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     }
     ResidualNorm rn;
     rn.load_w(a.norm_w, H);
+    // phase-1 role: row quad qd over the hidden slice [c0, c1) (16-byte units)
+    const int qd = warp % QUADS, ks = warp / QUADS;
+    const int seg = (H8 + KSL - 1) / KSL;
+    const int c0 = min(H8, ks * seg), c1 = min(H8, c0 + seg);
+    // phase-2 role: two halves of the features when 2 * H8 threads suffice
+    const bool halves = 2 * H8 <= FM_THREADS;
+    const int part = halves && tid >= H8 ? 1 : 0;
+    const int hgp = tid - part * H8;              // this thread's h-group in halves mode
     __syncthreads();
     pdl_trigger();
     pdl_wait();
 
     rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
     XRegs xr;
-    xr.load(s_xh, H8);
+    xr.load(s_xh + c0 * 8, c1 - c0);
 
     float y[MAXHG][8];
 #pragma unroll
@@ -711,45 +778,82 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
         const int s = k % ns;
         if (!mbar_wait(&bar[s], (uint32_t)((k / ns) & 1))) s_err = 1;
         const uint8_t* st = ring + (size_t)s * stage_bytes;
-        // gate / up rows: four per warp (2 * FC <= 32 rows over 8 warps)
-        if (warp * 4 < 2 * FC) {
+        {   // gate / up rows 4qd..4qd+3 over this warp's slice
             const uint4* rp[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                rp[q] = reinterpret_cast<const uint4*>(st + (size_t)min(warp * 4 + q, 2 * FC - 1) * H * 2);
-            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, H8);
-            const int rr = warp * 4 + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            if ((lane & 7) == 0 && rr < 2 * FC) s_g[k & 1][rr] = v;
+            for (int q = 0; q < 4; ++q) rp[q] = reinterpret_cast<const uint4*>(st + (size_t)(qd * 4 + q) * H * 2) + c0;
+            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0);
+            const int rr = qd * 4 + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            if ((lane & 7) == 0) s_g[k & 1][ks][rr] = v;
         }
         __syncthreads();   // s_g[k & 1] complete; chunk k - 1 fully consumed
         if (tid == 0 && k >= 1 && k - 1 + ns < my_n) issue(k - 1 + ns);
-        float act[FC];
-#pragma unroll
-        for (int j = 0; j < FC; ++j) {
-            const float gt = s_g[k & 1][2 * j], up = s_g[k & 1][2 * j + 1];
-            act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
-        }
         const uint4* wd = reinterpret_cast<const uint4*>(st + (size_t)4 * FC * H);
+        if (halves) {
+            if (tid < 2 * H8) {
 #pragma unroll
-        for (int q = 0; q < MAXHG; ++q) {
-            const int hg = tid + q * FM_THREADS;
-            if (hg < H8) {
+                for (int jj = 0; jj < FC / 2; ++jj) {
+                    const int j = part * (FC / 2) + jj;
+                    float gt = 0.f, up = 0.f;
 #pragma unroll
-                for (int j = 0; j < FC; ++j) {
+                    for (int z = 0; z < KSL; ++z) {
+                        gt += s_g[k & 1][z][2 * j];
+                        up += s_g[k & 1][z][2 * j + 1];
+                    }
+                    const float act = __fdividef(gt, 1.f + __expf(-gt)) * up;
                     float w[8];
-                    unpack8_f16(lds128(wd + (size_t)j * H8 + hg), w);
+                    unpack8_f16(lds128(wd + (size_t)j * H8 + hgp), w);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) y[q][u] = fmaf(w[u], act[j], y[q][u]);
+                    for (int u = 0; u < 8; ++u) y[0][u] = fmaf(w[u], act, y[0][u]);
+                }
+            }
+        } else {
+            float act[FC];
+#pragma unroll
+            for (int j = 0; j < FC; ++j) {
+                float gt = 0.f, up = 0.f;
+#pragma unroll
+                for (int z = 0; z < KSL; ++z) {
+                    gt += s_g[k & 1][z][2 * j];
+                    up += s_g[k & 1][z][2 * j + 1];
+                }
+                act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
+            }
+#pragma unroll
+            for (int q = 0; q < MAXHG; ++q) {
+                const int hg = tid + q * FM_THREADS;
+                if (hg < H8) {
+#pragma unroll
+                    for (int j = 0; j < FC; ++j) {
+                        float w[8];
+                        unpack8_f16(lds128(wd + (size_t)j * H8 + hg), w);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) y[q][u] = fmaf(w[u], act[j], y[q][u]);
+                    }
                 }
             }
         }
     }
+    if (halves) {   // the second half's sums join the first half's
+        if (part == 1 && tid < 2 * H8) {
+            reinterpret_cast<float4*>(s_y)[2 * hgp] = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
+            reinterpret_cast<float4*>(s_y)[2 * hgp + 1] = make_float4(y[0][4], y[0][5], y[0][6], y[0][7]);
+        }
+        __syncthreads();
+        if (part == 0 && tid < H8 && my_n > 0) {
+            const float4 b0 = reinterpret_cast<const float4*>(s_y)[2 * tid];
+            const float4 b1 = reinterpret_cast<const float4*>(s_y)[2 * tid + 1];
+            red_add4(a.z_acc + 8 * tid, y[0][0] + b0.x, y[0][1] + b0.y, y[0][2] + b0.z, y[0][3] + b0.w);
+            red_add4(a.z_acc + 8 * tid + 4, y[0][4] + b1.x, y[0][5] + b1.y, y[0][6] + b1.z, y[0][7] + b1.w);
+        }
+    } else {
 #pragma unroll
-    for (int q = 0; q < MAXHG; ++q) {
-        const int hg = tid + q * FM_THREADS;
-        if (hg < H8 && my_n > 0) {
-            red_add4(a.z_acc + 8 * hg, y[q][0], y[q][1], y[q][2], y[q][3]);
-            red_add4(a.z_acc + 8 * hg + 4, y[q][4], y[q][5], y[q][6], y[q][7]);
+        for (int q = 0; q < MAXHG; ++q) {
+            const int hg = tid + q * FM_THREADS;
+            if (hg < H8 && my_n > 0) {
+                red_add4(a.z_acc + 8 * hg, y[q][0], y[q][1], y[q][2], y[q][3]);
+                red_add4(a.z_acc + 8 * hg + 4, y[q][4], y[q][5], y[q][6], y[q][7]);
+            }
         }
     }
     if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
@@ -779,7 +883,7 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     if (p.smem_attn > 200 * 1024) return no("attention block needs > 200 KB of shared memory");
     // MLP chunk size: the largest FC in {16, 8, 4} (dividing F) whose two-stage
     // ring still fits beside the attention kernel on one SM; else FC = 4.
-    const int fixed = H * 4 + 256;
+    const int fixed = ((H * 2 + 15) / 16) * 16 + H * 4 + 256;   // s_xh (f16) + s_y (f32) + alignment
     const int budget = 227 * 1024 - p.smem_attn - 2 * 1024;
     p.fc = 0;
     for (int fc : {16, 8, 4})
