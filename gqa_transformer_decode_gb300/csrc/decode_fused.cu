@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [8][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
     // mbarriers: 0 q/k/v weights, 1 K/V tile, 2 o_proj weights, 3 q/k/v rows
-    // received from the cluster, 4 attention output received from the cluster
+    // received from the cluster, 4 attention output received from the cluster,
+    // 5 second K/V tile buffer
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);
     __shared__ int s_err;
 
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     // ---- before the wait: immutable weights only ----
     if (tid == 0) {
         s_err = 0;
-        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (r1 > r0) {
             mbar_expect_tx(&bar[0], (uint32_t)((r1 - r0) * rowb));
@@ -392,17 +393,25 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     const int kz = (seq * a.L + a.layer) * a.NKV + g;     // (seq, layer, kv head) plane
     const bool owner = ok && pos >= lo && pos < hi;
     const bool attn_cta = !solo || r == 0;                // receives q/k/v and runs attention
-    uint32_t kv_phase = 0;
-    auto issue_tile = [&](int t0) {
-        const uint32_t bytes = (uint32_t)(2 * NSUB * FA_KT * 128);
-        mbar_expect_tx(&bar[1], bytes);
+    // CTA 0 alone over more than one tile: the second tile goes to the q/k/v
+    // weight buffer as soon as the rows are done (the CTA's o_proj rows follow
+    // there after attention), so two tiles are in flight
+    constexpr int TILE = FA_KT * D * 2;
+    const bool dual = solo && r == 0 && n_keys > FA_KT && Lo.x - Lo.w >= 2 * TILE;
+    uint8_t* sK1 = reinterpret_cast<uint8_t*>(sW);
+    uint8_t* sV1 = sK1 + TILE;
+    auto issue_tile = [&](int t0, int buf) {   // buffer 0: sK/sV on barrier 1; 1: sK1/sV1 on barrier 5
+        uint8_t* kd = buf ? sK1 : sK;
+        uint8_t* vd = buf ? sV1 : sV;
+        uint64_t* b = buf ? &bar[5] : &bar[1];
+        mbar_expect_tx(b, (uint32_t)(2 * TILE));
         for (int sb = 0; sb < NSUB; ++sb) {
-            tma_load_3d(sK + sb * FA_KT * 128, &k_map, sb * 64, t0, kz, &bar[1]);
-            tma_load_3d(sV + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, &bar[1]);
+            tma_load_3d(kd + sb * FA_KT * 128, &k_map, sb * 64, t0, kz, b);
+            tma_load_3d(vd + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, b);
         }
     };
     if (tid == 0) {
-        if (hi > lo) issue_tile(lo);
+        if (hi > lo) issue_tile(lo, 0);
         if (attn_cta) mbar_expect_tx(&bar[3], (uint32_t)(Rg * 4));
         mbar_expect_tx(&bar[4], (uint32_t)(GD * 4));
     }
@@ -442,10 +451,15 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     if (attn_cta && ok && tid < D) s_cs[tid] = cs_v;
     __syncthreads();   // the q/k/v weights are consumed; s_cs is complete
 
-    // o_proj rows into the (now free) weight buffer, while attention runs
-    if (tid == 0 && o1 > o0) {   // one bulk copy: the slice is contiguous
+    // o_proj rows into the (now free) weight buffer, while attention runs --
+    // or, where the buffer takes the second K/V tile, after attention
+    auto issue_wo = [&]() {   // one bulk copy: the slice is contiguous
         mbar_expect_tx(&bar[2], wo_bytes);
         bulk_g2s(sW, wo_cta, wo_bytes, &bar[2]);
+    };
+    if (tid == 0) {
+        if (dual) issue_tile(lo + FA_KT, 1);
+        else if (o1 > o0) issue_wo();
     }
 
     if (attn_cta) {
@@ -519,18 +533,23 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4, lane/4 + 8
         const int g4 = lane >> 2, q4 = lane & 3;
-        for (int t0 = lo; t0 < hi; t0 += FA_KT) {
+        uint32_t ph0 = 0, ph1 = 0;
+        for (int t0 = lo, j = 0; t0 < hi; t0 += FA_KT, ++j) {
             const int nt = min(FA_KT, hi - t0);
-            if (!mbar_wait(&bar[1], kv_phase)) s_err = 1;
-            kv_phase ^= 1;
+            const int b = dual ? (j & 1) : 0;
+            uint8_t* sKt = b ? sK1 : sK;
+            uint8_t* sVt = b ? sV1 : sV;
+            if (!mbar_wait(b ? &bar[5] : &bar[1], b ? ph1 : ph0)) s_err = 1;
+            if (b) ph1 ^= 1;
+            else ph0 ^= 1;
             if (owner && pos >= t0 && pos < t0 + nt && tid < D / 8) {   // the row the TMA read stale
-                const int j = pos - t0, cq = tid;
+                const int jr = pos - t0, cq = tid;
                 const float* kk8 = s_qkv + GD + cq * 8;
                 const float* vv8 = s_qkv + GD + D + cq * 8;
-                *reinterpret_cast<uint4*>(sK + kv_off(j, cq)) =
+                *reinterpret_cast<uint4*>(sKt + kv_off(jr, cq)) =
                     make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
                                pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
-                *reinterpret_cast<uint4*>(sV + kv_off(j, cq)) =
+                *reinterpret_cast<uint4*>(sVt + kv_off(jr, cq)) =
                     make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
                                pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
             }
@@ -544,7 +563,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
                 for (int kk = 0; kk < KS; ++kk) {
                     const int mi = lane >> 3;
                     uint32_t b0, b1, b2, b3;
-                    ldsm4(sa_u32(sK + kv_off(r0k + (mi >> 1) * 8 + (lane & 7), 2 * kk + (mi & 1))), b0, b1, b2, b3);
+                    ldsm4(sa_u32(sKt + kv_off(r0k + (mi >> 1) * 8 + (lane & 7), 2 * kk + (mi & 1))), b0, b1, b2, b3);
                     mma16816(s[0], qa[kk], bf2_to_h2(b0), bf2_to_h2(b1));
                     mma16816(s[1], qa[kk], bf2_to_h2(b2), bf2_to_h2(b3));
                 }
@@ -583,14 +602,17 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
                 for (int dn = 0; dn < NT; dn += 2) {
                     const int mi = lane >> 3;
                     uint32_t v0, v1, v2, v3;
-                    ldsm4t(sa_u32(sV + kv_off(r0k + (mi & 1) * 8 + (lane & 7), dn + (mi >> 1))), v0, v1, v2, v3);
+                    ldsm4t(sa_u32(sVt + kv_off(r0k + (mi & 1) * 8 + (lane & 7), dn + (mi >> 1))), v0, v1, v2, v3);
                     mma16816(o[dn], pa, bf2_to_h2(v0), bf2_to_h2(v1));
                     mma16816(o[dn + 1], pa, bf2_to_h2(v2), bf2_to_h2(v3));
                 }
             }
             __syncthreads();
-            if (tid == 0 && t0 + FA_KT < hi) issue_tile(t0 + FA_KT);
+            // refill this buffer: with two buffers the tile after next, else the next
+            const int nx = t0 + (dual ? 2 : 1) * FA_KT;
+            if (tid == 0 && nx < hi) issue_tile(nx, b);
         }
+        if (dual && tid == 0 && o1 > o0) issue_wo();   // the second buffer has been read
         // the 8 warps' states -> this CTA's partial (m, l, acc) per head
         l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
         l0 += __shfl_xor_sync(FULL_MASK, l0, 2);

@@ -275,12 +275,16 @@ def test_tensor_core_chunked_prefill(stream):
 
 
 @pytest.mark.parametrize("shape,n_prompt,n_steps,seq", [(MID_QWEN2, 1, 20, 0),
+                                                        (MID_QWEN2, 124, 8, 0),
+                                                        (MID_QWEN2, 380, 8, 1),
                                                         (MID_LLAMA, 2100, 6, 1),
                                                         (MID_D128, 300, 8, 1)])
 def test_fused_batch1_decode_matches_oracle(shape, n_prompt, n_steps, seq, stream):
     """Batch-1 decode on the two-kernels-per-layer path (head_dim 64 / 128): one
-    key, a context of more than 16 tiles of 128 keys (every CTA of a cluster
-    loops over two tiles), q/k norm with head_dim 128; second cache slot."""
+    key; contexts crossing 128 keys (one CTA, second tile double-buffered) and
+    384 keys (one CTA -> keys spread over the cluster); a context of more than
+    16 tiles of 128 keys (every CTA of a cluster loops over two tiles); three
+    tiles in one CTA and q/k norm with head_dim 128; second cache slot."""
     w, om, gm = model_pair(shape, max_tokens=max(512, n_prompt + 16))
     prompt = synth.prompt_ids(shape, n_prompt)
     toks, olg, _ = om.greedy(prompt, n_steps)
