@@ -254,6 +254,74 @@ class EncodeJob:
         return lin + att
 
 
+def _family(name: str) -> str:
+    return name.split("<")[0]
+
+
+def decode_family_bytes(shape, B: int, ctx: int) -> dict:
+    """Algorithmic HBM bytes per decode step of each kernel family (weights
+    in bf16, once; K/V rows of ctx keys per sequence and kv head, bf16; the
+    f32 residual stream: read x and z, write x, zero z, accumulate z)."""
+    H, D, F, V, L = shape.hidden, shape.head_dim, shape.ff, shape.vocab, shape.layers
+    NH, NKV = shape.n_heads, shape.n_kv_heads
+    qkv = (NH + 2 * NKV) * D * H * 2 + (NH + 2 * NKV) * D * 4 * shape.qkv_bias
+    o = H * NH * D * 2
+    mlp = 3 * F * H * 2
+    kv_read = B * NKV * D * 2 * 2 * ctx
+    kv_write = B * NKV * D * 2 * 2
+    resid = 5 * B * H * 4
+    head = V * H * 2
+    return {
+        # batch-1 fused path: the attention block carries its projections
+        "k_fused_attn": L * (qkv + o + kv_read + kv_write + resid),
+        "k_fused_mlp": L * (mlp + resid),
+        "k_gemv": head,
+        # batched path: projections and head on the tensor-core GEMM, attention
+        # reads the cache
+        "k_gemm_tcp": L * (qkv + o + mlp) + head,
+        "k_gemm_tc": L * (qkv + o + mlp) + head,
+        "k_attn_decode_mma": L * (kv_read + kv_write),
+        "k_attn_decode": L * (kv_read + kv_write),
+    }
+
+
+def decode_roofline(job, hbm_peak):
+    """The dominant kernel of a decode step: one step run through
+    ember_decode_step_traced (eager, one kernel at a time, CUDA events around
+    every launch on the launching stream), kernels grouped by family; the
+    family with the most device time gets achieved = its algorithmic bytes
+    per launch / its mean launch time."""
+    m, kv, s = job.model, job.kv, job.stream
+    ctx = job.P + job.S + 1          # keys a sequence holds after the traced step
+    trace = m.decode_step_traced(kv, job.seqs, job.cur, None, argmax=job.cur, stream=s)
+    fam = {}
+    for name, us in trace:
+        f = fam.setdefault(_family(name), {"us": 0.0, "n": 0, "name": name})
+        f["us"] += us
+        f["n"] += 1
+    total = sum(f["us"] for f in fam.values())
+    top = max(fam, key=lambda k: fam[k]["us"])
+    nbytes = decode_family_bytes(job.wl.model, job.B, ctx).get(top)
+    t = fam[top]
+    avg_us = t["us"] / t["n"]
+    out = {"kernel": t["name"], "bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
+           "launches_per_step": t["n"], "avg_launch_us": round(avg_us, 2),
+           "share_of_step": round(t["us"] / total, 4),
+           "timing": "one decode step via ember_decode_step_traced: launches serialised (a one-off graph), "
+                     "CUDA events on the launching stream",
+           "traffic": None,
+           "step_launches": {k: {"n": v["n"], "us": round(v["us"], 1)} for k, v in
+                             sorted(fam.items(), key=lambda kv_: -kv_[1]["us"])}}
+    if nbytes is None:
+        out.update({"achieved": None, "frac": None, "bytes_per_launch": None})
+    else:
+        per = nbytes / t["n"]
+        gbs = per / (avg_us * 1e-6) / 1e9
+        out.update({"achieved": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                    "bytes_per_launch": int(per)})
+    return out
+
+
 def gemv_roofline(stream, hbm_peak, n_launch=30):
     """Live CUDA-event timing of the split GEMV (the decode projections'
     kernel) on the LM-head shape of the workload, alone, inputs > L2."""
@@ -357,7 +425,16 @@ def run_gpu(args):
                "unit": "tok/s", "h2d_bytes_per_step": int(host_ids.numel() * 4),
                "d2h_bytes_per_step": int(host_out.numel() * 4)}
 
-    roof = gemv_roofline(stream, hbm_peak)
+    if encoder:   # the whole encode job, tensor-core bound (projections + attention)
+        roof = {"kernel": "encode job (all launches)", "bound": "tensor", "unit": "TFLOP/s",
+                "achieved": round(job.flops_per_job() / (step_ms * 1e-3) / 1e12, 1),
+                "peak": bf16_peak, "traffic": None,
+                "timing": "CUDA events around each timed job on the launching stream"}
+        roof["frac"] = round(roof["achieved"] / bf16_peak, 4)
+    else:
+        roof = decode_roofline(job, hbm_peak)
+        assert job.model.sync_status(stream) == 0
+    gemv_alone = gemv_roofline(stream, hbm_peak)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -381,6 +458,7 @@ def run_gpu(args):
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(step_gbs / hbm_peak, 4),
                      "peak_source": peak_src},
         "roofline": roof,
+        "lm_head_gemv_alone": gemv_alone,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),

@@ -1,13 +1,13 @@
 // decode_attn_mma.cu -- split-KV decode attention on the warp tensor cores
 // (head_dim 64 / 128, up to 16 query heads per kv head).
 //
-// One CTA = (token b, kv head g, key split); 4 warps.  The G query heads of
+// One CTA = (token b, kv head g, key split); 8 warps.  The G query heads of
 // the group are the 16-row A operand (rows >= G are zero): per 128-key tile,
-// warp w takes keys 32w..32w+31 in two blocks of 16 and computes S = Q K^T with mma.m16n8k16
+// warp w takes keys 16w..16w+15 and computes S = Q K^T with mma.m16n8k16
 // (f16 operands, f32 accumulators; K fragments by ldmatrix from a swizzled
 // shared tile), keeps an online softmax per row in the base-2 domain, packs P
 // to f16 in registers as the A operand of O += P V (V fragments by
-// ldmatrix.trans).  The four warps' states are merged in shared memory; the
+// ldmatrix.trans).  The eight warps' states are merged in shared memory; the
 // split partials are merged by the last CTA of the (token, kv head) as in
 // the SIMT kernel.  K/V tiles of 128 keys stream through a 2-3 stage ring of
 // bulk tensor copies (bf16, 128-byte swizzle) issued as soon as the position
@@ -24,7 +24,9 @@ namespace ember {
 
 namespace {
 
-constexpr int AM_THREADS = 128;
+constexpr int AM_THREADS = 256;
+constexpr int AM_WARPS = AM_THREADS / 32;
+constexpr int AM_KW = 128 / AM_WARPS;     // keys of a tile per warp (blocks of 16)
 constexpr int AM_TK = 128;              // keys per tile (the TMA box height)
 constexpr int AM_MIN_CHUNK = 64;        // keys per split at least
 constexpr int AM_MAX_SPLITS = 32;       // partial buffer layout (same as the SIMT kernel)
@@ -66,8 +68,8 @@ struct AmSmem {
     static constexpr int R0 = 4096;                      // ring (1024-aligned)
     static constexpr int BAR = R0 + NS * 2 * TILE;
     static constexpr int END = BAR + 64;
-    // after the key loop the ring holds the warps' states [4][16][D + 2] f32
-    static_assert(4 * 16 * (D + 2) * 4 <= NS * 2 * TILE, "merge scratch");
+    // after the key loop the ring holds the warps' states [AM_WARPS][16][D + 2] f32
+    static_assert(AM_WARPS * 16 * (D + 2) * 4 <= NS * 2 * TILE, "merge scratch");
     static_assert(16 * D * 2 <= R0, "q tile");
     static constexpr int TOTAL = END + 1024;
 };
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
         ldsm4(sa_u32(sm + L::Q + q_off<D>(r, c)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
 
-    // ---- keys [lo, hi): tiles of 128 from the ring; warp w takes keys 32w..32w+31 ----
+    // ---- keys [lo, hi): tiles of 128 from the ring; warp w takes keys AM_KW*w.. ----
     float o[NT][4];
 #pragma unroll
     for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
@@ -219,8 +221,8 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
         }
         __syncthreads();
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            const int r0k = warp * 32 + blk * 16;       // first key row of this block in the tile
+        for (int blk = 0; blk < AM_KW / 16; ++blk) {
+            const int r0k = warp * AM_KW + blk * 16;    // first key row of this block in the tile
             const int kw = t0 + r0k;
             if (kw >= hi) continue;                     // warp-uniform
             float s[2][4];
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
     }
     if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
 
-    // ---- merge the four warps: [4][16][D + 2] f32 = (m, l, O) per warp and row ----
+    // ---- merge the warps: [AM_WARPS][16][D + 2] f32 = (m, l, O) per warp and row ----
     l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
     l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
     l1 += __shfl_xor_sync(FULL_MASK, l1, 1);
@@ -309,13 +311,13 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
         const int h = e / (D + 2), k = e % (D + 2);   // k: 0 = m, 1 = l, 2.. = O
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < AM_WARPS; ++w) {
             const float* st = ws + ((size_t)w * 16 + h) * (D + 2);
             if (st[1] > 0.f) M = fmaxf(M, st[0]);
         }
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < AM_WARPS; ++w) {
             const float* st = ws + ((size_t)w * 16 + h) * (D + 2);
             if (st[1] > 0.f) v = fmaf(k == 0 ? 0.f : st[k], exp2f(st[0] - M), v);
         }
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
             if (k >= 2) {
                 float Ls = 0.f;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int w = 0; w < AM_WARPS; ++w) {
                     const float* st = ws + ((size_t)w * 16 + h) * (D + 2);
                     if (st[1] > 0.f) Ls = fmaf(st[1], exp2f(st[0] - M), Ls);
                 }

@@ -184,13 +184,15 @@ struct ResidualNorm {
 // lane l keeps chunks c = l + 32*i (8 f16 values each) of the input, so
 // shared memory only streams the weights.  Eight partial sums per lane, then
 // a 5-step butterfly (every lane gets the row's value).
-constexpr int XR_MAX = 8;          // chunks per lane: input length <= 8 * 32 * 8 = 2048
+// XI chunks per lane: input length <= XI * 32 * 8 (XI = 4: 1024, 8: 2048); the
+// kernels are instantiated for both so that short inputs run no dead code.
+template <int XI>
 struct XRegs {
-    uint4 v[XR_MAX];
+    uint4 v[XI];
     __device__ __forceinline__ void load(const uint16_t* xh, int n8) {   // f16 input
         const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int i = 0; i < XR_MAX; ++i) {
+        for (int i = 0; i < XI; ++i) {
             const int c = lane + 32 * i;
             v[i] = c < n8 ? reinterpret_cast<const uint4*>(xh)[c] : make_uint4(0, 0, 0, 0);
         }
@@ -198,7 +200,7 @@ struct XRegs {
     __device__ __forceinline__ void load_f32(const float* x, int n8) {  // f32 input, rounded to f16
         const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int i = 0; i < XR_MAX; ++i) {
+        for (int i = 0; i < XI; ++i) {
             const int c = lane + 32 * i;
             if (c < n8) {
                 const float4 a = reinterpret_cast<const float4*>(x)[2 * c];
@@ -235,12 +237,13 @@ __device__ __forceinline__ float fma8_h(const uint4& w, const uint4& x) {
 // independent streams of loads and FMAs), then a transposing butterfly that
 // leaves row ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1) summed in every lane of
 // its group of 8 (6 shuffles instead of 20).  Rows may repeat (padding).
+template <int XI>
 __device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, const uint4* r2,
-                                           const uint4* r3, const XRegs& x, int n8) {
+                                           const uint4* r3, const XRegs<XI>& x, int n8) {
     const int lane = threadIdx.x & 31;
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-    for (int i = 0; i < XR_MAX; ++i) {
+    for (int i = 0; i < XI; ++i) {
         const int c = lane + 32 * i;
         if (c < n8) {
             const uint4 xv = x.v[i];
@@ -299,7 +302,7 @@ __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int n
     return L;
 }
 
-template <int D>
+template <int D, int XI>
 __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_constant__ CUtensorMap k_map,
                                                            const __grid_constant__ CUtensorMap v_map,
                                                            FusedAttnArgs a) {
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     if (r1 > r0 && !mbar_wait(&bar[0], 0)) s_err = 1;
     cluster_wait();
     {
-        XRegs xr;
+        XRegs<XI> xr;
         xr.load(s_xh, H / 8);
         const int nrow = r1 - r0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1), l8 = lane & 7;
@@ -707,7 +710,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     // ---- o_proj: this CTA's rows of the group's column block, into the residual ----
     if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
     {
-        XRegs xr;
+        XRegs<XI> xr;
         xr.load_f32(s_att, GD / 8);
         const int nrow = o1 - o0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
@@ -734,7 +737,7 @@ constexpr int FM_THREADS = 256;
 // (down_proj) gives each thread 8 outputs; when the hidden size leaves half
 // of the threads idle, the two halves take the two halves of the chunk's
 // features and their sums are added once at the end.
-template <int FC>
+template <int FC, int XI>
 __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     constexpr int MAXHG = 2;                      // h-groups of 8 per thread: H <= 4096
     constexpr int QUADS = FC / 2;                 // row quads of a chunk's 2*FC gate/up rows
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     pdl_wait();
 
     rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
-    XRegs xr;
+    XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
 
     float y[MAXHG][8];
@@ -892,8 +895,9 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     if (D != 64 && D != 128) return no("head_dim is not 64 or 128");
     if (NH % NKV) return no("n_heads % n_kv_heads != 0");
     const int G = NH / NKV;
-    if (G > 16 || H % 8 || H > XR_MAX * 256 || F % 4 || (G * D) % 8)
-        return no("group > 16 heads, hidden % 8, hidden > 2048 or ff % 4");
+    if (G > 16 || H % 8 || H > 2048 || G * D > 2048 || F % 4 || (G * D) % 8)
+        return no("group > 16 heads, hidden % 8, hidden or group width > 2048, or ff % 4");
+    p.xi = (H <= 1024 && G * D <= 1024) ? 4 : 8;
     const int C = FA_C;
     p.C = C;
     p.nr = ((G + 2) * D + C - 1) / C;
@@ -941,15 +945,20 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - (int)fa.sharedSizeBytes);
     };
-    if (D == 64) setup(k_fused_attn<64>, p.smem_attn);
-    else setup(k_fused_attn<128>, p.smem_attn);
-    if (e == cudaSuccess) {
-        e = D == 64 ? cudaFuncSetAttribute(k_fused_attn<64>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)
-                    : cudaFuncSetAttribute(k_fused_attn<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    }
-    setup(k_fused_mlp<4>, p.smem_mlp);
-    setup(k_fused_mlp<8>, p.smem_mlp);
-    setup(k_fused_mlp<16>, p.smem_mlp);
+    auto setup_attn = [&](auto kern) {
+        setup(kern, p.smem_attn);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    };
+    setup_attn(k_fused_attn<64, 4>);
+    setup_attn(k_fused_attn<64, 8>);
+    setup_attn(k_fused_attn<128, 4>);
+    setup_attn(k_fused_attn<128, 8>);
+    setup(k_fused_mlp<4, 4>, p.smem_mlp);
+    setup(k_fused_mlp<8, 4>, p.smem_mlp);
+    setup(k_fused_mlp<16, 4>, p.smem_mlp);
+    setup(k_fused_mlp<4, 8>, p.smem_mlp);
+    setup(k_fused_mlp<8, 8>, p.smem_mlp);
+    setup(k_fused_mlp<16, 8>, p.smem_mlp);
     if (e != cudaSuccess) return no("kernel attributes rejected");
     // one cluster of C CTAs must fit somewhere on the chip
     cudaLaunchConfig_t cfg = {};
@@ -964,8 +973,10 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    e = D == 64 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64>, &cfg)
-                : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128>, &cfg);
+    e = D == 64 ? (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 4>, &cfg)
+                             : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 8>, &cfg))
+                : (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 4>, &cfg)
+                             : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 8>, &cfg));
     if (e != cudaSuccess) return no("cluster occupancy query failed");
     if (n < 1) return no("a cluster of 16 CTAs does not fit");
     p.ok = true;
@@ -973,7 +984,7 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     return true;
 }
 
-void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int smem,
+void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int xi, int smem,
                        cudaStream_t s) {
     count_launches(1);
     cudaLaunchConfig_t cfg = {};
@@ -992,15 +1003,23 @@ void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
     const CUtensorMap& km = *reinterpret_cast<const CUtensorMap*>(k_map);
     const CUtensorMap& vm = *reinterpret_cast<const CUtensorMap*>(v_map);
-    if (a.D == 64) cudaLaunchKernelEx(&cfg, k_fused_attn<64>, km, vm, a);
-    else cudaLaunchKernelEx(&cfg, k_fused_attn<128>, km, vm, a);
+    auto kern = a.D == 64 ? (xi == 4 ? k_fused_attn<64, 4> : k_fused_attn<64, 8>)
+                          : (xi == 4 ? k_fused_attn<128, 4> : k_fused_attn<128, 8>);
+    trace_launch(reinterpret_cast<const void*>(kern), s);
+    cudaLaunchKernelEx(&cfg, kern, km, vm, a);
 }
 
-void launch_fused_mlp(const FusedMlpArgs& a, int fc, int grid, int smem, cudaStream_t s) {
+void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s) {
     const dim3 g(grid), b(FM_THREADS);
-    if (fc == 16) launch_k(k_fused_mlp<16>, g, b, (size_t)smem, s, a);
-    else if (fc == 8) launch_k(k_fused_mlp<8>, g, b, (size_t)smem, s, a);
-    else launch_k(k_fused_mlp<4>, g, b, (size_t)smem, s, a);
+    if (xi == 4) {
+        if (fc == 16) launch_k(k_fused_mlp<16, 4>, g, b, (size_t)smem, s, a);
+        else if (fc == 8) launch_k(k_fused_mlp<8, 4>, g, b, (size_t)smem, s, a);
+        else launch_k(k_fused_mlp<4, 4>, g, b, (size_t)smem, s, a);
+    } else {
+        if (fc == 16) launch_k(k_fused_mlp<16, 8>, g, b, (size_t)smem, s, a);
+        else if (fc == 8) launch_k(k_fused_mlp<8, 8>, g, b, (size_t)smem, s, a);
+        else launch_k(k_fused_mlp<4, 8>, g, b, (size_t)smem, s, a);
+    }
 }
 
 // wdT[f][h] = wd[h][f] (16-bit elements), 32x32 tiles through shared memory

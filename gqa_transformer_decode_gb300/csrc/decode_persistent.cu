@@ -92,6 +92,7 @@ cudaError_t launch_persist(const PersistArgs& a, int grid, int smem, cudaStream_
     PkKernel k = pk_kernel(a);
     if (!k) return cudaErrorInvalidValue;
     count_launches(1);
+    trace_launch(reinterpret_cast<const void*>(k), s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(PK_THREADS);

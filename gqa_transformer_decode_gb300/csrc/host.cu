@@ -122,9 +122,31 @@ std::atomic<unsigned long long> g_kv_gen{0};   // a unique id per KV cache ever 
 }  // namespace
 
 namespace ember {
+// Launch trace of ember_decode_step_traced: an event before every kernel
+// launch of the calling thread (and one after the last), with the kernel.
+struct LaunchTrace {
+    std::vector<cudaEvent_t> ev;
+    std::vector<const void*> fn;
+    cudaError_t err = cudaSuccess;
+};
+thread_local LaunchTrace* g_trace = nullptr;
+void trace_launch(const void* fn, cudaStream_t s) {
+    if (!g_trace) return;
+    cudaEvent_t e = nullptr;
+    cudaError_t r = cudaEventCreate(&e);
+    // External: under stream capture the record becomes an event node of the graph
+    if (r == cudaSuccess) r = cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    if (r != cudaSuccess) {
+        if (g_trace->err == cudaSuccess) g_trace->err = r;
+        if (e) cudaEventDestroy(e);
+        return;
+    }
+    g_trace->ev.push_back(e);
+    g_trace->fn.push_back(fn);
+}
 bool pdl_enabled() {
     static const bool on = !(getenv("EMBER_NO_PDL") && atoi(getenv("EMBER_NO_PDL")));
-    return on;
+    return on && !g_trace;   // traced launches run one after another
 }
 void count_launches(long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 unsigned long long launches_so_far() { return (unsigned long long)g_launches.load(); }
@@ -880,7 +902,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.C = fp.C;
             a.nr = fp.nr;
             a.no = fp.no;
-            launch_fused_attn(kv->k_map, kv->v_map, a, fp.smem_attn, s);
+            launch_fused_attn(kv->k_map, kv->v_map, a, fp.xi, fp.smem_attn, s);
             FusedMlpArgs f{};
             f.wgu = L.wgu;
             f.wdT = L.wdT;
@@ -891,7 +913,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             io(f.x_in, f.z_in, f.x_out, f.z_zero, f.z_acc);
             f.status = m->status;
             f.ns = fp.ns;
-            launch_fused_mlp(f, fp.fc, fp.mlp_grid, fp.smem_mlp, s);
+            launch_fused_mlp(f, fp.fc, fp.xi, fp.mlp_grid, fp.smem_mlp, s);
         }
         GemvArgs g{};
         g.W = m->embed;
@@ -1140,6 +1162,58 @@ extern "C" ember_status ember_decode_step(ember_model* m, ember_kv* kv, int32_t 
     m->graphs.push_back({kv->gen, batch, seqs, ids, positions, logits, argmax, exec, kernels});
     CK(cudaGraphLaunch(exec, s));
     count_launches(kernels);
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_decode_step_traced(ember_model* m, ember_kv* kv, int32_t batch,
+                                                 const int32_t* seqs, const int32_t* ids,
+                                                 const int32_t* positions, float* logits, int32_t* argmax,
+                                                 ember_stream_t stream, float* launch_us, const char** names,
+                                                 int32_t cap, int32_t* n) {
+    if (!m || !kv || !seqs || !ids || !n || cap < 0 || (cap > 0 && (!launch_us || !names)))
+        return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv, seqs, ids, n, or trace buffers");
+    if (kv->m != m) return fail(EMBER_ERR_INVALID_ARG, "kv belongs to another model");
+    if (batch <= 0) return fail(EMBER_ERR_INVALID_ARG, "batch must be > 0");
+    if (batch > MAX_DECODE_BATCH || batch > m->T || batch > kv->max_seqs)
+        return fail(EMBER_ERR_CAPACITY, "batch %d exceeds the decode capacity", batch);
+    std::lock_guard<std::mutex> lock(m->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaStreamCaptureStatus capst = cudaStreamCaptureStatusNone;
+    CK(cudaStreamIsCapturing(s, &capst));
+    if (capst != cudaStreamCaptureStatusNone)
+        return fail(EMBER_ERR_INVALID_ARG, "a traced step cannot be captured");
+    // captured into a one-off graph (event-record nodes between the kernel
+    // nodes), so that host launch latency adds no gaps between launches
+    LaunchTrace tr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        g_trace = &tr;
+        decode_enqueue(m, kv, batch, seqs, ids, positions, logits, argmax, s);
+        trace_launch(nullptr, s);   // the end of the last launch
+        g_trace = nullptr;
+        const cudaError_t le = cudaGetLastError();
+        e = cudaStreamEndCapture(s, &graph);
+        if (e == cudaSuccess) e = le;
+        if (e == cudaSuccess) e = tr.err;
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e == cudaSuccess) e = cudaGraphLaunch(exec, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
+    const int k = (int)tr.ev.size() - 1;
+    *n = k < 0 ? 0 : k;
+    for (int i = 0; e == cudaSuccess && i < k && i < cap; ++i) {
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, tr.ev[i], tr.ev[i + 1]);
+        launch_us[i] = ms * 1e3f;
+        const char* nm = nullptr;
+        names[i] = cudaFuncGetName(&nm, tr.fn[i]) == cudaSuccess && nm ? nm : "?";
+    }
+    for (cudaEvent_t ev : tr.ev) cudaEventDestroy(ev);
+    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "traced decode step: %s", cudaGetErrorString(e));
     return EMBER_OK;
 }
 

@@ -8,6 +8,9 @@ namespace ember {
 
 // Host-side count of kernel launches (every launch_* call adds its kernels).
 void count_launches(long long n);
+// Records an event before the launch of kernel fn when the calling thread
+// traces a decode step (ember_decode_step_traced); otherwise does nothing.
+void trace_launch(const void* fn, cudaStream_t s);
 unsigned long long launches_so_far();
 
 // Launch with the programmatic-stream-serialization attribute (PDL) unless
@@ -18,6 +21,7 @@ template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                             cudaStream_t s, Args&&... args) {
     count_launches(1);
+    trace_launch(reinterpret_cast<const void*>(kern), s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -310,6 +314,7 @@ struct FusedPlan {
     int smem_attn = 0, smem_mlp = 0;
     int ns = 0;          // weight ring stages of the MLP kernel
     int fc = 0;          // intermediate features per MLP chunk (4, 8 or 16)
+    int xi = 0;          // 16-byte input chunks per lane in the row dots (4: inputs <= 1024, 8: <= 2048)
     int mlp_grid = 0;
     bool ok = false;
     const char* why = "not planned";   // reason when !ok
@@ -342,7 +347,7 @@ struct FusedAttnArgs {
     int C, nr, no;
 };
 // k_map / v_map: 3-D TMA maps (D, max_len, seqs*layers*kv heads), box 64 x 128 x 1
-void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int smem,
+void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int xi, int smem,
                        cudaStream_t s);
 
 struct FusedMlpArgs {
@@ -359,7 +364,7 @@ struct FusedMlpArgs {
     int* status;
     int ns;
 };
-void launch_fused_mlp(const FusedMlpArgs& a, int fc, int grid, int smem, cudaStream_t s);
+void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
 
 // out[c][r] = in[r][c] for 16-bit elements
 void launch_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols, cudaStream_t s);

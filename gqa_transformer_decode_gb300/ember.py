@@ -80,6 +80,8 @@ def load():
         "ember_kv_layout": (st, [P, C.POINTER(P), C.POINTER(P), C.POINTER(C.c_int64)]),
         "ember_prefill": (st, [P, P, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_decode_step": (st, [P, P, C.c_int32, P, P, P, P, P, P]),
+        "ember_decode_step_traced": (st, [P, P, C.c_int32, P, P, P, P, P, P, C.POINTER(C.c_float),
+                                          C.POINTER(C.c_char_p), C.c_int32, C.POINTER(C.c_int32)]),
         "ember_encode": (st, [P, P, C.c_int32, C.c_int32, P, P, P]),
         "ember_sync_status": (st, [P, P]),
         "ember_last_error": (C.c_char_p, []),
@@ -164,6 +166,31 @@ def ember_prefill(m, kv, seq, ids, n, start_pos, logits, argmax, hidden, stream)
 
 def ember_decode_step(m, kv, batch, seqs, ids, positions, logits, argmax, stream):
     return load().ember_decode_step(m, kv, batch, seqs, ids, positions, logits, argmax, stream)
+
+
+def ember_decode_step_traced(m, kv, batch, seqs, ids, positions, logits, argmax, stream, cap=4096):
+    """-> (status, [(mangled kernel name, device us)] in launch order)."""
+    us = (C.c_float * cap)()
+    names = (C.c_char_p * cap)()
+    n = C.c_int32(0)
+    st = load().ember_decode_step_traced(m, kv, batch, seqs, ids, positions, logits, argmax, stream,
+                                         us, names, cap, C.byref(n))
+    k = min(n.value, cap) if st == EMBER_OK else 0
+    return st, [(names[i].decode(errors="replace"), float(us[i])) for i in range(k)]
+
+
+def kernel_name(mangled: str) -> str:
+    """k_fused_attn<64,4> from the runtime's mangled name of an ember kernel."""
+    import re
+    m = re.match(r"_ZN5ember(\d+)", mangled)
+    if not m:
+        return mangled
+    n = int(m.group(1))
+    name, rest = mangled[m.end():m.end() + n], mangled[m.end() + n:]
+    t = re.match(r"I((?:L[a-z]\d+E)+)E", rest)
+    if not t:
+        return name
+    return name + "<" + ",".join(re.findall(r"L[a-z](\d+)E", t.group(1))) + ">"
 
 
 def ember_encode(m, ids, B, T, out, hidden, stream):

@@ -81,6 +81,15 @@ class Model:
 
         E.check(st, "ember_decode_step")
 
+    def decode_step_traced(self, kv, seqs, ids, positions, logits=None, argmax=None, stream=None):
+        """The same step run eagerly, one kernel at a time, each launch timed
+        with CUDA events: [(kernel name, device us)] in launch order."""
+        st, tr = E.ember_decode_step_traced(self.handle, kv.handle, ids.numel(), _ptr(seqs), _ptr(ids),
+                                            _ptr(positions), _ptr(logits), _ptr(argmax),
+                                            _stream_ptr(stream))
+        E.check(st, "ember_decode_step_traced")
+        return [(E.kernel_name(n), us) for n, us in tr]
+
     def encode(self, ids, B, T, out=None, hidden=None, stream=None):
         st = E.ember_encode(self.handle, _ptr(ids), B, T, _ptr(out), _ptr(hidden),
                             _stream_ptr(stream))

@@ -185,6 +185,26 @@ ember_status ember_decode_step(ember_model *m, ember_kv *kv, int32_t batch, cons
                                const int32_t *ids, const int32_t *positions, float *logits,
                                int32_t *argmax, ember_stream_t stream);
 
+/* One decode step exactly as ember_decode_step computes it, run for
+ * profiling: each kernel starts only after the previous one has finished (no
+ * programmatic launch overlap), with a CUDA event recorded on `stream` before
+ * every launch and after the last; the sequence runs as a one-off CUDA graph
+ * so that host launch latency leaves no gaps.  Waits for the stream.
+ *   launch_us [cap]  device time of launch i (its event to the next event)
+ *   names     [cap]  launch i's kernel name as the CUDA runtime reports it
+ *                    (mangled; static strings owned by the runtime)
+ *   n                the step's number of launches (may exceed cap; entries
+ *                    i >= cap are not written)
+ * The times are those of serialised launches (each kernel's weight loads no
+ * longer overlap its predecessor), an upper bound on a launch's share of a
+ * graph-replayed step.  Errors as ember_decode_step, plus INVALID_ARG for a
+ * stream that is being captured or NULL trace buffers with cap > 0, and CUDA
+ * when an event cannot be created or timed. */
+ember_status ember_decode_step_traced(ember_model *m, ember_kv *kv, int32_t batch, const int32_t *seqs,
+                                      const int32_t *ids, const int32_t *positions, float *logits,
+                                      int32_t *argmax, ember_stream_t stream, float *launch_us,
+                                      const char **names, int32_t cap, int32_t *n);
+
 /* Bidirectional (or causal, per the config) forward of B independent
  * sequences of T tokens each, positions restarting at 0 per sequence, no KV
  * cache (PII-Tracer forward()).

@@ -304,6 +304,38 @@ def test_fused_batch1_decode_matches_oracle(shape, n_prompt, n_steps, seq, strea
     assert E.ember_kernel_launches() - l0 == 2 * shape.layers + 3
 
 
+def test_traced_decode_step_matches_the_step_and_names_its_launches(stream):
+    """ember_decode_step_traced computes the same step (logits, argmax, cache
+    cursor) as ember_decode_step and reports every launch in order: embed, an
+    attention and an MLP kernel per layer, the LM head and finish, each with
+    a positive device time."""
+    shape = MID_QWEN2
+    w, om, gm = model_pair(shape, max_tokens=64)
+    prompt = synth.prompt_ids(shape, 40)
+    kv = gm.kv_alloc(2, 64)
+    V = shape.vocab
+    lg = torch.empty((2, V), dtype=torch.float32, device="cuda")
+    am = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for seq in (0, 1):
+            gm.prefill(kv, seq, i32(prompt), 0, argmax=am[seq:seq + 1], stream=stream)
+        gm.decode_step(kv, i32([0]), am[0:1].clone(), None, logits=lg[0], stream=stream)
+    trace = gm.decode_step_traced(kv, i32([1]), am[1:2].clone(), None, logits=lg[1],
+                                  argmax=am[1:2], stream=stream)
+    assert gm.sync_status(stream) == 0
+    g = lg.cpu().numpy()
+    assert_close(g[0:1], g[1:2], "traced vs graph-replayed step")   # split-K sums: order may differ
+    assert int(am[1].item()) == first_argmax(g[1])
+    names = [n.split("<")[0] for n, _ in trace]
+    L = shape.layers
+    assert names == ["k_embed"] + ["k_fused_attn", "k_fused_mlp"] * L + ["k_gemv", "k_finish"], names
+    assert all(us > 0 for _, us in trace)
+    # the cursor advanced: the next normal step of slot 1 is accepted at position 41
+    with torch.cuda.stream(stream):
+        gm.decode_step(kv, i32([1]), am[1:2].clone(), i32([41]), stream=stream)
+    assert gm.sync_status(stream) == 0
+
+
 @pytest.mark.parametrize("shape", [SMALL_QWEN2, MID_QWEN2])
 def test_decode_graph_follows_a_new_cache_with_the_same_buffers(shape, stream):
     """A decode graph is bound to the KV cache it was captured against: the same
