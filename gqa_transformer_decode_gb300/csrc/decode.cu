@@ -111,21 +111,37 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     int tile = blockIdx.x;
     if (tile < n_tiles) gemv_load_tile<TPR>(a, tile, r, sub, K8, w);
     pdl_wait();
-    // XA (one row): x + x_add staged once in shared memory
+    // XA (one row): the normalised input rmsnorm(x + x_add) = (x + x_add) *
+    // norm_w / rms staged once in shared memory, so that the tile loop reads
+    // only weights and this vector
     extern __shared__ float s_xa[];
     if (XA) {
+        float ss = 0.f;
         for (int i = tid * 4; i < a.K; i += GEMV_THREADS * 4) {
             const float4 u = __ldcg(reinterpret_cast<const float4*>(a.x + i));
             const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x_add + i));
-            *reinterpret_cast<float4*>(s_xa + i) = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+            const float4 t = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+            ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+            *reinterpret_cast<float4*>(s_xa + i) = t;
+        }
+        if (a.norm_w) {
+            ss = block_sum(ss, s_red);
+            const float rinv = rsqrtf(ss / (float)a.K + a.eps);
+            for (int i = tid * 4; i < a.K; i += GEMV_THREADS * 4) {   // the elements this thread wrote
+                const float4 n = reinterpret_cast<const float4*>(a.norm_w)[i / 4];
+                float4 t = *reinterpret_cast<float4*>(s_xa + i);
+                t.x *= n.x * rinv; t.y *= n.y * rinv; t.z *= n.z * rinv; t.w *= n.w * rinv;
+                *reinterpret_cast<float4*>(s_xa + i) = t;
+            }
         }
         __syncthreads();
     }
+    const bool wnorm = a.norm_w && !XA;   // otherwise the input already carries the norm
 
     // RMSNorm statistics of every input row (ember reference_forward.py rmsnorm()).
     for (int b = 0; b < NB; ++b) {
         float rinv = 1.f;
-        if (a.norm_w && b < nb) {
+        if (wnorm && b < nb) {
             const float* xb = XA ? s_xa : a.x + (size_t)b * a.ldx;
             float ss = 0.f;
             for (int i = tid; i < a.K; i += GEMV_THREADS) ss += xb[i] * xb[i];
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
             if (rv && c < K8) {
                 float wf[8];
                 unpack8w<WF16>(w[j], wf);
-                if (a.norm_w) {
+                if (wnorm) {
                     const float4 n0 = reinterpret_cast<const float4*>(a.norm_w)[2 * c];
                     const float4 n1 = reinterpret_cast<const float4*>(a.norm_w)[2 * c + 1];
                     wf[0] *= n0.x; wf[1] *= n0.y; wf[2] *= n0.z; wf[3] *= n0.w;
