@@ -3,7 +3,7 @@
 // One CTA = 128 query rows of one query head h (kv head g = h / G: ember
 // internals "grouped-query attention").  Per key tile of 128 keys:
 //   S = Q . K^T                  tcgen05.mma M=128, N=128, K=D  -> TMEM
-//   softmax rows (online)        4 warps, thread r owns query row r (tcgen05.ld)
+//   softmax rows (online)        8 warps: query row r is two threads, one per 64 score columns
 //   P -> shared memory           f16, the 128-byte-swizzled K-major A operand
 //   O += P . V                   tcgen05.mma (f16) M=128, N=D, K=128, accumulating
 //                                in TMEM across all key tiles
@@ -20,7 +20,7 @@
 // (bf16 -> f16 is exact for these magnitudes; P in [0, 1] keeps 11 bits
 // instead of bf16's 8).
 // Warp 0: TMA producer (Q once, K and Vt double-buffered); warp 1: TMEM
-// allocation and the MMA issuer; warps 2-5: softmax and output.  Every
+// allocation and the MMA issuer; warps 2-9: softmax and output.  Every
 // mbarrier wait is bounded; a timeout raises EMBER_ERR_TIMEOUT and the CTA
 // drains its copies and frees TMEM.
 #include <cuda_fp16.h>
@@ -31,7 +31,7 @@
 
 namespace ember {
 
-constexpr int AT_THREADS = 192;
+constexpr int AT_THREADS = 320;   // producer, MMA issuer, 8 softmax warps
 constexpr int AT_BQ = 128;   // query rows per CTA
 constexpr int AT_BK = 128;   // keys per tile
 
@@ -69,6 +69,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint64_t* o_full = bar + 7;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
     uint64_t* kconv = bar + 12;     // [2] K tile of the stage converted to f16
+    uint64_t* xb = bar + 14;        // [4] the two softmax halves of a TMEM lane quarter
+    __shared__ float s_mx[2][2][AT_BQ];   // [tile parity][half][row] maxima
+    __shared__ float s_lh[2][AT_BQ];      // [half][row] final sums
     int* sflag = reinterpret_cast<int*>(bar + 10);   // [0] failed, [1] issued, [2] consumed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,7 +93,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_init(s_full, 1);
         mbar_init(&kconv[0], 1);
         mbar_init(&kconv[1], 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 256);
+        for (int q = 0; q < 4; ++q) mbar_init(&xb[q], 64);
         mbar_init(o_full, 1);
         sflag[0] = 0;
         sflag[1] = 0;
@@ -207,17 +211,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             sflag[2] = j;
         }
     } else {   // ------------------------------------------------ softmax warps
-        // Thread = query row.  O accumulates in TMEM across key tiles; the row
-        // keeps a reference maximum m and rescales O (and l) only when a tile's
-        // maximum exceeds m by more than RESCALE (log2 units), so p = 2^(s - m)
-        // stays <= 2^RESCALE (f16-safe).  The rescale is a TMEM read-scale-write
-        // by the whole warp after the previous P.V has completed.
+        // Eight warps: thread = (query row, half); half 0 takes score columns
+        // 0-63 and O columns 0..D/2-1, half 1 the rest.  The two threads of a
+        // row exchange their halves' maxima through shared memory (pair
+        // mbarrier xb[quarter], 64 arrivals per tile).  O accumulates in TMEM
+        // across key tiles; the row keeps a reference maximum m and rescales O
+        // (and l) only when a tile's maximum exceeds m by more than RESCALE
+        // (log2 units), so p = 2^(s - m) stays <= 2^RESCALE (f16-safe).  The
+        // rescale is a TMEM read-scale-write after the previous P.V completed.
         constexpr float RESCALE = 8.f;
+        constexpr int DH = D / 2;
         const int qw = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = qw * 32 + lane;                 // query row within the tile
         const int qp = a.pos0 + q_first + r;          // its position
         const int qmin = a.pos0 + q_first;            // the tile's first position
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const int cs0 = half * 64;                    // this half's score columns
+        const int co0 = half * DH;                    // this half's O columns
         const float sc_log2 = 1.4426950408889634f * rsqrtf((float)D);
         float m = -INFINITY, l = 0.f;
         uint8_t* sP = sm + L::OFF_P;
@@ -230,26 +241,31 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             tc_fence_after();
             const int key0 = j * AT_BK;
             const bool full = key0 + AT_BK <= a.n_keys && (!a.causal || key0 + AT_BK - 1 <= qmin);
-            // pass 1: row maximum of the visible scores (64 columns per TMEM wait)
+            // pass 1: this half's 64 scores (kept in registers) and their maximum
+            uint32_t v[64];
+            tmem_ld32(tS + lane_off + cs0, v);
+            tmem_ld32(tS + lane_off + cs0 + 32, v + 32);
+            tmem_ld_wait();
             float mt = -INFINITY;
+            if (full) {
 #pragma unroll
-            for (int c0 = 0; c0 < AT_BK; c0 += 64) {
-                uint32_t v[64];
-                tmem_ld32(tS + lane_off + c0, v);
-                tmem_ld32(tS + lane_off + c0 + 32, v + 32);
-                tmem_ld_wait();
-                if (full) {
+                for (int i = 0; i < 64; ++i) mt = fmaxf(mt, __uint_as_float(v[i]));
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mt = fmaxf(mt, __uint_as_float(v[i]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const int kp = key0 + c0 + i;
-                        if (kp < a.n_keys && (!a.causal || kp <= qp)) mt = fmaxf(mt, __uint_as_float(v[i]));
-                    }
+                for (int i = 0; i < 64; ++i) {
+                    const int kp = key0 + cs0 + i;
+                    const bool vis = kp < a.n_keys && (!a.causal || kp <= qp);
+                    if (!vis) v[i] = __float_as_uint(-INFINITY);
+                    mt = fmaxf(mt, __uint_as_float(v[i]));
                 }
             }
-            mt *= sc_log2;
+            s_mx[j & 1][half][r] = mt;
+            mbar_arrive(&xb[qw]);
+            if (!mbar_wait(&xb[qw], (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            mt = fmaxf(s_mx[j & 1][0][r], s_mx[j & 1][1][r]) * sc_log2;
             // reference maximum: move it (and rescale O, l) only when it falls behind
             const bool move = mt > m + RESCALE;
             const float mref = move ? mt : m;
@@ -262,60 +278,39 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 tc_fence_after();
                 if (__any_sync(FULL_MASK, move)) {
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(tO + lane_off + c0, v);
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + lane_off + co0 + c0, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-                        tmem_st16(tO + lane_off + c0, v);
-                        tmem_st16(tO + lane_off + c0 + 16, v + 16);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        tmem_st16(tO + lane_off + co0 + c0, o);
+                        tmem_st16(tO + lane_off + co0 + c0 + 16, o + 16);
                     }
                     tmem_st_wait();
                 }
             }
             l *= corr;
             m = mref;
-            // pass 2: p = 2^(s - m), row sum, P -> shared (swizzled K-major)
+            // pass 2: p = 2^(s - m) (masked scores are -inf: p = 0), row sum,
+            // P -> shared (K-major block `half`, 128-byte swizzle)
             float rs = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < AT_BK; c0 += 64) {
-                uint32_t v[64];
-                tmem_ld32(tS + lane_off + c0, v);
-                tmem_ld32(tS + lane_off + c0 + 32, v + 32);
-                tmem_ld_wait();
+            for (int h32 = 0; h32 < 64; h32 += 32) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int h32 = 0; h32 < 64; h32 += 32) {
-                    uint32_t pk[16];
-                    if (full) {
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(v[h32 + i]), sc_log2, -m));
+                    const float p1 = ex2(fmaf(__uint_as_float(v[h32 + i + 1]), sc_log2, -m));
+                    rs += p0 + p1;
+                    pk[i / 2] = pack_f16x2(p0, p1);
+                }
+                uint8_t* rowp = sP + half * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const float p0 = ex2(fmaf(__uint_as_float(v[h32 + i]), sc_log2, -m));
-                            const float p1 = ex2(fmaf(__uint_as_float(v[h32 + i + 1]), sc_log2, -m));
-                            rs += p0 + p1;
-                            pk[i / 2] = pack_f16x2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int kp = key0 + c0 + h32 + i;
-                            const bool v0 = kp < a.n_keys && (!a.causal || kp <= qp);
-                            const bool v1 = kp + 1 < a.n_keys && (!a.causal || kp + 1 <= qp);
-                            const float p0 = v0 ? ex2(fmaf(__uint_as_float(v[h32 + i]), sc_log2, -m)) : 0.f;
-                            const float p1 = v1 ? ex2(fmaf(__uint_as_float(v[h32 + i + 1]), sc_log2, -m)) : 0.f;
-                            rs += p0 + p1;
-                            pk[i / 2] = pack_f16x2(p0, p1);
-                        }
-                    }
-                    const int cc = c0 + h32;
-                    const int kb = cc / 64;
-                    uint8_t* rowp = sP + kb * AT_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int chunk = ((cc % 64) / 8) + t;
-                        *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
-                            make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-                    }
+                for (int t = 0; t < 4; ++t) {
+                    const int chunk = h32 / 8 + t;
+                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) * 16)) =
+                        make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -323,26 +318,32 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             mbar_arrive(p_full);
             l += rs;
         }
+        // the row's sum over both halves (one more phase of the pair barrier)
+        if (ok) {
+            s_lh[half][r] = l;
+            mbar_arrive(&xb[qw]);
+            if (!mbar_wait(&xb[qw], (uint32_t)nkt & 1u)) ok = false;
+        }
         if (ok && nkt > 0 && !mbar_wait(o_full, (uint32_t)(nkt - 1) & 1u)) ok = false;
         if (!ok) sflag[0] = 1;
         tc_fence_after();
         if (ok) {
-            const float inv = 1.f / l;
+            const float inv = 1.f / (s_lh[0][r] + s_lh[1][r]);
             const bool live = q_first + r < a.T_per_seq;
-            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + q_first + r) * a.ld_att + h * D;
+            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + q_first + r) * a.ld_att + h * D + co0;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tO + lane_off + c0, v);
+            for (int c0 = 0; c0 < DH; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + lane_off + co0 + c0, o);
                 tmem_ld_wait();
                 if (live) {
 #pragma unroll
                     for (int d = 0; d < 32; d += 8) {
                         uint4 w;
-                        w.x = pack_f16x2(__uint_as_float(v[d]) * inv, __uint_as_float(v[d + 1]) * inv);
-                        w.y = pack_f16x2(__uint_as_float(v[d + 2]) * inv, __uint_as_float(v[d + 3]) * inv);
-                        w.z = pack_f16x2(__uint_as_float(v[d + 4]) * inv, __uint_as_float(v[d + 5]) * inv);
-                        w.w = pack_f16x2(__uint_as_float(v[d + 6]) * inv, __uint_as_float(v[d + 7]) * inv);
+                        w.x = pack_f16x2(__uint_as_float(o[d]) * inv, __uint_as_float(o[d + 1]) * inv);
+                        w.y = pack_f16x2(__uint_as_float(o[d + 2]) * inv, __uint_as_float(o[d + 3]) * inv);
+                        w.z = pack_f16x2(__uint_as_float(o[d + 4]) * inv, __uint_as_float(o[d + 5]) * inv);
+                        w.w = pack_f16x2(__uint_as_float(o[d + 6]) * inv, __uint_as_float(o[d + 7]) * inv);
                         *reinterpret_cast<uint4*>(out + c0 + d) = w;
                     }
                 }
