@@ -19,8 +19,9 @@
 // transposed f16 copy Vt [kv head][D][keys] so that it is K-major for the MMA
 // (bf16 -> f16 is exact for these magnitudes; P in [0, 1] keeps 11 bits
 // instead of bf16's 8).
-// Warp 0: TMA producer (Q once, K and Vt double-buffered); warp 1: TMEM
-// allocation and the MMA issuer; warps 2-9: softmax and output.  Every
+// Warp 0: TMA producer (Q once; K and Vt through a ring of 4 stages for
+// head_dim 64, 2 for 128); warp 1: TMEM allocation and the MMA issuer;
+// warps 2-9: softmax and output.  Every
 // mbarrier wait is bounded; a timeout raises EMBER_ERR_TIMEOUT and the CTA
 // drains its copies and frees TMEM.
 #include <cuda_fp16.h>
@@ -39,14 +40,15 @@ template <int D>
 struct AtSmem {
     static constexpr int KB = D / 64;                    // 64-element K blocks of Q / K rows
     static constexpr int Q_BYTES = KB * AT_BQ * 128;
+    static constexpr int NSTG = D == 64 ? 4 : 2;        // K/V ring stages (shared memory bound)
     static constexpr int K_BYTES = KB * AT_BK * 128;     // one stage
     static constexpr int V_BLOCK = D * 128;              // [D rows][64 keys] f16
     static constexpr int V_BYTES = 2 * V_BLOCK;          // one stage: 128 keys
     static constexpr int P_BYTES = 2 * AT_BQ * 128;      // [128 rows][128 keys] f16
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-    static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
+    static constexpr int OFF_V = OFF_K + NSTG * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NSTG * V_BYTES;
     static constexpr int OFF_BAR = OFF_P + P_BYTES;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;   // + barriers, + alignment slack
     static constexpr uint32_t TMEM_COLS = (128 + D) <= 256 ? 256 : 512;
@@ -61,18 +63,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) &
                                              ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    constexpr int NSTG = L::NSTG;
     uint64_t* q_full = bar + 0;
-    uint64_t* kv_full = bar + 1;    // [2]
-    uint64_t* kv_empty = bar + 3;   // [2]
-    uint64_t* s_full = bar + 5;
-    uint64_t* p_full = bar + 6;
-    uint64_t* o_full = bar + 7;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
-    uint64_t* kconv = bar + 12;     // [2] K tile of the stage converted to f16
-    uint64_t* xb = bar + 14;        // [4] the two softmax halves of a TMEM lane quarter
+    uint64_t* s_full = bar + 1;
+    uint64_t* p_full = bar + 2;
+    uint64_t* o_full = bar + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
+    int* sflag = reinterpret_cast<int*>(bar + 5);   // [0] failed, [1] issued, [2] consumed
+    uint64_t* kv_full = bar + 8;    // [NSTG]
+    uint64_t* kv_empty = bar + 12;  // [NSTG]
+    uint64_t* kconv = bar + 16;     // [NSTG] K tile of the stage converted to f16
+    uint64_t* xb = bar + 20;        // [4] the two softmax halves of a TMEM lane quarter
     __shared__ float s_mx[2][2][AT_BQ];   // [tile parity][half][row] maxima
     __shared__ float s_lh[2][AT_BQ];      // [half][row] final sums
-    int* sflag = reinterpret_cast<int*>(bar + 10);   // [0] failed, [1] issued, [2] consumed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x;        // heaviest (last) query tiles first
@@ -86,13 +89,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSTG; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
+            mbar_init(&kconv[s], 1);
         }
         mbar_init(s_full, 1);
-        mbar_init(&kconv[0], 1);
-        mbar_init(&kconv[1], 1);
         mbar_init(p_full, 256);
         for (int q = 0; q < 4; ++q) mbar_init(&xb[q], 64);
         mbar_init(o_full, 1);
@@ -117,12 +119,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     pdl_wait();   // Q, K and Vt are the previous kernels' outputs
 
     if (warp == 0) {   // ------------------------------- TMA producer + K converter
-        // Tiles j and j + 1 are in flight; K arrives as bf16 from the cache and
+        // Up to NSTG tiles are in flight; K arrives as bf16 from the cache and
         // the whole warp rewrites it in place as f16 (the queries are f16) before
-        // releasing it to the MMA warp; tile j + 1 is issued once the MMAs of
-        // tile j - 1 have freed its stage.
+        // releasing it to the MMA warp; tile j - 1 + NSTG is issued once the
+        // MMAs of tile j - 1 have freed its stage.
         auto issue = [&](int j) {
-            const int s = j & 1;
+            const int s = j % NSTG;
             mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
             for (int kb = 0; kb < L::KB; ++kb)
                 tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
@@ -137,13 +139,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             mbar_expect_tx(q_full, L::Q_BYTES);
             for (int kb = 0; kb < L::KB; ++kb)
                 tma_load_2d(sm + L::OFF_Q + kb * AT_BQ * 128, &tmQ, h * D + kb * 64, qrow0, q_full);
-            for (; issued < 2 && issued < nkt; ++issued) issue(issued);
+            for (; issued < NSTG && issued < nkt; ++issued) issue(issued);
         }
         issued = __shfl_sync(FULL_MASK, issued, 0);
         bool fail = false;
         for (int j = 0; j < nkt && !fail; ++j) {
-            const int s = j & 1;
-            if (!mbar_wait(&kv_full[s], (uint32_t)(j >> 1) & 1u)) {
+            const int s = j % NSTG;
+            if (!mbar_wait(&kv_full[s], (uint32_t)(j / NSTG) & 1u)) {
                 fail = true;
                 break;
             }
@@ -157,10 +159,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&kconv[s]);
-                if (j >= 1 && j + 1 < nkt) {   // stage of tile j - 1 -> tile j + 1
-                    if (!mbar_wait(&kv_empty[(j + 1) & 1], (uint32_t)((j - 1) >> 1) & 1u)) fail = true;
+                if (j >= 1 && j - 1 + NSTG < nkt) {   // stage of tile j - 1 -> tile j - 1 + NSTG
+                    if (!mbar_wait(&kv_empty[(j - 1) % NSTG], (uint32_t)((j - 1) / NSTG) & 1u)) fail = true;
                     else {
-                        issue(j + 1);
+                        issue(j - 1 + NSTG);
                         ++issued;
                     }
                 }
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             bool ok = mbar_wait(q_full, 0);
             int j = 0;
             for (; ok && j < nkt; ++j) {
-                const int s = j & 1;
-                const uint32_t u = (uint32_t)(j >> 1);
+                const int s = j % NSTG;
+                const uint32_t u = (uint32_t)(j / NSTG);
                 if (!mbar_wait(&kconv[s], u & 1u)) break;
                 tc_fence_after();
                 const uint32_t q0 = smem_u32(sm + L::OFF_Q);
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (warp == 0 && lane == 0 && sflag[0]) {
         // drain K/V copies issued but never consumed
         for (int j = sflag[2]; j < sflag[1]; ++j)
-            (void)mbar_wait(&kv_full[j & 1], (uint32_t)(j >> 1) & 1u);
+            (void)mbar_wait(&kv_full[j % NSTG], (uint32_t)(j / NSTG) & 1u);
     }
     if (warp == 1) {
         tc_fence_after();
