@@ -125,6 +125,57 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
         }
         return;
     }
+    if (D % 64 == 0) {   // per-head RMSNorm, then RoPE: a warp per head, lane l holds
+        // rotate-half pairs i = l*PPL .. l*PPL + PPL - 1 (both halves) in registers
+        const int PPL = D / 64;   // 1 or 2
+        const int i0 = lane * PPL;
+        const float* cs = a.cos_t + (size_t)pos * H2;
+        const float* sn = a.sin_t + (size_t)pos * H2;
+        for (int h = warp; h < a.NH + a.NKV; h += blockDim.x / 32) {
+            const float* x = row + h * D;
+            const float* w = h < a.NH ? a.q_norm : a.k_norm;
+            float lo[2] = {0.f, 0.f}, hi[2] = {0.f, 0.f};
+            if (PPL == 2) {
+                const float2 u = *reinterpret_cast<const float2*>(x + i0);
+                const float2 v = *reinterpret_cast<const float2*>(x + H2 + i0);
+                lo[0] = u.x; lo[1] = u.y; hi[0] = v.x; hi[1] = v.y;
+            } else {
+                lo[0] = x[i0];
+                hi[0] = x[H2 + i0];
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) ss += lo[k] * lo[k] + hi[k] * hi[k];
+            ss = warp_sum(ss);
+            const float ri = rsqrtf(ss / (float)D + a.eps);
+            float r0[2] = {0.f, 0.f}, r1[2] = {0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (k < PPL) {
+                    const int i = i0 + k;
+                    rope_pair(lo[k] * ri * w[i], hi[k] * ri * w[H2 + i], cs[i], sn[i], r0[k], r1[k]);
+                }
+            }
+            uint16_t* dst;
+            const bool isq = h < a.NH;   // queries f16 (the attention operand), keys bf16 (the cache)
+            if (isq) dst = a.q_out + (size_t)t * nq + h * D;
+            else dst = a.kc + z * a.seq_stride + (h - a.NH) * a.head_stride + (long long)pos * D;
+            if (PPL == 2) {
+                *reinterpret_cast<uint32_t*>(dst + i0) = isq ? pack_f16x2(r0[0], r0[1]) : pack_bf16x2(r0[0], r0[1]);
+                *reinterpret_cast<uint32_t*>(dst + H2 + i0) = isq ? pack_f16x2(r1[0], r1[1]) : pack_bf16x2(r1[0], r1[1]);
+            } else {
+                dst[i0] = isq ? f32_to_f16(r0[0]) : f32_to_bf16(r0[0]);
+                dst[H2 + i0] = isq ? f32_to_f16(r1[0]) : f32_to_bf16(r1[0]);
+            }
+        }
+        for (int f = tid * 4; f < nkv; f += blockDim.x * 4) {   // V rows: bf16 into the cache
+            const int g = f / D, d = f % D;
+            const float4 v = *reinterpret_cast<const float4*>(row + nq + nkv + f);
+            *reinterpret_cast<uint2*>(a.vc + z * a.seq_stride + g * a.head_stride + (long long)pos * D + d) =
+                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        }
+        return;
+    }
     for (int e = tid; e < nq + 2 * nkv; e += blockDim.x) sm[e] = row[e];
     __syncthreads();
     if (a.q_norm) {   // PII-Tracer forward(): per-head RMSNorm of q and k before RoPE
@@ -165,7 +216,9 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
 }
 
 void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s) {
-    const size_t smem = (size_t)(a.NH + 2 * a.NKV) * a.D * sizeof(float);
+    // only the per-head-norm path for head_dim % 64 != 0 stages the row in shared memory
+    const bool staged = a.q_norm && (a.D % 64) != 0;
+    const size_t smem = staged ? (size_t)(a.NH + 2 * a.NKV) * a.D * sizeof(float) : 0;
     launch_k(k_rope_kv, dim3(a.n), dim3(128), smem, s, a);
 }
 
