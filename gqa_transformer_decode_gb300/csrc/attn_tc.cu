@@ -392,8 +392,46 @@ __global__ void __launch_bounds__(256) k_vt(VtArgs a) {
     }
 }
 
+// The same for D % 8 == 0, D <= 128, with 16-byte accesses on both sides:
+// key rows in as 8-value chunks, f16 tile [64 keys][D] (row pitch D + 8),
+// 8-key runs of one column out.
+__global__ void __launch_bounds__(256) k_vt16(VtArgs a) {
+    __shared__ __align__(16) uint16_t tile[64][136];
+    const int z = blockIdx.y;
+    const int key0 = blockIdx.x * 64;
+    const int D = a.D, C8 = D / 8;
+    pdl_trigger();
+    pdl_wait();
+    const uint16_t* src =
+        a.v + (size_t)(z / a.nkv) * a.v_z_stride + (size_t)(z % a.nkv) * a.v_h_stride;
+    for (int e = threadIdx.x; e < 64 * C8; e += blockDim.x) {
+        const int k = e / C8, c = e % C8;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (key0 + k < a.n_keys) {
+            const uint4 b = *reinterpret_cast<const uint4*>(src + (size_t)(key0 + k) * D + 8 * c);
+            u = make_uint4(pack_f16x2(bf16_lo(b.x), bf16_hi(b.x)), pack_f16x2(bf16_lo(b.y), bf16_hi(b.y)),
+                           pack_f16x2(bf16_lo(b.z), bf16_hi(b.z)), pack_f16x2(bf16_lo(b.w), bf16_hi(b.w)));
+        }
+        *reinterpret_cast<uint4*>(&tile[k][8 * c]) = u;
+    }
+    __syncthreads();
+    uint16_t* dst = a.vt + (size_t)z * D * a.keys_pad;
+    for (int e = threadIdx.x; e < D * 8; e += blockDim.x) {
+        const int d = e / 8, kc = e % 8;   // column d, keys 8kc..8kc+7 of the block
+        if (key0 + 8 * kc >= a.keys_pad) continue;   // keys_pad % 8 == 0: whole runs
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = (uint32_t)tile[8 * kc + 2 * j][d] | ((uint32_t)tile[8 * kc + 2 * j + 1][d] << 16);
+        *reinterpret_cast<uint4*>(dst + (size_t)d * a.keys_pad + key0 + 8 * kc) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 void launch_vt(const VtArgs& a, int zs, cudaStream_t s) {
-    launch_k(k_vt, dim3((a.keys_pad + 63) / 64, zs), dim3(256), 0, s, a);
+    if (a.D % 8 == 0 && a.D <= 128 && a.keys_pad % 8 == 0)
+        launch_k(k_vt16, dim3((a.keys_pad + 63) / 64, zs), dim3(256), 0, s, a);
+    else
+        launch_k(k_vt, dim3((a.keys_pad + 63) / 64, zs), dim3(256), 0, s, a);
 }
 
 template <int D>

@@ -60,8 +60,48 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     }
 }
 
+// A warp per row for H <= 2048 (H % 128 == 0): the row in registers (H/128
+// 16-byte loads per lane), a warp reduction, no block barrier; 8 rows per CTA.
+template <int NV>
+__global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const float* w, float eps, int H,
+                                                      int n, uint16_t* out) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    pdl_trigger();
+    pdl_wait();
+    if (t >= n) return;
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        v[q] = __ldcg(xr + lane + 32 * q);
+        ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+    }
+    ss = warp_sum(ss);
+    const float ri = rsqrtf(ss / (float)H + eps);
+    uint2* o = reinterpret_cast<uint2*>(out + (size_t)t * H);
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        const float4 g = __ldg(reinterpret_cast<const float4*>(w) + lane + 32 * q);
+        o[lane + 32 * q] = make_uint2(pack_f16x2(v[q].x * ri * g.x, v[q].y * ri * g.y),
+                                      pack_f16x2(v[q].z * ri * g.z, v[q].w * ri * g.w));
+    }
+}
+
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
+    const dim3 g((n + 7) / 8), b(256);
+    if (H % 128 == 0 && H <= 2048) {
+        switch (H / 128) {
+            case 1: launch_k(k_rmsnorm_warp<1>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            case 2: launch_k(k_rmsnorm_warp<2>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            case 4: launch_k(k_rmsnorm_warp<4>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            case 8: launch_k(k_rmsnorm_warp<8>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            case 16: launch_k(k_rmsnorm_warp<16>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            default: break;
+        }
+    }
     launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
 }
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
