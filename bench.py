@@ -285,6 +285,11 @@ def decode_family_bytes(shape, B: int, ctx: int) -> dict:
     }
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from the ncu capture
+# summarised in profiles/decode_step_qwen2.5-0.5b_b1.md (kernel unchanged since)
+MEASURED_TRAFFIC = {"k_fused_mlp<8,4>": 26200832, "k_fused_attn<64,4>": 3889152}
+
+
 def decode_roofline(job, hbm_peak):
     """The dominant kernel of a decode step: one step run through
     ember_decode_step_traced (eager, one kernel at a time, CUDA events around
@@ -309,7 +314,7 @@ def decode_roofline(job, hbm_peak):
            "share_of_step": round(t["us"] / total, 4),
            "timing": "one decode step via ember_decode_step_traced: launches serialised (a one-off graph), "
                      "CUDA events on the launching stream",
-           "traffic": None,
+           "traffic": MEASURED_TRAFFIC.get(t["name"]),
            "step_launches": {k: {"n": v["n"], "us": round(v["us"], 1)} for k, v in
                              sorted(fam.items(), key=lambda kv_: -kv_[1]["us"])}}
     if nbytes is None:
