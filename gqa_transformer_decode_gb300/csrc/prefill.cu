@@ -60,8 +60,9 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     }
 }
 
-// A warp per row for H <= 2048 (H % 128 == 0): the row in registers (H/128
-// 16-byte loads per lane), a warp reduction, no block barrier; 8 rows per CTA.
+// A warp per row for H <= 2048 (H % 128 == 0) and at least 1024 rows: the
+// row in registers (H/128 16-byte loads per lane), a warp reduction, no
+// block barrier; 8 rows per CTA.
 template <int NV>
 __global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const float* w, float eps, int H,
                                                       int n, uint16_t* out) {
@@ -92,13 +93,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const floa
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
     const dim3 g((n + 7) / 8), b(256);
-    if (H % 128 == 0 && H <= 2048) {
+    // a warp per row pays off with many rows; a few rows (decode batches,
+    // short prompts) keep a CTA per row so that they spread over the SMs
+    if (n >= 1024 && H % 128 == 0 && H <= 2048) {
         switch (H / 128) {
-            case 1: launch_k(k_rmsnorm_warp<1>, g, b, 0, s, x, w, eps, H, n, xb); return;
-            case 2: launch_k(k_rmsnorm_warp<2>, g, b, 0, s, x, w, eps, H, n, xb); return;
-            case 4: launch_k(k_rmsnorm_warp<4>, g, b, 0, s, x, w, eps, H, n, xb); return;
-            case 8: launch_k(k_rmsnorm_warp<8>, g, b, 0, s, x, w, eps, H, n, xb); return;
-            case 16: launch_k(k_rmsnorm_warp<16>, g, b, 0, s, x, w, eps, H, n, xb); return;
+#define EMBER_RMS_WARP(NV) \
+    case NV: launch_k(k_rmsnorm_warp<NV>, g, b, 0, s, x, w, eps, H, n, xb); return;
+            EMBER_RMS_WARP(1) EMBER_RMS_WARP(2) EMBER_RMS_WARP(3) EMBER_RMS_WARP(4)
+            EMBER_RMS_WARP(5) EMBER_RMS_WARP(6) EMBER_RMS_WARP(7) EMBER_RMS_WARP(8)
+            EMBER_RMS_WARP(9) EMBER_RMS_WARP(10) EMBER_RMS_WARP(11) EMBER_RMS_WARP(12)
+            EMBER_RMS_WARP(13) EMBER_RMS_WARP(14) EMBER_RMS_WARP(15) EMBER_RMS_WARP(16)
+#undef EMBER_RMS_WARP
             default: break;
         }
     }
