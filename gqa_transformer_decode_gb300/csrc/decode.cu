@@ -252,26 +252,23 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
 }
 
 template <int TPR>
-static void gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
+static cudaError_t gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
     const dim3 g(grid), b(GEMV_THREADS);
-    if (a.x_add) {   // batch-1 head over a residual held as two buffers (K <= 12288)
-        launch_k(k_gemv<TPR, 1, false, true>, g, b, (size_t)a.K * 4, s, a);
-        return;
-    }
+    if (a.x_add)   // batch-1 head over a residual held as two buffers (K <= 12288)
+        return launch_k(k_gemv<TPR, 1, false, true>, g, b, (size_t)a.K * 4, s, a);
     if (a.w_f16) {
-        if (a.nb <= 1) launch_k(k_gemv<TPR, 1, true>, g, b, 0, s, a);
-        else if (a.nb <= 2) launch_k(k_gemv<TPR, 2, true>, g, b, 0, s, a);
-        else if (a.nb <= 4) launch_k(k_gemv<TPR, 4, true>, g, b, 0, s, a);
-        else launch_k(k_gemv<TPR, 8, true>, g, b, 0, s, a);
-    } else {
-        if (a.nb <= 1) launch_k(k_gemv<TPR, 1, false>, g, b, 0, s, a);
-        else if (a.nb <= 2) launch_k(k_gemv<TPR, 2, false>, g, b, 0, s, a);
-        else if (a.nb <= 4) launch_k(k_gemv<TPR, 4, false>, g, b, 0, s, a);
-        else launch_k(k_gemv<TPR, 8, false>, g, b, 0, s, a);
+        if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, true>, g, b, 0, s, a);
+        if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, true>, g, b, 0, s, a);
+        if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, true>, g, b, 0, s, a);
+        return launch_k(k_gemv<TPR, 8, true>, g, b, 0, s, a);
     }
+    if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, false>, g, b, 0, s, a);
+    if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, false>, g, b, 0, s, a);
+    if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, false>, g, b, 0, s, a);
+    return launch_k(k_gemv<TPR, 8, false>, g, b, 0, s, a);
 }
 
-void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
     const int K8 = a.K >> 3;
     int tpr = 8;
     while (tpr * GEMV_MAXJ < K8) tpr <<= 1;   // <= 8 loads per thread
@@ -282,12 +279,12 @@ void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
     const int tiles = (a.N + R - 1) / R;
     const int grid = tiles < num_sms * 8 ? tiles : num_sms * 8;
     switch (tpr) {
-        case 8: gemv_nb<8>(a, s, grid); break;
-        case 16: gemv_nb<16>(a, s, grid); break;
-        case 32: gemv_nb<32>(a, s, grid); break;
-        case 64: gemv_nb<64>(a, s, grid); break;
-        case 128: gemv_nb<128>(a, s, grid); break;
-        default: gemv_nb<256>(a, s, grid); break;
+        case 8: return gemv_nb<8>(a, s, grid);
+        case 16: return gemv_nb<16>(a, s, grid);
+        case 32: return gemv_nb<32>(a, s, grid);
+        case 64: return gemv_nb<64>(a, s, grid);
+        case 128: return gemv_nb<128>(a, s, grid);
+        default: return gemv_nb<256>(a, s, grid);
     }
 }
 

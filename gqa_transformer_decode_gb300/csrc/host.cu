@@ -174,12 +174,6 @@ struct ember_model {
     bool q_map_ok = false;
     int enc_positions = 0;
     GemmPlan p_head;   // tied head on bf16 final states (encode without labels)
-    // persistent batch-1 decode kernel
-    PersistLayer* pk_layers = nullptr;
-    unsigned* pk_bar = nullptr;
-    PersistArgs pk{};
-    int pk_grid = 0, pk_smem = 0;
-    bool pk_ok = false;
     // fused batch-1 decode (two kernels per layer)
     FusedPlan fp;
     float* fx[2] = {nullptr, nullptr};             // residual stream copies [H]
@@ -319,8 +313,6 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     aa.add(&m->tok_ok, (size_t)B);
     aa.add(&m->tok_pos, (size_t)B);
     aa.add(&m->status, 1);
-    aa.add(&m->pk_layers, (size_t)c.layers);
-    aa.add(&m->pk_bar, 32 + 1024);
     if (m->fp.ok) {
         for (auto& p : m->fx) aa.add(&p, (size_t)H);
         for (auto& p : m->fz) aa.add(&p, (size_t)H);
@@ -424,44 +416,6 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     if (e == cudaSuccess) e = cudaMemsetAsync(m->counters, 0, (size_t)B * NKV * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->keys, 0, (size_t)B * 8, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->status, 0, 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(m->pk_bar, 0, (32 + 1024) * 4, s);
-    if (e == cudaSuccess && c.causal && c.n_labels == 0) {
-        std::vector<PersistLayer> pl(c.layers);
-        for (int l = 0; l < c.layers; ++l) {
-            const LayerDev& L = m->layers[l];
-            pl[l] = {L.wqkv, L.wo, L.wgu, L.wd, L.attn_norm, L.mlp_norm,
-                     c.qkv_bias ? L.bqkv : nullptr, c.qk_norm ? L.q_norm : nullptr,
-                     c.qk_norm ? L.k_norm : nullptr};
-        }
-        e = cudaMemcpy(m->pk_layers, pl.data(), pl.size() * sizeof(PersistLayer),
-                       cudaMemcpyHostToDevice);
-        PersistArgs& a = m->pk;
-        a.L = c.layers;
-        a.H = H;
-        a.NH = c.n_heads;
-        a.NKV = NKV;
-        a.D = D;
-        a.F = F;
-        a.V = V;
-        a.qkv_n = m->qkv_n;
-        a.qk_norm = c.qk_norm;
-        a.eps = (float)c.rms_eps;
-        a.embed = m->embed;
-        a.final_norm = m->final_norm;
-        a.layers = m->pk_layers;
-        a.x = m->x;
-        a.qkv = m->qkv;
-        a.att = m->att_f;
-        a.act = m->act_f;
-        a.part = m->part;
-        a.counters = m->counters;
-        a.keys = m->keys;
-        a.bar = m->pk_bar;
-        a.status = m->status;
-        // opt-in: on this chip the PDL-chained kernels are faster for now
-        const bool on = getenv("EMBER_PERSIST") && atoi(getenv("EMBER_PERSIST"));
-        m->pk_ok = on && persist_prepare(a, m->pk_grid, m->pk_smem);
-    }
     if (e == cudaSuccess && !c.causal) {
         std::vector<float> cs, sn;
         rope_tables(m->c, m->c.max_positions, cs, sn);
@@ -613,7 +567,6 @@ ember_status ember_sync_status(ember_model* m, ember_stream_t stream) {
     int st = 0;
     CK(cudaMemcpy(&st, m->status, 4, cudaMemcpyDeviceToHost));
     CK(cudaMemset(m->status, 0, 4));
-    if (st == EMBER_ERR_TIMEOUT) CK(cudaMemset(m->pk_bar, 0, (32 + 1024) * 4));   // abort + epochs
     if (st != 0) return fail((ember_status)st, "device reported status %d", st);
     return EMBER_OK;
 }
@@ -839,23 +792,6 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     ea.tok_ok = m->tok_ok;
     ea.tok_pos = m->tok_pos;
     ea.pf_seq = -1;
-    if (B == 1 && m->pk_ok) {   // one persistent kernel for the whole step
-        PersistArgs a = m->pk;
-        a.ids = ids;
-        a.seqs = seqs;
-        a.positions = positions;
-        a.logits = logits;
-        a.argmax = argmax;
-        a.kc = kv->k;
-        a.vc = kv->v;
-        a.max_len = kv->max_len;
-        a.max_seqs = kv->max_seqs;
-        a.cursor = kv->cursor;
-        a.cos_t = kv->cos_t;
-        a.sin_t = kv->sin_t;
-        launch_persist(a, m->pk_grid, m->pk_smem, s);
-        return;
-    }
     if (B == 1 && m->fp.ok && kv->k_map_ok && kv->v_map_ok) {
         // two kernels per layer; kernel n reads fx[(n-1)%2] + fz[(n-1)%3], writes
         // fx[n%2], zeroes fz[(n-2)%3] and accumulates into fz[n%3] (embed: n = 0)
@@ -1424,14 +1360,16 @@ extern "C" ember_status ember_gemv_argmax_noalloc(const uint16_t* W, int32_t N, 
     g.nb = nb;
     g.mode = EPI_ARGMAX;
     g.keys = keys;
-    launch_gemv(g, s, sms);
-    CK(cudaGetLastError());
-    cudaError_t e = launch_k(k_noalloc_finish, dim3(1), dim3(32), 0, s, keys, (int)nb, argmax);
+    // Only the two launches' own return codes are checked: an error the caller
+    // left pending on this thread is not this call's failure.  Once the GEMV
+    // may be queued, any failure leaves keys that nothing clears, so the next
+    // call redoes the set-up (which clears them on its stream).
+    cudaError_t e = launch_gemv(g, s, sms);
+    if (e == cudaSuccess) e = launch_k(k_noalloc_finish, dim3(1), dim3(32), 0, s, keys, (int)nb, argmax);
     if (e != cudaSuccess) {
-        // the GEMV ran but nothing will clear its keys: redo the set-up next time
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
         g_noalloc_ptr[dev] = nullptr;
-        return fail(EMBER_ERR_CUDA, "argmax finish launch failed: %s", cudaGetErrorString(e));
+        return fail(EMBER_ERR_CUDA, "no-alloc LM head launch failed: %s", cudaGetErrorString(e));
     }
     return EMBER_OK;
 }

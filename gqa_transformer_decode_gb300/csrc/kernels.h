@@ -80,7 +80,8 @@ struct GemvArgs {
     int* status;
     const float* x_add;          // [ldx] added to x (residual accumulator; nb == 1, bf16 W), or nullptr
 };
-void launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms);
+// Returns the launch's own error (not the thread's pending last error).
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms);
 
 // ------------------------------------------------------- decode attention --
 // Split-KV flash decoding: one CTA per (token, kv head, split), all G query
@@ -132,43 +133,6 @@ struct FinishArgs {
 };
 void launch_finish(const FinishArgs& a, cudaStream_t s);
 void launch_set_cursor(int32_t* cursor, int seq, int pos, cudaStream_t s);
-
-// ------------------------------------------------- persistent batch-1 decode --
-struct PersistLayer {
-    const uint16_t *wqkv, *wo, *wgu, *wd;
-    const float *attn_norm, *mlp_norm, *bqkv, *q_norm, *k_norm;
-};
-struct PersistArgs {
-    int L, H, NH, NKV, D, F, V, qkv_n, qk_norm;
-    float eps;
-    const uint16_t* embed;
-    const float* final_norm;
-    const PersistLayer* layers;      // device array [L]
-    // the step
-    const int32_t* ids;
-    const int32_t* seqs;
-    const int32_t* positions;        // nullable: the sequence's cursor
-    float* logits;                   // nullable
-    int32_t* argmax;                 // nullable
-    // KV cache
-    uint16_t* kc;
-    uint16_t* vc;
-    int max_len, max_seqs;
-    int32_t* cursor;
-    const float* cos_t;
-    const float* sin_t;
-    // workspace
-    float *x, *qkv, *att, *act, *part;
-    unsigned* counters;
-    unsigned long long* keys;
-    unsigned* bar;                   // grid barrier: [0] abort, [32 + cta] epochs (1024 max)
-    int* status;
-    // shared-memory plan (persist_prepare)
-    int ring_slots, chunk_bytes, scratch_bytes;
-};
-// Fills the shared-memory plan; false if the shapes do not fit this kernel.
-bool persist_prepare(PersistArgs& a, int& grid, int& smem);
-cudaError_t launch_persist(const PersistArgs& a, int grid, int smem, cudaStream_t s);
 
 // ------------------------------------------------------------- prefill side --
 // xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)

@@ -1,8 +1,7 @@
-"""Parity of the alternative batch-1 decode paths, each run in a child process
-so its switch is read at model creation: the persistent weight-streaming
-kernel (opt-in, EMBER_PERSIST=1) and the chained per-projection kernels
-(EMBER_NO_FUSED=1, the path batch 2..8 takes): same greedy continuation and
-logits as the oracle."""
+"""Parity of the alternative batch-1 decode path, run in a child process so
+its switch is read at model creation: the chained per-projection kernels
+(EMBER_NO_FUSED=1, the path batch 2..8 takes) give the same greedy
+continuation and logits as the oracle."""
 import os
 import subprocess
 import sys
@@ -30,7 +29,6 @@ shapes = [synth.TINY,
           synth.ModelShape("s-d64", vocab=700, hidden=192, layers=2, n_heads=6, n_kv_heads=2,
                            head_dim=64, ff=256, rope_theta=1e6, qkv_bias=1)]
 from gqa_transformer_decode_gb300 import ember as E
-persist = %(persist)r
 s = torch.cuda.Stream()
 for shape in shapes:
     w = synth.weights_bf16(shape)
@@ -52,9 +50,9 @@ for shape in shapes:
             m.decode_step(kv, seqs, torch.tensor([toks[i - 1]], dtype=torch.int32, device="cuda"),
                           None, logits=lg[i], argmax=am[i:i + 1], stream=s)
     assert m.sync_status(s) == 0
-    # which path ran: one persistent kernel, or embed + 5 per layer + head + finish
+    # which path ran: embed + 5 per layer + head + finish
     launches = E.ember_kernel_launches() - l0
-    assert launches == (1 if persist else 5 * shape.layers + 3), (shape.name, launches)
+    assert launches == 5 * shape.layers + 3, (shape.name, launches)
     glg, gam = lg.cpu().numpy(), am.cpu().numpy()
     assert_close(olg, glg, shape.name + " logits")
     assert_tokens(olg, toks, gam, shape.name + " tokens")
@@ -63,11 +61,9 @@ print("decode path ok")
 """
 
 
-@pytest.mark.parametrize("switch", ["EMBER_PERSIST", "EMBER_NO_FUSED"])
-def test_alternative_decode_path_matches_oracle(switch):
-    env = dict(os.environ, **{switch: "1"})
-    code = CHILD % {"root": ROOT, "tests": os.path.join(ROOT, "tests"),
-                    "persist": switch == "EMBER_PERSIST"}
+def test_chained_decode_path_matches_oracle():
+    env = dict(os.environ, EMBER_NO_FUSED="1")
+    code = CHILD % {"root": ROOT, "tests": os.path.join(ROOT, "tests")}
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and "decode path ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
