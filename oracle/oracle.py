@@ -267,6 +267,24 @@ class OracleCache:
     def len(self):
         return self.ptr.contents.len
 
+    def load(self, k_bits, v_bits, length):
+        """Start from a given cache: rows [0, length) of K and V (bf16 bit
+        patterns [L, NKV, >= length, D], decoded exactly by the oracle's own
+        bf16 decode) become the cache contents and the cursor becomes length
+        ([EI] kv cache: the cursor counts the rows every layer has stored).  A
+        cached step then computes the next token from exactly that history."""
+        L, NKV, max_len, D = self._shape
+        if not 0 <= length <= max_len:
+            raise ValueError("length outside the cache")
+        k, v = self.arrays()
+        for dst, src in ((k, k_bits), (v, v_bits)):
+            src = np.asarray(src).view(np.uint16)[:, :, :length]
+            if src.shape != (L, NKV, length, D):
+                raise ValueError(f"cache rows of shape {src.shape}, want {(L, NKV, length, D)}")
+            dst[:, :, :length] = bf16_decode(np.ascontiguousarray(src))
+            dst[:, :, length:] = 0.0
+        self.ptr.contents.len = int(length)
+
     def arrays(self):
         """(K, V) as float64 views [L, NKV, max_len, D] of the oracle's cache."""
         n = int(np.prod(self._shape))

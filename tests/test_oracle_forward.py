@@ -214,6 +214,38 @@ def test_kv_bf16_option_rounds_the_stored_rows():
     assert not np.array_equal(ka[0, :, :6], kb[0, :, :6])
 
 
+def test_loaded_cache_continues_exactly_like_the_original():
+    """OracleCache.load: a bf16 cache exported as bit patterns and loaded into
+    a fresh cache continues with the same next-token logits, bit for bit; a
+    wrong row count or a corrupted row is seen (the step is conditioned on the
+    loaded history, as the conditional-parity GPU tests need)."""
+    shape = SMALL_QWEN2
+    om = O.OracleModel(shape, synth.weights_bf16(shape))
+    ids = synth.prompt_ids(shape, 12)
+    a = om.new_cache(16, kv_bf16=True)
+    om.forward_cached(a, ids[:11])
+    ka, va = a.arrays()
+    bits = lambda x: (np.ascontiguousarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kb, vb = bits(ka), bits(va)
+    assert np.array_equal(O.bf16_decode(kb), ka.astype(np.float32))   # the rows are bf16 values
+    b = om.new_cache(16, kv_bf16=True)
+    b.load(kb, vb, 11)
+    assert b.len == 11
+    rc1, h1, l1 = om.forward_cached(a, ids[11:])
+    rc2, h2, l2 = om.forward_cached(b, ids[11:])
+    assert rc1 == rc2 == 0
+    assert np.array_equal(l1, l2) and np.array_equal(h1, h2)
+    # a corrupted history row changes the step
+    c = om.new_cache(16, kv_bf16=True)
+    kc = kb.copy()
+    kc[1, 0, 3] ^= np.uint16(0x4000)
+    c.load(kc, vb, 11)
+    _, _, l3 = om.forward_cached(c, ids[11:])
+    assert not np.allclose(l1, l3, rtol=1e-6, atol=1e-6)
+    with pytest.raises(ValueError):
+        c.load(kb[:, :, :5], vb[:, :, :5], 11)
+
+
 def test_cache_errors_and_validation():
     shape = synth.TINY
     om = O.OracleModel(shape, synth.weights_bf16(shape))
