@@ -48,3 +48,20 @@ def assert_tokens(ref_logits, ref_tokens, got_tokens, what):
 def first_argmax(v):
     """np.argmax: first index of the maximum (NaN counts as the maximum)."""
     return int(np.argmax(np.asarray(v)))
+
+
+def oracle_step_on_gpu_cache(om, kv, seq, length, token, max_len=None):
+    """One oracle cached step of `token` at position `length`, starting from
+    rows [0, length) of the GPU's bf16 cache of sequence `seq` (decoded
+    exactly): conditional parity of a decode step at any context length.
+    Returns (final-normed hidden [H], logits [V], oracle K / V rows at
+    position `length` [L, NKV, D])."""
+    K, V = kv.tensors()
+    kb = K[seq][:, :, :length].cpu().numpy()
+    vb = V[seq][:, :, :length].cpu().numpy()
+    oc = om.new_cache(max_len or length + 1, kv_bf16=True)
+    oc.load(kb, vb, length)
+    rc, hid, lg = om.forward_cached(oc, np.array([token], np.int32))
+    assert rc == 0, rc
+    ok, ov = oc.arrays()
+    return hid[0], lg, ok[:, :, length].copy(), ov[:, :, length].copy()

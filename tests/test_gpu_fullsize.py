@@ -14,7 +14,7 @@ from gqa_transformer_decode_gb300 import runtime as R
 from gqa_transformer_decode_gb300 import synth
 from oracle import oracle as O
 
-from parity_util import assert_close, assert_tokens, first_argmax
+from parity_util import assert_close, assert_tokens, first_argmax, oracle_step_on_gpu_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -58,15 +58,15 @@ def greedy_gpu(model, kv, prompt, forced, stream, seq=0):
 
 
 def test_qwen25_05b_prefill_and_decode(stream):
-    """Qwen2.5-0.5B shape, batch 1: the benchmark's 128-token prompt and 8
+    """Qwen2.5-0.5B shape, batch 1: the benchmark's 128-token prompt and 32
     greedy steps (fused decode path) against the oracle."""
     name = "qwen2.5-0.5b"
     shape = synth.WORKLOADS[name].model
     w = weights(name)
     prompt = synth.prompt_ids(shape, 128)
-    toks, olg, _ = O.OracleModel(shape, w).greedy(prompt, 8, kv_bf16=True)
+    toks, olg, _ = O.OracleModel(shape, w).greedy(prompt, 32, kv_bf16=True)
     m = R.Model(shape, w, max_tokens=128)
-    kv = m.kv_alloc(1, 128 + 16)
+    kv = m.kv_alloc(1, 128 + 40)
     glg, gam, _ = greedy_gpu(m, kv, prompt, toks[:-1], stream)
     assert_close(olg, glg, "logits")
     assert_tokens(olg, toks, gam, "greedy tokens")
@@ -104,6 +104,21 @@ def test_llama32_1b_prefix_and_full_prompt(stream):
     assert_close(ghd, hid[:128].cpu().numpy(), "prefix rows of the 2048-token prefill")
     lgn = lg.cpu().numpy()
     assert_close(lgn[0:1], lgn[1:2], "2048-token prefill vs two chunks")
+    # sampled rows of the 2048-token prefill against the oracle: row t from the
+    # GPU's cache rows [0, t) and token t (conditional parity), the last row's
+    # logits too, and the K / V rows the prefill wrote at position t
+    om = O.OracleModel(shape, w)
+    K, Vc = kv.tensors()
+    hidn = hid.cpu().numpy()
+    for t in (500, 1300, 2047):
+        oh, olg_t, ok, ov = oracle_step_on_gpu_cache(om, kv, 0, t, int(full[t]))
+        assert_close(oh[None], hidn[t:t + 1], f"prefill row {t} hidden")
+        if t == 2047:
+            assert_close(olg_t[None], lgn[0:1], "prefill last-position logits")
+        gk = O.bf16_decode(K[0][:, :, t].cpu().numpy().view(np.uint16))
+        gv = O.bf16_decode(Vc[0][:, :, t].cpu().numpy().view(np.uint16))
+        assert_close(ok.reshape(-1, 64), gk.reshape(-1, 64), f"prefill K row {t}")
+        assert_close(ov.reshape(-1, 64), gv.reshape(-1, 64), f"prefill V row {t}")
     # four decode steps of both caches in one batch, both fed slot 0's argmax
     # (teacher forcing keeps the histories equal): the rows must agree
     ids = i32([first_argmax(lgn[0])] * 2)
@@ -165,9 +180,20 @@ def test_batch64_decode_sampled_sequences(stream):
                       stream=stream)
     ids0 = cur.clone()
     lgb = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    amb = torch.empty(B, dtype=torch.int32, device="cuda")
     with torch.cuda.stream(stream):
-        m.decode_step(kv, seqs, ids0, None, logits=lgb, stream=stream)
+        m.decode_step(kv, seqs, ids0, None, logits=lgb, argmax=amb, stream=stream)
     assert m.sync_status(stream) == 0
+    # every sequence's 4096-key step against one oracle step from the GPU's own
+    # cache rows (conditional parity of the decode step; a prefill of 64 x 4096
+    # tokens is out of the oracle's reach)
+    glb, gab, idn = lgb.cpu().numpy(), amb.cpu().numpy(), ids0.cpu().numpy()
+    checked = 0
+    for b in range(B):
+        _, olg_b, _, _ = oracle_step_on_gpu_cache(om, kv, b, P, int(idn[b]))
+        assert_close(olg_b[None], glb[b:b + 1], f"seq {b}: 4096-key step vs oracle")
+        checked += assert_tokens(olg_b[None], [first_argmax(olg_b)], gab[b:b + 1], f"seq {b} token")
+    assert checked > B // 2
     for b in (0, 37, 63):
         lg1 = torch.empty((1, V), dtype=torch.float32, device="cuda")
         with torch.cuda.stream(stream):
@@ -197,3 +223,43 @@ def test_encoder_8x512_sampled_sequence(stream):
     ohd, _, ocl = O.OracleModel(shape, w).forward_full(ids[b * T:(b + 1) * T], logits=False, cls=True)
     assert_close(ocl, out[b * T:(b + 1) * T].cpu().numpy(), "label logits")
     assert_close(ohd, hid[b * T:(b + 1) * T].cpu().numpy(), "final hidden states")
+
+
+@pytest.mark.slow
+def test_batch64_full_run_of_one_sequence_against_oracle(stream):
+    """Qwen2.5-0.5B shape, 64 sequences of 4096-token caches: the oracle's
+    whole run of one sequence (its 4096-token prefill and 64 greedy steps,
+    bf16 cache) against that sequence inside the batched GPU run, with the
+    oracle's tokens fed to it (teacher forcing) so every step stays
+    comparable; the other 63 sequences decode their own argmax beside it."""
+    name = "qwen2.5-0.5b"
+    shape = synth.WORKLOADS[name].model
+    w = weights(name)
+    B, P, S, s = 64, 4096, 64, 21
+    m = R.Model(shape, w, max_tokens=4096)
+    V = shape.vocab
+    prompt_s = synth.prompt_ids(shape, P, seq=s)
+    otoks, olg, _ = O.OracleModel(shape, w).greedy(prompt_s, S, kv_bf16=True, hidden=False)
+    kv = m.kv_alloc(B, P + S + 1)
+    cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    plg = torch.empty(V, dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            m.prefill(kv, b, i32(synth.prompt_ids(shape, P, seq=b)), 0, argmax=cur[b:b + 1],
+                      logits=plg if b == s else None, stream=stream)
+    seqs = torch.arange(B, dtype=torch.int32, device="cuda")
+    lg = torch.empty((S, V), dtype=torch.float32, device="cuda")
+    am = torch.empty((S, B), dtype=torch.int32, device="cuda")
+    full = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    forced = i32(otoks[:S])
+    with torch.cuda.stream(stream):
+        for i in range(S):
+            cur[s:s + 1].copy_(forced[i:i + 1])
+            m.decode_step(kv, seqs, cur, None, logits=full, argmax=cur, stream=stream)
+            lg[i].copy_(full[s])
+            am[i].copy_(cur)
+    assert m.sync_status(stream) == 0
+    glg = np.concatenate([plg.cpu().numpy()[None], lg.cpu().numpy()])
+    gam = np.concatenate([[first_argmax(glg[0])], am.cpu().numpy()[:, s]])
+    assert_close(olg, glg, f"seq {s}: prefill + {S} batched steps vs the oracle's run")
+    assert assert_tokens(olg, otoks, gam, f"seq {s} greedy tokens") > S // 2

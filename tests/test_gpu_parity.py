@@ -10,7 +10,7 @@ from gqa_transformer_decode_gb300 import runtime as R
 from gqa_transformer_decode_gb300 import synth
 from oracle import oracle as O
 
-from parity_util import assert_close, assert_tokens, first_argmax
+from parity_util import assert_close, assert_tokens, first_argmax, oracle_step_on_gpu_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -358,3 +358,70 @@ def test_decode_graph_follows_a_new_cache_with_the_same_buffers(shape, stream):
         toks, olg, _ = om.greedy(prompt, 4)
         assert_tokens(olg, toks, out.cpu().numpy(), f"cache {k} greedy")
         kv.close()
+
+
+@pytest.mark.parametrize("shape", [MID_QWEN2, MID_LLAMA, MID_D128])
+def test_batched_tensor_core_decode_attention_at_multi_split_contexts(shape, stream):
+    """Batch 3 (head_dim 64 / 128: k_attn_decode_mma) at ragged contexts of 130,
+    700 and 2100 keys -- 3, 11 and 32 key splits whose partials the last CTA of
+    each (token, kv head) merges -- for G = 7, 4 and 2, two steps, against the
+    oracle's whole run (bf16 cache on both sides)."""
+    w, om, gm = model_pair(shape, max_tokens=2112)
+    lens = [130, 700, 2100]
+    B, n_steps = 3, 2
+    kv = gm.kv_alloc(B, 2100 + 8)
+    prompts = [synth.prompt_ids(shape, n, seq=b) for b, n in enumerate(lens)]
+    nxt = [synth.uniform_ids(11, f"mma.{b}", n_steps, shape.vocab) for b in range(B)]
+    lg = torch.empty((n_steps, B, shape.vocab), dtype=torch.float32, device="cuda")
+    am = torch.empty((n_steps, B), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            gm.prefill(kv, b, i32(prompts[b]), 0, stream=stream)
+        seqs = i32(list(range(B)))
+        for s in range(n_steps):
+            gm.decode_step(kv, seqs, i32([nxt[b][s] for b in range(B)]),
+                           i32([lens[b] + s for b in range(B)]), logits=lg[s], argmax=am[s],
+                           stream=stream)
+    assert gm.sync_status(stream) == 0
+    glg, gam = lg.cpu().numpy(), am.cpu().numpy()
+    for b in range(B):
+        # greedy with the forced tokens: logits of the prompt's last position,
+        # then of each forced step
+        _, olg, _ = om.greedy(prompts[b], n_steps, forced=nxt[b], kv_bf16=True)
+        assert_close(olg[1:], glg[:, b], f"{shape.name} seq {b} ({lens[b]} keys)")
+        for s in range(n_steps):
+            assert gam[s, b] == first_argmax(glg[s, b])
+
+
+@pytest.mark.parametrize("shape", [MID_LLAMA, MID_D128])
+def test_batch64_decode_ring_wraps_against_oracle_on_the_gpu_cache(shape, stream):
+    """64 sequences with ragged contexts up to 3100 keys: two key splits per
+    (token, kv head), so one CTA streams up to 13 tiles of 128 keys through its
+    2-3 stage copy ring (the ring wraps several times); the projections run on
+    the tensor-core GEMMs (batch > 8).  Every sequence's step is checked
+    against one oracle step started from the GPU's own cache rows."""
+    w, om, gm = model_pair(shape, max_tokens=3200)
+    B = 64
+    lens = [200 + (97 * b) % 2900 for b in range(B)]
+    assert max(lens) > 3000
+    kv = gm.kv_alloc(B, 3200)
+    nxt = synth.uniform_ids(13, "ring", B, shape.vocab)
+    lg = torch.empty((B, shape.vocab), dtype=torch.float32, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            gm.prefill(kv, b, i32(synth.prompt_ids(shape, lens[b], seq=b)), 0, stream=stream)
+        gm.decode_step(kv, torch.arange(B, dtype=torch.int32, device="cuda"), i32(nxt), None,
+                       logits=lg, argmax=am, stream=stream)
+    assert gm.sync_status(stream) == 0
+    glg, gam = lg.cpu().numpy(), am.cpu().numpy()
+    K, V = kv.tensors()
+    for b in range(B):
+        _, olg, ok, ov = oracle_step_on_gpu_cache(om, kv, b, lens[b], nxt[b])
+        assert_close(olg[None], glg[b:b + 1], f"{shape.name} seq {b} ({lens[b]} keys)")
+        assert gam[b] == first_argmax(glg[b])
+        if b % 16 == 0:   # the new K / V row the step wrote, against the oracle's
+            gk = O.bf16_decode(K[b][:, :, lens[b]].cpu().numpy().view(np.uint16))
+            gv = O.bf16_decode(V[b][:, :, lens[b]].cpu().numpy().view(np.uint16))
+            assert_close(ok.reshape(-1, shape.head_dim), gk.reshape(-1, shape.head_dim), "K row")
+            assert_close(ov.reshape(-1, shape.head_dim), gv.reshape(-1, shape.head_dim), "V row")
