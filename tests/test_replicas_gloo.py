@@ -79,3 +79,16 @@ def test_reference_arm_under_the_launcher_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["config"]["workload"] == "tiny"
+
+
+def test_gpus_flag_without_a_launcher_spawns_the_replicas():
+    """bench.py --gpus 2 run directly re-launches itself under
+    torch.distributed.run with two processes; still one line, from rank 0."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "3", "--workload", "tiny"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
