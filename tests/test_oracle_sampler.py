@@ -4,7 +4,8 @@ what the page and the mathematics fix: temperature 0 is greedy; a single
 survivor is drawn with certainty; known distributions are drawn at the right
 boundaries; a stratified sweep of the draw reproduces the probabilities; the
 filters keep ties with the threshold, follow the page's order, and reduce to
-the unfiltered softmax when disabled; a fully masked row is uniform."""
+the unfiltered softmax when disabled; a fully masked row is uniform; the
+probabilities are the f64 softmax of the f32 logits, summed in order."""
 import numpy as np
 import pytest
 
@@ -113,8 +114,8 @@ def test_top_k_then_top_p_in_the_pages_order():
 
 def test_fully_masked_row_is_uniform():
     x = np.full(4, -np.inf, dtype=F32)
-    d = S.softmax_f32(x)
-    assert np.array_equal(d, np.full(4, 0.25, dtype=F32))
+    d = S.softmax_f64(x)
+    assert np.array_equal(d, np.full(4, 0.25))
     assert S.categorical(d, 0.0) == 0 and S.categorical(d, 0.5) == 2 and S.categorical(d, 0.999) == 3
 
 
@@ -125,17 +126,38 @@ def test_rounding_fallback_takes_the_last_maximal_index():
     assert S.categorical(d, 1.5) == 2
 
 
-def test_running_sums_are_f32_in_index_order():
-    """The page's loops add one term at a time in f32: the sampler's running
-    sums are that order (numpy's own float32 sum is pairwise and may differ)."""
+def test_running_sums_are_in_index_order_and_f64():
+    """The page's loops add one term at a time: the sampler's running sums are
+    that order, in f64 (numpy's own sum is pairwise and may differ in the last
+    bit); the distribution sums to 1 within f64 rounding over a vocabulary-
+    sized row, where an f32 running sum would drift by ~1e-4."""
     rng = np.random.default_rng(4)
-    e = rng.random(100003).astype(F32)
-    s = F32(0.0)
+    e = rng.random(100003)
+    s = 0.0
     for v in e[:5000]:
-        s = F32(s + v)
-    assert np.add.accumulate(e[:5000], dtype=F32)[-1] == s
-    d = S.softmax_f32(np.log(e).astype(F32))
-    assert abs(float(np.sum(d, dtype=np.float64)) - 1.0) < 1e-3
+        s = s + v
+    assert np.add.accumulate(e[:5000])[-1] == s
+    x = np.log(e).astype(F32)
+    d = S.softmax_f64(x)
+    assert d.dtype == np.float64 and abs(float(d.sum()) - 1.0) < 1e-12
+    # the probabilities are the f64 softmax of the f32 logits
+    ref = np.exp(x.astype(np.float64) - x.max())
+    assert np.allclose(d, ref / ref.sum(), rtol=1e-13, atol=0)
+
+
+def test_boundary_draws_in_f64_follow_the_exact_cdf():
+    """Probabilities that are exact binary fractions: a draw exactly at a
+    cumulative boundary goes to the next token (r < cum is strict), a draw one
+    f32 step below it stays; the f64 sums are exact here, so no rounding
+    enters the decision."""
+    x = log_probs([0.25, 0.25, 0.5])
+    d = S.sample_distribution(np.log(np.array([1, 1, 2], np.float64)).astype(F32), 1.0, 0, 1.0)
+    assert np.allclose(d, [0.25, 0.25, 0.5], atol=1e-7)
+    q = np.array([0.25, 0.25, 0.5])
+    assert S.categorical(q, 0.25) == 1 and S.categorical(q, 0.5) == 2
+    assert S.categorical(q, float(np.nextafter(F32(0.25), F32(0)))) == 0
+    assert S.categorical(q, float(np.nextafter(F32(0.5), F32(0)))) == 1
+    assert x.dtype == F32
 
 
 def test_rows_use_their_own_draws():
