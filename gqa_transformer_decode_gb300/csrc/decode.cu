@@ -53,11 +53,13 @@ __global__ void k_embed(EmbedArgs a) {
     const uint16_t* row = a.E + (size_t)s_id * a.H;
     float* out = a.x + (size_t)t * a.H;
     for (int i = threadIdx.x; i < a.H; i += blockDim.x) out[i] = bf16_to_f32(row[i]);
-    if (a.zero0)
-        for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
-            a.zero0[(size_t)t * a.H + i] = 0.f;
-            a.zero1[(size_t)t * a.H + i] = 0.f;
+    if (a.zero0) {
+        const int zl = a.zlen > 0 ? a.zlen : a.H;
+        for (int i = threadIdx.x; i < zl; i += blockDim.x) {
+            a.zero0[(size_t)t * zl + i] = 0.f;
+            a.zero1[(size_t)t * zl + i] = 0.f;
         }
+    }
 }
 
 void launch_embed(const EmbedArgs& a, cudaStream_t s) {
@@ -118,9 +120,11 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     if (XA) {
         float ss = 0.f;
         for (int i = tid * 4; i < a.K; i += GEMV_THREADS * 4) {
-            const float4 u = __ldcg(reinterpret_cast<const float4*>(a.x + i));
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x_add + i));
-            const float4 t = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+            float4 t = __ldcg(reinterpret_cast<const float4*>(a.x + i));
+            for (int z = 0; z < a.x_add_slots; ++z) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x_add + (size_t)z * a.K + i));
+                t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+            }
             ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
             *reinterpret_cast<float4*>(s_xa + i) = t;
         }

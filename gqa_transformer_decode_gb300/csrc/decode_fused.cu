@@ -98,6 +98,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// relaxed load (a hint read while another kernel may write the word)
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -118,12 +124,17 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
                  : "memory");
 }
 
-// RMSNorm of the residual x = x_in + z_in (H floats, H % 4 == 0, H <= 4096
-// for 256 threads).  The weights are loaded into registers before the
-// programmatic-launch wait (load_w); apply() issues all of its 16-byte loads
-// at once, writes this CTA's slice of x_out (= x) and of z_zero (= 0) from
-// the values it holds, and leaves f16(x * rsqrt(mean(x^2) + eps) * w) in s_xh
-// (the projections' input, at the precision of the tensor-core GEMM operands).
+// RMSNorm of the residual x = x_in + the sum of the ZI copies of z_in (H
+// floats, H % 4 == 0, H <= 4096 for 256 threads).  The weights are loaded
+// into registers before the programmatic-launch wait (load_w); apply() issues
+// all of its 16-byte loads at once, writes this CTA's slice of x_out (= x) and
+// of the ZZ copies of z_zero (= 0) from the values it holds, and leaves
+// f16(x * rsqrt(mean(x^2) + eps) * w) in s_xh (the projections' input, at the
+// precision of the tensor-core GEMM operands).  The MLP block accumulates into
+// ZSLOTS copies (152+ CTAs add into every element), the attention block into
+// one (one cluster per kv head adds into an element): the attention block
+// reads ZSLOTS copies and clears ZSLOTS for the MLP block after it, the MLP
+// block reads one and clears one.
 struct ResidualNorm {
     static constexpr int MAXV = 4;
     float4 w[MAXV];
@@ -135,6 +146,7 @@ struct ResidualNorm {
             w[q] = i < H4 ? __ldg(reinterpret_cast<const float4*>(wp) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    template <int ZI, int ZZ>
     __device__ __forceinline__ void apply(const float* x_in, const float* z_in, float* x_out, float* z_zero,
                                           float eps, int H, int cta, int ncta, uint16_t* s_xh, float* s_red) {
         const int H4 = H >> 2;
@@ -146,9 +158,15 @@ struct ResidualNorm {
         for (int q = 0; q < MAXV; ++q) {
             const int i = threadIdx.x + q * blockDim.x;
             if (i < H4) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(x_in) + i);
-                const float4 b = __ldcg(reinterpret_cast<const float4*>(z_in) + i);
-                v[q] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+                float4 b[ZI];
+#pragma unroll
+                for (int z = 0; z < ZI; ++z) b[z] = __ldcg(reinterpret_cast<const float4*>(z_in + (size_t)z * H) + i);
+                float4 t = __ldcg(reinterpret_cast<const float4*>(x_in) + i);
+#pragma unroll
+                for (int z = 0; z < ZI; ++z) {
+                    t.x += b[z].x; t.y += b[z].y; t.z += b[z].z; t.w += b[z].w;
+                }
+                v[q] = t;
             }
         }
 #pragma unroll
@@ -158,7 +176,9 @@ struct ResidualNorm {
                 ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
                 if (i >= e0 && i < e1) {
                     reinterpret_cast<float4*>(x_out)[i] = v[q];
-                    reinterpret_cast<float4*>(z_zero)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int z = 0; z < ZZ; ++z)
+                        reinterpret_cast<float4*>(z_zero + (size_t)z * H)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
         }
@@ -363,6 +383,25 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     const uint32_t wo_bytes = o1 > o0 ? (uint32_t)((o1 - o0) * GD * 2) : 0u;
     for (uint32_t off = (uint32_t)tid * 16384u; off < wo_bytes; off += FA_THREADS * 16384u)
         prefetch_l2(reinterpret_cast<const uint8_t*>(wo_cta) + off, min(16384u, wo_bytes - off));
+    // The K/V rows this CTA will read, into L2 before the wait: the position
+    // is taken from the previous step's resolved position (a hint; the real
+    // one is read after the wait), so all keys but the newest are prefetched.
+    {
+        const int hseq = ld_relaxed(a.seqs);
+        const int hpos = ld_relaxed(a.tok_pos) + 1;
+        if (hseq >= 0 && hseq < a.max_seqs && hpos > 0 && hpos < a.max_len) {
+            const int hn = hpos + 1;
+            const int hper = hn <= FA_SOLO ? hn : (hn + C - 1) / C;
+            const int hlo = hn <= FA_SOLO ? (r == 0 ? 0 : hn) : min(hn, r * hper);
+            const int hhi = hn <= FA_SOLO ? hn : min(hn, hlo + hper);
+            const size_t row0 = ((size_t)((hseq * a.L + a.layer) * a.NKV + g) * a.max_len + hlo) * D;
+            const uint32_t bytes = (uint32_t)(hhi - hlo) * D * 2;
+            for (uint32_t off = (uint32_t)tid * 16384u; off < bytes; off += FA_THREADS * 16384u) {
+                prefetch_l2(reinterpret_cast<const uint8_t*>(a.kc + row0) + off, min(16384u, bytes - off));
+                prefetch_l2(reinterpret_cast<const uint8_t*>(a.vc + row0) + off, min(16384u, bytes - off));
+            }
+        }
+    }
     ResidualNorm rn;
     rn.load_w(a.norm_w, H);
     float* s_bias = s_part;   // the biases of this CTA's rows, until the partials are written
@@ -382,7 +421,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     // the step's token state, loaded beside the residual (used after the norm)
     const int ok_raw = __ldcg(a.tok_ok);
     const int pos_raw = __ldcg(a.tok_pos);
-    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
+    rn.apply<ZSLOTS, ZSLOTS>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
 
     const int ok = ok_raw;
     const int pos = ok ? pos_raw : 0;
@@ -775,6 +814,15 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
         prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
         prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
     }
+    // the first pf_late CTAs prefetch the chunks of the last pf_late CTAs,
+    // which launch only when the attention CTAs leave their SMs
+    if ((int)blockIdx.x < a.pf_late) {
+        const int lb = (int)gridDim.x - a.pf_late + (int)blockIdx.x;
+        for (int ch = lb + tid * (int)gridDim.x; ch < n_chunks; ch += FM_THREADS * (int)gridDim.x) {
+            prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
+            prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
+        }
+    }
     ResidualNorm rn;
     rn.load_w(a.norm_w, H);
     // phase-1 role: row quad qd over the hidden slice [c0, c1) (16-byte units)
@@ -789,7 +837,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     pdl_trigger();
     pdl_wait();
 
-    rn.apply(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
+    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
     XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
 
@@ -859,6 +907,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
             }
         }
     }
+    float* z_acc = a.z_acc + (size_t)(blockIdx.x % ZSLOTS) * H;
     if (halves) {   // the second half's sums join the first half's
         if (part == 1 && tid < 2 * H8) {
             reinterpret_cast<float4*>(s_y)[2 * hgp] = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
@@ -868,16 +917,16 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
         if (part == 0 && tid < H8 && my_n > 0) {
             const float4 b0 = reinterpret_cast<const float4*>(s_y)[2 * tid];
             const float4 b1 = reinterpret_cast<const float4*>(s_y)[2 * tid + 1];
-            red_add4(a.z_acc + 8 * tid, y[0][0] + b0.x, y[0][1] + b0.y, y[0][2] + b0.z, y[0][3] + b0.w);
-            red_add4(a.z_acc + 8 * tid + 4, y[0][4] + b1.x, y[0][5] + b1.y, y[0][6] + b1.z, y[0][7] + b1.w);
+            red_add4(z_acc + 8 * tid, y[0][0] + b0.x, y[0][1] + b0.y, y[0][2] + b0.z, y[0][3] + b0.w);
+            red_add4(z_acc + 8 * tid + 4, y[0][4] + b1.x, y[0][5] + b1.y, y[0][6] + b1.z, y[0][7] + b1.w);
         }
     } else {
 #pragma unroll
         for (int q = 0; q < MAXHG; ++q) {
             const int hg = tid + q * FM_THREADS;
             if (hg < H8 && my_n > 0) {
-                red_add4(a.z_acc + 8 * hg, y[q][0], y[q][1], y[q][2], y[q][3]);
-                red_add4(a.z_acc + 8 * hg + 4, y[q][4], y[q][5], y[q][6], y[q][7]);
+                red_add4(z_acc + 8 * hg, y[q][0], y[q][1], y[q][2], y[q][3]);
+                red_add4(z_acc + 8 * hg + 4, y[q][4], y[q][5], y[q][6], y[q][7]);
             }
         }
     }
@@ -907,28 +956,51 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     p.smem_attn = fa_layout(D, G, H, p.nr, p.no).total;
     if (p.smem_attn < 116 * 1024) p.smem_attn = 116 * 1024;
     if (p.smem_attn > 200 * 1024) return no("attention block needs > 200 KB of shared memory");
-    // MLP chunk size: the largest FC in {16, 8, 4} (dividing F) whose two-stage
-    // ring still fits beside the attention kernel on one SM; else FC = 4.
+    // MLP plan.  Resident: the CTA's chunks all fit its shared memory, so the
+    // weights are in place before the wait and nothing is refilled after it;
+    // the grid has two CTAs per SM and a CTA fits beside an attention CTA (the
+    // CTAs that find no room launch when the attention CTAs leave, their
+    // weights prefetched to L2 by the first CTAs).  Otherwise a ring: the
+    // largest FC in {16, 8, 4} (dividing F) whose two-stage ring still fits
+    // beside the attention kernel on one SM (else FC = 4), one CTA per SM,
+    // chunks beyond the ring refilled from L2.
     const int fixed = ((H * 2 + 15) / 16) * 16 + H * 4 + 256;   // s_xh (f16) + s_y (f32) + alignment
     const int budget = 227 * 1024 - p.smem_attn - 2 * 1024;
     p.fc = 0;
-    for (int fc : {16, 8, 4})
-        if (F % fc == 0 && 2 * 6 * fc * H + fixed <= budget) {
+    for (int fc : {16, 8, 4}) {
+        if (F % fc) continue;
+        const int n_chunks = F / fc;
+        const int cpc = (n_chunks + 2 * num_sms - 1) / (2 * num_sms);
+        const int smem = cpc * 6 * fc * H + fixed;
+        if (cpc <= 8 && smem <= budget && 2 * (smem + 1024) <= 228 * 1024) {
             p.fc = fc;
+            p.ns = cpc;
+            p.mlp_grid = (n_chunks + cpc - 1) / cpc;
+            p.smem_mlp = smem;
+            p.resident = true;
+            p.pf_late = C * NKV < p.mlp_grid ? C * NKV : 0;
             break;
         }
-    const bool coresident = p.fc != 0;
-    if (!coresident) p.fc = 4;
-    const int stage = 6 * p.fc * H;
-    const int n_chunks = F / p.fc;
-    p.mlp_grid = n_chunks < num_sms ? n_chunks : num_sms;
-    const int per_cta = (n_chunks + p.mlp_grid - 1) / p.mlp_grid;
-    int ns = ((coresident ? budget : 200 * 1024) - fixed) / stage;
-    if (ns > per_cta) ns = per_cta;
-    if (ns > 8) ns = 8;
-    if (ns < 2) ns = 2;
-    p.ns = ns;
-    p.smem_mlp = ns * stage + fixed;
+    }
+    if (!p.resident) {
+        for (int fc : {16, 8, 4})
+            if (F % fc == 0 && 2 * 6 * fc * H + fixed <= budget) {
+                p.fc = fc;
+                break;
+            }
+        const bool coresident = p.fc != 0;
+        if (!coresident) p.fc = 4;
+        const int stage = 6 * p.fc * H;
+        const int n_chunks = F / p.fc;
+        p.mlp_grid = n_chunks < num_sms ? n_chunks : num_sms;
+        const int per_cta = (n_chunks + p.mlp_grid - 1) / p.mlp_grid;
+        int ns = ((coresident ? budget : 200 * 1024) - fixed) / stage;
+        if (ns > per_cta) ns = per_cta;
+        if (ns > 8) ns = 8;
+        if (ns < 2) ns = 2;
+        p.ns = ns;
+        p.smem_mlp = ns * stage + fixed;
+    }
     if (p.smem_mlp > 227 * 1024) return no("MLP ring does not fit shared memory");
     // The limit is a property of the function, shared by every model in the
     // process: raise it to the device maximum so that no model lowers it

@@ -315,7 +315,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     aa.add(&m->status, 1);
     if (m->fp.ok) {
         for (auto& p : m->fx) aa.add(&p, (size_t)H);
-        for (auto& p : m->fz) aa.add(&p, (size_t)H);
+        for (auto& p : m->fz) aa.add(&p, (size_t)H * ZSLOTS);
     }
     if (!c.causal) {
         aa.add(&m->enc_k, (size_t)T * m->kv);
@@ -798,6 +798,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         ea.x = m->fx[0];
         ea.zero0 = m->fz[0];
         ea.zero1 = m->fz[1];
+        ea.zlen = c.hidden * ZSLOTS;
         launch_embed(ea, s);
         const FusedPlan& fp = m->fp;
         int n = 1;
@@ -829,6 +830,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.kc = kv->k;
             a.vc = kv->v;
             a.max_len = kv->max_len;
+            a.max_seqs = kv->max_seqs;
             a.seqs = seqs;
             a.tok_pos = m->tok_pos;
             a.tok_ok = m->tok_ok;
@@ -849,6 +851,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             io(f.x_in, f.z_in, f.x_out, f.z_zero, f.z_acc);
             f.status = m->status;
             f.ns = fp.ns;
+            f.pf_late = fp.pf_late;
             launch_fused_mlp(f, fp.fc, fp.xi, fp.mlp_grid, fp.smem_mlp, s);
         }
         GemvArgs g{};
@@ -857,6 +860,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         g.K = c.hidden;
         g.x = m->fx[(n - 1) % 2];
         g.x_add = m->fz[(n - 1) % 3];
+        g.x_add_slots = ZSLOTS;
         g.ldx = c.hidden;
         g.norm_w = m->final_norm;
         g.eps = eps;

@@ -55,8 +55,9 @@ struct EmbedArgs {
     int32_t* tok_pos;            // [n] resolved position (positions[t] or the cursor)
     // prefill check (pf_seq < 0: none)
     int pf_seq, pf_start;
-    float* zero0;                // [n][H] set to 0 when non-null (residual accumulators)
+    float* zero0;                // [n][zlen] set to 0 when non-null (residual accumulators)
     float* zero1;
+    int zlen;                    // floats per token zeroed in zero0 / zero1 (0: H)
 };
 void launch_embed(const EmbedArgs& a, cudaStream_t s);
 
@@ -78,7 +79,9 @@ struct GemvArgs {
     int mode;                    // EpiMode
     unsigned long long* keys;    // [nb] argmax keys (EPI_ARGMAX)
     int* status;
-    const float* x_add;          // [ldx] added to x (residual accumulator; nb == 1, bf16 W), or nullptr
+    const float* x_add;          // [x_add_slots][K] summed into x (split-K accumulator copies;
+                                 // nb == 1, bf16 W), or nullptr
+    int x_add_slots;
 };
 // Returns the launch's own error (not the thread's pending last error).
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms);
@@ -272,6 +275,11 @@ void launch_vt(const VtArgs& a, int zs, cudaStream_t s);
 // Two kernels per decoder layer (decode_fused.cu).  Residual stream of kernel
 // n: x_n = x_in + z_in; the kernel writes x_out = x_n, zeroes z_zero and adds
 // its output into z_acc (three rotating accumulators, two x buffers).
+// The batch-1 decode's split-K accumulators have ZSLOTS copies of the
+// hidden vector: a CTA adds into copy (CTA index % ZSLOTS) and a reader sums
+// the copies, so that ZSLOTS times fewer atomic additions meet at one address.
+constexpr int ZSLOTS = 8;
+
 struct FusedPlan {
     int C = 0;           // CTAs per cluster (one cluster per kv head)
     int nr = 0, no = 0;  // q/k/v rows and o_proj rows per CTA
@@ -280,6 +288,8 @@ struct FusedPlan {
     int fc = 0;          // intermediate features per MLP chunk (4, 8 or 16)
     int xi = 0;          // 16-byte input chunks per lane in the row dots (4: inputs <= 1024, 8: <= 2048)
     int mlp_grid = 0;
+    bool resident = false;   // every MLP CTA's chunks fit its shared memory (ns = chunks per CTA)
+    int pf_late = 0;         // CTAs whose chunks the first CTAs prefetch to L2 (resident plan)
     bool ok = false;
     const char* why = "not planned";   // reason when !ok
 };
@@ -301,7 +311,7 @@ struct FusedAttnArgs {
     float* z_acc;
     uint16_t* kc;                // K / V cache [seq][layer][kv head][max_len][D] bf16
     uint16_t* vc;
-    int max_len;
+    int max_len, max_seqs;
     const int32_t* seqs;
     const int32_t* tok_pos;
     const int* tok_ok;
@@ -327,6 +337,7 @@ struct FusedMlpArgs {
     float* z_acc;
     int* status;
     int ns;
+    int pf_late;                 // the first pf_late CTAs prefetch the last pf_late CTAs' chunks to L2
 };
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
 
