@@ -29,6 +29,8 @@
 #include "tc_common.cuh"
 #include "mma_common.cuh"
 
+#include <cstdlib>
+
 namespace ember {
 
 namespace {
@@ -97,6 +99,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 // relaxed load (a hint read while another kernel may write the word)
 __device__ __forceinline__ int ld_relaxed(const int* p) {
@@ -291,30 +298,43 @@ __device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, con
 }  // namespace
 
 // ================================================================== D1 ==
-constexpr int FA_THREADS = 256;
 constexpr int FA_KT = 128;     // keys per K/V tile (the TMA box height)
 constexpr int FA_C = 16;       // CTAs per cluster (one cluster per kv head)
 constexpr int FA_SOLO = 384;   // up to this many keys one CTA of the cluster does the attention
 
 // Shared-memory plan of D1 (host and device compute it the same way).
+// Resident (res): two K/V tile buffers and separate q/k/v and o_proj weight
+// buffers, all filled before the programmatic-launch wait.  Otherwise one
+// tile buffer, and one weight buffer that takes the q/k/v rows, then the
+// o_proj rows (or, for CTA 0 alone over more than one tile, the second tile).
 struct FaLayout {
-    int k, v, w, x, qkv, part, att, qh, wm, cs, red, bar, total;
+    int k, v, k1, v1, w, wo, x, qkv, part, att, qh, wm, cs, red, bar, total;
 };
-__host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int no) {
+__host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int no, bool res, int nw = 8) {
     FaLayout L;
     const int tile = FA_KT * D * 2;              // one K (or V) tile, bf16
     int o = 0;
     L.k = o; o += tile;
     L.v = o; o += tile;
+    L.k1 = L.v1 = 0;
+    if (res) {
+        L.k1 = o; o += tile;
+        L.v1 = o; o += tile;
+    }
     L.w = o;
-    const int wb = 2 * (nr * H > no * G * D ? nr * H : no * G * D);
+    const int wb = res ? 2 * nr * H : 2 * (nr * H > no * G * D ? nr * H : no * G * D);
     o += (wb + 1023) / 1024 * 1024;
+    L.wo = L.w;
+    if (res) {
+        L.wo = o;
+        o += (2 * no * G * D + 1023) / 1024 * 1024;
+    }
     L.x = o; o += ((H * 4 + 15) / 16) * 16;
     L.qkv = o; o += (((G + 2) * D * 4 + 15) / 16) * 16;
     L.part = o; o += ((G * (D + 2) * 4 + 15) / 16) * 16;
     L.att = o; o += ((G * D * 4 + 15) / 16) * 16;
     L.qh = o; o += 16 * D * 2;                    // q as the f16 A tile of the key mma
-    L.wm = o; o += 8 * G * (D + 2) * 4;           // the 8 warps' (m, l, O) per head
+    L.wm = o; o += nw * G * (D + 2) * 4;          // the warps' (m, l, O) per head
     L.cs = o; o += D * 4;                         // RoPE row of the position: cos | sin
     L.red = o; o += 32 * 4;
     L.bar = o; o += 8 * 8;
@@ -322,33 +342,42 @@ __host__ __device__ inline FaLayout fa_layout(int D, int G, int H, int nr, int n
     return L;
 }
 
-template <int D, int XI>
-__global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_constant__ CUtensorMap k_map,
+// NW warps: 8 (two CTAs may share an SM), or 16 in the partitioned plan,
+// where the CTA has its SM alone and a pass over the keys takes two tiles.
+template <int D, int XI, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const __grid_constant__ CUtensorMap k_map,
                                                            const __grid_constant__ CUtensorMap v_map,
                                                            FusedAttnArgs a) {
     constexpr int H2 = D / 2;
+    constexpr int NTH = NW * 32;   // threads
+    constexpr int TPI = NW / 8;   // K/V tiles per pass (warp w takes keys 16*(w % 8) of tile w / 8)
     constexpr int NSUB = D / 64;               // 64-column TMA sub-tiles per row
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, G = a.NH / a.NKV;
     constexpr int C = FA_C;
     const int Rg = (G + 2) * D;
-    const FaLayout Lo = fa_layout(D, G, H, a.nr, a.no);
+    const bool res = a.resident != 0;
+    const FaLayout Lo = fa_layout(D, G, H, a.nr, a.no, res, NW);
     uint8_t* sK = sm + Lo.k;
     uint8_t* sV = sm + Lo.v;
     uint16_t* sW = reinterpret_cast<uint16_t*>(sm + Lo.w);
+    uint16_t* sWo = reinterpret_cast<uint16_t*>(sm + Lo.wo);  // o_proj rows (== sW unless res)
     uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + Lo.x);  // normed input, f16
     float* s_qkv = reinterpret_cast<float*>(sm + Lo.qkv);    // [G*D q | D k | D v]
     float* s_part = reinterpret_cast<float*>(sm + Lo.part);  // [G][m, l, acc[D]]
     float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads
     uint8_t* sQh = sm + Lo.qh;                                 // [16][D] f16, swizzled
-    float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [8][G][D + 2]
+    float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [NW][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
     // mbarriers: 0 q/k/v weights, 1 K/V tile, 2 o_proj weights, 3 q/k/v rows
     // received from the cluster, 4 attention output received from the cluster,
     // 5 second K/V tile buffer
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lo.bar);
     __shared__ int s_err;
+    __shared__ int s_ph[2];   // resident mode: phases of the two tile barriers after the speculative copies
+    __shared__ float s_sc[16 * NW];   // per head and warp: the weight of the warp's softmax state
+    __shared__ float s_ml[2 * 16];    // per head: the maximum and the total of the weighted sums
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = (int)cluster_rank();
@@ -378,15 +407,68 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             }
         }
     }
-    // o_proj rows of this CTA (group g's block, contiguous): into L2 now, shared memory later
+    // o_proj rows of this CTA (group g's block, contiguous): resident mode
+    // copies them now, otherwise into L2 now and shared memory later
     const uint16_t* wo_cta = a.wo + ((size_t)g * H + o0) * GD;
     const uint32_t wo_bytes = o1 > o0 ? (uint32_t)((o1 - o0) * GD * 2) : 0u;
-    for (uint32_t off = (uint32_t)tid * 16384u; off < wo_bytes; off += FA_THREADS * 16384u)
-        prefetch_l2(reinterpret_cast<const uint8_t*>(wo_cta) + off, min(16384u, wo_bytes - off));
+    auto issue_wo = [&]() {   // one bulk copy: the slice is contiguous
+        mbar_expect_tx(&bar[2], wo_bytes);
+        bulk_g2s(sWo, wo_cta, wo_bytes, &bar[2]);
+    };
+    if (res) {
+        if (tid == 0 && o1 > o0) issue_wo();
+    } else {
+        for (uint32_t off = (uint32_t)tid * 16384u; off < wo_bytes; off += NTH * 16384u)
+            prefetch_l2(reinterpret_cast<const uint8_t*>(wo_cta) + off, min(16384u, wo_bytes - off));
+    }
+    constexpr int TILE = FA_KT * D * 2;
+    uint8_t* sK1 = res ? sm + Lo.k1 : reinterpret_cast<uint8_t*>(sW);
+    uint8_t* sV1 = res ? sm + Lo.v1 : reinterpret_cast<uint8_t*>(sW) + TILE;
+    // K/V tile t0.. of plane kz into buffer 0 (sK/sV, barrier 1) or 1 (sK1/sV1, barrier 5)
+    auto issue_tile = [&](int t0, int buf, int kz) {
+        uint8_t* kd = buf ? sK1 : sK;
+        uint8_t* vd = buf ? sV1 : sV;
+        uint64_t* b = buf ? &bar[5] : &bar[1];
+        mbar_expect_tx(b, (uint32_t)(2 * TILE));
+        for (int sb = 0; sb < NSUB; ++sb) {
+            tma_load_3d(kd + sb * FA_KT * 128, &k_map, sb * 64, t0, kz, b);
+            tma_load_3d(vd + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, b);
+        }
+    };
+    // this CTA's key range [lo, hi) for n_keys keys
+    auto key_range = [&](int n_keys, int& lo_, int& hi_) {
+        const int per_ = n_keys <= FA_SOLO ? n_keys : (n_keys + C - 1) / C;
+        lo_ = n_keys <= FA_SOLO ? (r == 0 ? 0 : n_keys) : min(n_keys, r * per_);
+        hi_ = n_keys <= FA_SOLO ? n_keys : min(n_keys, lo_ + per_);
+    };
+    // Resident mode: the first two K/V tiles of the position the step will
+    // use, issued now.  That position is already fixed (an explicit position,
+    // or the cursor the previous step left); the rows before it were written
+    // by earlier steps.  The embed kernel's checks are read after the wait,
+    // and a token they reject or move makes the CTA drain these copies and
+    // issue the right ones.
+    int spec_seq = -1, spec_pos = -1, spec_n = 0;
+    if (res && tid == 0) {
+        const int sq = ld_relaxed(a.seqs);
+        if (sq >= 0 && sq < a.max_seqs) {
+            const int ps = a.positions ? ld_relaxed(a.positions) : ld_relaxed(a.cursor + sq);
+            if (ps >= 0 && ps < a.max_len) {
+                int slo, shi;
+                key_range(ps + 1, slo, shi);
+                const int kzs = (sq * a.L + a.layer) * a.NKV + g;
+                for (int j = 0; j < 2 && slo + j * FA_KT < shi; ++j) {
+                    issue_tile(slo + j * FA_KT, j, kzs);
+                    ++spec_n;
+                }
+                spec_seq = sq;
+                spec_pos = ps;
+            }
+        }
+    }
     // The K/V rows this CTA will read, into L2 before the wait: the position
     // is taken from the previous step's resolved position (a hint; the real
     // one is read after the wait), so all keys but the newest are prefetched.
-    {
+    if (!res) {
         const int hseq = ld_relaxed(a.seqs);
         const int hpos = ld_relaxed(a.tok_pos) + 1;
         if (hseq >= 0 && hseq < a.max_seqs && hpos > 0 && hpos < a.max_len) {
@@ -396,7 +478,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             const int hhi = hn <= FA_SOLO ? hn : min(hn, hlo + hper);
             const size_t row0 = ((size_t)((hseq * a.L + a.layer) * a.NKV + g) * a.max_len + hlo) * D;
             const uint32_t bytes = (uint32_t)(hhi - hlo) * D * 2;
-            for (uint32_t off = (uint32_t)tid * 16384u; off < bytes; off += FA_THREADS * 16384u) {
+            for (uint32_t off = (uint32_t)tid * 16384u; off < bytes; off += NTH * 16384u) {
                 prefetch_l2(reinterpret_cast<const uint8_t*>(a.kc + row0) + off, min(16384u, bytes - off));
                 prefetch_l2(reinterpret_cast<const uint8_t*>(a.vc + row0) + off, min(16384u, bytes - off));
             }
@@ -414,7 +496,10 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         s_bias[tid] = a.bqkv[src];
     }
     __syncthreads();
-    cluster_arrive_relaxed();   // barriers initialised; matched by cluster_wait() before the first remote store
+    // every CTA's barriers initialised before any remote store: the whole
+    // cluster barrier runs before the wait, off the critical path
+    cluster_arrive_relaxed();
+    cluster_wait();
     pdl_trigger();
     pdl_wait();
 
@@ -428,32 +513,35 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     const int n_keys = ok ? pos + 1 : 0;
     // short contexts: CTA 0 takes every key and no partials need merging
     const bool solo = n_keys <= FA_SOLO;
-    const int per = solo ? n_keys : (n_keys + C - 1) / C;
-    const int lo = solo ? (r == 0 ? 0 : n_keys) : min(n_keys, r * per);
-    const int hi = solo ? n_keys : min(n_keys, lo + per);
+    int lo, hi;
+    key_range(n_keys, lo, hi);
     const int seq = ok ? a.seqs[0] : 0;
     const int kz = (seq * a.L + a.layer) * a.NKV + g;     // (seq, layer, kv head) plane
     const bool owner = ok && pos >= lo && pos < hi;
     const bool attn_cta = !solo || r == 0;                // receives q/k/v and runs attention
-    // CTA 0 alone over more than one tile: the second tile goes to the q/k/v
-    // weight buffer as soon as the rows are done (the CTA's o_proj rows follow
-    // there after attention), so two tiles are in flight
-    constexpr int TILE = FA_KT * D * 2;
-    const bool dual = solo && r == 0 && n_keys > FA_KT && Lo.x - Lo.w >= 2 * TILE;
-    uint8_t* sK1 = reinterpret_cast<uint8_t*>(sW);
-    uint8_t* sV1 = sK1 + TILE;
-    auto issue_tile = [&](int t0, int buf) {   // buffer 0: sK/sV on barrier 1; 1: sK1/sV1 on barrier 5
-        uint8_t* kd = buf ? sK1 : sK;
-        uint8_t* vd = buf ? sV1 : sV;
-        uint64_t* b = buf ? &bar[5] : &bar[1];
-        mbar_expect_tx(b, (uint32_t)(2 * TILE));
-        for (int sb = 0; sb < NSUB; ++sb) {
-            tma_load_3d(kd + sb * FA_KT * 128, &k_map, sb * 64, t0, kz, b);
-            tma_load_3d(vd + sb * FA_KT * 128, &v_map, sb * 64, t0, kz, b);
-        }
-    };
+    // Two tiles in flight: always in resident mode; otherwise for CTA 0 alone
+    // over more than one tile, the second tile going to the q/k/v weight
+    // buffer as soon as the rows are done (the CTA's o_proj rows follow there
+    // after attention).
+    const bool dual = res || (solo && r == 0 && n_keys > FA_KT && Lo.x - Lo.w >= 2 * TILE);
     if (tid == 0) {
-        if (hi > lo) issue_tile(lo, 0);
+        if (res) {
+            // the speculative tiles stand when the step uses their position;
+            // otherwise they are drained before the buffers are refilled
+            const bool keep = ok && seq == spec_seq && pos == spec_pos;
+            int ph0 = 0, ph1 = 0;
+            if (!keep) {
+                if (spec_n > 0 && !mbar_wait(&bar[1], 0)) s_err = 1;
+                if (spec_n > 1 && !mbar_wait(&bar[5], 0)) s_err = 1;
+                ph0 = spec_n > 0;
+                ph1 = spec_n > 1;
+                for (int j = 0; j < 2 && lo + j * FA_KT < hi; ++j) issue_tile(lo + j * FA_KT, j, kz);
+            }
+            s_ph[0] = ph0;
+            s_ph[1] = ph1;
+        } else if (hi > lo) {
+            issue_tile(lo, 0, kz);
+        }
         if (attn_cta) mbar_expect_tx(&bar[3], (uint32_t)(Rg * 4));
         mbar_expect_tx(&bar[4], (uint32_t)(GD * 4));
     }
@@ -466,13 +554,12 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
     // run attention: st.async into their shared memory, counted on their
     // barrier 3 ----
     if (r1 > r0 && !mbar_wait(&bar[0], 0)) s_err = 1;
-    cluster_wait();
     {
         XRegs<XI> xr;
         xr.load(s_xh, H / 8);
         const int nrow = r1 - r0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1), l8 = lane & 7;
-        for (int base = warp * 4; base < nrow; base += FA_THREADS / 8) {   // 4 rows per warp
+        for (int base = warp * 4; base < nrow; base += NTH / 8) {   // 4 rows per warp
             const uint4* rp[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -495,12 +582,8 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
 
     // o_proj rows into the (now free) weight buffer, while attention runs --
     // or, where the buffer takes the second K/V tile, after attention
-    auto issue_wo = [&]() {   // one bulk copy: the slice is contiguous
-        mbar_expect_tx(&bar[2], wo_bytes);
-        bulk_g2s(sW, wo_cta, wo_bytes, &bar[2]);
-    };
-    if (tid == 0) {
-        if (dual) issue_tile(lo + FA_KT, 1);
+    if (tid == 0 && !res) {
+        if (dual) issue_tile(lo + FA_KT, 1, kz);
         else if (o1 > o0) issue_wo();
     }
 
@@ -508,7 +591,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         if (!mbar_wait_cluster(&bar[3], 0)) s_err = 1;
         // ---- optional per-head q/k RMSNorm, then RoPE (q pre-scaled, base 2) ----
         if (a.q_norm) {
-            for (int h = warp; h < G + 1; h += FA_THREADS / 32) {
+            for (int h = warp; h < G + 1; h += NTH / 32) {
                 float* v = h < G ? s_qkv + h * D : s_qkv + GD;
                 const float* w = h < G ? a.q_norm : a.k_norm;
                 float ss = 0.f;
@@ -524,7 +607,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         if (ok) {
             const float* cs = s_cs;
             const float* sn = s_cs + H2;
-            for (int e = tid; e < (G + 1) * H2; e += FA_THREADS) {
+            for (int e = tid; e < (G + 1) * H2; e += NTH) {
                 const int h = e / H2, i = e % H2;
                 float* v = h < G ? s_qkv + h * D : s_qkv + GD;
                 float r0v, r1v;
@@ -541,7 +624,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         __syncthreads();
         if (owner) {   // the new K/V row: to the cache (bf16) and, below, into the tile
             const size_t off = ((size_t)kz * a.max_len + pos) * D;
-            for (int d = tid; d < D; d += FA_THREADS) {
+            for (int d = tid; d < D; d += NTH) {
                 a.kc[off + d] = f32_to_bf16(s_qkv[GD + d]);
                 a.vc[off + d] = f32_to_bf16(s_qkv[GD + D + d]);
             }
@@ -552,7 +635,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         // of each 128-key tile; online softmax per row in registers; P (f16) is
         // the A operand of O += P V ----
         constexpr int KS = D / 16, NT = D / 8;
-        for (int e = tid; e < 16 * (D / 8); e += FA_THREADS) {
+        for (int e = tid; e < 16 * (D / 8); e += NTH) {
             const int rq = e / (D / 8), cq = e % (D / 8);
             uint4 val = make_uint4(0, 0, 0, 0);
             if (rq < G) {
@@ -575,28 +658,39 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         for (int dn = 0; dn < NT; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows lane/4, lane/4 + 8
         const int g4 = lane >> 2, q4 = lane & 3;
-        uint32_t ph0 = 0, ph1 = 0;
-        for (int t0 = lo, j = 0; t0 < hi; t0 += FA_KT, ++j) {
-            const int nt = min(FA_KT, hi - t0);
-            const int b = dual ? (j & 1) : 0;
-            uint8_t* sKt = b ? sK1 : sK;
-            uint8_t* sVt = b ? sV1 : sV;
-            if (!mbar_wait(b ? &bar[5] : &bar[1], b ? ph1 : ph0)) s_err = 1;
-            if (b) ph1 ^= 1;
-            else ph0 ^= 1;
-            if (owner && pos >= t0 && pos < t0 + nt && tid < D / 8) {   // the row the TMA read stale
-                const int jr = pos - t0, cq = tid;
-                const float* kk8 = s_qkv + GD + cq * 8;
-                const float* vv8 = s_qkv + GD + D + cq * 8;
-                *reinterpret_cast<uint4*>(sKt + kv_off(jr, cq)) =
-                    make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
-                               pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
-                *reinterpret_cast<uint4*>(sVt + kv_off(jr, cq)) =
-                    make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
-                               pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
+        uint32_t ph0 = res ? (uint32_t)s_ph[0] : 0u, ph1 = res ? (uint32_t)s_ph[1] : 0u;
+        for (int t0 = lo, j = 0; t0 < hi; t0 += TPI * FA_KT, j += TPI) {
+            // every thread waits for every tile of the pass (uniform phases)
+#pragma unroll
+            for (int v = 0; v < TPI; ++v) {
+                const int tv = t0 + v * FA_KT;
+                if (tv < hi) {
+                    const int bv = dual ? ((j + v) & 1) : 0;
+                    if (!mbar_wait(bv ? &bar[5] : &bar[1], bv ? ph1 : ph0)) s_err = 1;
+                    if (bv) ph1 ^= 1;
+                    else ph0 ^= 1;
+                    if (owner && pos >= tv && pos < min(hi, tv + FA_KT) && tid < D / 8) {   // the row the TMA read stale
+                        uint8_t* kt = bv ? sK1 : sK;
+                        uint8_t* vt = bv ? sV1 : sV;
+                        const int jr = pos - tv, cq = tid;
+                        const float* kk8 = s_qkv + GD + cq * 8;
+                        const float* vv8 = s_qkv + GD + D + cq * 8;
+                        *reinterpret_cast<uint4*>(kt + kv_off(jr, cq)) =
+                            make_uint4(pack_bf16x2(kk8[0], kk8[1]), pack_bf16x2(kk8[2], kk8[3]),
+                                       pack_bf16x2(kk8[4], kk8[5]), pack_bf16x2(kk8[6], kk8[7]));
+                        *reinterpret_cast<uint4*>(vt + kv_off(jr, cq)) =
+                            make_uint4(pack_bf16x2(vv8[0], vv8[1]), pack_bf16x2(vv8[2], vv8[3]),
+                                       pack_bf16x2(vv8[4], vv8[5]), pack_bf16x2(vv8[6], vv8[7]));
+                    }
+                }
             }
             __syncthreads();
-            const int r0k = warp * 16;
+            const int u = warp / 8, tu = t0 + u * FA_KT;
+            const int nt = min(FA_KT, hi - tu);   // <= 0 when this warp's tile is past the range
+            const int b = dual ? ((j + u) & 1) : 0;
+            uint8_t* sKt = b ? sK1 : sK;
+            uint8_t* sVt = b ? sV1 : sV;
+            const int r0k = (warp % 8) * 16;
             if (r0k < nt) {   // warp-uniform
                 float s[2][4];
 #pragma unroll
@@ -650,11 +744,15 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
                 }
             }
             __syncthreads();
-            // refill this buffer: with two buffers the tile after next, else the next
-            const int nx = t0 + (dual ? 2 : 1) * FA_KT;
-            if (tid == 0 && nx < hi) issue_tile(nx, b);
+            // refill the pass's buffers: with two buffers the tiles two on, else the next
+            if (tid == 0)
+#pragma unroll
+                for (int v = 0; v < TPI; ++v) {
+                    const int nx = t0 + v * FA_KT + (dual ? 2 : 1) * FA_KT;
+                    if (nx < hi) issue_tile(nx, dual ? ((j + v) & 1) : 0, kz);
+                }
         }
-        if (dual && tid == 0 && o1 > o0) issue_wo();   // the second buffer has been read
+        if (!res && dual && tid == 0 && o1 > o0) issue_wo();   // the second buffer has been read
         // the 8 warps' states -> this CTA's partial (m, l, acc) per head
         l0 += __shfl_xor_sync(FULL_MASK, l0, 1);
         l0 += __shfl_xor_sync(FULL_MASK, l0, 2);
@@ -677,34 +775,59 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
             }
         }
         __syncthreads();
-        for (int e = tid; e < G * (D + 2); e += FA_THREADS) {
-            const int hh = e / (D + 2), k = e % (D + 2);
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
-                if (st[1] > 0.f) M = fmaxf(M, st[0]);
+        // per head (a warp each): the warps' maxima -> weight f_w of each warp's
+        // state and the head's total l; the combine then reads each state once
+        for (int hh = warp; hh < G; hh += NW) {
+            float mw = -INFINITY, lw = 0.f;
+            if (lane < NW) {
+                const float* st = s_wm + ((size_t)lane * G + hh) * (D + 2);
+                lw = st[1];
+                if (lw > 0.f) mw = st[0];
             }
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float* st = s_wm + ((size_t)w * G + hh) * (D + 2);
-                if (st[1] > 0.f) v = fmaf(st[k], exp2f(st[0] - M), v);
+            const float M = warp_max(mw);
+            const float f = lw > 0.f ? exp2f(mw - M) : 0.f;
+            const float Ls = warp_sum(f * lw);
+            if (lane < NW) s_sc[hh * NW + lane] = f;
+            if (lane == 0) {
+                s_ml[2 * hh] = M;
+                s_ml[2 * hh + 1] = Ls;
             }
-            s_part[e] = k == 0 ? M : v;
         }
+        __syncthreads();
         if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA
-            __syncthreads();
-            for (int e = 4 * tid; e < GD; e += 4 * FA_THREADS) {   // D % 4 == 0: one head per quad
-                const float* ph = s_part + (e / D) * (D + 2);
-                const float l = ph[1];
-                const float* acc = ph + 2 + e % D;
-                const float O0 = l > 0.f ? acc[0] / l : 0.f, O1 = l > 0.f ? acc[1] / l : 0.f;
-                const float O2 = l > 0.f ? acc[2] / l : 0.f, O3 = l > 0.f ? acc[3] / l : 0.f;
+            for (int e = 4 * tid; e < GD; e += 4 * NTH) {   // D % 4 == 0: one head per quad
+                const int hh = e / D, d = e % D;
+                float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float f = s_sc[hh * NW + w];
+                    const float* acc = s_wm + ((size_t)w * G + hh) * (D + 2) + 2 + d;
+                    O0 = fmaf(acc[0], f, O0);
+                    O1 = fmaf(acc[1], f, O1);
+                    O2 = fmaf(acc[2], f, O2);
+                    O3 = fmaf(acc[3], f, O3);
+                }
+                const float l = s_ml[2 * hh + 1];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                O0 *= inv; O1 *= inv; O2 *= inv; O3 *= inv;
 #pragma unroll
                 for (int cc = 0; cc < C; ++cc) st_async4(dsmem(&s_att[e], cc), O0, O1, O2, O3, dsmem(&bar[4], cc));
             }
         } else {
+        // this CTA's partial (m, l, acc) per head, for the merge across the cluster
+        for (int e = tid; e < G * (D + 2); e += NTH) {
+            const int hh = e / (D + 2), k = e % (D + 2);
+            float v;
+            if (k < 2) {
+                v = s_ml[2 * hh + k];
+            } else {
+                v = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w)
+                    v = fmaf(s_wm[((size_t)w * G + hh) * (D + 2) + k], s_sc[hh * NW + w], v);
+            }
+            s_part[e] = v;
+        }
         cluster_sync_all();   // every CTA's partial is in its shared memory
 
         // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
@@ -753,11 +876,11 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_fused_attn(const __grid_const
         xr.load_f32(s_att, GD / 8);
         const int nrow = o1 - o0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-        for (int base = warp * 4; base < nrow; base += FA_THREADS / 8) {   // 4 rows per warp
+        for (int base = warp * 4; base < nrow; base += NTH / 8) {   // 4 rows per warp
             const uint4* rp[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                rp[k] = reinterpret_cast<const uint4*>(sW + (size_t)min(base + k, nrow - 1) * GD);
+                rp[k] = reinterpret_cast<const uint4*>(sWo + (size_t)min(base + k, nrow - 1) * GD);
             const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, GD / 8);
             const int ri = base + my;
             if (ri < nrow && (lane & 7) == 0) red_add(a.z_acc + o0 + ri, v);
@@ -933,8 +1056,143 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
 }
 
+// ============================================================ D2, resident ==
+// The MLP block on its own SMs (the partitioned plan): CTA b owns the
+// contiguous features [b*F/grid, (b+1)*F/grid), all of whose gate/up rows and
+// down_proj^T rows sit in shared memory before the wait.  Phase 1: the
+// gate/up rows in row quads, the hidden dimension in two slices (a warp keeps its slice of the
+// normalised input in registers), partial sums in s_g; then SwiGLU per
+// feature into s_act.  Phase 2: thread t takes outputs 8*(t % H8).. over one
+// of S = 512 / H8 feature slices, the slices meet in the freed gate/up
+// buffer, and one red.add.v4 per four outputs goes into the CTA's
+// accumulator copy.
+constexpr int FR_THREADS = 512;
+constexpr int FR_KSL = 2;
+
+__host__ __device__ inline int fr_smem(int nf, int H) {
+    return nf * 6 * H + ((H * 2 + 15) / 16) * 16 + ((FR_KSL * 2 * nf * 4 + 15) / 16) * 16 +
+           ((nf * 4 + 15) / 16) * 16 + 128;
+}
+
+template <int XI>
+__global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int H = a.H, H8 = H / 8;
+    const int f0 = (int)(((long long)blockIdx.x * a.F) / gridDim.x);
+    const int f1 = (int)(((long long)(blockIdx.x + 1) * a.F) / gridDim.x);
+    const int nf = f1 - f0;
+    uint16_t* s_gu = reinterpret_cast<uint16_t*>(sm);                        // [2 nf][H]
+    uint16_t* s_wd = s_gu + (size_t)2 * nf * H;                               // [nf][H]
+    uint16_t* s_xh = s_wd + (size_t)nf * H;                                   // [H]
+    float* s_g = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_xh) + ((H * 2 + 15) / 16) * 16);  // [KSL][2 nf]
+    float* s_act = s_g + ((FR_KSL * 2 * nf + 3) / 4) * 4;                      // [nf]
+    float* s_y = reinterpret_cast<float*>(sm);                                // [S][H] after phase 1
+    __shared__ float s_red[32];
+    __shared__ __align__(8) uint64_t bar[1];
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_err = 0;
+        mbar_init(&bar[0], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    ResidualNorm rn;
+    rn.load_w(a.norm_w, H);
+    // phase-1 role: the warps split into FR_KSL groups, one per hidden slice
+    constexpr int WPS = (FR_THREADS / 32) / FR_KSL;   // warps per slice
+    const int ks = warp / WPS, wq = warp % WPS;
+    const int seg = (H8 + FR_KSL - 1) / FR_KSL;
+    const int c0 = min(H8, ks * seg), c1 = min(H8, c0 + seg);
+    __syncthreads();
+    pdl_trigger();
+    // The CTA's weights, ~220 KB, copied by the last thread.  The CTAs of
+    // this kernel arrive as the previous MLP block leaves, just when the
+    // attention block reads the residual from L2; a 26 MB burst of copies
+    // then stalls those reads (measured: 1.2 -> 3-4 us), so the copies start
+    // load_delay_ns later (0 without programmatic launch overlap).
+    if (tid == FR_THREADS - 1 && nf > 0) {
+        if (a.load_delay_ns > 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < (unsigned long long)a.load_delay_ns) {
+            }
+        }
+        const uint32_t gu_b = (uint32_t)(2 * nf * H * 2), wd_b = (uint32_t)(nf * H * 2);
+        mbar_expect_tx(&bar[0], gu_b + wd_b);
+        const uint8_t* g_src = reinterpret_cast<const uint8_t*>(a.wgu + (size_t)2 * f0 * H);
+        const uint8_t* d_src = reinterpret_cast<const uint8_t*>(a.wdT + (size_t)f0 * H);
+        for (uint32_t o = 0; o < gu_b; o += 32768u)
+            bulk_g2s(reinterpret_cast<uint8_t*>(s_gu) + o, g_src + o, min(32768u, gu_b - o), &bar[0]);
+        for (uint32_t o = 0; o < wd_b; o += 32768u)
+            bulk_g2s(reinterpret_cast<uint8_t*>(s_wd) + o, d_src + o, min(32768u, wd_b - o), &bar[0]);
+    }
+    pdl_wait();
+
+    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
+    XRegs<XI> xr;
+    xr.load(s_xh + c0 * 8, c1 - c0);
+    if (nf > 0 && !mbar_wait(&bar[0], 0)) s_err = 1;
+
+    // ---- phase 1: gate / up rows (2 nf of them) over this warp's slice ----
+    const int nrow = 2 * nf;
+    for (int base = wq * 4; base < nrow; base += WPS * 4) {
+        const uint4* rp[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            rp[q] = reinterpret_cast<const uint4*>(s_gu + (size_t)min(base + q, nrow - 1) * H) + c0;
+        const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0);
+        const int rr = base + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+        if ((lane & 7) == 0 && rr < nrow) s_g[ks * nrow + rr] = v;
+    }
+    __syncthreads();   // s_g complete; the gate/up buffer is free for s_y
+    for (int j = tid; j < nf; j += FR_THREADS) {
+        float gt = 0.f, up = 0.f;
+#pragma unroll
+        for (int z = 0; z < FR_KSL; ++z) {
+            gt += s_g[z * nrow + 2 * j];
+            up += s_g[z * nrow + 2 * j + 1];
+        }
+        s_act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
+    }
+    __syncthreads();
+
+    // ---- phase 2: SwiGLU and down_proj over feature slice sl, outputs 8 hg.. ----
+    const int S = max(1, min(FR_THREADS / H8, nf));
+    const int hg = tid % H8, sl = tid / H8;
+    if (sl < S && nf > 0) {
+        const int j0 = (sl * nf) / S, j1 = ((sl + 1) * nf) / S;
+        float y[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) y[u] = 0.f;
+        const uint4* wd = reinterpret_cast<const uint4*>(s_wd);
+        for (int j = j0; j < j1; ++j) {
+            const float act = s_act[j];
+            float w[8];
+            unpack8_f16(lds128(wd + (size_t)j * H8 + hg), w);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = fmaf(w[u], act, y[u]);
+        }
+        float4* yo = reinterpret_cast<float4*>(s_y + (size_t)sl * H + 8 * hg);
+        yo[0] = make_float4(y[0], y[1], y[2], y[3]);
+        yo[1] = make_float4(y[4], y[5], y[6], y[7]);
+    }
+    __syncthreads();
+    float* z_acc = a.z_acc + (size_t)(blockIdx.x % ZSLOTS) * H;
+    if (nf > 0)
+        for (int i = tid; i < H / 4; i += FR_THREADS) {
+            float4 t = reinterpret_cast<const float4*>(s_y)[i];
+            for (int q = 1; q < S; ++q) {
+                const float4 u = reinterpret_cast<const float4*>(s_y + (size_t)q * H)[i];
+                t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+            }
+            red_add4(z_acc + 4 * i, t.x, t.y, t.z, t.w);
+        }
+    if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
+}
+
 // ================================================================ host ==
-bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int num_sms) {
+static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int num_sms, bool allow_part) {
     p = FusedPlan{};
     auto no = [&](const char* why) {
         p.why = why;
@@ -951,9 +1209,37 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     p.C = C;
     p.nr = ((G + 2) * D + C - 1) / C;
     p.no = (H + C - 1) / C;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return no("device attributes unavailable");
+    // Partitioned plan (a layer small enough to sit on chip): the attention
+    // clusters take C * NKV SMs with their q/k/v and o_proj rows and two K/V
+    // tiles resident, the MLP block takes every other SM with all of its
+    // features resident, and neither fits beside the other -- so while one
+    // block computes, the next launch of the other is already on its own SMs
+    // loading its weights.
+    {
+        const int n_attn = C * NKV, mg = num_sms - n_attn;
+        const int smem_a = fa_layout(D, G, H, p.nr, p.no, true).total;
+        if (allow_part && D == 64 && mg >= 1 && F >= mg) {
+            const int nfm = (F + mg - 1) / mg;
+            const int smem_m = fr_smem(nfm, H);
+            // static shared memory of the two kernels, with slack
+            if (smem_a <= optin - 4096 && smem_m <= optin - 1024 && smem_a + smem_m > 228 * 1024 &&
+                smem_a > 116 * 1024) {
+                p.part = true;
+                p.mlp_delay_ns = 2000;
+                p.smem_attn = smem_a;
+                p.smem_mlp = smem_m;
+                p.mlp_grid = mg;
+            }
+        }
+    }
+    if (!p.part) {
     // more than half an SM's shared memory: one attention CTA per SM, so a
     // cluster spreads over 16 SMs instead of packing two CTAs onto each
-    p.smem_attn = fa_layout(D, G, H, p.nr, p.no).total;
+    p.smem_attn = fa_layout(D, G, H, p.nr, p.no, false).total;
     if (p.smem_attn < 116 * 1024) p.smem_attn = 116 * 1024;
     if (p.smem_attn > 200 * 1024) return no("attention block needs > 200 KB of shared memory");
     // MLP plan.  Resident: the CTA's chunks all fit its shared memory, so the
@@ -1002,13 +1288,11 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
         p.smem_mlp = ns * stage + fixed;
     }
     if (p.smem_mlp > 227 * 1024) return no("MLP ring does not fit shared memory");
+    }   // !p.part
     // The limit is a property of the function, shared by every model in the
     // process: raise it to the device maximum so that no model lowers it
     // below what another one launches with.
-    int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess && (p.smem_attn > optin - 1024 || p.smem_mlp > optin - 1024))
+    if (p.smem_attn > optin - 1024 || p.smem_mlp > optin - 1024)
         return no("shared memory above the device limit");
     auto setup = [&](auto kern, int) {   // the limit covers static + dynamic shared memory
         cudaFuncAttributes fa{};
@@ -1021,21 +1305,29 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
         setup(kern, p.smem_attn);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     };
-    setup_attn(k_fused_attn<64, 4>);
-    setup_attn(k_fused_attn<64, 8>);
-    setup_attn(k_fused_attn<128, 4>);
-    setup_attn(k_fused_attn<128, 8>);
+    setup_attn(k_fused_attn<64, 4, 8>);
+    setup_attn(k_fused_attn<64, 8, 8>);
+    setup_attn(k_fused_attn<128, 4, 8>);
+    setup_attn(k_fused_attn<128, 8, 8>);
     setup(k_fused_mlp<4, 4>, p.smem_mlp);
     setup(k_fused_mlp<8, 4>, p.smem_mlp);
     setup(k_fused_mlp<16, 4>, p.smem_mlp);
     setup(k_fused_mlp<4, 8>, p.smem_mlp);
     setup(k_fused_mlp<8, 8>, p.smem_mlp);
     setup(k_fused_mlp<16, 8>, p.smem_mlp);
+    setup(k_fused_mlp_res<2>, p.smem_mlp);
+    setup(k_fused_mlp_res<4>, p.smem_mlp);
     if (e != cudaSuccess) return no("kernel attributes rejected");
+    if (p.part) {   // the partitioned MLP kernel's static shared memory must leave room
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, p.xi == 4 ? k_fused_mlp_res<2> : k_fused_mlp_res<4>);
+        if (e != cudaSuccess || p.smem_mlp + (int)fa.sharedSizeBytes > optin) p.part = false;
+        if (!p.part) return plan_impl(p, H, NH, NKV, D, F, num_sms, false);
+    }
     // one cluster of C CTAs must fit somewhere on the chip
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, NKV);
-    cfg.blockDim = dim3(FA_THREADS);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = p.smem_attn;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1045,10 +1337,10 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    e = D == 64 ? (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 4>, &cfg)
-                             : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 8>, &cfg))
-                : (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 4>, &cfg)
-                             : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 8>, &cfg));
+    e = D == 64 ? (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 4, 8>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<64, 8, 8>, &cfg))
+                    : (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 4, 8>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 8, 8>, &cfg));
     if (e != cudaSuccess) return no("cluster occupancy query failed");
     if (n < 1) return no("a cluster of 16 CTAs does not fit");
     p.ok = true;
@@ -1056,12 +1348,16 @@ bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int n
     return true;
 }
 
+bool fused_decode_plan(FusedPlan& p, int H, int NH, int NKV, int D, int F, int num_sms) {
+    return plan_impl(p, H, NH, NKV, D, F, num_sms, !(getenv("EMBER_NO_PARTITION") && atoi(getenv("EMBER_NO_PARTITION"))));
+}
+
 void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs& a, int xi, int smem,
                        cudaStream_t s) {
     count_launches(1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.C, a.NKV);
-    cfg.blockDim = dim3(FA_THREADS);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[2];
@@ -1075,10 +1371,16 @@ void launch_fused_attn(const void* k_map, const void* v_map, const FusedAttnArgs
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
     const CUtensorMap& km = *reinterpret_cast<const CUtensorMap*>(k_map);
     const CUtensorMap& vm = *reinterpret_cast<const CUtensorMap*>(v_map);
-    auto kern = a.D == 64 ? (xi == 4 ? k_fused_attn<64, 4> : k_fused_attn<64, 8>)
-                          : (xi == 4 ? k_fused_attn<128, 4> : k_fused_attn<128, 8>);
+    auto kern = a.D == 64 ? (xi == 4 ? k_fused_attn<64, 4, 8> : k_fused_attn<64, 8, 8>)
+                          : (xi == 4 ? k_fused_attn<128, 4, 8> : k_fused_attn<128, 8, 8>);
     trace_launch(reinterpret_cast<const void*>(kern), s);
     cudaLaunchKernelEx(&cfg, kern, km, vm, a);
+}
+
+void launch_fused_mlp_res(const FusedMlpArgs& a, int xi, int grid, int smem, cudaStream_t s) {
+    const dim3 g(grid), b(FR_THREADS);
+    if (xi == 4) launch_k(k_fused_mlp_res<2>, g, b, (size_t)smem, s, a);
+    else launch_k(k_fused_mlp_res<4>, g, b, (size_t)smem, s, a);
 }
 
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s) {

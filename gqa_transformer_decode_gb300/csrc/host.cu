@@ -268,8 +268,10 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     if (c.causal && !(getenv("EMBER_NO_FUSED") && atoi(getenv("EMBER_NO_FUSED"))))
         fused_decode_plan(m->fp, H, c.n_heads, NKV, D, F, m->sms);
     if (getenv("EMBER_VERBOSE") && atoi(getenv("EMBER_VERBOSE")))
-        fprintf(stderr, "ember: fused batch-1 decode %s%s\n", m->fp.ok ? "on" : "off: ",
-                m->fp.ok ? "" : m->fp.why);
+        fprintf(stderr, "ember: fused batch-1 decode %s%s (%s, attention smem %d, MLP grid %d smem %d fc %d ns %d)\n",
+                m->fp.ok ? "on" : "off: ", m->fp.ok ? "" : m->fp.why,
+                m->fp.part ? "partitioned" : (m->fp.resident ? "resident MLP" : "MLP ring"), m->fp.smem_attn,
+                m->fp.mlp_grid, m->fp.smem_mlp, m->fp.fc, m->fp.ns);
 
     // ---- weights ----
     Arena wa;
@@ -831,6 +833,9 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.vc = kv->v;
             a.max_len = kv->max_len;
             a.max_seqs = kv->max_seqs;
+            a.positions = positions;
+            a.cursor = kv->cursor;
+            a.resident = fp.part ? 1 : 0;
             a.seqs = seqs;
             a.tok_pos = m->tok_pos;
             a.tok_ok = m->tok_ok;
@@ -852,7 +857,9 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             f.status = m->status;
             f.ns = fp.ns;
             f.pf_late = fp.pf_late;
-            launch_fused_mlp(f, fp.fc, fp.xi, fp.mlp_grid, fp.smem_mlp, s);
+            f.load_delay_ns = pdl_enabled() ? fp.mlp_delay_ns : 0;
+            if (fp.part) launch_fused_mlp_res(f, fp.xi, fp.mlp_grid, fp.smem_mlp, s);
+            else launch_fused_mlp(f, fp.fc, fp.xi, fp.mlp_grid, fp.smem_mlp, s);
         }
         GemvArgs g{};
         g.W = m->embed;

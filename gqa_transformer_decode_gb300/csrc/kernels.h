@@ -289,6 +289,8 @@ struct FusedPlan {
     int xi = 0;          // 16-byte input chunks per lane in the row dots (4: inputs <= 1024, 8: <= 2048)
     int mlp_grid = 0;
     bool resident = false;   // every MLP CTA's chunks fit its shared memory (ns = chunks per CTA)
+    bool part = false;       // partitioned: attention and MLP blocks on disjoint SMs, all weights resident
+    int mlp_delay_ns = 0;    // partitioned: MLP weight copies start this long after the CTA arrives
     int pf_late = 0;         // CTAs whose chunks the first CTAs prefetch to L2 (resident plan)
     bool ok = false;
     const char* why = "not planned";   // reason when !ok
@@ -315,6 +317,9 @@ struct FusedAttnArgs {
     const int32_t* seqs;
     const int32_t* tok_pos;
     const int* tok_ok;
+    const int32_t* positions;    // the step's explicit positions (nullptr: the cursor)
+    const int32_t* cursor;       // [max_seqs] the cache's cursors
+    int resident;                // resident plan: o_proj rows and two K/V tiles loaded before the wait
     const float* cos_t;
     const float* sin_t;
     int* status;
@@ -338,8 +343,11 @@ struct FusedMlpArgs {
     int* status;
     int ns;
     int pf_late;                 // the first pf_late CTAs prefetch the last pf_late CTAs' chunks to L2
+    int load_delay_ns;           // partitioned plan: delay of the weight copies after the CTA arrives
 };
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
+// The partitioned plan's MLP block: grid CTAs of 512 threads on their own SMs.
+void launch_fused_mlp_res(const FusedMlpArgs& a, int xi, int grid, int smem, cudaStream_t s);
 
 // out[c][r] = in[r][c] for 16-bit elements
 void launch_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols, cudaStream_t s);
