@@ -302,6 +302,7 @@ def decode_family_bytes(shape, B: int, ctx: int) -> dict:
         # batch-1 fused path: the attention block carries its projections
         "k_fused_attn": L * (qkv + o + kv_read + kv_write + resid),
         "k_fused_mlp": L * (mlp + resid),
+        "k_fused_mlp_res": L * (mlp + resid),
         "k_gemv": head,
         # batched path: projections and head on the tensor-core GEMM, attention
         # reads the cache
@@ -316,6 +317,9 @@ def decode_family_bytes(shape, B: int, ctx: int) -> dict:
 # ncu capture of this build's kernel (the same source) on the same workload;
 # a kernel without an entry reports null.
 NCU_TRAFFIC = {}
+# The same counters summed over the launches of one decode step (workload ->
+# bytes); null without a capture of the current kernels.
+NCU_STEP_TRAFFIC = {}
 
 
 def decode_roofline(job, hbm_peak):
@@ -353,6 +357,13 @@ def decode_roofline(job, hbm_peak):
         out.update({"achieved": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
                     "bytes_per_launch": int(per)})
     return out
+
+
+def decode_step_kernels(job) -> str:
+    L = job.wl.model.layers
+    if job.B == 1:
+        return f"{L} x (k_fused_attn, k_fused_mlp*) + k_gemv LM head, argmax fused"
+    return f"{L} x (k_gemm_tc projections, k_attn_decode_mma, k_rmsnorm) + k_gemm_tc LM head"
 
 
 def gemv_roofline(stream, hbm_peak, n_launch=30):
@@ -454,7 +465,19 @@ def measure(wl, weights, args, stream, n_jobs, world, local, pk, headline):
                                        "achieved": round(ptf, 1), "peak": bf16_peak,
                                        "frac": round(ptf / bf16_peak, 4),
                                        "flops": job.prefill_flops(), "traffic": None}
-        rec["roofline"] = decode_roofline(job, hbm_peak)
+        # The unit the step launches is one CUDA graph: the layers' kernels are
+        # chained with programmatic launch, each prefetching its weights while
+        # its predecessor computes, so a kernel's own serialised time is not
+        # its cost in the step.  The roofline is that of the graph launch; the
+        # per-kernel breakdown of a serialised step follows it.
+        rec["roofline"] = {"kernel": "decode step: one CUDA graph launch (%s)" % decode_step_kernels(job),
+                           "bound": "hbm", "unit": "GB/s", "achieved": round(step_gbs, 1),
+                           "peak": hbm_peak, "frac": round(step_gbs / hbm_peak, 4),
+                           "bytes_per_launch": step_bytes, "avg_launch_us": round(step_s * 1e6, 2),
+                           "traffic": NCU_STEP_TRAFFIC.get(wl.key),
+                           "timing": "median over the timed jobs of CUDA events on the launching stream "
+                                     "around the decode steps, divided by the steps"}
+        rec["kernel_breakdown"] = decode_roofline(job, hbm_peak)
         assert job.model.sync_status(stream) == 0
     rec["clocks"] = clocks
     rec["gpu_launches"] = launches
@@ -510,7 +533,8 @@ def run_gpu(args):
     out = {
         "metric": METRIC, "value": rec["value"], "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16*f16+f32 (bf16 weights and KV cache; f16 tensor-core operands, f32 accumulation)",
         "data": "synthetic (seeded random bf16 weights N(0,0.02), norms 1+N(0,0.1); uniform ids)",
         "config": {"workload": wl.key, "model_shape": wl.model.name, "batch": wl.batch,
                    "prompt": wl.prompt, "decode_steps": wl.steps,
@@ -521,7 +545,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}"},
     }
     for k in ("decode_tok_s", "decode_step_us", "prefill_tok_s", "encode_tflops", "step_hbm",
-              "prefill_roofline", "roofline", "e2e", "gpu_launches", "clocks", "wall_s",
+              "prefill_roofline", "roofline", "kernel_breakdown", "e2e", "gpu_launches", "clocks", "wall_s",
               "cpu_baseline"):
         if k in rec:
             out[k] = rec[k]

@@ -1221,7 +1221,14 @@ extern "C" ember_status ember_encode(ember_model* m, const int32_t* ids, int32_t
         if (c.n_labels > 0) {
             launch_cls_head(h, n, c.hidden, m->cls_w, m->cls_b, c.n_labels, out, s);
         } else {
-            return fail(EMBER_ERR_UNSUPPORTED, "encode with the tied vocabulary head is not built yet");
+            // tied vocabulary head at every position: the final states in bf16
+            // (the embedding's type) times the embedding rows, one GEMM
+            launch_rmsnorm_bf16(m->x, m->final_norm, (float)c.rms_eps, n, c.hidden, m->hb, s);
+            GemmEpilogue e{};
+            e.mode = EPI_STORE;
+            e.out_f32 = out;
+            e.ldo = c.vocab;
+            launch_gemm(m->p_head, n, e, m->status, s);
         }
     }
     CK(cudaGetLastError());
@@ -1278,6 +1285,29 @@ extern "C" ember_status ember_gemv_bf16(const uint16_t* W, int32_t N, int32_t K,
     g.mode = EPI_STORE;
     launch_gemv(g, (cudaStream_t)stream, sms);
     CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_sample(const float* logits, int32_t B, int32_t V, int32_t ldl,
+                                     float temperature, int32_t top_k, float top_p, const float* r,
+                                     int32_t* out, ember_stream_t stream) {
+    if (!logits || !out || (temperature > 0.f && !r))
+        return fail(EMBER_ERR_INVALID_ARG, "NULL logits, out, or draws (r is needed when temperature > 0)");
+    if (B <= 0 || V <= 0 || ldl < V) return fail(EMBER_ERR_INVALID_ARG, "bad sizes (B, V > 0, ldl >= V)");
+    if (top_k < 0) return fail(EMBER_ERR_INVALID_ARG, "top_k < 0");
+    if (top_p != top_p || temperature != temperature) return fail(EMBER_ERR_INVALID_ARG, "NaN temperature or top_p");
+    SampleArgs a{};
+    a.logits = logits;
+    a.B = B;
+    a.V = V;
+    a.ldl = ldl;
+    a.t = temperature;
+    a.k = top_k;
+    a.p = top_p;
+    a.r = r;
+    a.out = out;
+    const cudaError_t e = launch_sample(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "sampler launch failed: %s", cudaGetErrorString(e));
     return EMBER_OK;
 }
 

@@ -349,6 +349,22 @@ void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem,
 // The partitioned plan's MLP block: grid CTAs of 512 threads on their own SMs.
 void launch_fused_mlp_res(const FusedMlpArgs& a, int xi, int grid, int smem, cudaStream_t s);
 
+// ---------------------------------------------------------------- sampler --
+// One token per row of logits [B][ldl] (V used): temperature t (t <= 0:
+// greedy), top-k (0 < k < V), top-p (0 < p < 1), softmax, inverse-CDF draw
+// with r[b] in [0, 1).  sampler.cu.
+struct SampleArgs {
+    const float* logits;
+    int B, V;
+    long long ldl;
+    float t;
+    int k;
+    float p;
+    const float* r;
+    int32_t* out;
+};
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+
 // out[c][r] = in[r][c] for 16-bit elements
 void launch_transpose16(const uint16_t* in, uint16_t* out, int rows, int cols, cudaStream_t s);
 

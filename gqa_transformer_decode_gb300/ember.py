@@ -89,6 +89,8 @@ def load():
         "ember_gemm_bf16": (st, [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]),
         "ember_gemv_bf16": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P]),
         "ember_gemv_argmax_noalloc": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P, P]),
+        "ember_sample": (st, [P, C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_int32, C.c_float, P, P,
+                              P]),
         "ember_kernel_launches": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():
@@ -215,6 +217,10 @@ def ember_gemv_bf16(W, N, K, x, nb, y, stream):
 
 def ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream):
     return load().ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream)
+
+
+def ember_sample(logits, B, V, ldl, temperature, top_k, top_p, r, out, stream):
+    return load().ember_sample(logits, B, V, ldl, temperature, top_k, top_p, r, out, stream)
 
 
 def ember_kernel_launches() -> int:

@@ -221,6 +221,34 @@ ember_status ember_sync_status(ember_model *m, ember_stream_t stream);
 
 const char *ember_last_error(void);
 
+/* ---- token sampler ------------------------------------------------------- */
+
+/* One token per row of logits, the five stages of "ember internals" §sampler
+ * in order: (1) temperature -- x = logit / temperature when temperature > 0;
+ * temperature <= 0 is greedy and returns the first maximal logit (NaN counts
+ * as maximal); (2) top-k -- for 0 < top_k < V every x below the top_k-th
+ * largest is masked (ties with it are kept; 0 or >= V: no-op); (3) top-p --
+ * for 0 < top_p < 1 the x whose softmax probability lies below the smallest
+ * probability of the shortest most-probable set holding more than top_p of
+ * the mass are masked (otherwise no-op); (4) softmax over the survivors
+ * (uniform when every logit is -inf); (5) the first index whose running sum
+ * of probabilities, in index order, exceeds r[b] (the last maximal index
+ * when rounding leaves r[b] above the total).
+ *   logits [B, ldl] f32, the first V columns used      (device)
+ *   r      [B] f32 draws in [0, 1), one per row         (device; unused and
+ *                                                        nullable when greedy)
+ *   out    [B] int32 token ids                          (device)
+ * Arithmetic: the division of stage 1 is IEEE f32; stages 2-3 select by exact
+ * comparisons of x; the masses of stages 3-5 are exp(x - max) in f32 rounded
+ * to multiples of 2^-40 and summed exactly (64-bit integers), so a call is
+ * deterministic and its decisions differ from exact arithmetic only for draws
+ * (or top_p) within ~1e-6 of a boundary.  Asynchronous on `stream`; reads
+ * nothing else and allocates nothing.  Errors: INVALID_ARG (NULL pointers,
+ * B or V <= 0, ldl < V, top_k < 0, NaN temperature or top_p), CUDA. */
+ember_status ember_sample(const float *logits, int32_t B, int32_t V, int32_t ldl, float temperature,
+                          int32_t top_k, float top_p, const float *r, int32_t *out,
+                          ember_stream_t stream);
+
 /* ---- kernel-level entry points used by the parity tests ------------------ */
 
 /* The RoPE-and-store step of the K cache write, alone: for each of n_tok rows

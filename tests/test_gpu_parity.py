@@ -204,6 +204,31 @@ def test_encoder_matches_oracle(B, T, stream):
         assert_close(cls, go[b * T:(b + 1) * T], f"encoder labels seq {b}")
 
 
+SMALL_ENC_TIED = synth.ModelShape("s-enc-tied", vocab=700, hidden=256, layers=2, n_heads=4,
+                                  n_kv_heads=2, head_dim=128, ff=384, rope_theta=1e6, qk_norm=1,
+                                  causal=0, n_labels=0)
+
+
+@pytest.mark.parametrize("B,T", [(3, 9), (2, 70), (1, 200)])
+def test_encoder_with_the_tied_vocabulary_head(B, T, stream):
+    """n_labels = 0: ember_encode writes the tied-head logits E . h at every
+    position ([B*T, vocab]); B*T <= 128 runs the one-row-tile GEMM, more rows
+    the persistent one."""
+    shape = SMALL_ENC_TIED
+    w, om, gm = model_pair(shape)
+    ids = np.stack([synth.prompt_ids(shape, T, seq=b) for b in range(B)])
+    out = torch.empty((B * T, shape.vocab), dtype=torch.float32, device="cuda")
+    hid = torch.empty((B * T, shape.hidden), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        gm.encode(i32(ids.reshape(-1)), B, T, out=out, hidden=hid, stream=stream)
+    assert gm.sync_status(stream) == 0
+    go, gh = out.cpu().numpy(), hid.cpu().numpy()
+    for b in range(B):
+        h, lg, _ = om.forward_full(ids[b], logits=True)
+        assert_close(h, gh[b * T:(b + 1) * T], f"encoder hidden seq {b}")
+        assert_close(lg, go[b * T:(b + 1) * T], f"tied-head logits seq {b}")
+
+
 def test_graph_replayed_greedy_loop_with_cursor_positions(stream):
     """positions = NULL (each token at its sequence's cursor) and argmax fed
     back as the next ids: one CUDA graph replayed every step; then the cursor
