@@ -326,8 +326,10 @@ static void final_heads(const orc_model *m, const double *x, int T, double *hidd
     free(h);
 }
 
-int orc_forward_full(const orc_model *m, const int32_t *ids, int T, double *hidden,
-                     double *logits, double *cls) {
+/* The whole-sequence forward; acts (nullable) collects the residual stream at
+ * the last position after every block ([EI] forward_with_activations). */
+static int forward_full(const orc_model *m, const int32_t *ids, int T, double *hidden,
+                        double *logits, int logits_rows, double *cls, double *acts) {
     const orc_config *c = &m->cfg;
     if (orc_validate(c) || T <= 0) return ORC_EINVAL;
     if (check_ids(c, ids, T)) return ORC_ETOKEN;
@@ -360,11 +362,40 @@ int orc_forward_full(const orc_model *m, const int32_t *ids, int T, double *hidd
                           s.att + (size_t)t * NH * D);
         }
         oproj_mlp(m, ly, x, T, &s);
+        if (acts) memcpy(acts + (size_t)l * H, x + (size_t)(T - 1) * H, sizeof(double) * H);
     }
-    final_heads(m, x, T, hidden, logits, logits ? T : 0, cls);
+    final_heads(m, x, T, hidden, logits, logits_rows, cls);
     scratch_free(&s);
     free(x); free(inv); free(K); free(V);
     return ORC_OK;
+}
+
+int orc_forward_full(const orc_model *m, const int32_t *ids, int T, double *hidden,
+                     double *logits, double *cls) {
+    return forward_full(m, ids, T, hidden, logits, logits ? T : 0, cls, NULL);
+}
+
+int orc_forward_activations(const orc_model *m, const int32_t *ids, int T, double *acts,
+                            double *logits) {
+    if (!acts) return ORC_EINVAL;
+    return forward_full(m, ids, T, NULL, logits, logits ? 1 : 0, NULL, acts);
+}
+
+/* [PII] forward(): the sensitivity head reads the mean over positions of the
+ * final-normed states, sens_j = mean_t(h[t]) . w[j] + b[j]. */
+void orc_mean_pooled_head(const double *hidden, int T, int H, const float *w, const float *b,
+                          int n_out, double *out) {
+    double *mean = calloc((size_t)H, sizeof(double));
+    if (!mean) return;
+    for (int t = 0; t < T; ++t)
+        for (int i = 0; i < H; ++i) mean[i] += hidden[(size_t)t * H + i];
+    for (int i = 0; i < H; ++i) mean[i] /= (double)T;
+    for (int j = 0; j < n_out; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < H; ++i) acc += mean[i] * (double)w[(size_t)j * H + i];
+        out[j] = acc + (b ? (double)b[j] : 0.0);
+    }
+    free(mean);
 }
 
 orc_cache *orc_cache_new(const orc_config *cfg, int max_len, int kv_bf16) {

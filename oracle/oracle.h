@@ -118,6 +118,17 @@ int  orc_validate(const orc_config *cfg);      /* 0 ok, <0 error ([FH] validate)
 int  orc_forward_full(const orc_model *m, const int32_t *ids, int T,
                       double *hidden, double *logits, double *cls);
 
+/* [EI] ForwardModel forward_with_activations(): the same whole-sequence
+ * forward, collecting the residual stream at the last position after every
+ * decoder block, acts [L, H]; logits: [V] at the last position (nullable). */
+int  orc_forward_activations(const orc_model *m, const int32_t *ids, int T, double *acts,
+                             double *logits);
+
+/* [PII] forward() sensitivity head: out[j] = mean_t(hidden[t]) . w[j] + b[j]
+ * over hidden [T, H] (the final-normed states), w [n_out, H], b [n_out] or NULL. */
+void orc_mean_pooled_head(const double *hidden, int T, int H, const float *w, const float *b,
+                          int n_out, double *out);
+
 orc_cache *orc_cache_new(const orc_config *cfg, int max_len, int kv_bf16);
 void       orc_cache_free(orc_cache *c);
 

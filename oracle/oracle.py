@@ -65,6 +65,8 @@ def lib():
         L.orc_attention.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, C.c_long, C.c_long, P]
         L.orc_validate.argtypes = [C.POINTER(OrcConfig)]
         L.orc_forward_full.argtypes = [C.POINTER(OrcModel), P, C.c_int, P, P, P]
+        L.orc_forward_activations.argtypes = [C.POINTER(OrcModel), P, C.c_int, P, P]
+        L.orc_mean_pooled_head.argtypes = [P, C.c_int, C.c_int, P, P, C.c_int, P]
         L.orc_cache_new.argtypes = [C.POINTER(OrcConfig), C.c_int, C.c_int]
         L.orc_cache_new.restype = C.POINTER(OrcCache)
         L.orc_cache_free.argtypes = [C.POINTER(OrcCache)]
@@ -172,6 +174,18 @@ def attention(q, k, v, n_heads, n_kv_heads, head_dim, n_keys=None):
     return out
 
 
+def mean_pooled_head(hidden, w, b=None):
+    """[PII] forward() sensitivity head over final-normed states hidden [T, H]:
+    mean over positions, then . w[j] + b[j] for w [n_out, H] (f32 values)."""
+    h = np.ascontiguousarray(hidden, dtype=np.float64)
+    T, H = h.shape
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1, H)
+    bb = None if b is None else np.ascontiguousarray(b, dtype=np.float32)
+    out = np.empty(w.shape[0], dtype=np.float64)
+    lib().orc_mean_pooled_head(_p(h), T, H, _p(w), _p(bb), w.shape[0], _p(out))
+    return out
+
+
 def num_threads() -> int:
     return int(lib().orc_num_threads())
 
@@ -226,6 +240,17 @@ class OracleModel:
         if rc != 0:
             raise RuntimeError(f"orc_forward_full rc={rc}")
         return hid, lg, cl
+
+    def forward_activations(self, ids, logits=True):
+        """[EI] forward_with_activations: the residual stream at the last
+        position after every block [L, H], and the last position's logits."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        acts = np.empty((self.cfg.layers, self.H), dtype=np.float64)
+        lg = np.empty(self.V, dtype=np.float64) if logits else None
+        rc = lib().orc_forward_activations(C.byref(self._m), _p(ids), ids.size, _p(acts), _p(lg))
+        if rc != 0:
+            raise RuntimeError(f"orc_forward_activations rc={rc}")
+        return acts, lg
 
     def new_cache(self, max_len, kv_bf16=False):
         return OracleCache(self, max_len, kv_bf16)
