@@ -692,9 +692,9 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     launch_gemm(L.p_d, n, e, m->status, s);
 }
 
-extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq, const int32_t* ids,
-                                      int32_t n, int32_t start_pos, float* logits, int32_t* argmax,
-                                      float* hidden, ember_stream_t stream) {
+static ember_status prefill_impl(ember_model* m, ember_kv* kv, int32_t seq, const int32_t* ids,
+                                 int32_t n, int32_t start_pos, float* logits, int32_t* argmax,
+                                 float* hidden, float* acts, ember_stream_t stream) {
     if (!m || !kv || !ids) return fail(EMBER_ERR_INVALID_ARG, "NULL model, kv or ids");
     if (kv->m != m) return fail(EMBER_ERR_INVALID_ARG, "kv belongs to another model");
     if (n <= 0) return fail(EMBER_ERR_INVALID_ARG, "input_ids must not be empty");
@@ -743,6 +743,8 @@ extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq,
         cv.cos_t = kv->cos_t;
         cv.sin_t = kv->sin_t;
         layer_tc(m, l, n, cv, s);
+        if (acts)   // the residual stream after block l, at the last position
+            launch_copy_f32(acts + (size_t)l * c.hidden, m->x + (size_t)(n - 1) * c.hidden, c.hidden, s);
     }
     if (hidden) launch_rmsnorm_f32(m->x, m->final_norm, (float)c.rms_eps, n, c.hidden, hidden, s);
     GemvArgs g{};
@@ -769,6 +771,31 @@ extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq,
     f.pf_end = start_pos + n;
     launch_finish(f, s);
     CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_prefill(ember_model* m, ember_kv* kv, int32_t seq, const int32_t* ids,
+                                      int32_t n, int32_t start_pos, float* logits, int32_t* argmax,
+                                      float* hidden, ember_stream_t stream) {
+    return prefill_impl(m, kv, seq, ids, n, start_pos, logits, argmax, hidden, nullptr, stream);
+}
+
+extern "C" ember_status ember_prefill_activations(ember_model* m, ember_kv* kv, int32_t seq,
+                                                  const int32_t* ids, int32_t n, int32_t start_pos,
+                                                  float* acts, float* logits, int32_t* argmax,
+                                                  ember_stream_t stream) {
+    if (!acts) return fail(EMBER_ERR_INVALID_ARG, "NULL acts");
+    return prefill_impl(m, kv, seq, ids, n, start_pos, logits, argmax, nullptr, acts, stream);
+}
+
+extern "C" ember_status ember_mean_pooled_head(const float* hidden, int32_t B, int32_t T, int32_t H,
+                                               const uint16_t* w, const uint16_t* b, int32_t n_out,
+                                               float* out, ember_stream_t stream) {
+    if (!hidden || !w || !out) return fail(EMBER_ERR_INVALID_ARG, "NULL hidden, w or out");
+    if (B <= 0 || T <= 0 || H <= 0 || n_out <= 0) return fail(EMBER_ERR_INVALID_ARG, "bad sizes");
+    if (H > 12288) return fail(EMBER_ERR_INVALID_ARG, "hidden > 12288");
+    const cudaError_t e = launch_pooled_head(hidden, B, T, H, w, b, n_out, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(EMBER_ERR_CUDA, "pooled head launch failed: %s", cudaGetErrorString(e));
     return EMBER_OK;
 }
 

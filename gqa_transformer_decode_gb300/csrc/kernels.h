@@ -186,6 +186,12 @@ void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s);
 void launch_cls_head(const float* h, int n, int H, const uint16_t* W, const float* b, int labels,
                      float* out, cudaStream_t s);
 
+// out[b][j] = mean_t h[b*T + t] . W[j] + bias[j] (mean-pooled head; bf16 W, bias)
+cudaError_t launch_pooled_head(const float* h, int B, int T, int H, const uint16_t* W, const uint16_t* b,
+                               int n_out, float* out, cudaStream_t s);
+// dst[0..n) = src[0..n) (f32), ordered after the previous kernel
+void launch_copy_f32(float* dst, const float* src, int n, cudaStream_t s);
+
 // Standalone RoPE + bf16 store (kernel-level parity entry point).
 void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const float* cos_t,
                        const float* sin_t, uint16_t* out, cudaStream_t s);

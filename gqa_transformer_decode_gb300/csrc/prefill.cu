@@ -435,6 +435,48 @@ void launch_cls_head(const float* h, int n, int H, const uint16_t* W, const floa
     launch_k(k_cls_head, dim3((n + 7) / 8), dim3(256), 0, s, h, n, H, W, b, labels, out);
 }
 
+// ============================================= mean-pooled (sensitivity) head ==
+// Sequence b: the mean over its T rows of h (each column summed in position
+// order), then out[b][j] = mean . W[j] + b[j] by block reductions.
+__global__ void __launch_bounds__(256) k_pooled_head(const float* h, int T, int H, const uint16_t* W,
+                                                     const uint16_t* bias, int n_out, float* out) {
+    extern __shared__ float s_mean[];   // [H]
+    __shared__ float s_red[32];
+    pdl_trigger();
+    pdl_wait();
+    const float* hb = h + (size_t)blockIdx.x * T * H;
+    const float inv = 1.f / (float)T;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+        float acc = 0.f;
+        for (int t = 0; t < T; ++t) acc += __ldg(hb + (size_t)t * H + k);
+        s_mean[k] = acc * inv;
+    }
+    __syncthreads();
+    for (int j = 0; j < n_out; ++j) {
+        const uint16_t* w = W + (size_t)j * H;
+        float s = 0.f;
+        for (int k = threadIdx.x; k < H; k += blockDim.x) s = fmaf(s_mean[k], bf16_to_f32(w[k]), s);
+        s = block_sum(s, s_red);
+        if (threadIdx.x == 0) out[(size_t)blockIdx.x * n_out + j] = s + (bias ? bf16_to_f32(bias[j]) : 0.f);
+    }
+}
+
+cudaError_t launch_pooled_head(const float* h, int B, int T, int H, const uint16_t* W, const uint16_t* b,
+                               int n_out, float* out, cudaStream_t s) {
+    return launch_k(k_pooled_head, dim3(B), dim3(256), (size_t)H * sizeof(float), s, h, T, H, W, b, n_out, out);
+}
+
+// ================================================================ row copy ==
+__global__ void k_copy_f32(float* dst, const float* src, int n) {
+    pdl_trigger();
+    pdl_wait();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
+void launch_copy_f32(float* dst, const float* src, int n, cudaStream_t s) {
+    launch_k(k_copy_f32, dim3((n + 255) / 256 < 64 ? (n + 255) / 256 : 64), dim3(256), 0, s, dst, src, n);
+}
+
 // ============================================== standalone RoPE + bf16 store ==
 __global__ void k_rope_store(const float* x, int n_heads, int D, const float* cos_t,
                              const float* sin_t, uint16_t* out) {

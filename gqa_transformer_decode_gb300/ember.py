@@ -91,6 +91,8 @@ def load():
         "ember_gemv_argmax_noalloc": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P, P]),
         "ember_sample": (st, [P, C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_int32, C.c_float, P, P,
                               P]),
+        "ember_prefill_activations": (st, [P, P, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]),
+        "ember_mean_pooled_head": (st, [P, C.c_int32, C.c_int32, C.c_int32, P, P, C.c_int32, P, P]),
         "ember_kernel_launches": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():
@@ -221,6 +223,14 @@ def ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream):
 
 def ember_sample(logits, B, V, ldl, temperature, top_k, top_p, r, out, stream):
     return load().ember_sample(logits, B, V, ldl, temperature, top_k, top_p, r, out, stream)
+
+
+def ember_prefill_activations(m, kv, seq, ids, n, start_pos, acts, logits, argmax, stream):
+    return load().ember_prefill_activations(m, kv, seq, ids, n, start_pos, acts, logits, argmax, stream)
+
+
+def ember_mean_pooled_head(hidden, B, T, H, w, b, n_out, out, stream):
+    return load().ember_mean_pooled_head(hidden, B, T, H, w, b, n_out, out, stream)
 
 
 def ember_kernel_launches() -> int:

@@ -75,6 +75,13 @@ class Model:
                              _ptr(logits), _ptr(argmax), _ptr(hidden), _stream_ptr(stream))
         E.check(st, "ember_prefill")
 
+    def prefill_activations(self, kv, seq, ids, start_pos, acts, logits=None, argmax=None, stream=None):
+        """Prefill that also writes the residual after every block at the last
+        position into acts [layers, hidden] (f32 device tensor)."""
+        st = E.ember_prefill_activations(self.handle, kv.handle, seq, _ptr(ids), ids.numel(), start_pos,
+                                         _ptr(acts), _ptr(logits), _ptr(argmax), _stream_ptr(stream))
+        E.check(st, "ember_prefill_activations")
+
     def decode_step(self, kv, seqs, ids, positions, logits=None, argmax=None, stream=None):
         st = E.ember_decode_step(self.handle, kv.handle, ids.numel(), _ptr(seqs), _ptr(ids),
                                  _ptr(positions), _ptr(logits), _ptr(argmax), _stream_ptr(stream))

@@ -215,6 +215,31 @@ ember_status ember_decode_step_traced(ember_model *m, ember_kv *kv, int32_t batc
 ember_status ember_encode(ember_model *m, const int32_t *ids, int32_t B, int32_t T, float *out,
                           float *hidden, ember_stream_t stream);
 
+/* ember_prefill that also records, after every decoder block, the residual
+ * stream at the last of the n positions ("ember internals" ForwardModel
+ * forward_with_activations: hidden states after each transformer block at
+ * the last token, the input of the probe mode).
+ *   acts [layers, hidden] f32 (device, required); logits / argmax as in
+ *   ember_prefill (nullable).  The cache and its cursor advance as in
+ *   ember_prefill.  Errors as ember_prefill, plus INVALID_ARG for NULL acts. */
+ember_status ember_prefill_activations(ember_model *m, ember_kv *kv, int32_t seq, const int32_t *ids,
+                                       int32_t n, int32_t start_pos, float *acts, float *logits,
+                                       int32_t *argmax, ember_stream_t stream);
+
+/* The mean-pooled sensitivity head of the bidirectional encoder
+ * (PII-Tracer-vLLM serving/reference_forward.py forward(): the mean over
+ * positions of the final-normed states, times the head's weight, plus its
+ * bias): out[b][j] = (1/T sum_t hidden[b*T + t]) . w[j] + bias[j].
+ *   hidden [B*T, H] f32 (device): the `hidden` output of ember_encode
+ *   w      [n_out, H] bf16 bits, bias [n_out] bf16 bits or NULL (device;
+ *          the caller's, not copied)
+ *   out    [B, n_out] f32 (device)
+ * Each column's sum runs in position order.  H <= 12288.  Asynchronous on
+ * `stream`.  Errors: INVALID_ARG, CUDA. */
+ember_status ember_mean_pooled_head(const float *hidden, int32_t B, int32_t T, int32_t H,
+                                    const uint16_t *w, const uint16_t *bias, int32_t n_out,
+                                    float *out, ember_stream_t stream);
+
 /* Synchronise the stream, read and clear the device status word.  Returns
  * the first device-side error raised since the last call, else EMBER_OK. */
 ember_status ember_sync_status(ember_model *m, ember_stream_t stream);
