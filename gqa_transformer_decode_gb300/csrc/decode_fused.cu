@@ -76,8 +76,9 @@ __device__ __forceinline__ void st_async1(uint32_t addr, float a, uint32_t bar) 
                  : "memory");
 }
 // mbarrier wait whose completion orders the stores of other CTAs of the
-// cluster (st.async complete_tx releases at cluster scope); false after ~1 s
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+// cluster (st.async complete_tx releases at cluster scope); false once
+// `budget` SM cycles have passed without it
+__device__ __forceinline__ bool mbar_wait_cluster_for(uint64_t* bar, uint32_t parity, long long budget) {
     const uint32_t addr = smem_u32(bar);
     const long long t0 = clock64();
     for (;;) {
@@ -90,8 +91,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
             : "r"(addr), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (clock64() - t0 > TC_WAIT_CYCLES) return false;
+        if (clock64() - t0 > budget) return false;
     }
+}
+// the kernels' cluster wait: false after ~1 s
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_cluster_for(bar, parity, TC_WAIT_CYCLES);
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -1189,6 +1194,27 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
             red_add4(z_acc + 4 * i, t.x, t.y, t.z, t.w);
         }
     if (tid == 0 && s_err) raise_status(a.status, EMBER_ERR_TIMEOUT);
+}
+
+// ============================================================= wait probe ==
+// Runs one of the kernels' bounded waits on an mbarrier that nothing ever
+// completes, with the given budget: the wait gives up, the kernel raises
+// EMBER_ERR_TIMEOUT into the status word and returns -- the path every
+// waiting kernel takes when a copy or a peer never arrives.
+__global__ void k_wait_probe(int which, long long budget, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const bool ok = which == 0 ? mbar_wait_for(&bar, 0, budget) : mbar_wait_cluster_for(&bar, 0, budget);
+    if (!ok && threadIdx.x == 0) raise_status(status, EMBER_ERR_TIMEOUT);
+}
+
+void launch_wait_probe(int which, long long budget, int* status, cudaStream_t s) {
+    count_launches(1);
+    k_wait_probe<<<1, 32, 0, s>>>(which, budget, status);
 }
 
 // ================================================================ host ==

@@ -1338,6 +1338,17 @@ extern "C" ember_status ember_sample(const float* logits, int32_t B, int32_t V, 
     return EMBER_OK;
 }
 
+extern "C" ember_status ember_test_bounded_wait(ember_model* m, int32_t which, int64_t budget_cycles,
+                                                ember_stream_t stream) {
+    if (!m) return fail(EMBER_ERR_INVALID_ARG, "NULL model");
+    if (which != 0 && which != 1) return fail(EMBER_ERR_INVALID_ARG, "which must be 0 or 1");
+    if (budget_cycles < 0 || budget_cycles > 200000000ll)
+        return fail(EMBER_ERR_INVALID_ARG, "budget must be in [0, 2e8] cycles");
+    launch_wait_probe(which, budget_cycles, m->status, (cudaStream_t)stream);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
 extern "C" uint64_t ember_kernel_launches(void) { return (uint64_t)launches_so_far(); }
 
 // ====================================== greedy LM head without allocation ==

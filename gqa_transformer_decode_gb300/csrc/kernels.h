@@ -352,6 +352,9 @@ struct FusedMlpArgs {
     int load_delay_ns;           // partitioned plan: delay of the weight copies after the CTA arrives
 };
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
+// One bounded mbarrier wait that nothing completes (which: 0 the CTA wait,
+// 1 the cluster-scope wait), raising EMBER_ERR_TIMEOUT into status.
+void launch_wait_probe(int which, long long budget, int* status, cudaStream_t s);
 // The partitioned plan's MLP block: grid CTAs of 512 threads on their own SMs.
 void launch_fused_mlp_res(const FusedMlpArgs& a, int xi, int grid, int smem, cudaStream_t s);
 

@@ -36,15 +36,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once `budget`
+// SM cycles have passed without it.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, long long budget) {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(addr, parity)) {
-        if (clock64() - t0 > TC_WAIT_CYCLES) return false;
+        if (clock64() - t0 > budget) return false;
     }
     return true;
+}
+// The kernels' wait: false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, TC_WAIT_CYCLES);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1,

@@ -93,6 +93,7 @@ def load():
                               P]),
         "ember_prefill_activations": (st, [P, P, C.c_int32, P, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_mean_pooled_head": (st, [P, C.c_int32, C.c_int32, C.c_int32, P, P, C.c_int32, P, P]),
+        "ember_test_bounded_wait": (st, [P, C.c_int32, C.c_int64, P]),
         "ember_kernel_launches": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():

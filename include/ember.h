@@ -339,6 +339,17 @@ ember_status ember_gemv_argmax_noalloc(const uint16_t *W, int32_t N, int32_t K, 
                                        int32_t nb, float *y, int32_t *argmax,
                                        ember_stream_t stream);
 
+/* Test-only (failure detection): runs one of the library's bounded device
+ * waits -- which = 0 the shared-memory mbarrier wait of the TMA / tensor-core
+ * kernels, 1 the cluster-scope wait of the fused batch-1 decode -- on an
+ * mbarrier that nothing completes, with a budget of budget_cycles SM cycles
+ * (<= 2e8) instead of the kernels' ~1 s.  The wait gives up and the kernel
+ * raises EMBER_ERR_TIMEOUT in m's status word, which the next
+ * ember_sync_status returns (and clears); nothing else is touched.  The
+ * method this library implements has no counterpart to it. */
+ember_status ember_test_bounded_wait(ember_model *m, int32_t which, int64_t budget_cycles,
+                                     ember_stream_t stream);
+
 /* Number of kernels this library has launched in this process so far (a
  * CUDA-graph replay counts each kernel node it runs).  For accounting. */
 uint64_t ember_kernel_launches(void);
