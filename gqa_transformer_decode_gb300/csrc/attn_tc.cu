@@ -339,15 +339,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 tmem_ld32(tO + lane_off + co0 + c0, o);
                 tmem_ld_wait();
                 if (live) {
+                    bool bad = false;
 #pragma unroll
                     for (int d = 0; d < 32; d += 8) {
                         uint4 w;
-                        w.x = pack_f16x2(__uint_as_float(o[d]) * inv, __uint_as_float(o[d + 1]) * inv);
-                        w.y = pack_f16x2(__uint_as_float(o[d + 2]) * inv, __uint_as_float(o[d + 3]) * inv);
-                        w.z = pack_f16x2(__uint_as_float(o[d + 4]) * inv, __uint_as_float(o[d + 5]) * inv);
-                        w.w = pack_f16x2(__uint_as_float(o[d + 6]) * inv, __uint_as_float(o[d + 7]) * inv);
+                        w.x = pack_f16x2_chk(__uint_as_float(o[d]) * inv, __uint_as_float(o[d + 1]) * inv, bad);
+                        w.y = pack_f16x2_chk(__uint_as_float(o[d + 2]) * inv, __uint_as_float(o[d + 3]) * inv, bad);
+                        w.z = pack_f16x2_chk(__uint_as_float(o[d + 4]) * inv, __uint_as_float(o[d + 5]) * inv, bad);
+                        w.w = pack_f16x2_chk(__uint_as_float(o[d + 6]) * inv, __uint_as_float(o[d + 7]) * inv, bad);
                         *reinterpret_cast<uint4*>(out + c0 + d) = w;
                     }
+                    if (bad) raise_status(a.status, EMBER_ERR_RANGE);
                 }
             }
         }

@@ -51,6 +51,23 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
+// 2^e as an f32 (e in [-126, 127]): a layer matrix whose bf16 values exceed
+// the f16 range is stored as f16(W * 2^-e) and its products multiplied back
+// by 2^e, an exact rescaling (e = 0 for every matrix within range).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Activations rounded to f16 must lie within its range: `bad` records a value
+// beyond +-65504 (or NaN) so the kernel can raise EMBER_ERR_RANGE.
+constexpr float F16_MAX = 65504.f;
+__device__ __forceinline__ bool f16_out_of_range(float v) { return !(fabsf(v) <= F16_MAX); }
+__device__ __forceinline__ uint32_t pack_f16x2_chk(float lo, float hi, bool& bad) {
+    bad |= f16_out_of_range(lo) | f16_out_of_range(hi);
+    return pack_f16x2(lo, hi);
+}
+__device__ __forceinline__ uint16_t f32_to_f16_chk(float f, bool& bad) {
+    bad |= f16_out_of_range(f);
+    return f32_to_f16(f);
+}
 __device__ __forceinline__ void unpack8_f16(const uint4& w, float* f) {
     const __half2* h = reinterpret_cast<const __half2*>(&w);
 #pragma unroll

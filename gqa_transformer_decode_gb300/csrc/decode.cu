@@ -7,6 +7,8 @@
 // loop this path runs, one token per sequence); ember internals "kv cache"
 // (cursor advances after all layers, explicit positions) and "grouped-query
 // attention" (query head h reads kv head h / G).
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
             float v = 0.f;
 #pragma unroll
             for (int q = 0; q < WPR; ++q) v += s_part[re][q][be];
-            v *= s_rinv[be];
+            v *= s_rinv[be] * pow2f(a.w_exp);
             if (rowe < a.N && be < nb) {
                 float* o = a.out + (size_t)be * a.ldo;
                 if (a.mode == EPI_STORE) {
@@ -492,7 +494,11 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
             const int e = tid + i * ATT_THREADS;
             if (e < G * D) {
                 const float o = acc[i] / s_l[e / D];
-                if (a.att_b) a.att_b[out0 + e] = f32_to_f16(o);
+                if (a.att_b) {
+                    bool bad = false;
+                    a.att_b[out0 + e] = f32_to_f16_chk(o, bad);
+                    if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+                }
                 else a.att[out0 + e] = o;
             }
         }
@@ -552,7 +558,11 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_decode(AttnDecodeArgs a) {
         for (int s2 = 0; s2 < S; ++s2)
             O = fmaf(__ldcg(pb + ((size_t)s2 * G + h) * (D + 2) + 2 + d), s_pm[s2 * G + h], O);
         O *= s_scale[h];
-        if (a.att_b) a.att_b[out0 + e] = f32_to_f16(O);
+        if (a.att_b) {
+            bool bad = false;
+            a.att_b[out0 + e] = f32_to_f16_chk(O, bad);
+            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+        }
         else a.att[out0 + e] = O;
     }
     if (tid == 0) a.counters[b * a.NKV + g] = 0u;
@@ -606,17 +616,41 @@ __global__ void k_bf16_to_f32(const uint16_t* in, float* out, long long n) {
         out[i] = bf16_to_f32(in[i]);
 }
 
-__global__ void k_bf16_to_f16(uint16_t* p, long long n) {
+__global__ void k_bf16_to_f16(uint16_t* p, long long n, float scale) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x)
-        p[i] = f32_to_f16(bf16_to_f32(p[i]));
+        p[i] = f32_to_f16(bf16_to_f32(p[i]) * scale);
 }
 
-void launch_bf16_to_f16_inplace(uint16_t* p, long long n, cudaStream_t s) {
+void launch_bf16_to_f16_inplace(uint16_t* p, long long n, int exp, cudaStream_t s) {
     if (n <= 0) return;
     count_launches(1);
     long long blocks = (n + 255) / 256;
-    k_bf16_to_f16<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(p, n);
+    k_bf16_to_f16<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(p, n, std::ldexp(1.f, -exp));
+}
+
+// out = max |p[i]| over n bf16 values, as f32 bits (non-negative floats order
+// like their bits); NaN entries are skipped
+__global__ void k_absmax_bf16(const uint16_t* p, long long n, unsigned* out) {
+    unsigned m = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const unsigned b = ((unsigned)p[i] & 0x7FFFu) << 16;
+        if (b <= 0x7F800000u) m = b > m ? b : m;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned t = __shfl_xor_sync(FULL_MASK, m, o);
+        m = t > m ? t : m;
+    }
+    if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+
+void launch_absmax_bf16(const uint16_t* p, long long n, unsigned* out, cudaStream_t s) {
+    if (n <= 0) return;
+    count_launches(1);
+    long long blocks = (n + 255) / 256;
+    k_absmax_bf16<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(p, n, out);
 }
 
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s) {

@@ -331,7 +331,11 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
                     if (st[1] > 0.f) Ls = fmaf(st[1], exp2f(st[0] - M), Ls);
                 }
                 const float out = Ls > 0.f ? v / Ls : 0.f;
-                if (a.att_b) a.att_b[out0 + (size_t)h * D + k - 2] = f32_to_f16(out);
+                if (a.att_b) {
+                    bool bad = false;
+                    a.att_b[out0 + (size_t)h * D + k - 2] = f32_to_f16_chk(out, bad);
+                    if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+                }
                 else a.att[out0 + (size_t)h * D + k - 2] = out;
             }
         } else {
@@ -381,7 +385,11 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
         for (int s2 = 0; s2 < S; ++s2)
             O = fmaf(__ldcg(pb + ((size_t)s2 * G + h) * (D + 2) + 2 + d), s_pm[s2 * G + h], O);
         O *= s_inv[h];
-        if (a.att_b) a.att_b[out0 + e] = f32_to_f16(O);
+        if (a.att_b) {
+            bool bad = false;
+            a.att_b[out0 + e] = f32_to_f16_chk(O, bad);
+            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+        }
         else a.att[out0 + e] = O;
     }
     if (tid == 0) a.counters[b * a.NKV + g] = 0u;

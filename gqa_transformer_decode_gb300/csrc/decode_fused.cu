@@ -160,7 +160,8 @@ struct ResidualNorm {
     }
     template <int ZI, int ZZ>
     __device__ __forceinline__ void apply(const float* x_in, const float* z_in, float* x_out, float* z_zero,
-                                          float eps, int H, int cta, int ncta, uint16_t* s_xh, float* s_red) {
+                                          float eps, int H, int cta, int ncta, uint16_t* s_xh, float* s_red,
+                                          int* status) {
         const int H4 = H >> 2;
         const int per = (H4 + ncta - 1) / ncta;
         const int e0 = cta * per, e1 = e0 + per;
@@ -200,14 +201,16 @@ struct ResidualNorm {
         float tot = 0.f;
         for (int k = 0; k < (int)(blockDim.x >> 5); ++k) tot += s_red[k];
         const float ri = rsqrtf(tot / (float)H + eps);
+        bool bad = false;
 #pragma unroll
         for (int q = 0; q < MAXV; ++q) {
             const int i = threadIdx.x + q * blockDim.x;
             if (i < H4)
                 reinterpret_cast<uint2*>(s_xh)[i] =
-                    make_uint2(pack_f16x2(v[q].x * ri * w[q].x, v[q].y * ri * w[q].y),
-                               pack_f16x2(v[q].z * ri * w[q].z, v[q].w * ri * w[q].w));
+                    make_uint2(pack_f16x2_chk(v[q].x * ri * w[q].x, v[q].y * ri * w[q].y, bad),
+                               pack_f16x2_chk(v[q].z * ri * w[q].z, v[q].w * ri * w[q].w, bad));
         }
+        if (bad) raise_status(status, EMBER_ERR_RANGE);
         __syncthreads();
     }
 };
@@ -229,7 +232,7 @@ struct XRegs {
             v[i] = c < n8 ? reinterpret_cast<const uint4*>(xh)[c] : make_uint4(0, 0, 0, 0);
         }
     }
-    __device__ __forceinline__ void load_f32(const float* x, int n8) {  // f32 input, rounded to f16
+    __device__ __forceinline__ void load_f32(const float* x, int n8, bool& bad) {  // f32 input, rounded to f16
         const int lane = threadIdx.x & 31;
 #pragma unroll
         for (int i = 0; i < XI; ++i) {
@@ -237,8 +240,8 @@ struct XRegs {
             if (c < n8) {
                 const float4 a = reinterpret_cast<const float4*>(x)[2 * c];
                 const float4 b = reinterpret_cast<const float4*>(x)[2 * c + 1];
-                v[i] = make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(b.x, b.y),
-                                  pack_f16x2(b.z, b.w));
+                v[i] = make_uint4(pack_f16x2_chk(a.x, a.y, bad), pack_f16x2_chk(a.z, a.w, bad),
+                                  pack_f16x2_chk(b.x, b.y, bad), pack_f16x2_chk(b.z, b.w, bad));
             } else {
                 v[i] = make_uint4(0, 0, 0, 0);
             }
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     // the step's token state, loaded beside the residual (used after the norm)
     const int ok_raw = __ldcg(a.tok_ok);
     const int pos_raw = __ldcg(a.tok_pos);
-    rn.apply<ZSLOTS, ZSLOTS>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red);
+    rn.apply<ZSLOTS, ZSLOTS>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red, a.status);
 
     const int ok = ok_raw;
     const int pos = ok ? pos_raw : 0;
@@ -569,7 +572,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 rp[k] = reinterpret_cast<const uint4*>(sW + (size_t)min(base + k, nrow - 1) * H);
-            float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, H / 8);
+            float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, H / 8) * pow2f(a.qkv_exp);
             const int ri = base + my;
             if (ri < nrow) {
                 if (a.bqkv) v += s_bias[ri];
@@ -878,7 +881,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
     {
         XRegs<XI> xr;
-        xr.load_f32(s_att, GD / 8);
+        bool bad = false;
+        xr.load_f32(s_att, GD / 8, bad);
+        if (bad) raise_status(a.status, EMBER_ERR_RANGE);
         const int nrow = o1 - o0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
         for (int base = warp * 4; base < nrow; base += NTH / 8) {   // 4 rows per warp
@@ -886,7 +891,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 rp[k] = reinterpret_cast<const uint4*>(sWo + (size_t)min(base + k, nrow - 1) * GD);
-            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, GD / 8);
+            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, GD / 8) * pow2f(a.o_exp);
             const int ri = base + my;
             if (ri < nrow && (lane & 7) == 0) red_add(a.z_acc + o0 + ri, v);
         }
@@ -965,7 +970,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     pdl_trigger();
     pdl_wait();
 
-    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
+    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status);
     XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
 
@@ -983,7 +988,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
             const uint4* rp[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) rp[q] = reinterpret_cast<const uint4*>(st + (size_t)(qd * 4 + q) * H * 2) + c0;
-            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0);
+            const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0) * pow2f(a.gu_exp);
             const int rr = qd * 4 + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
             if ((lane & 7) == 0) s_g[k & 1][ks][rr] = v;
         }
@@ -1001,7 +1006,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
                         gt += s_g[k & 1][z][2 * j];
                         up += s_g[k & 1][z][2 * j + 1];
                     }
-                    const float act = __fdividef(gt, 1.f + __expf(-gt)) * up;
+                    const float act = __fdividef(gt, 1.f + __expf(-gt)) * up * pow2f(a.d_exp);
                     float w[8];
                     unpack8_f16(lds128(wd + (size_t)j * H8 + hgp), w);
 #pragma unroll
@@ -1018,7 +1023,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
                     gt += s_g[k & 1][z][2 * j];
                     up += s_g[k & 1][z][2 * j + 1];
                 }
-                act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
+                act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up * pow2f(a.d_exp);
             }
 #pragma unroll
             for (int q = 0; q < MAXHG; ++q) {
@@ -1134,7 +1139,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
     }
     pdl_wait();
 
-    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red);
+    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status);
     XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
     if (nf > 0 && !mbar_wait(&bar[0], 0)) s_err = 1;
@@ -1146,7 +1151,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             rp[q] = reinterpret_cast<const uint4*>(s_gu + (size_t)min(base + q, nrow - 1) * H) + c0;
-        const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0);
+        const float v = wdot4_f16(rp[0], rp[1], rp[2], rp[3], xr, c1 - c0) * pow2f(a.gu_exp);
         const int rr = base + ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
         if ((lane & 7) == 0 && rr < nrow) s_g[ks * nrow + rr] = v;
     }
@@ -1158,7 +1163,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
             gt += s_g[z * nrow + 2 * j];
             up += s_g[z * nrow + 2 * j + 1];
         }
-        s_act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up;
+        s_act[j] = __fdividef(gt, 1.f + __expf(-gt)) * up * pow2f(a.d_exp);
     }
     __syncthreads();
 

@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;
         const int row = m0 + q * 32 + lane;
         unsigned long long best = 0ull;   // EPI_ARGMAX
+        bool f16bad = false;              // EPI_SWIGLU: an output beyond the f16 range
+        const float wsc = pow2f(e.w_exp);   // the weights' storage scale
         if (!mbar_wait(tfull, 0)) {
             sflag[0] = 1;
         } else {
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (row >= M || n >= N || nk == 0) continue;
                 float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * wsc;
                 const bool fullc = (n + 32 <= N);
                 if (e.mode == EPI_ARGMAX) {   // logits (optional) and the row's best key
                     if (e.out_f32) {
@@ -188,8 +190,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         for (int i = 0; i < 8; ++i) {
                             const float g0 = v[4 * i], u0 = v[4 * i + 1];
                             const float g1 = v[4 * i + 2], u1 = v[4 * i + 3];
-                            pk[i] = pack_f16x2(g0 / (1.f + __expf(-g0)) * u0,
-                                                g1 / (1.f + __expf(-g1)) * u1);
+                            pk[i] = pack_f16x2_chk(g0 / (1.f + __expf(-g0)) * u0,
+                                                   g1 / (1.f + __expf(-g1)) * u1, f16bad);
                         }
                         uint4* o4 = reinterpret_cast<uint4*>(o);
                         o4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     } else {
                         for (int i = 0; i < 16 && n + 2 * i + 1 < N; ++i) {
                             const float g = v[2 * i], u = v[2 * i + 1];
-                            o[i] = f32_to_f16(g / (1.f + __expf(-g)) * u);
+                            o[i] = f32_to_f16_chk(g / (1.f + __expf(-g)) * u, f16bad);
                         }
                     }
                 } else {
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             if (e.mode == EPI_ARGMAX && row < M && best) atomicMax(e.keys + row, best);
+            if (f16bad) raise_status(status, EMBER_ERR_RANGE);
         }
     }
 

@@ -29,7 +29,8 @@ constexpr int GP_THREADS = 192;
 // [n0, n0 + BN), read from TMEM at tbase (lane quadrant already applied).
 template <int BN>
 __device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tbase, int row, int n0,
-                                              int M, int N, unsigned long long& best) {
+                                              int M, int N, unsigned long long& best, bool& f16bad) {
+    const float wsc = pow2f(e.w_exp);   // the weights' storage scale
     for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
         tmem_ld16(tbase + c, r);
@@ -39,7 +40,7 @@ __device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tb
         if (row >= M || n >= N) continue;
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * wsc;
         const bool fullc = (n + 32 <= N);
         if (e.mode == EPI_ARGMAX) {
             if (e.out_f32) {
@@ -59,8 +60,8 @@ __device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tb
                 for (int i = 0; i < 8; ++i) {
                     const float g0 = v[4 * i], u0 = v[4 * i + 1];
                     const float g1 = v[4 * i + 2], u1 = v[4 * i + 3];
-                    pk[i] = pack_f16x2(__fdividef(g0, 1.f + __expf(-g0)) * u0,
-                                       __fdividef(g1, 1.f + __expf(-g1)) * u1);
+                    pk[i] = pack_f16x2_chk(__fdividef(g0, 1.f + __expf(-g0)) * u0,
+                                           __fdividef(g1, 1.f + __expf(-g1)) * u1, f16bad);
                 }
                 uint4* o4 = reinterpret_cast<uint4*>(o);
                 o4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -68,7 +69,7 @@ __device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tb
             } else {
                 for (int i = 0; i < 16 && n + 2 * i + 1 < N; ++i) {
                     const float g = v[2 * i], u = v[2 * i + 1];
-                    o[i] = f32_to_f16(__fdividef(g, 1.f + __expf(-g)) * u);
+                    o[i] = f32_to_f16_chk(__fdividef(g, 1.f + __expf(-g)) * u, f16bad);
                 }
             }
         } else {
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         const int q = warp & 3;
         unsigned long long best = 0ull;
         int best_row = -1;
+        bool f16bad = false;   // EPI_SWIGLU: an output beyond the f16 range
         for (int li = 0; li < my_tiles; ++li) {
             const int b = li & 1;
             int m0, n0;
@@ -241,12 +243,13 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
                 best_row = row;
             }
             tile_epilogue<BN>(e, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), row, n0, M, N,
-                              best);
+                              best, f16bad);
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
         }
         if (e.mode == EPI_ARGMAX && best && best_row >= 0 && best_row < M)
             atomicMax(e.keys + best_row, best);
+        if (f16bad) raise_status(status, EMBER_ERR_RANGE);
     }
 
     tc_fence_before();

@@ -106,6 +106,9 @@ struct LayerDev {
     uint16_t* woG = nullptr;   // f16 [NKV][H][G*D] o_proj grouped by kv head (fused decode)
     float *attn_norm, *mlp_norm, *bqkv, *q_norm, *k_norm;
     GemmPlan p_qkv, p_o, p_gu, p_d;
+    // storage scales 2^-e of wqkv, wo, wgu, wd: e > 0 only for a matrix whose
+    // bf16 values exceed the f16 range (its products are multiplied by 2^e)
+    int e_qkv = 0, e_o = 0, e_gu = 0, e_d = 0;
 };
 
 struct GraphEntry {
@@ -371,13 +374,48 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
             e = cudaMemcpy2DAsync(L.wgu + H, (size_t)4 * H, W.w_up, (size_t)2 * H, (size_t)2 * H, F,
                                   D2D, s);
         cp(L.wd, W.w_down, (size_t)H * F * 2);
-        // the layer matrices run as f16 (more mantissa for the f16 activations
-        // they meet in the tensor-core GEMMs); embedding / head stay bf16
+    }
+    // The layer matrices run as f16 (more mantissa for the f16 activations
+    // they meet in the tensor-core GEMMs); embedding / head stay bf16.  A
+    // matrix whose largest |w| exceeds the f16 range (65504) is stored as
+    // f16(W * 2^-e), the smallest such e, and every product with it is
+    // multiplied by 2^e: the rescaling is exact, so a bf16 checkpoint with
+    // large weights keeps its values.
+    unsigned* d_max = nullptr;
+    std::vector<unsigned> h_max((size_t)4 * c.layers, 0u);
+    if (e == cudaSuccess) e = cudaMalloc(&d_max, h_max.size() * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_max, 0, h_max.size() * sizeof(unsigned), s);
+    for (int l = 0; l < c.layers && e == cudaSuccess; ++l) {
+        LayerDev& L = m->layers[l];
+        launch_absmax_bf16(L.wqkv, (long long)m->qkv_n * H, d_max + 4 * l + 0, s);
+        launch_absmax_bf16(L.wo, (long long)H * m->q, d_max + 4 * l + 1, s);
+        launch_absmax_bf16(L.wgu, (long long)2 * F * H, d_max + 4 * l + 2, s);
+        launch_absmax_bf16(L.wd, (long long)H * F, d_max + 4 * l + 3, s);
+    }
+    if (e == cudaSuccess) e = cudaMemcpy(h_max.data(), d_max, h_max.size() * sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (d_max) cudaFree(d_max);
+    auto exp_for = [](unsigned bits) {
+        float v;
+        std::memcpy(&v, &bits, 4);
+        int ex = 0;
+        while (v > 65504.f && ex < 126) {
+            v *= 0.5f;
+            ++ex;
+        }
+        return ex;
+    };
+    for (int l = 0; l < c.layers; ++l) {
+        const ember_layer_weights& W = w->layers[l];
+        LayerDev& L = m->layers[l];
+        L.e_qkv = exp_for(h_max[4 * l + 0]);
+        L.e_o = exp_for(h_max[4 * l + 1]);
+        L.e_gu = exp_for(h_max[4 * l + 2]);
+        L.e_d = exp_for(h_max[4 * l + 3]);
         if (e == cudaSuccess) {
-            launch_bf16_to_f16_inplace(L.wqkv, (long long)m->qkv_n * H, s);
-            launch_bf16_to_f16_inplace(L.wo, (long long)H * m->q, s);
-            launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, s);
-            launch_bf16_to_f16_inplace(L.wd, (long long)H * F, s);
+            launch_bf16_to_f16_inplace(L.wqkv, (long long)m->qkv_n * H, L.e_qkv, s);
+            launch_bf16_to_f16_inplace(L.wo, (long long)H * m->q, L.e_o, s);
+            launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, L.e_gu, s);
+            launch_bf16_to_f16_inplace(L.wd, (long long)H * F, L.e_d, s);
             if (L.wdT) launch_transpose16(L.wd, L.wdT, H, F, s);
             if (L.woG) {   // group g's o_proj columns as one [H][G*D] block
                 const size_t gd = (size_t)m->G * D;
@@ -604,12 +642,13 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     const ember_config& c = m->c;
     LayerDev& L = m->layers[l];
     const float eps = (float)c.rms_eps;
-    launch_rmsnorm_h(m->x, L.attn_norm, eps, n, c.hidden, m->xb, s);
+    launch_rmsnorm_h(m->x, L.attn_norm, eps, n, c.hidden, m->xb, m->status, s);
     GemmEpilogue e{};
     e.mode = EPI_STORE;
     e.out_f32 = m->qkv;
     e.ldo = m->qkv_n;
     e.bias = c.qkv_bias ? L.bqkv : nullptr;
+    e.w_exp = L.e_qkv;
     launch_gemm(L.p_qkv, n, e, m->status, s);
     RopeKVArgs r{};
     r.qkv = m->qkv;
@@ -672,23 +711,27 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     a.seq_stride = cv.seq_stride;
     a.head_stride = cv.head_stride;
     a.att = m->att_b;
+    a.status = m->status;
     launch_attn_prefill(a, s);
     }
     e = GemmEpilogue{};
     e.mode = EPI_RESID;
     e.out_f32 = m->x;
     e.ldo = c.hidden;
+    e.w_exp = L.e_o;
     launch_gemm(L.p_o, n, e, m->status, s);
-    launch_rmsnorm_h(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, s);
+    launch_rmsnorm_h(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, m->status, s);
     e = GemmEpilogue{};
     e.mode = EPI_SWIGLU;
     e.out_h = m->act_b;
     e.ldo = c.ff;
+    e.w_exp = L.e_gu;
     launch_gemm(L.p_gu, n, e, m->status, s);
     e = GemmEpilogue{};
     e.mode = EPI_RESID;
     e.out_f32 = m->x;
     e.ldo = c.hidden;
+    e.w_exp = L.e_d;
     launch_gemm(L.p_d, n, e, m->status, s);
 }
 
@@ -849,6 +892,8 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.q_norm = c.qk_norm ? L.q_norm : nullptr;
             a.k_norm = c.qk_norm ? L.k_norm : nullptr;
             a.wo = L.woG;
+            a.qkv_exp = L.e_qkv;
+            a.o_exp = L.e_o;
             a.H = c.hidden;
             a.NH = c.n_heads;
             a.NKV = c.n_kv_heads;
@@ -875,6 +920,8 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             launch_fused_attn(kv->k_map, kv->v_map, a, fp.xi, fp.smem_attn, s);
             FusedMlpArgs f{};
             f.wgu = L.wgu;
+            f.gu_exp = L.e_gu;
+            f.d_exp = L.e_d;
             f.wdT = L.wdT;
             f.norm_w = L.mlp_norm;
             f.eps = eps;
@@ -933,6 +980,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         if (gemv) {
             GemvArgs g{};
             g.W = L.wqkv; g.w_f16 = 1;
+            g.w_exp = L.e_qkv;
             g.N = m->qkv_n;
             g.K = c.hidden;
             g.x = m->x;
@@ -947,7 +995,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
         } else {
-            launch_rmsnorm_h(m->x, L.attn_norm, eps, B, c.hidden, m->xb, s);
+            launch_rmsnorm_h(m->x, L.attn_norm, eps, B, c.hidden, m->xb, m->status, s);
             GemmEpilogue e{};
             e.mode = EPI_STORE;
             e.out_f32 = m->qkv;
@@ -957,6 +1005,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
                 cudaMemsetAsync(m->qkv, 0, (size_t)B * m->qkv_n * 4, s);
                 e.zeroed = 1;
             }
+            e.w_exp = L.e_qkv;
             launch_gemm(L.p_qkv, B, e, m->status, s);
         }
         AttnDecodeArgs a{};
@@ -991,6 +1040,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         if (gemv) {
             GemvArgs g{};
             g.W = L.wo; g.w_f16 = 1;
+            g.w_exp = L.e_o;
             g.N = c.hidden;
             g.K = m->q;
             g.x = m->att_f;
@@ -1003,6 +1053,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             launch_gemv(g, s, m->sms);
             g = GemvArgs{};
             g.W = L.wgu; g.w_f16 = 1;
+            g.w_exp = L.e_gu;
             g.N = 2 * c.ff;
             g.K = c.hidden;
             g.x = m->x;
@@ -1017,6 +1068,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             launch_gemv(g, s, m->sms);
             g = GemvArgs{};
             g.W = L.wd; g.w_f16 = 1;
+            g.w_exp = L.e_d;
             g.N = c.hidden;
             g.K = c.ff;
             g.x = m->act_f;
@@ -1033,17 +1085,20 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             e.mode = EPI_RESID;
             e.out_f32 = m->x;
             e.ldo = c.hidden;
+            e.w_exp = L.e_o;
             launch_gemm(L.p_o, B, e, m->status, s);
-            launch_rmsnorm_h(m->x, L.mlp_norm, eps, B, c.hidden, m->xb, s);
+            launch_rmsnorm_h(m->x, L.mlp_norm, eps, B, c.hidden, m->xb, m->status, s);
             e = GemmEpilogue{};
             e.mode = EPI_SWIGLU;
             e.out_h = m->act_b;
             e.ldo = c.ff;
+            e.w_exp = L.e_gu;
             launch_gemm(L.p_gu, B, e, m->status, s);
             e = GemmEpilogue{};
             e.mode = EPI_RESID;
             e.out_f32 = m->x;
             e.ldo = c.hidden;
+            e.w_exp = L.e_d;
             launch_gemm(L.p_d, B, e, m->status, s);
         }
     }

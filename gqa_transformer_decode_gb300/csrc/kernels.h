@@ -79,6 +79,7 @@ struct GemvArgs {
     int mode;                    // EpiMode
     unsigned long long* keys;    // [nb] argmax keys (EPI_ARGMAX)
     int* status;
+    int w_exp;                   // W stored scaled by 2^-w_exp: products multiplied by 2^w_exp
     const float* x_add;          // [x_add_slots][K] summed into x (split-K accumulator copies;
                                  // nb == 1, bf16 W), or nullptr
     int x_add_slots;
@@ -140,7 +141,7 @@ void launch_set_cursor(int32_t* cursor, int seq, int pos, cudaStream_t s);
 // ------------------------------------------------------------- prefill side --
 // xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
-                         cudaStream_t s);
+                      int* status, cudaStream_t s);
 // xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tied-head GEMM)
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s);
@@ -179,6 +180,7 @@ struct AttnPrefillArgs {
     const uint16_t* vc;
     long long seq_stride, head_stride;
     uint16_t* att;               // [n][NH*D] f16 (GEMM operand)
+    int* status;
 };
 void launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t s);
 
@@ -199,7 +201,9 @@ void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const floa
 // bf16 [n] -> f32 [n] (weight repack of norms / biases)
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s);
 // bf16 bits -> f16 bits in place (weight repack of the layer matrices)
-void launch_bf16_to_f16_inplace(uint16_t* p, long long n, cudaStream_t s);
+void launch_bf16_to_f16_inplace(uint16_t* p, long long n, int exp, cudaStream_t s);
+// *out = max(*out, max |p[i]|) as f32 bits, over n bf16 values (NaN skipped)
+void launch_absmax_bf16(const uint16_t* p, long long n, unsigned* out, cudaStream_t s);
 
 // ----------------------------------------------------------- tcgen05 GEMM --
 // D[M,N] = A[M,K] . B[N,K]^T (bf16 in, f32 accumulate in TMEM) with a fused
@@ -212,6 +216,7 @@ struct GemmEpilogue {
     const float* bias;           // EPI_STORE, nullable
     unsigned long long* keys;    // EPI_ARGMAX: [M] argmax keys (start at 0)
     int ksplit;                  // set by launch_gemm: K split over grid.z (red.add outputs)
+    int w_exp;                   // B is stored scaled by 2^-w_exp: products are multiplied by 2^w_exp
     int zeroed;                  // EPI_STORE: out_f32 is zero, so K may be split
 };
 
@@ -326,6 +331,7 @@ struct FusedAttnArgs {
     const int32_t* positions;    // the step's explicit positions (nullptr: the cursor)
     const int32_t* cursor;       // [max_seqs] the cache's cursors
     int resident;                // resident plan: o_proj rows and two K/V tiles loaded before the wait
+    int qkv_exp, o_exp;          // storage scales of wqkv / wo (2^-e), undone on the products
     const float* cos_t;
     const float* sin_t;
     int* status;
@@ -350,6 +356,7 @@ struct FusedMlpArgs {
     int ns;
     int pf_late;                 // the first pf_late CTAs prefetch the last pf_late CTAs' chunks to L2
     int load_delay_ns;           // partitioned plan: delay of the weight copies after the CTA arrives
+    int gu_exp, d_exp;           // storage scales of wgu / wdT (2^-e), undone on the products
 };
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
 // One bounded mbarrier wait that nothing completes (which: 0 the CTA wait,

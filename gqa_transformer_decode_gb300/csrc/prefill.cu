@@ -15,7 +15,7 @@ namespace ember {
 // OUT: 0 = f32, 1 = f16 (projection GEMM operand), 2 = bf16 (tied-head GEMM operand)
 template <int OUT>
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w, float eps, int H,
-                                                 void* out) {
+                                                 void* out, int* status) {
     // one row per CTA; H % 4 == 0 and H <= 8192 (the weights are loaded into
     // registers before the wait, the row in one batch of 16-byte loads)
     constexpr int MAXV = 8;
@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     for (int k = 0; k < 8; ++k) tot += red[k];
     const float ri = rsqrtf(tot / (float)H + eps);
 #pragma unroll
+    bool bad = false;
     for (int q = 0; q < MAXV; ++q) {
         const int i = threadIdx.x + q * 256;
         if (i >= H4) continue;
@@ -54,10 +55,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
             reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H)[i] = make_float4(a0, a1, a2, a3);
         } else {
             uint2* o = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + (size_t)t * H);
-            o[i] = OUT == 1 ? make_uint2(pack_f16x2(a0, a1), pack_f16x2(a2, a3))
+            o[i] = OUT == 1 ? make_uint2(pack_f16x2_chk(a0, a1, bad), pack_f16x2_chk(a2, a3, bad))
                             : make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
         }
     }
+    if (bad) raise_status(status, EMBER_ERR_RANGE);
 }
 
 // A warp per row for H <= 2048 (H % 128 == 0) and at least 1024 rows: the
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
 // block barrier; 8 rows per CTA.
 template <int NV>
 __global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const float* w, float eps, int H,
-                                                      int n, uint16_t* out) {
+                                                      int n, uint16_t* out, int* status) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     pdl_trigger();
@@ -82,23 +84,25 @@ __global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const floa
     ss = warp_sum(ss);
     const float ri = rsqrtf(ss / (float)H + eps);
     uint2* o = reinterpret_cast<uint2*>(out + (size_t)t * H);
+    bool bad = false;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
         const float4 g = __ldg(reinterpret_cast<const float4*>(w) + lane + 32 * q);
-        o[lane + 32 * q] = make_uint2(pack_f16x2(v[q].x * ri * g.x, v[q].y * ri * g.y),
-                                      pack_f16x2(v[q].z * ri * g.z, v[q].w * ri * g.w));
+        o[lane + 32 * q] = make_uint2(pack_f16x2_chk(v[q].x * ri * g.x, v[q].y * ri * g.y, bad),
+                                      pack_f16x2_chk(v[q].z * ri * g.z, v[q].w * ri * g.w, bad));
     }
+    if (bad) raise_status(status, EMBER_ERR_RANGE);
 }
 
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
-                         cudaStream_t s) {
+                      int* status, cudaStream_t s) {
     const dim3 g((n + 7) / 8), b(256);
     // a warp per row pays off with many rows; a few rows (decode batches,
     // short prompts) keep a CTA per row so that they spread over the SMs
     if (n >= 1024 && H % 128 == 0 && H <= 2048) {
         switch (H / 128) {
 #define EMBER_RMS_WARP(NV) \
-    case NV: launch_k(k_rmsnorm_warp<NV>, g, b, 0, s, x, w, eps, H, n, xb); return;
+    case NV: launch_k(k_rmsnorm_warp<NV>, g, b, 0, s, x, w, eps, H, n, xb, status); return;
             EMBER_RMS_WARP(1) EMBER_RMS_WARP(2) EMBER_RMS_WARP(3) EMBER_RMS_WARP(4)
             EMBER_RMS_WARP(5) EMBER_RMS_WARP(6) EMBER_RMS_WARP(7) EMBER_RMS_WARP(8)
             EMBER_RMS_WARP(9) EMBER_RMS_WARP(10) EMBER_RMS_WARP(11) EMBER_RMS_WARP(12)
@@ -107,15 +111,15 @@ void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, u
             default: break;
         }
     }
-    launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
+    launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, status);
 }
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
-    launch_k(k_rmsnorm<2>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb);
+    launch_k(k_rmsnorm<2>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, (int*)nullptr);
 }
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
                         cudaStream_t s) {
-    launch_k(k_rmsnorm<0>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h);
+    launch_k(k_rmsnorm<0>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h, (int*)nullptr);
 }
 
 // =================================================== q/k norm, RoPE, K/V write ==
@@ -377,7 +381,11 @@ __global__ void __launch_bounds__(APF_THREADS) k_attn_prefill(AttnPrefillArgs a,
 #pragma unroll
         for (int c = 0; c < DL; ++c) {
             const int d = lane + 32 * c;
-            if (d < D) o[d] = f32_to_f16(acc[k][c] * inv);
+            if (d < D) {
+                bool bad = false;
+                o[d] = f32_to_f16_chk(acc[k][c] * inv, bad);
+                if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+            }
         }
     }
 }

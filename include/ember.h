@@ -65,7 +65,9 @@ typedef enum ember_status {
     EMBER_ERR_TIMEOUT = 5,     /* a bounded device wait gave up                          */
     EMBER_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed                    */
     EMBER_ERR_OOM = 7,         /* device allocation failed                               */
-    EMBER_ERR_UNSUPPORTED = 8  /* a valid request this build does not serve              */
+    EMBER_ERR_UNSUPPORTED = 8, /* a valid request this build does not serve              */
+    EMBER_ERR_RANGE = 9        /* an activation outside the f16 range of the tensor-core
+                                  operands (|v| > 65504 or NaN; found on the device)     */
 } ember_status;
 
 /* Model hyper-parameters.  Field names follow the HuggingFace config.json
