@@ -158,10 +158,10 @@ struct ResidualNorm {
             w[q] = i < H4 ? __ldg(reinterpret_cast<const float4*>(wp) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    template <int ZI, int ZZ>
+    template <int ZMAX>
     __device__ __forceinline__ void apply(const float* x_in, const float* z_in, float* x_out, float* z_zero,
                                           float eps, int H, int cta, int ncta, uint16_t* s_xh, float* s_red,
-                                          int* status) {
+                                          int* status, int ZI, int ZZ) {
         const int H4 = H >> 2;
         const int per = (H4 + ncta - 1) / ncta;
         const int e0 = cta * per, e1 = e0 + per;
@@ -171,12 +171,14 @@ struct ResidualNorm {
         for (int q = 0; q < MAXV; ++q) {
             const int i = threadIdx.x + q * blockDim.x;
             if (i < H4) {
-                float4 b[ZI];
+                float4 b[ZMAX];
 #pragma unroll
-                for (int z = 0; z < ZI; ++z) b[z] = __ldcg(reinterpret_cast<const float4*>(z_in + (size_t)z * H) + i);
+                for (int z = 0; z < ZMAX; ++z)
+                    b[z] = z < ZI ? __ldcg(reinterpret_cast<const float4*>(z_in + (size_t)z * H) + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 float4 t = __ldcg(reinterpret_cast<const float4*>(x_in) + i);
 #pragma unroll
-                for (int z = 0; z < ZI; ++z) {
+                for (int z = 0; z < ZMAX; ++z) {
                     t.x += b[z].x; t.y += b[z].y; t.z += b[z].z; t.w += b[z].w;
                 }
                 v[q] = t;
@@ -190,8 +192,8 @@ struct ResidualNorm {
                 if (i >= e0 && i < e1) {
                     reinterpret_cast<float4*>(x_out)[i] = v[q];
 #pragma unroll
-                    for (int z = 0; z < ZZ; ++z)
-                        reinterpret_cast<float4*>(z_zero + (size_t)z * H)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int z = 0; z < ZMAX; ++z)
+                        if (z < ZZ) reinterpret_cast<float4*>(z_zero + (size_t)z * H)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
         }
@@ -514,7 +516,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     // the step's token state, loaded beside the residual (used after the norm)
     const int ok_raw = __ldcg(a.tok_ok);
     const int pos_raw = __ldcg(a.tok_pos);
-    rn.apply<ZSLOTS, ZSLOTS>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red, a.status);
+    rn.apply<ZSLOTS>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, g * C + r, a.NKV * C, s_xh, s_red, a.status,
+                     a.zs, a.zs);
 
     const int ok = ok_raw;
     const int pos = ok ? pos_raw : 0;
@@ -970,7 +973,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
     pdl_trigger();
     pdl_wait();
 
-    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status);
+    rn.apply<1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status, 1, 1);
     XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
 
@@ -1040,7 +1043,7 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
             }
         }
     }
-    float* z_acc = a.z_acc + (size_t)(blockIdx.x % ZSLOTS) * H;
+    float* z_acc = a.z_acc + (size_t)(blockIdx.x % a.zs) * H;
     if (halves) {   // the second half's sums join the first half's
         if (part == 1 && tid < 2 * H8) {
             reinterpret_cast<float4*>(s_y)[2 * hgp] = make_float4(y[0][0], y[0][1], y[0][2], y[0][3]);
@@ -1139,7 +1142,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
     }
     pdl_wait();
 
-    rn.apply<1, 1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status);
+    rn.apply<1>(a.x_in, a.z_in, a.x_out, a.z_zero, a.eps, H, blockIdx.x, gridDim.x, s_xh, s_red, a.status, 1, 1);
     XRegs<XI> xr;
     xr.load(s_xh + c0 * 8, c1 - c0);
     if (nf > 0 && !mbar_wait(&bar[0], 0)) s_err = 1;
@@ -1188,7 +1191,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1) k_fused_mlp_res(FusedMlpArgs a)
         yo[1] = make_float4(y[4], y[5], y[6], y[7]);
     }
     __syncthreads();
-    float* z_acc = a.z_acc + (size_t)(blockIdx.x % ZSLOTS) * H;
+    float* z_acc = a.z_acc + (size_t)(blockIdx.x % a.zs) * H;
     if (nf > 0)
         for (int i = tid; i < H / 4; i += FR_THREADS) {
             float4 t = reinterpret_cast<const float4*>(s_y)[i];
@@ -1260,6 +1263,7 @@ static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int nu
             if (smem_a <= optin - 4096 && smem_m <= optin - 1024 && smem_a + smem_m > 228 * 1024 &&
                 smem_a > 116 * 1024) {
                 p.part = true;
+                p.zs = ZSLOTS;
                 p.mlp_delay_ns = 2000;
                 p.smem_attn = smem_a;
                 p.smem_mlp = smem_m;
@@ -1295,6 +1299,7 @@ static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int nu
             p.mlp_grid = (n_chunks + cpc - 1) / cpc;
             p.smem_mlp = smem;
             p.resident = true;
+            p.zs = ZSLOTS;
             p.pf_late = C * NKV < p.mlp_grid ? C * NKV : 0;
             break;
         }

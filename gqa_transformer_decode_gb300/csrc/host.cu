@@ -893,6 +893,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             a.k_norm = c.qk_norm ? L.k_norm : nullptr;
             a.wo = L.woG;
             a.qkv_exp = L.e_qkv;
+            a.zs = fp.zs;
             a.o_exp = L.e_o;
             a.H = c.hidden;
             a.NH = c.n_heads;
@@ -921,6 +922,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             FusedMlpArgs f{};
             f.wgu = L.wgu;
             f.gu_exp = L.e_gu;
+            f.zs = fp.zs;
             f.d_exp = L.e_d;
             f.wdT = L.wdT;
             f.norm_w = L.mlp_norm;
@@ -941,7 +943,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
         g.K = c.hidden;
         g.x = m->fx[(n - 1) % 2];
         g.x_add = m->fz[(n - 1) % 3];
-        g.x_add_slots = ZSLOTS;
+        g.x_add_slots = m->fp.zs;
         g.ldx = c.hidden;
         g.norm_w = m->final_norm;
         g.eps = eps;

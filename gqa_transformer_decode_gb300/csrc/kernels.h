@@ -301,6 +301,7 @@ struct FusedPlan {
     int mlp_grid = 0;
     bool resident = false;   // every MLP CTA's chunks fit its shared memory (ns = chunks per CTA)
     bool part = false;       // partitioned: attention and MLP blocks on disjoint SMs, all weights resident
+    int zs = ZSLOTS;         // copies of the MLP block's split-K accumulator (1..ZSLOTS)
     int mlp_delay_ns = 0;    // partitioned: MLP weight copies start this long after the CTA arrives
     int pf_late = 0;         // CTAs whose chunks the first CTAs prefetch to L2 (resident plan)
     bool ok = false;
@@ -332,6 +333,7 @@ struct FusedAttnArgs {
     const int32_t* cursor;       // [max_seqs] the cache's cursors
     int resident;                // resident plan: o_proj rows and two K/V tiles loaded before the wait
     int qkv_exp, o_exp;          // storage scales of wqkv / wo (2^-e), undone on the products
+    int zs;                      // accumulator copies the MLP block before this one added into
     const float* cos_t;
     const float* sin_t;
     int* status;
@@ -357,6 +359,7 @@ struct FusedMlpArgs {
     int pf_late;                 // the first pf_late CTAs prefetch the last pf_late CTAs' chunks to L2
     int load_delay_ns;           // partitioned plan: delay of the weight copies after the CTA arrives
     int gu_exp, d_exp;           // storage scales of wgu / wdT (2^-e), undone on the products
+    int zs;                      // accumulator copies to add into (CTA index % zs)
 };
 void launch_fused_mlp(const FusedMlpArgs& a, int fc, int xi, int grid, int smem, cudaStream_t s);
 // One bounded mbarrier wait that nothing completes (which: 0 the CTA wait,
