@@ -318,8 +318,10 @@ def decode_family_bytes(shape, B: int, ctx: int) -> dict:
 # a kernel without an entry reports null.
 NCU_TRAFFIC = {}
 # The same counters summed over the launches of one decode step (workload ->
-# bytes); null without a capture of the current kernels.
-NCU_STEP_TRAFFIC = {}
+# bytes), from an ncu capture of this build's kernels (dram__bytes_read.sum +
+# dram__bytes_write.sum of every launch in the "decode/" range, one step of
+# 51 launches); a workload without a capture of the current kernels reports null.
+NCU_STEP_TRAFFIC = {"qwen2.5-0.5b": 995974866}
 
 
 def decode_roofline(job, hbm_peak):
