@@ -138,6 +138,75 @@ void orc_rope_store_bf16_f32(const float *x, int n_heads, int head_dim,
     }
 }
 
+/* IEEE half (f16) bits of an f32 value, nearest even, with subnormals and
+ * overflow to infinity; and the exact f32 value of an f16 bit pattern. */
+uint16_t orc_f16_round(float x) {
+    if (isnan(x)) return 0x7E00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs((double)x);
+    if (isinf(a)) return sign | 0x7C00;
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);             /* a in [2^(e-1), 2^e) */
+    int qexp = e - 11;              /* weight of the last kept bit (11 significant bits) */
+    if (qexp < -24) qexp = -24;     /* f16 subnormal spacing 2^-24 */
+    double r = rint(ldexp(a, -qexp));
+    double y = ldexp(r, qexp);
+    if (y >= 65520.0) return sign | 0x7C00;   /* rounds past 65504 */
+    if (y == 0.0) return sign;
+    int ye;
+    double m = frexp(y, &ye);       /* y = m * 2^ye, m in [0.5, 1) */
+    if (ye - 1 < -14)               /* subnormal: y = k * 2^-24 */
+        return sign | (uint16_t)ldexp(y, 24);
+    return sign | (uint16_t)(((ye - 1 + 15) << 10) | ((uint16_t)ldexp(m * 2.0 - 1.0, 10) & 0x3FF));
+}
+
+float orc_f16_decode(uint16_t h) {
+    int s = h >> 15, ex = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (ex == 0) v = ldexp((double)m, -24);
+    else if (ex == 31) v = m ? NAN : INFINITY;
+    else v = ldexp(1.0 + m / 1024.0, ex - 15);
+    return (float)(s ? -v : v);
+}
+
+/* [EI] q8_0 block quantization: a block encodes 32 values in 34 bytes -- a
+ * little-endian f16 scale d, then 32 signed int8 codes q; value j is q_j * d
+ * (the pages' decoding loop). */
+void orc_q8_0_dequant(const uint8_t *src, long n_blocks, float *dst) {
+    for (long i = 0; i < n_blocks; ++i) {
+        const uint8_t *b = src + i * 34;
+        const float d = orc_f16_decode((uint16_t)(b[0] | (b[1] << 8)));
+        for (int j = 0; j < 32; ++j) dst[i * 32 + j] = (float)(int8_t)b[2 + j] * d;
+    }
+}
+
+/* The encoder, which the pages do not print (their weights arrive quantized):
+ * per block, amax = max |x|, d = amax / 127 in f32, stored as f16 (nearest
+ * even); q_j = x_j / d in f32 rounded to the nearest integer (ties to even),
+ * clamped to [-127, 127]; a block of zeros has d = 0 and q = 0. */
+void orc_q8_0_quantize(const float *x, long n, uint8_t *dst) {
+    for (long i = 0; i < n / 32; ++i) {
+        const float *xb = x + i * 32;
+        float amax = 0.f;
+        for (int j = 0; j < 32; ++j) {
+            const float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        const float d = amax / 127.0f;
+        const uint16_t dh = orc_f16_round(d);
+        uint8_t *b = dst + i * 34;
+        b[0] = (uint8_t)(dh & 0xFF);
+        b[1] = (uint8_t)(dh >> 8);
+        for (int j = 0; j < 32; ++j) {
+            float q = d > 0.f ? rintf(xb[j] / d) : 0.f;
+            if (q > 127.f) q = 127.f;
+            if (q < -127.f) q = -127.f;
+            b[2 + j] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
 /* [EI] softmax: subtract the row maximum before exponentiating; a row whose
  * maximum is -inf (every entry masked) becomes the uniform distribution. */
 void orc_softmax(double *s, int n) {

@@ -109,6 +109,15 @@ void   orc_rope_store_bf16_f32(const float *x /*[n_heads*D]*/, int n_heads, int 
                                const float *cos_t, const float *sin_t /*[D/2] at pos*/,
                                uint16_t *out);
 
+/* f16 (IEEE half) bits of an f32 value, nearest even; the f32 value of f16 bits. */
+uint16_t orc_f16_round(float x);
+float    orc_f16_decode(uint16_t h);
+/* [EI] q8_0: 34-byte blocks (little-endian f16 scale d, 32 int8 codes q),
+ * value q * d.  quantize: d = amax / 127 (f32) stored as f16, q = nearest
+ * integer (ties even) of x / d in f32, clamped to +-127; n a multiple of 32. */
+void     orc_q8_0_dequant(const uint8_t *src, long n_blocks, float *dst);
+void     orc_q8_0_quantize(const float *x, long n, uint8_t *dst);
+
 /* ---- whole forward ------------------------------------------------------ */
 int  orc_validate(const orc_config *cfg);      /* 0 ok, <0 error ([FH] validate) */
 

@@ -67,6 +67,12 @@ def lib():
         L.orc_forward_full.argtypes = [C.POINTER(OrcModel), P, C.c_int, P, P, P]
         L.orc_forward_activations.argtypes = [C.POINTER(OrcModel), P, C.c_int, P, P]
         L.orc_mean_pooled_head.argtypes = [P, C.c_int, C.c_int, P, P, C.c_int, P]
+        L.orc_f16_round.argtypes = [C.c_float]
+        L.orc_f16_round.restype = C.c_uint16
+        L.orc_f16_decode.argtypes = [C.c_uint16]
+        L.orc_f16_decode.restype = C.c_float
+        L.orc_q8_0_dequant.argtypes = [P, C.c_long, P]
+        L.orc_q8_0_quantize.argtypes = [P, C.c_long, P]
         L.orc_cache_new.argtypes = [C.POINTER(OrcConfig), C.c_int, C.c_int]
         L.orc_cache_new.restype = C.POINTER(OrcCache)
         L.orc_cache_free.argtypes = [C.POINTER(OrcCache)]
@@ -171,6 +177,31 @@ def attention(q, k, v, n_heads, n_kv_heads, head_dim, n_keys=None):
     out = np.empty(n_heads * head_dim, dtype=np.float64)
     lib().orc_attention(_p(q), _p(k), _p(v), n_heads, n_kv_heads, head_dim, S * head_dim,
                         int(n_keys), _p(out))
+    return out
+
+
+def f16_round(x: float) -> int:
+    return int(lib().orc_f16_round(float(x)))
+
+
+def f16_decode(h: int) -> float:
+    return float(lib().orc_f16_decode(int(h)))
+
+
+def q8_0_quantize(x) -> np.ndarray:
+    """[EI] q8_0 blocks (uint8 [n/32, 34]) of f32 values x (n a multiple of 32)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    assert x.size % 32 == 0
+    out = np.empty((x.size // 32, 34), dtype=np.uint8)
+    lib().orc_q8_0_quantize(_p(x), x.size, _p(out))
+    return out
+
+
+def q8_0_dequant(blocks) -> np.ndarray:
+    """f32 values of q8_0 blocks (uint8 [n_blocks, 34])."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 34)
+    out = np.empty(b.shape[0] * 32, dtype=np.float32)
+    lib().orc_q8_0_dequant(_p(b), b.shape[0], _p(out))
     return out
 
 
