@@ -77,23 +77,64 @@ void launch_embed(const EmbedArgs& a, cudaStream_t s) {
 constexpr int GEMV_THREADS = 256;
 constexpr int GEMV_MAXJ = 8;
 
+// Weight formats of the GEMV: bf16, f16, or q8_0 ("ember internals" q8_0
+// block quantization: 32 int8 codes per f16 scale d, value q * d; stored here
+// as codes [N][K] and scales [N][K/32]).  A unit is 8 consecutive weights of
+// a row: 16 bytes of bf16 / f16, 8 bytes of codes.
+enum { WF_BF16 = 0, WF_F16 = 1, WF_Q8 = 2 };
+
+__device__ __forceinline__ uint2 ld_stream8(const uint2* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
 // Issue the weight loads of one row tile (immutable data: may run before
 // the predecessor kernel has finished).
-template <int TPR>
+template <int TPR, int WF>
 __device__ __forceinline__ void gemv_load_tile(const GemvArgs& a, int tile, int r, int sub, int K8,
-                                               uint4 (&w)[GEMV_MAXJ]) {
+                                               uint4 (&w)[GEMV_MAXJ], float (&sc)[GEMV_MAXJ]) {
     constexpr int R = GEMV_THREADS / TPR;
     const int row = tile * R + r;
     if (row >= a.N) return;
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.W + (size_t)row * a.K);
+    if (WF == WF_Q8) {
+        const uint2* qrow = reinterpret_cast<const uint2*>(a.Wq + (size_t)row * a.K);
+        const __half* drow = reinterpret_cast<const __half*>(a.Wd) + (size_t)row * (a.K / 32);
 #pragma unroll
-    for (int j = 0; j < GEMV_MAXJ; ++j) {
-        const int c = sub + j * TPR;
-        if (c < K8) w[j] = ld_stream(wrow + c);
+        for (int j = 0; j < GEMV_MAXJ; ++j) {
+            const int c = sub + j * TPR;
+            if (c < K8) {
+                const uint2 q = ld_stream8(qrow + c);
+                w[j].x = q.x;
+                w[j].y = q.y;
+                sc[j] = __half2float(__ldg(drow + (c >> 2)));
+            }
+        }
+    } else {
+        const uint4* wrow = reinterpret_cast<const uint4*>(a.W + (size_t)row * a.K);
+#pragma unroll
+        for (int j = 0; j < GEMV_MAXJ; ++j) {
+            const int c = sub + j * TPR;
+            if (c < K8) w[j] = ld_stream(wrow + c);
+        }
     }
 }
 
-template <int TPR, int NB, bool WF16, bool XA = false>
+// the 8 weights of a unit as f32 (q8_0: code times the block's scale, exact)
+template <int WF>
+__device__ __forceinline__ void gemv_unpack(const uint4& w, float scale, float* f) {
+    if (WF == WF_Q8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[i] = (float)(int8_t)((w.x >> (8 * i)) & 0xFF) * scale;
+            f[4 + i] = (float)(int8_t)((w.y >> (8 * i)) & 0xFF) * scale;
+        }
+    } else {
+        unpack8w<WF == WF_F16>(w, f);
+    }
+}
+
+template <int TPR, int NB, int WF, bool XA = false>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     constexpr int R = GEMV_THREADS / TPR;
     constexpr int GL = TPR < 32 ? TPR : 32;       // lanes reduced by shuffles
@@ -113,7 +154,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
     // The first tile's weights stream in while the previous kernel drains.
     uint4 w[GEMV_MAXJ];
     int tile = blockIdx.x;
-    if (tile < n_tiles) gemv_load_tile<TPR>(a, tile, r, sub, K8, w);
+    float wsc[GEMV_MAXJ];   // q8_0: the scale of each unit's block
+#pragma unroll
+    for (int j = 0; j < GEMV_MAXJ; ++j) wsc[j] = 0.f;
+    if (tile < n_tiles) gemv_load_tile<TPR, WF>(a, tile, r, sub, K8, w, wsc);
     pdl_wait();
     // XA (one row): the normalised input rmsnorm(x + x_add) = (x + x_add) *
     // norm_w / rms staged once in shared memory, so that the tile loop reads
@@ -174,7 +218,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
             const int c = sub + j * TPR;
             if (rv && c < K8) {
                 float wf[8];
-                unpack8w<WF16>(w[j], wf);
+                gemv_unpack<WF>(w[j], wsc[j], wf);
                 if (wnorm) {
                     const float4 n0 = reinterpret_cast<const float4*>(a.norm_w)[2 * c];
                     const float4 n1 = reinterpret_cast<const float4*>(a.norm_w)[2 * c + 1];
@@ -198,7 +242,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv(GemvArgs a) {
             }
         }
         // next tile's weights fly during this tile's reduction and epilogue
-        if (tile + (int)gridDim.x < n_tiles) gemv_load_tile<TPR>(a, tile + gridDim.x, r, sub, K8, w);
+        if (tile + (int)gridDim.x < n_tiles) gemv_load_tile<TPR, WF>(a, tile + gridDim.x, r, sub, K8, w, wsc);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
 #pragma unroll
@@ -261,17 +305,23 @@ template <int TPR>
 static cudaError_t gemv_nb(const GemvArgs& a, cudaStream_t s, int grid) {
     const dim3 g(grid), b(GEMV_THREADS);
     if (a.x_add)   // batch-1 head over a residual held as two buffers (K <= 12288)
-        return launch_k(k_gemv<TPR, 1, false, true>, g, b, (size_t)a.K * 4, s, a);
-    if (a.w_f16) {
-        if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, true>, g, b, 0, s, a);
-        if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, true>, g, b, 0, s, a);
-        if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, true>, g, b, 0, s, a);
-        return launch_k(k_gemv<TPR, 8, true>, g, b, 0, s, a);
+        return launch_k(k_gemv<TPR, 1, WF_BF16, true>, g, b, (size_t)a.K * 4, s, a);
+    if (a.Wq) {
+        if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, WF_Q8>, g, b, 0, s, a);
+        if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, WF_Q8>, g, b, 0, s, a);
+        if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, WF_Q8>, g, b, 0, s, a);
+        return launch_k(k_gemv<TPR, 8, WF_Q8>, g, b, 0, s, a);
     }
-    if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, false>, g, b, 0, s, a);
-    if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, false>, g, b, 0, s, a);
-    if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, false>, g, b, 0, s, a);
-    return launch_k(k_gemv<TPR, 8, false>, g, b, 0, s, a);
+    if (a.w_f16) {
+        if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, WF_F16>, g, b, 0, s, a);
+        if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, WF_F16>, g, b, 0, s, a);
+        if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, WF_F16>, g, b, 0, s, a);
+        return launch_k(k_gemv<TPR, 8, WF_F16>, g, b, 0, s, a);
+    }
+    if (a.nb <= 1) return launch_k(k_gemv<TPR, 1, WF_BF16>, g, b, 0, s, a);
+    if (a.nb <= 2) return launch_k(k_gemv<TPR, 2, WF_BF16>, g, b, 0, s, a);
+    if (a.nb <= 4) return launch_k(k_gemv<TPR, 4, WF_BF16>, g, b, 0, s, a);
+    return launch_k(k_gemv<TPR, 8, WF_BF16>, g, b, 0, s, a);
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, int num_sms) {
@@ -627,6 +677,42 @@ void launch_bf16_to_f16_inplace(uint16_t* p, long long n, int exp, cudaStream_t 
     count_launches(1);
     long long blocks = (n + 255) / 256;
     k_bf16_to_f16<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(p, n, std::ldexp(1.f, -exp));
+}
+
+// q8_0 block quantization of n bf16 values (n % 32 == 0), one warp per block
+// of 32: amax = max |x|; the codes are x / (amax / 127) in f32 rounded to the
+// nearest integer (ties to even) and clamped to [-127, 127], zero for a block
+// of zeros; the block's scale is amax / 127 stored as f16 (nearest even).
+// Decoding is q * d ("ember internals", q8_0 block format).  With f16_out
+// set, the decoded value times f16_scale is written there as f16 (in place of
+// the bf16 input when f16_out == p): the tensor-core GEMMs' copy of the
+// quantized matrix.
+__global__ void k_q8_0_quantize(const uint16_t* p, long long n, int8_t* q, uint16_t* d, uint16_t* f16_out,
+                                float f16_scale) {
+    const long long stride = (long long)gridDim.x * blockDim.x;   // a multiple of 32
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
+        // n % 32 == 0: the 32 lanes of a warp are all in range or all out
+        const float x = bf16_to_f32(p[i]);
+        float amax = fabsf(x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
+        const float d32 = __fdiv_rn(amax, 127.f);
+        float c = d32 > 0.f ? rintf(__fdiv_rn(x, d32)) : 0.f;
+        c = fminf(fmaxf(c, -127.f), 127.f);
+        q[i] = (int8_t)c;
+        const __half dh = __float2half_rn(d32);
+        if ((threadIdx.x & 31) == 0) d[i >> 5] = __half_as_ushort(dh);
+        if (f16_out) f16_out[i] = f32_to_f16(c * __half2float(dh) * f16_scale);
+    }
+}
+
+void launch_q8_0_quantize(const uint16_t* p, long long n, int8_t* q, uint16_t* d, uint16_t* f16_out,
+                          int f16_exp, cudaStream_t s) {
+    if (n <= 0) return;
+    count_launches(1);
+    long long blocks = (n + 255) / 256;
+    k_q8_0_quantize<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(p, n, q, d, f16_out,
+                                                                         std::ldexp(1.f, -f16_exp));
 }
 
 // out = max |p[i]| over n bf16 values, as f32 bits (non-negative floats order

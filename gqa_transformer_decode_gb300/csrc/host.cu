@@ -109,6 +109,10 @@ struct LayerDev {
     // storage scales 2^-e of wqkv, wo, wgu, wd: e > 0 only for a matrix whose
     // bf16 values exceed the f16 range (its products are multiplied by 2^e)
     int e_qkv = 0, e_o = 0, e_gu = 0, e_d = 0;
+    // q8_0 copies (weights_q8): codes [N][K] and f16 scales [N][K/32] of the
+    // same four matrices, read by the decode GEMVs
+    int8_t *q_qkv = nullptr, *q_o = nullptr, *q_gu = nullptr, *q_d = nullptr;
+    uint16_t *d_qkv = nullptr, *d_o = nullptr, *d_gu = nullptr, *d_d = nullptr;
 };
 
 struct GraphEntry {
@@ -220,6 +224,9 @@ static ember_status validate(const ember_config* c) {
         return fail(EMBER_ERR_INVALID_ARG, "invalid llama3 rope scaling");
     if (c->n_labels < 0 || c->max_tokens < 0 || c->max_positions < 0)
         return fail(EMBER_ERR_INVALID_ARG, "negative n_labels / max_tokens / max_positions");
+    if (c->weights_q8 != 0 && c->weights_q8 != 1) return fail(EMBER_ERR_INVALID_ARG, "weights_q8 must be 0 or 1");
+    if (c->weights_q8 && (c->hidden % 32 || c->ff % 32 || (c->n_heads * c->head_dim) % 32))
+        return fail(EMBER_ERR_UNSUPPORTED, "weights_q8 needs hidden, ff and n_heads*head_dim to be multiples of 32");
     return EMBER_OK;
 }
 
@@ -268,7 +275,9 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
     m->layers.resize(c.layers);
-    if (c.causal && !(getenv("EMBER_NO_FUSED") && atoi(getenv("EMBER_NO_FUSED"))))
+    // the fused batch-1 kernels stream f16 weights only: q8_0 models decode
+    // batch 1 through the q8_0 GEMVs
+    if (c.causal && !c.weights_q8 && !(getenv("EMBER_NO_FUSED") && atoi(getenv("EMBER_NO_FUSED"))))
         fused_decode_plan(m->fp, H, c.n_heads, NKV, D, F, m->sms);
     if (getenv("EMBER_VERBOSE") && atoi(getenv("EMBER_VERBOSE")))
         fprintf(stderr, "ember: fused batch-1 decode %s%s (%s, attention smem %d, MLP grid %d smem %d fc %d ns %d)\n",
@@ -292,6 +301,16 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
         if (m->fp.ok) {
             wa.add(&L.wdT, (size_t)F * H);
             wa.add(&L.woG, (size_t)H * m->q);
+        }
+        if (c.weights_q8) {
+            wa.add(&L.q_qkv, (size_t)m->qkv_n * H);
+            wa.add(&L.q_o, (size_t)H * m->q);
+            wa.add(&L.q_gu, (size_t)2 * F * H);
+            wa.add(&L.q_d, (size_t)H * F);
+            wa.add(&L.d_qkv, (size_t)m->qkv_n * H / 32);
+            wa.add(&L.d_o, (size_t)H * m->q / 32);
+            wa.add(&L.d_gu, (size_t)2 * F * H / 32);
+            wa.add(&L.d_d, (size_t)H * F / 32);
         }
         wa.add(&L.attn_norm, H);
         wa.add(&L.mlp_norm, H);
@@ -394,9 +413,21 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     }
     if (e == cudaSuccess) e = cudaMemcpy(h_max.data(), d_max, h_max.size() * sizeof(unsigned), cudaMemcpyDeviceToHost);
     if (d_max) cudaFree(d_max);
-    auto exp_for = [](unsigned bits) {
+    // q8_0: the decoded values reach 127 * f16(amax / 127) <= amax * (1 + 2^-11)
+    const float grow = c.weights_q8 ? 1.f + 1.f / 1024.f : 1.f;
+    if (c.weights_q8) {
+        for (unsigned bits : h_max) {
+            float v;
+            std::memcpy(&v, &bits, 4);
+            if (!(v / 127.f <= 65504.f))
+                return cleanup(fail(EMBER_ERR_UNSUPPORTED,
+                                    "weights_q8: a layer weight of magnitude %g has a q8_0 scale beyond f16", v));
+        }
+    }
+    auto exp_for = [grow](unsigned bits) {
         float v;
         std::memcpy(&v, &bits, 4);
+        v *= grow;
         int ex = 0;
         while (v > 65504.f && ex < 126) {
             v *= 0.5f;
@@ -411,11 +442,18 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
         L.e_o = exp_for(h_max[4 * l + 1]);
         L.e_gu = exp_for(h_max[4 * l + 2]);
         L.e_d = exp_for(h_max[4 * l + 3]);
-        if (e == cudaSuccess) {
+        if (e == cudaSuccess && c.weights_q8) {   // codes + scales, and f16 of the decoded values
+            launch_q8_0_quantize(L.wqkv, (long long)m->qkv_n * H, L.q_qkv, L.d_qkv, L.wqkv, L.e_qkv, s);
+            launch_q8_0_quantize(L.wo, (long long)H * m->q, L.q_o, L.d_o, L.wo, L.e_o, s);
+            launch_q8_0_quantize(L.wgu, (long long)2 * F * H, L.q_gu, L.d_gu, L.wgu, L.e_gu, s);
+            launch_q8_0_quantize(L.wd, (long long)H * F, L.q_d, L.d_d, L.wd, L.e_d, s);
+        } else if (e == cudaSuccess) {
             launch_bf16_to_f16_inplace(L.wqkv, (long long)m->qkv_n * H, L.e_qkv, s);
             launch_bf16_to_f16_inplace(L.wo, (long long)H * m->q, L.e_o, s);
             launch_bf16_to_f16_inplace(L.wgu, (long long)2 * F * H, L.e_gu, s);
             launch_bf16_to_f16_inplace(L.wd, (long long)H * F, L.e_d, s);
+        }
+        if (e == cudaSuccess) {
             if (L.wdT) launch_transpose16(L.wd, L.wdT, H, F, s);
             if (L.woG) {   // group g's o_proj columns as one [H][G*D] block
                 const size_t gd = (size_t)m->G * D;
@@ -968,6 +1006,14 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
     }
     launch_embed(ea, s);
     const bool gemv = B <= GEMV_MAX_BATCH;
+    // a q8_0 model's GEMVs read its codes and scales (the decoded values,
+    // unscaled) instead of the f16 copy
+    auto q8 = [](GemvArgs& g, const int8_t* q, const uint16_t* d) {
+        if (!q) return;
+        g.Wq = q;
+        g.Wd = d;
+        g.w_exp = 0;
+    };
     // key splits per (token, kv head): the SIMT kernel wants ~8 CTAs per SM;
     // the tensor-core kernel streams best as one wave of long-lived CTAs at
     // 2 per SM (each with a deep copy ring), so it takes the most splits
@@ -983,6 +1029,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             GemvArgs g{};
             g.W = L.wqkv; g.w_f16 = 1;
             g.w_exp = L.e_qkv;
+            q8(g, L.q_qkv, L.d_qkv);
             g.N = m->qkv_n;
             g.K = c.hidden;
             g.x = m->x;
@@ -1043,6 +1090,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             GemvArgs g{};
             g.W = L.wo; g.w_f16 = 1;
             g.w_exp = L.e_o;
+            q8(g, L.q_o, L.d_o);
             g.N = c.hidden;
             g.K = m->q;
             g.x = m->att_f;
@@ -1056,6 +1104,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g = GemvArgs{};
             g.W = L.wgu; g.w_f16 = 1;
             g.w_exp = L.e_gu;
+            q8(g, L.q_gu, L.d_gu);
             g.N = 2 * c.ff;
             g.K = c.hidden;
             g.x = m->x;
@@ -1071,6 +1120,7 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g = GemvArgs{};
             g.W = L.wd; g.w_f16 = 1;
             g.w_exp = L.e_d;
+            q8(g, L.q_d, L.d_d);
             g.N = c.hidden;
             g.K = c.ff;
             g.x = m->act_f;
@@ -1359,6 +1409,42 @@ extern "C" ember_status ember_gemv_bf16(const uint16_t* W, int32_t N, int32_t K,
     CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     GemvArgs g{};
     g.W = W;
+    g.N = N;
+    g.K = K;
+    g.x = x;
+    g.ldx = K;
+    g.out = y;
+    g.ldo = N;
+    g.nb = nb;
+    g.mode = EPI_STORE;
+    launch_gemv(g, (cudaStream_t)stream, sms);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_q8_0_quantize(const uint16_t* w, int64_t n, int8_t* q, uint16_t* d,
+                                           ember_stream_t stream) {
+    if (!w || !q || !d) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (n <= 0 || n % 32) return fail(EMBER_ERR_INVALID_ARG, "n must be a positive multiple of 32");
+    launch_q8_0_quantize(w, n, q, d, nullptr, 0, (cudaStream_t)stream);
+    CK(cudaGetLastError());
+    return EMBER_OK;
+}
+
+extern "C" ember_status ember_gemv_q8_0(const int8_t* q, const uint16_t* d, int32_t N, int32_t K,
+                                        const float* x, int32_t nb, float* y, ember_stream_t stream) {
+    if (!q || !d || !x || !y) return fail(EMBER_ERR_INVALID_ARG, "NULL pointer");
+    if (N <= 0 || K <= 0 || K % 32 || K > 16384 || nb <= 0 || nb > GEMV_MAX_BATCH)
+        return fail(EMBER_ERR_INVALID_ARG, "N, K > 0, K %% 32 == 0, K <= 16384, 1 <= nb <= 8");
+    if ((reinterpret_cast<uintptr_t>(q) & 7) | (reinterpret_cast<uintptr_t>(d) & 1) |
+        (reinterpret_cast<uintptr_t>(x) & 15))
+        return fail(EMBER_ERR_INVALID_ARG, "q must be 8-byte, d 2-byte and x 16-byte aligned");
+    int dev = 0, sms = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    GemvArgs g{};
+    g.Wq = q;
+    g.Wd = d;
     g.N = N;
     g.K = K;
     g.x = x;

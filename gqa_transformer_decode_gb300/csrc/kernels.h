@@ -65,9 +65,11 @@ void launch_embed(const EmbedArgs& a, cudaStream_t s);
 // Batch-1..8 decode projections: y[b][n] = rinv_b * sum_k W[n][k] x[b][k] w_k
 // with the RMSNorm of x fused into the prologue when norm_w != nullptr.
 struct GemvArgs {
-    const uint16_t* W;           // [N][K] bf16, or f16 when w_f16
+    const uint16_t* W;           // [N][K] bf16, or f16 when w_f16 (unused when Wq is set)
     int N, K;
     int w_f16;
+    const int8_t* Wq;            // q8_0 weights: codes [N][K] (K % 32 == 0), or nullptr
+    const uint16_t* Wd;          // q8_0 scales [N][K/32] (f16 bits)
     const float* x;              // [nb][ldx] f32
     int ldx;
     const float* norm_w;         // [K] f32 or nullptr
@@ -201,6 +203,11 @@ void launch_rope_store(const float* x, int n_tok, int n_heads, int D, const floa
 // bf16 [n] -> f32 [n] (weight repack of norms / biases)
 void launch_bf16_to_f32(const uint16_t* in, float* out, long long n, cudaStream_t s);
 // bf16 bits -> f16 bits in place (weight repack of the layer matrices)
+// q8_0 quantization of n bf16 values at p (n % 32 == 0): codes q[n], f16
+// scales d[n/32]; f16_out (nullable, may be p) receives the f16 of the
+// decoded values times 2^-f16_exp.
+void launch_q8_0_quantize(const uint16_t* p, long long n, int8_t* q, uint16_t* d, uint16_t* f16_out,
+                          int f16_exp, cudaStream_t s);
 void launch_bf16_to_f16_inplace(uint16_t* p, long long n, int exp, cudaStream_t s);
 // *out = max(*out, max |p[i]|) as f32 bits, over n bf16 values (NaN skipped)
 void launch_absmax_bf16(const uint16_t* p, long long n, unsigned* out, cudaStream_t s);

@@ -32,7 +32,8 @@ class ember_config(C.Structure):
                 ("rope_llama3", C.c_int32), ("rs_factor", C.c_double), ("rs_low", C.c_double),
                 ("rs_high", C.c_double), ("rs_orig_max_pos", C.c_int32), ("qkv_bias", C.c_int32),
                 ("qk_norm", C.c_int32), ("causal", C.c_int32), ("n_labels", C.c_int32),
-                ("max_tokens", C.c_int32), ("max_positions", C.c_int32)]
+                ("max_tokens", C.c_int32), ("max_positions", C.c_int32),
+                ("weights_q8", C.c_int32)]
 
 
 LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "bq", "bk", "bv", "q_norm", "k_norm", "wo",
@@ -88,6 +89,8 @@ def load():
         "ember_rope_store": (st, [P, C.c_int32, C.c_int32, C.c_int32, P, P, P, P]),
         "ember_gemm_bf16": (st, [P, P, P, C.c_int32, C.c_int32, C.c_int32, P]),
         "ember_gemv_bf16": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P]),
+        "ember_q8_0_quantize": (st, [P, C.c_int64, P, P, P]),
+        "ember_gemv_q8_0": (st, [P, P, C.c_int32, C.c_int32, P, C.c_int32, P, P]),
         "ember_gemv_argmax_noalloc": (st, [P, C.c_int32, C.c_int32, P, C.c_int32, P, P, P]),
         "ember_sample": (st, [P, C.c_int32, C.c_int32, C.c_int32, C.c_float, C.c_int32, C.c_float, P, P,
                               P]),
@@ -113,7 +116,7 @@ def check(status: int, where: str):
         raise EmberError(status, where, last_error())
 
 
-def make_config(shape, max_tokens: int = 0, max_positions: int = 0) -> ember_config:
+def make_config(shape, max_tokens: int = 0, max_positions: int = 0, weights_q8: int = 0) -> ember_config:
     d = shape if isinstance(shape, dict) else shape.asdict()
     c = ember_config()
     for name, _ in ember_config._fields_:
@@ -121,6 +124,7 @@ def make_config(shape, max_tokens: int = 0, max_positions: int = 0) -> ember_con
             setattr(c, name, d[name])
     c.max_tokens = max_tokens
     c.max_positions = max_positions
+    c.weights_q8 = weights_q8
     return c
 
 
@@ -220,6 +224,14 @@ def ember_gemv_bf16(W, N, K, x, nb, y, stream):
 
 def ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream):
     return load().ember_gemv_argmax_noalloc(W, N, K, x, nb, y, argmax, stream)
+
+
+def ember_q8_0_quantize(w, n, q, d, stream):
+    return load().ember_q8_0_quantize(w, n, q, d, stream)
+
+
+def ember_gemv_q8_0(q, d, N, K, x, nb, y, stream):
+    return load().ember_gemv_q8_0(q, d, N, K, x, nb, y, stream)
 
 
 def ember_sample(logits, B, V, ldl, temperature, top_k, top_p, r, out, stream):

@@ -29,10 +29,10 @@ class Model:
     """One model on the current CUDA device."""
 
     def __init__(self, shape, weights: dict, max_tokens: int = 0, max_positions: int = 0,
-                 device="cuda"):
+                 device="cuda", weights_q8: int = 0):
         self.shape = shape
         self.device = torch.device(device)
-        self.cfg = E.make_config(shape, max_tokens, max_positions)
+        self.cfg = E.make_config(shape, max_tokens, max_positions, weights_q8)
         up = {}
         for name, a in weights.items():
             a = np.ascontiguousarray(a)

@@ -91,6 +91,17 @@ typedef struct ember_config {
     int32_t max_tokens;      /* capacity of one prefill / encode / decode call in
                                 tokens (0 -> 4096); sizes the workspace           */
     int32_t max_positions;   /* RoPE table length for encode (0 -> max_tokens)    */
+    int32_t weights_q8;      /* 1: the layer matrices (q/k/v, o, gate/up, down)
+                                are quantized to q8_0 blocks at model creation
+                                (ember internals, q8_0: 32 int8 codes per f16
+                                scale d, value = code * d; codes = the nearest
+                                integer to w / (amax/127), d = f16(amax/127)) and
+                                every later product uses the decoded values, not
+                                the bf16 inputs.  Needs hidden, ff and
+                                n_heads*head_dim to be multiples of 32 and every
+                                |w| / 127 within the f16 range (else
+                                UNSUPPORTED).  Embedding, head and norms stay as
+                                given.                                           */
 } ember_config;
 
 /* One layer's weights: device pointers to bf16 bit patterns, HuggingFace
@@ -302,6 +313,27 @@ ember_status ember_gemm_bf16(const uint16_t *A, const uint16_t *B, float *D, int
  * prologue / epilogue.  Errors: INVALID_ARG. */
 ember_status ember_gemv_bf16(const uint16_t *W, int32_t N, int32_t K, const float *x, int32_t nb,
                              float *y, ember_stream_t stream);
+
+/* q8_0 block quantization (ember internals, q8_0 block format; the encoder
+ * the pages leave implicit, read as: per block of 32 values amax = max |w|,
+ * codes = w / (amax / 127) in f32 rounded to the nearest integer, ties to
+ * even, clamped to [-127, 127], zero for a zero block; scale = amax / 127
+ * rounded to f16, nearest even) of n bf16 values w (n a positive multiple of
+ * 32).  Writes the int8 codes q[n] and the f16 scales d[n/32] (bit patterns):
+ * the planar form of the pages' 34-byte blocks (scale, then 32 codes), which
+ * this library keeps as two arrays so that the codes stay 8-byte aligned.
+ * It is the quantizer ember_model_create runs for weights_q8.  All pointers
+ * are device pointers owned by the caller.  Errors: INVALID_ARG. */
+ember_status ember_q8_0_quantize(const uint16_t *w, int64_t n, int8_t *q, uint16_t *d,
+                                 ember_stream_t stream);
+
+/* y[b][n] = sum_k (q[n][k] * d[n][k/32]) * x[b][k] for b < nb (nb <= 8): the
+ * split GEMV of ember_gemv_bf16 reading q8_0 weights (codes q int8 [N][K],
+ * f16 scales d [N][K/32] as ember_q8_0_quantize writes them), the decode
+ * projections of a weights_q8 model.  K a multiple of 32, K <= 16384; q
+ * 8-byte and x 16-byte aligned.  Errors: INVALID_ARG. */
+ember_status ember_gemv_q8_0(const int8_t *q, const uint16_t *d, int32_t N, int32_t K,
+                             const float *x, int32_t nb, float *y, ember_stream_t stream);
 
 /* ---- greedy LM head with no allocation ----------------------------------- */
 
