@@ -151,7 +151,7 @@ class DecodeJob:
         m = wl.model
         self.B, self.P, self.S = wl.batch, wl.prompt, wl.steps
         self.stream = stream
-        self.model = R.Model(m, weights, max_tokens=max(self.P, 64))
+        self.model = R.Model(m, weights, max_tokens=max(self.P, 64), weights_q8=wl.weights_q8)
         self.kv = self.model.kv_alloc(self.B, self.P + self.S + 1)
         self.prompts = [torch.as_tensor(synth.prompt_ids(m, self.P, seq=b)).cuda()
                         for b in range(self.B)]
@@ -212,6 +212,8 @@ class DecodeJob:
         (layers + tied head) plus the KV rows read and the new rows written."""
         m = self.wl.model
         weights = 2 * m.params() - 2 * m.hidden   # bf16; final norm not re-read per token
+        if self.wl.weights_q8:   # layer matrices as 34-byte blocks of 32 weights
+            weights -= int((2 - 34 / 32) * m.layers * layer_matrix_params(m))
         kv_tok = m.layers * 2 * m.n_kv_heads * m.head_dim * 2
         return weights + self.B * kv_tok * (ctx_mid + 1)
 
@@ -285,19 +287,30 @@ def _family(name: str) -> str:
     return name.split("<")[0]
 
 
-def decode_family_bytes(shape, B: int, ctx: int) -> dict:
+def layer_matrix_params(shape) -> int:
+    H, D, F = shape.hidden, shape.head_dim, shape.ff
+    return (shape.n_heads + 2 * shape.n_kv_heads) * D * H + H * shape.n_heads * D + 3 * F * H
+
+
+def decode_family_bytes(shape, B: int, ctx: int, q8: bool = False) -> dict:
     """Algorithmic HBM bytes per decode step of each kernel family (weights
-    in bf16, once; K/V rows of ctx keys per sequence and kv head, bf16; the
-    f32 residual stream: read x and z, write x, zero z, accumulate z)."""
+    in bf16, or the layer matrices as q8_0 at 34 bytes per 32 weights, once;
+    K/V rows of ctx keys per sequence and kv head, bf16; the f32 residual
+    stream: read x and z, write x, zero z, accumulate z)."""
     H, D, F, V, L = shape.hidden, shape.head_dim, shape.ff, shape.vocab, shape.layers
     NH, NKV = shape.n_heads, shape.n_kv_heads
-    qkv = (NH + 2 * NKV) * D * H * 2 + (NH + 2 * NKV) * D * 4 * shape.qkv_bias
-    o = H * NH * D * 2
-    mlp = 3 * F * H * 2
+    wb = 34 / 32 if q8 else 2
+    qkv = int((NH + 2 * NKV) * D * H * wb) + (NH + 2 * NKV) * D * 4 * shape.qkv_bias
+    o = int(H * NH * D * wb)
+    mlp = int(3 * F * H * wb)
     kv_read = B * NKV * D * 2 * 2 * ctx
     kv_write = B * NKV * D * 2 * 2
     resid = 5 * B * H * 4
     head = V * H * 2
+    if q8:   # every decode batch of a q8_0 model runs the split GEMVs
+        return {"k_gemv": L * (qkv + o + mlp) + head,
+                "k_attn_decode_mma": L * (kv_read + kv_write),
+                "k_attn_decode": L * (kv_read + kv_write)}
     return {
         # batch-1 fused path: the attention block carries its projections
         "k_fused_attn": L * (qkv + o + kv_read + kv_write + resid),
@@ -340,7 +353,7 @@ def decode_roofline(job, hbm_peak):
         f["n"] += 1
     total = sum(f["us"] for f in fam.values())
     top = max(fam, key=lambda k: fam[k]["us"])
-    nbytes = decode_family_bytes(job.wl.model, job.B, ctx).get(top)
+    nbytes = decode_family_bytes(job.wl.model, job.B, ctx, bool(job.wl.weights_q8)).get(top)
     t = fam[top]
     avg_us = t["us"] / t["n"]
     out = {"kernel": t["name"], "bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
@@ -363,6 +376,9 @@ def decode_roofline(job, hbm_peak):
 
 def decode_step_kernels(job) -> str:
     L = job.wl.model.layers
+    if job.wl.weights_q8:
+        return (f"{L} x (k_gemv q8_0 qkv / o_proj / gate-up / down, k_attn_decode*) + k_gemv LM head, "
+                "argmax fused")
     if job.B == 1:
         return f"{L} x (k_fused_attn, k_fused_mlp*) + k_gemv LM head, argmax fused"
     return f"{L} x (k_gemm_tc projections, k_attn_decode_mma, k_rmsnorm) + k_gemm_tc LM head"
@@ -506,8 +522,8 @@ def measure(wl, weights, args, stream, n_jobs, world, local, pk, headline):
     return rec, job
 
 
-SUB_WORKLOADS = ("llama-3.2-1b", "qwen2.5-0.5b-b64", "qwen3-encoder")
-SUB_JOBS = {"llama-3.2-1b": 3, "qwen2.5-0.5b-b64": 5, "qwen3-encoder": 10}
+SUB_WORKLOADS = ("llama-3.2-1b", "qwen2.5-0.5b-b64", "qwen3-encoder", "qwen2.5-0.5b-q8_0")
+SUB_JOBS = {"llama-3.2-1b": 3, "qwen2.5-0.5b-b64": 5, "qwen3-encoder": 10, "qwen2.5-0.5b-q8_0": 5}
 
 
 def run_gpu(args):
@@ -581,6 +597,8 @@ def oracle_sample(wl: synth.Workload, weights, job=None, steps: int = 4):
     threads, what the sample was)."""
     from oracle import oracle as O
     m = wl.model
+    if wl.weights_q8:   # the values a q8_0 model computes with (not timed)
+        weights = O.q8_0_layer_weights(weights, m.layers)
     om = O.OracleModel(m, weights)
     if m.causal == 0:   # encoder: one sequence's first ENC_SAMPLE tokens
         T = min(wl.prompt, ENC_SAMPLE)

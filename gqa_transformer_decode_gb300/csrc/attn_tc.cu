@@ -2,7 +2,7 @@
 //
 // One CTA = 128 query rows of one query head h (kv head g = h / G: ember
 // internals "grouped-query attention").  Per key tile of 128 keys:
-//   S = Q . K^T                  tcgen05.mma M=128, N=128, K=D  -> TMEM
+//   S = Q . K^T                  tcgen05.mma M=128, N=128, K=D  -> TMEM (f16 Q and K)
 //   softmax rows (online)        8 warps: query row r is two threads, one per 64 score columns
 //   P -> shared memory           f16, the 128-byte-swizzled K-major A operand
 //   O += P . V                   tcgen05.mma (f16) M=128, N=D, K=128, accumulating
@@ -14,12 +14,12 @@
 // f32 overflow, and the result is the same softmax.
 // Causal rows see keys at positions <= their own (LowLlamaBasic reference.py
 // self_attn()); the bidirectional encoder sees every key of its sequence
-// (PII-Tracer-vLLM forward()).  Q rows come from the RoPE'd bf16 queries, K
-// rows from the bf16 cache (or the encoder's K buffer), V through a
-// transposed f16 copy Vt [kv head][D][keys] so that it is K-major for the MMA
-// (bf16 -> f16 is exact for these magnitudes; P in [0, 1] keeps 11 bits
-// instead of bf16's 8).
-// Warp 0: TMA producer (Q once; K and Vt through a ring of 4 stages for
+// (PII-Tracer-vLLM forward()).  Q rows come from the RoPE'd f16 queries; K
+// and V from f16 copies of the bf16 cache (or the encoder's K / V buffers)
+// that k_vt16 writes before the attention: Kh [kv head][keys][D] and the
+// transposed Vt [kv head][D][keys], K-major for the MMA (bf16 -> f16 is exact
+// for these magnitudes; P in [0, 1] keeps 11 bits instead of bf16's 8).
+// Warp 0: TMA producer (Q once; Kh and Vt through a ring of 4 stages for
 // head_dim 64, 2 for 128); warp 1: TMEM allocation and the MMA issuer;
 // warps 2-9: softmax and output.  Every
 // mbarrier wait is bounded; a timeout raises EMBER_ERR_TIMEOUT and the CTA
@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     int* sflag = reinterpret_cast<int*>(bar + 5);   // [0] failed, [1] issued, [2] consumed
     uint64_t* kv_full = bar + 8;    // [NSTG]
     uint64_t* kv_empty = bar + 12;  // [NSTG]
-    uint64_t* kconv = bar + 16;     // [NSTG] K tile of the stage converted to f16
     uint64_t* xb = bar + 20;        // [4] the two softmax halves of a TMEM lane quarter
     __shared__ float s_mx[2][2][AT_BQ];   // [tile parity][half][row] maxima
     __shared__ float s_lh[2][AT_BQ];      // [half][row] final sums
@@ -81,8 +80,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int qt = gridDim.x - 1 - blockIdx.x;        // heaviest (last) query tiles first
     const int h = blockIdx.y, z = blockIdx.z;
     const int g = h / a.G;
-    const int kz = a.kv_z_base + z * a.NKV + g;       // K rows of this kv head
-    const int vz = z * a.NKV + g;                     // Vt rows of this kv head
+    const int vz = z * a.NKV + g;                     // Kh and Vt rows of this kv head
     const int q_first = qt * AT_BQ;                    // first query row within the sequence
     const int q_last = min(a.T_per_seq, q_first + AT_BQ) - 1;
     const int nkt = a.causal ? (a.pos0 + q_last) / AT_BK + 1 : (a.n_keys + AT_BK - 1) / AT_BK;
@@ -92,7 +90,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         for (int s = 0; s < NSTG; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
-            mbar_init(&kconv[s], 1);
         }
         mbar_init(s_full, 1);
         mbar_init(p_full, 256);
@@ -118,71 +115,48 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t tS = tmem, tO = tmem + 128;
     pdl_wait();   // Q, K and Vt are the previous kernels' outputs
 
-    if (warp == 0) {   // ------------------------------- TMA producer + K converter
-        // Up to NSTG tiles are in flight; K arrives as bf16 from the cache and
-        // the whole warp rewrites it in place as f16 (the queries are f16) before
-        // releasing it to the MMA warp; tile j - 1 + NSTG is issued once the
-        // MMAs of tile j - 1 have freed its stage.
-        auto issue = [&](int j) {
-            const int s = j % NSTG;
-            mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
-            for (int kb = 0; kb < L::KB; ++kb)
-                tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
-                            j * AT_BK, kz, &kv_full[s]);
-            for (int kb = 0; kb < 2; ++kb)
-                tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
-                            j * AT_BK + kb * 64, 0, vz, &kv_full[s]);
-        };
-        int issued = 0;
+    if (warp == 0) {   // ------------------------------------------ TMA producer
+        // Up to NSTG tiles are in flight; tile j + NSTG is issued once the
+        // MMAs of tile j have freed its stage.
         if (lane == 0) {
+            auto issue = [&](int j) {
+                const int s = j % NSTG;
+                mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * AT_BK * 128, &tmK, kb * 64,
+                                j * AT_BK, vz, &kv_full[s]);
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
+                                j * AT_BK + kb * 64, 0, vz, &kv_full[s]);
+            };
             const int qrow0 = z * a.T_per_seq + q_first;
             mbar_expect_tx(q_full, L::Q_BYTES);
             for (int kb = 0; kb < L::KB; ++kb)
                 tma_load_2d(sm + L::OFF_Q + kb * AT_BQ * 128, &tmQ, h * D + kb * 64, qrow0, q_full);
+            int issued = 0;
             for (; issued < NSTG && issued < nkt; ++issued) issue(issued);
-        }
-        issued = __shfl_sync(FULL_MASK, issued, 0);
-        bool fail = false;
-        for (int j = 0; j < nkt && !fail; ++j) {
-            const int s = j % NSTG;
-            if (!mbar_wait(&kv_full[s], (uint32_t)(j / NSTG) & 1u)) {
-                fail = true;
-                break;
-            }
-            uint4* kt = reinterpret_cast<uint4*>(sm + L::OFF_K + s * L::K_BYTES);
-            for (int i = lane; i < L::K_BYTES / 16; i += 32) {
-                const uint4 u = kt[i];
-                kt[i] = make_uint4(pack_f16x2(bf16_lo(u.x), bf16_hi(u.x)), pack_f16x2(bf16_lo(u.y), bf16_hi(u.y)),
-                                   pack_f16x2(bf16_lo(u.z), bf16_hi(u.z)), pack_f16x2(bf16_lo(u.w), bf16_hi(u.w)));
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&kconv[s]);
-                if (j >= 1 && j - 1 + NSTG < nkt) {   // stage of tile j - 1 -> tile j - 1 + NSTG
-                    if (!mbar_wait(&kv_empty[(j - 1) % NSTG], (uint32_t)((j - 1) / NSTG) & 1u)) fail = true;
-                    else {
-                        issue(j - 1 + NSTG);
-                        ++issued;
-                    }
+            bool fail = false;
+            for (; issued < nkt; ++issued) {   // stage of tile issued - NSTG -> tile issued
+                const int j = issued - NSTG;
+                if (!mbar_wait(&kv_empty[j % NSTG], (uint32_t)(j / NSTG) & 1u)) {
+                    fail = true;
+                    break;
                 }
+                issue(issued);
             }
-            fail = __shfl_sync(FULL_MASK, (int)fail, 0) != 0;
-        }
-        if (lane == 0) {
             if (fail) sflag[0] = 1;
             sflag[1] = issued;
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ------------------------------------------ MMA issuer
-            constexpr uint32_t idS = idesc_f16(AT_BQ, AT_BK);   // f16 queries, K converted to f16
+            constexpr uint32_t idS = idesc_f16(AT_BQ, AT_BK);   // f16 queries and keys
             constexpr uint32_t idO = idesc_f16(AT_BQ, D);
             bool ok = mbar_wait(q_full, 0);
             int j = 0;
             for (; ok && j < nkt; ++j) {
                 const int s = j % NSTG;
                 const uint32_t u = (uint32_t)(j / NSTG);
-                if (!mbar_wait(&kconv[s], u & 1u)) break;
+                if (!mbar_wait(&kv_full[s], u & 1u)) break;
                 tc_fence_after();
                 const uint32_t q0 = smem_u32(sm + L::OFF_Q);
                 const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);
@@ -359,7 +333,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     __syncthreads();
     if (threadIdx.x == 0 && sflag[0]) raise_status(a.status, EMBER_ERR_TIMEOUT);
     if (warp == 0 && lane == 0 && sflag[0]) {
-        // drain K/V copies issued but never consumed
+        // drain K/V copies issued but never consumed by the MMA warp
         for (int j = sflag[2]; j < sflag[1]; ++j)
             (void)mbar_wait(&kv_full[j % NSTG], (uint32_t)(j / NSTG) & 1u);
     }
@@ -370,7 +344,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
 }
 
-// Vt[z][d][key] = f16(V[z][key][d]); zero past n_keys.
+// Vt[z][d][key] = f16(V[z][key][d]) and Kh[z][key][d] = f16(K[z][key][d]);
+// zero past n_keys.
 __global__ void __launch_bounds__(256) k_vt(VtArgs a) {
     __shared__ uint16_t tile[64][129];   // [key][d], padded
     const int z = blockIdx.y;
@@ -391,6 +366,18 @@ __global__ void __launch_bounds__(256) k_vt(VtArgs a) {
         if (key0 + k < a.keys_pad)
             dst[(size_t)d * a.keys_pad + key0 + k] =
                 __half_as_ushort(__float2half_rn(bf16_to_f32(tile[k][d])));
+    }
+    if (a.kh) {
+        const uint16_t* ks =
+            a.k + (size_t)(z / a.nkv) * a.v_z_stride + (size_t)(z % a.nkv) * a.v_h_stride;
+        uint16_t* kd = a.kh + (size_t)z * a.keys_pad * D;
+        for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
+            const int k = e / D, d = e % D;
+            if (key0 + k < a.keys_pad)
+                kd[(size_t)(key0 + k) * D + d] =
+                    key0 + k < a.n_keys ? __half_as_ushort(__float2half_rn(bf16_to_f32(ks[(size_t)(key0 + k) * D + d])))
+                                        : (uint16_t)0;
+        }
     }
 }
 
@@ -427,6 +414,22 @@ __global__ void __launch_bounds__(256) k_vt16(VtArgs a) {
             w[j] = (uint32_t)tile[8 * kc + 2 * j][d] | ((uint32_t)tile[8 * kc + 2 * j + 1][d] << 16);
         *reinterpret_cast<uint4*>(dst + (size_t)d * a.keys_pad + key0 + 8 * kc) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    if (a.kh) {   // the K rows of the block, converted in 16-byte chunks
+        const uint16_t* ks =
+            a.k + (size_t)(z / a.nkv) * a.v_z_stride + (size_t)(z % a.nkv) * a.v_h_stride;
+        uint16_t* kd = a.kh + (size_t)z * a.keys_pad * D;
+        for (int e = threadIdx.x; e < 64 * C8; e += blockDim.x) {
+            const int k = e / C8, c = e % C8;
+            if (key0 + k >= a.keys_pad) continue;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (key0 + k < a.n_keys) {
+                const uint4 b = *reinterpret_cast<const uint4*>(ks + (size_t)(key0 + k) * D + 8 * c);
+                u = make_uint4(pack_f16x2(bf16_lo(b.x), bf16_hi(b.x)), pack_f16x2(bf16_lo(b.y), bf16_hi(b.y)),
+                               pack_f16x2(bf16_lo(b.z), bf16_hi(b.z)), pack_f16x2(bf16_lo(b.w), bf16_hi(b.w)));
+            }
+            *reinterpret_cast<uint4*>(kd + (size_t)(key0 + k) * D + 8 * c) = u;
+        }
+    }
 }
 
 void launch_vt(const VtArgs& a, int zs, cudaStream_t s) {
@@ -455,7 +458,9 @@ bool attn_tc_supported(int D) { return D == 64 || D == 128; }
 
 void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
                     int nseq, int D, cudaStream_t s) {
-    if (D == 64) launch_at<64>(map_q, map_k, map_vt, a, nseq, s);
+    // more than one query tile per sequence: two tiles per CTA in ping-pong
+    if (D == 64 && a.T_per_seq > AT_BQ) launch_attn_tc2(map_q, map_k, map_vt, a, nseq, s);
+    else if (D == 64) launch_at<64>(map_q, map_k, map_vt, a, nseq, s);
     else if (D == 128) launch_at<128>(map_q, map_k, map_vt, a, nseq, s);
 }
 

@@ -1,0 +1,359 @@
+// attn_tc2.cu -- whole-prompt GQA attention for head_dim 64 on the tcgen05
+// tensor cores, two query tiles per CTA in ping-pong.
+//
+// The same computation as k_attn_tc (attn_tc.cu): per key tile of 128 keys,
+// S = Q . K^T into TMEM, the online softmax of each query row, P (f16) to
+// shared memory and O += P . V accumulated in TMEM, with the lazy rescaling
+// of O and l when a row's maximum moves by more than 2^8.  What differs is
+// the schedule.  One CTA holds two 128-row query tiles A and B of one head,
+// each with its own four softmax warps (one thread per query row, all 128
+// score columns), its own S and O columns of TMEM and its own P buffer, and
+// the MMA warp interleaves them:
+//     PV_A(j), S_A(j+1)   while the B warps turn S_B(j) into P_B(j)
+//     PV_B(j), S_B(j+1)   while the A warps turn S_A(j+1) into P_A(j+1)
+// so the tensor cores work on one tile while the CUDA cores exponentiate the
+// other (with one tile per CTA the two alternate and each idles while the
+// other runs).  Both tiles walk the key tiles of tile B (the later one); the
+// causal mask zeroes tile A's share of the last one.
+// Warp 0: TMA producer (f16 Q, the f16 copy Kh of the keys and the
+// transposed Vt, as k_attn_tc reads them); warp 1:
+// TMEM allocation and MMA issue; warps 2-5: tile A; warps 6-9: tile B (a
+// warp reads the TMEM lanes of its index mod 4, so each group of four covers
+// its tile's 128 rows).  Every mbarrier wait is bounded; a timeout raises
+// EMBER_ERR_TIMEOUT and the CTA drains its copies and frees TMEM.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace ember {
+
+namespace {
+
+constexpr int P2_THREADS = 320;
+constexpr int P2_BQ = 128;    // query rows per tile (two tiles per CTA)
+constexpr int P2_BK = 128;    // keys per tile
+constexpr int P2_D = 64;
+
+struct P2Smem {
+    static constexpr int TILE = P2_BQ * 128;            // 128 rows x 64 f16 (one swizzled block)
+    static constexpr int NSTG = 3;                      // K/V ring stages
+    static constexpr int K_BYTES = P2_BK * 128;         // 128 keys x 64 f16
+    static constexpr int V_BLOCK = P2_D * 128;          // [64 dims][64 keys] f16
+    static constexpr int V_BYTES = 2 * V_BLOCK;         // 128 keys
+    static constexpr int P_BYTES = 2 * P2_BQ * 128;     // [128 rows][128 keys] f16
+    static constexpr int OFF_Q = 0;                     // Q_A, Q_B
+    static constexpr int OFF_K = OFF_Q + 2 * TILE;
+    static constexpr int OFF_V = OFF_K + NSTG * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NSTG * V_BYTES;   // P_A, P_B
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int TOTAL = OFF_BAR + 256 + 1024;     // + barriers, + alignment slack
+    static constexpr uint32_t TMEM_COLS = 512;             // S_A, S_B (128 each), O_A, O_B (64 each)
+};
+
+__global__ void __launch_bounds__(P2_THREADS, 1)
+    k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, AttnTcArgs a) {
+    using L = P2Smem;
+    constexpr int NSTG = L::NSTG;
+    extern __shared__ uint8_t p2_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p2_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* q_full = bar + 0;
+    uint64_t* s_full = bar + 1;     // [2] per tile
+    uint64_t* p_full = bar + 3;     // [2]
+    uint64_t* o_full = bar + 5;     // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 7);
+    int* sflag = reinterpret_cast<int*>(bar + 8);   // [0] failed, [1] issued, [2] consumed
+    uint64_t* kv_full = bar + 10;   // [NSTG]
+    uint64_t* kv_empty = bar + 14;  // [NSTG]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pt = gridDim.x - 1 - blockIdx.x;         // heaviest (last) tile pairs first
+    const int h = blockIdx.y, z = blockIdx.z;
+    const int g = h / a.G;
+    const int vz = z * a.NKV + g;                      // Kh and Vt rows of this kv head
+    const int q_first = pt * 2 * P2_BQ;                 // tile A's first row; tile B at + 128
+    const int q_last = min(a.T_per_seq, q_first + 2 * P2_BQ) - 1;
+    const int nkt = a.causal ? (a.pos0 + q_last) / P2_BK + 1 : (a.n_keys + P2_BK - 1) / P2_BK;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_full[t], 1);
+        }
+        for (int s = 0; s < NSTG; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        sflag[0] = 0;
+        sflag[1] = 0;
+        sflag[2] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(L::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // Q, K and Vt are the previous kernels' outputs
+
+    if (warp == 0) {   // ------------------------------------------ TMA producer
+        if (lane == 0) {
+            auto issue = [&](int j) {
+                const int s = j % NSTG;
+                mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
+                tma_load_3d(sm + L::OFF_K + s * L::K_BYTES, &tmK, 0, j * P2_BK, vz, &kv_full[s]);
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
+                                j * P2_BK + kb * 64, 0, vz, &kv_full[s]);
+            };
+            const int qrow0 = z * a.T_per_seq + q_first;
+            mbar_expect_tx(q_full, 2 * L::TILE);
+            for (int t = 0; t < 2; ++t)
+                tma_load_2d(sm + L::OFF_Q + t * L::TILE, &tmQ, h * P2_D, qrow0 + t * P2_BQ, q_full);
+            int issued = 0;
+            for (; issued < NSTG && issued < nkt; ++issued) issue(issued);
+            bool fail = false;
+            for (; issued < nkt; ++issued) {   // stage of tile issued - NSTG -> tile issued
+                const int j = issued - NSTG;
+                if (!mbar_wait(&kv_empty[j % NSTG], (uint32_t)(j / NSTG) & 1u)) {
+                    fail = true;
+                    break;
+                }
+                issue(issued);
+            }
+            if (fail) sflag[0] = 1;
+            sflag[1] = issued;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------ MMA issuer
+            constexpr uint32_t idS = idesc_f16(P2_BQ, P2_BK);
+            constexpr uint32_t idO = idesc_f16(P2_BQ, P2_D);
+            auto mma_s = [&](int t, int s) {   // S_t = Q_t . K(stage s)^T
+                const uint32_t q0 = smem_u32(sm + L::OFF_Q + t * L::TILE);
+                const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_bf16(tmem + t * 128, sdesc_sw128(q0 + k * 32), sdesc_sw128(k0 + k * 32), idS,
+                              k ? 1u : 0u);
+                umma_commit(&s_full[t]);
+            };
+            auto mma_pv = [&](int t, int s, bool acc) {   // O_t += P_t . V(stage s)
+                const uint32_t p0 = smem_u32(sm + L::OFF_P + t * L::P_BYTES);
+                const uint32_t v0 = smem_u32(sm + L::OFF_V + s * L::V_BYTES);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(tmem + 256 + t * P2_D, sdesc_sw128(p0 + kb * P2_BQ * 128 + k * 32),
+                                  sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO,
+                                  (acc || kb || k) ? 1u : 0u);
+                umma_commit(&o_full[t]);
+            };
+            bool ok = mbar_wait(q_full, 0) && (nkt == 0 || mbar_wait(&kv_full[0], 0));
+            int j = 0;
+            if (ok && nkt > 0) {
+                tc_fence_after();
+                mma_s(0, 0);
+                mma_s(1, 0);
+            }
+            for (; ok && j < nkt; ++j) {
+                const int s = j % NSTG;
+                const bool more = j + 1 < nkt;
+                const int s1 = (j + 1) % NSTG;
+                if (!mbar_wait(&p_full[0], (uint32_t)j & 1u)) break;
+                tc_fence_after();
+                mma_pv(0, s, j > 0);
+                if (more) {
+                    if (!mbar_wait(&kv_full[s1], (uint32_t)((j + 1) / NSTG) & 1u)) break;
+                    tc_fence_after();
+                    mma_s(0, s1);
+                }
+                if (!mbar_wait(&p_full[1], (uint32_t)j & 1u)) break;
+                tc_fence_after();
+                mma_pv(1, s, j > 0);
+                umma_commit(&kv_empty[s]);
+                if (more) mma_s(1, s1);
+            }
+            if (!ok || j < nkt) sflag[0] = 1;
+            sflag[2] = j;
+        }
+    } else {   // ------------------------------------------------ softmax warps
+        constexpr float RESCALE = 8.f;
+        const int t = (warp - 2) >> 2;                // query tile: 0 = A, 1 = B
+        const int qw = warp & 3;                      // TMEM lane quarter of this warp
+        const int r = qw * 32 + lane;                 // query row within the tile
+        const int row0 = q_first + t * P2_BQ;         // the tile's first row
+        const int qp = a.pos0 + row0 + r;             // this row's position
+        const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const uint32_t tS = tmem + t * 128 + lane_off;
+        const uint32_t tO = tmem + 256 + t * P2_D + lane_off;
+        const float sc_log2 = 1.4426950408889634f * rsqrtf((float)P2_D);
+        uint8_t* sP = sm + L::OFF_P + t * L::P_BYTES;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        // p = 2^(s - mr) for the row's 128 scores of the tile (masked: 0), 64
+        // columns per TMEM load; P -> shared as two K-major blocks of 64 keys
+        // with the 128-byte swizzle.  Returns the row sum; mt = the tile's
+        // largest visible scaled score.
+        auto emit = [&](float mr, int lim, float& mt) -> float {
+            const float mo = mr == -INFINITY ? 0.f : mr;   // no visible key yet: every p is 0
+            float rs = 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                uint32_t v[64];
+                tmem_ld32(tS + c0, v);
+                tmem_ld32(tS + c0 + 32, v + 32);
+                tmem_ld_wait();
+                uint8_t* rowp = sP + (c0 >> 6) * P2_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int c = q * 8 + i;
+                        const float x0 = c0 + c < lim ? __uint_as_float(v[c]) * sc_log2 : -INFINITY;
+                        const float x1 = c0 + c + 1 < lim ? __uint_as_float(v[c + 1]) * sc_log2 : -INFINITY;
+                        mt = fmaxf(mt, fmaxf(x0, x1));
+                        const float p0 = ex2(x0 - mo), p1 = ex2(x1 - mo);
+                        rs += p0 + p1;
+                        pk[i / 2] = pack_f16x2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+            return rs;
+        };
+        for (int j = 0; j < nkt; ++j) {
+            if (!mbar_wait(&s_full[t], (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int key0 = j * P2_BK;
+            int lim = a.n_keys - key0;                        // keys i < lim of the tile are visible
+            if (a.causal) lim = min(lim, qp - key0 + 1);
+            lim = max(0, min(P2_BK, lim));
+            if (j > 0) {   // PV(j-1) must be complete before O is touched or P is rewritten
+                if (!mbar_wait(&o_full[t], (uint32_t)(j - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            } else {       // the first tile sets the reference maximum
+                float mt = -INFINITY;
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 64) {
+                    uint32_t v[64];
+                    tmem_ld32(tS + c0, v);
+                    tmem_ld32(tS + c0 + 32, v + 32);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (c0 + i < lim) mt = fmaxf(mt, __uint_as_float(v[i]) * sc_log2);
+                }
+                m = mt;
+            }
+            // the reference maximum m moves (and O, l are rescaled) only when
+            // the tile's maximum exceeds it by more than RESCALE (log2 units),
+            // so p stays <= 2^RESCALE (f16-safe); then the tile is redone
+            float mt = -INFINITY;
+            float rs = emit(m, lim, mt);
+            const bool move = mt > m + RESCALE;
+            if (__any_sync(FULL_MASK, move)) {
+                const float mnew = move ? mt : m;
+                const float corr = move ? exp2f(m - mnew) : 1.f;
+                float mt2 = -INFINITY;
+                rs = emit(mnew, lim, mt2);
+                if (j > 0) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < P2_D; c0 += 16) {
+                        uint32_t o[16];
+                        tmem_ld16(tO + c0, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        tmem_st16(tO + c0, o);
+                    }
+                    tmem_st_wait();
+                }
+                l *= corr;
+                m = mnew;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+            l += rs;
+        }
+        if (ok && nkt > 0 && !mbar_wait(&o_full[t], (uint32_t)(nkt - 1) & 1u)) ok = false;
+        if (!ok) sflag[0] = 1;
+        tc_fence_after();
+        if (ok) {
+            const float inv = 1.f / l;
+            const bool live = row0 + r < a.T_per_seq;
+            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + row0 + r) * a.ld_att + h * P2_D;
+#pragma unroll
+            for (int c0 = 0; c0 < P2_D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c0, o);
+                tmem_ld_wait();
+                if (live) {
+                    bool bad = false;
+#pragma unroll
+                    for (int d = 0; d < 32; d += 8) {
+                        uint4 w;
+                        w.x = pack_f16x2_chk(__uint_as_float(o[d]) * inv, __uint_as_float(o[d + 1]) * inv, bad);
+                        w.y = pack_f16x2_chk(__uint_as_float(o[d + 2]) * inv, __uint_as_float(o[d + 3]) * inv, bad);
+                        w.z = pack_f16x2_chk(__uint_as_float(o[d + 4]) * inv, __uint_as_float(o[d + 5]) * inv, bad);
+                        w.w = pack_f16x2_chk(__uint_as_float(o[d + 6]) * inv, __uint_as_float(o[d + 7]) * inv, bad);
+                        *reinterpret_cast<uint4*>(out + c0 + d) = w;
+                    }
+                    if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && sflag[0]) raise_status(a.status, EMBER_ERR_TIMEOUT);
+    if (warp == 0 && lane == 0 && sflag[0]) {
+        // drain K/V copies issued but never consumed by the MMA warp
+        for (int j = sflag[2]; j < sflag[1]; ++j)
+            (void)mbar_wait(&kv_full[j % NSTG], (uint32_t)(j / NSTG) & 1u);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(L::TMEM_COLS));
+    }
+}
+
+}  // namespace
+
+void launch_attn_tc2(const void* mq, const void* mk, const void* mv, const AttnTcArgs& a, int nseq,
+                     cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, P2Smem::TOTAL);
+        attr = true;
+    }
+    dim3 grid((a.T_per_seq + 2 * P2_BQ - 1) / (2 * P2_BQ), a.NH, nseq);
+    launch_k(k_attn_tc2, grid, dim3(P2_THREADS), P2Smem::TOTAL, s,
+             *reinterpret_cast<const CUtensorMap*>(mq), *reinterpret_cast<const CUtensorMap*>(mk),
+             *reinterpret_cast<const CUtensorMap*>(mv), a);
+}
+
+}  // namespace ember

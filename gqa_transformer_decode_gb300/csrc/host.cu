@@ -177,6 +177,7 @@ struct ember_model {
     int32_t* tok_pos;
     float *enc_cos = nullptr, *enc_sin = nullptr;
     uint16_t* enc_vt = nullptr;          // transposed V of the encoder batch
+    uint16_t* enc_kh = nullptr;          // f16 K of the encoder batch
     alignas(64) unsigned char q_map[128];   // TMA map over the RoPE'd bf16 queries
     bool q_map_ok = false;
     int enc_positions = 0;
@@ -198,6 +199,7 @@ struct ember_kv {
     int32_t* cursor = nullptr;
     float *cos_t = nullptr, *sin_t = nullptr;
     uint16_t* vt = nullptr;              // transposed V of one layer's kv heads (prefill)
+    uint16_t* kh = nullptr;              // f16 K of one layer's kv heads (prefill)
     alignas(64) unsigned char k_map[128];   // TMA map over the whole K cache, 3-D
     bool k_map_ok = false;
     alignas(64) unsigned char v_map[128];   // the same over the V cache
@@ -345,6 +347,7 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
         aa.add(&m->enc_k, (size_t)T * m->kv);
         aa.add(&m->enc_v, (size_t)T * m->kv);
         aa.add(&m->enc_vt, (size_t)8 * T * m->kv);   // B * round8(T) <= 8 * B * T keys
+        aa.add(&m->enc_kh, (size_t)8 * T * m->kv);
         aa.add(&m->enc_cos, (size_t)m->c.max_positions * (D / 2));
         aa.add(&m->enc_sin, (size_t)m->c.max_positions * (D / 2));
     }
@@ -539,6 +542,8 @@ ember_status ember_kv_alloc(ember_model* m, int32_t max_seqs, int32_t max_len, e
     const int keys_cap = (max_len + 7) / 8 * 8;
     if (e == cudaSuccess && attn_tc_supported(m->c.head_dim))
         e = cudaMalloc(&kv->vt, (size_t)m->c.n_kv_heads * m->c.head_dim * keys_cap * 2);
+    if (e == cudaSuccess && attn_tc_supported(m->c.head_dim))
+        e = cudaMalloc(&kv->kh, (size_t)m->c.n_kv_heads * m->c.head_dim * keys_cap * 2);
     if (e != cudaSuccess) {
         cudaGetLastError();
         ember_kv_free(kv);
@@ -605,6 +610,7 @@ void ember_kv_free(ember_kv* kv) {
     cudaFree(kv->cos_t);
     cudaFree(kv->sin_t);
     cudaFree(kv->vt);
+    cudaFree(kv->kh);
     delete kv;
 }
 
@@ -659,10 +665,10 @@ struct CacheView {
     long long seq_stride, head_stride;
     int T_per_seq, pos0, causal;
     const float *cos_t, *sin_t;
-    // tensor-core attention (head_dim 64 / 128): K map, its z index of (z=0, g=0),
-    // the transposed-V buffer and its map (keys_pad keys per row)
-    const void* k_map = nullptr;
-    int kv_z_base = 0;
+    // tensor-core attention (head_dim 64 / 128): the f16 K and transposed-V
+    // staging buffers and their maps (keys_pad keys per kv head)
+    uint16_t* kh = nullptr;
+    const void* kh_map = nullptr;
     uint16_t* vt = nullptr;
     const void* vt_map = nullptr;
     int keys_pad = 0;
@@ -674,6 +680,14 @@ static bool make_vt_map(void* out, const uint16_t* vt, int keys_pad, int D, int 
     const uint64_t st[2] = {(uint64_t)keys_pad * 2, (uint64_t)keys_pad * D * 2};
     const uint32_t b[3] = {64, (uint32_t)D, 1};
     return encode_map_bf16(out, vt, 3, d, st, b);
+}
+
+// Map over an f16 K buffer [zs][keys_pad][D].
+static bool make_kh_map(void* out, const uint16_t* kh, int keys_pad, int D, int zs) {
+    const uint64_t d[3] = {(uint64_t)D, (uint64_t)keys_pad, (uint64_t)zs};
+    const uint64_t st[2] = {(uint64_t)D * 2, (uint64_t)keys_pad * D * 2};
+    const uint32_t b[3] = {64, 128, 1};
+    return encode_map_bf16(out, kh, 3, d, st, b);
 }
 
 static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStream_t s) {
@@ -708,11 +722,13 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     r.seq_stride = cv.seq_stride;
     r.head_stride = cv.head_stride;
     launch_rope_kv(r, s);
-    if (cv.k_map && cv.vt_map) {   // tensor-core attention
+    if (cv.kh_map && cv.vt_map) {   // tensor-core attention
         const int nseq = n / cv.T_per_seq;
         const int n_keys = cv.pos0 + cv.T_per_seq;
         VtArgs va{};
         va.v = cv.v;
+        va.k = cv.k;
+        va.kh = cv.kh;
         va.v_z_stride = cv.seq_stride;
         va.v_h_stride = cv.head_stride;
         va.nkv = c.n_kv_heads;
@@ -729,11 +745,10 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
         ta.NH = c.n_heads;
         ta.NKV = c.n_kv_heads;
         ta.G = c.n_heads / c.n_kv_heads;
-        ta.kv_z_base = cv.kv_z_base;
         ta.att = m->att_b;
         ta.ld_att = m->q;
         ta.status = m->status;
-        launch_attn_tc(m->q_map, cv.k_map, cv.vt_map, ta, nseq, c.head_dim, s);
+        launch_attn_tc(m->q_map, cv.kh_map, cv.vt_map, ta, nseq, c.head_dim, s);
     } else {
     AttnPrefillArgs a{};
     a.q = m->qr;
@@ -800,15 +815,16 @@ static ember_status prefill_impl(ember_model* m, ember_kv* kv, int32_t seq, cons
     ea.cursor = kv->cursor;
     launch_embed(ea, s);
     const long long head_stride = (long long)kv->max_len * c.head_dim;
-    alignas(64) unsigned char vt_map[128];
+    alignas(64) unsigned char vt_map[128], kh_map[128];
     const int keys_pad = (start_pos + n + 7) / 8 * 8;
-    const bool tc = m->q_map_ok && kv->k_map_ok &&
-                    make_vt_map(vt_map, kv->vt, keys_pad, c.head_dim, c.n_kv_heads);
+    const bool tc = m->q_map_ok && kv->vt && kv->kh &&
+                    make_vt_map(vt_map, kv->vt, keys_pad, c.head_dim, c.n_kv_heads) &&
+                    make_kh_map(kh_map, kv->kh, keys_pad, c.head_dim, c.n_kv_heads);
     for (int l = 0; l < c.layers; ++l) {
         CacheView cv{};
         if (tc) {
-            cv.k_map = kv->k_map;
-            cv.kv_z_base = (seq * c.layers + l) * c.n_kv_heads;
+            cv.kh = kv->kh;
+            cv.kh_map = kh_map;
             cv.vt = kv->vt;
             cv.vt_map = vt_map;
             cv.keys_pad = keys_pad;
@@ -1319,21 +1335,16 @@ extern "C" ember_status ember_encode(ember_model* m, const int32_t* ids, int32_t
     ea.status = m->status;
     ea.pf_seq = -1;
     launch_embed(ea, s);
-    alignas(64) unsigned char k_map[128], vt_map[128];
+    alignas(64) unsigned char kh_map[128], vt_map[128];
     const int keys_pad = (T + 7) / 8 * 8;
-    bool tc = m->q_map_ok;
-    if (tc) {
-        const uint64_t kd[3] = {(uint64_t)c.head_dim, (uint64_t)T, (uint64_t)B * c.n_kv_heads};
-        const uint64_t ks[2] = {(uint64_t)c.head_dim * 2, (uint64_t)T * c.head_dim * 2};
-        const uint32_t kb[3] = {64, 128, 1};
-        tc = encode_map_bf16(k_map, m->enc_k, 3, kd, ks, kb) &&
-             make_vt_map(vt_map, m->enc_vt, keys_pad, c.head_dim, B * c.n_kv_heads);
-    }
+    const bool tc = m->q_map_ok &&
+                    make_kh_map(kh_map, m->enc_kh, keys_pad, c.head_dim, B * c.n_kv_heads) &&
+                    make_vt_map(vt_map, m->enc_vt, keys_pad, c.head_dim, B * c.n_kv_heads);
     for (int l = 0; l < c.layers; ++l) {
         CacheView cv{};
         if (tc) {
-            cv.k_map = k_map;
-            cv.kv_z_base = 0;
+            cv.kh = m->enc_kh;
+            cv.kh_map = kh_map;
             cv.vt = m->enc_vt;
             cv.vt_map = vt_map;
             cv.keys_pad = keys_pad;

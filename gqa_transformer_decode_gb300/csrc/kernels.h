@@ -263,14 +263,14 @@ void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* stat
 
 // ------------------------------------------------ tensor-core attention --
 // Whole-prompt GQA attention on tcgen05 (head_dim 64 or 128).  Maps: Q over
-// the bf16 queries [rows][NH*D] (box 64 x 128); K over K rows [z][key][D]
-// (3-D, box 64 x 128 x 1); Vt over transposed f16 V [z][D][keys_pad] (3-D, box
-// 64 x D x 1).  Query row t of sequence z (t < T_per_seq) sits at position
-// pos0 + t; it reads K at z index kv_z_base + z*NKV + g and Vt at z*NKV + g.
+// the f16 queries [rows][NH*D] (box 64 x 128); K over the f16 copy of the K
+// rows Kh [z][keys_pad][D] (3-D, box 64 x 128 x 1); Vt over transposed f16 V
+// [z][D][keys_pad] (3-D, box 64 x D x 1).  Query row t of sequence z
+// (t < T_per_seq) sits at position pos0 + t; it reads Kh and Vt at z index
+// z*NKV + g.
 struct AttnTcArgs {
     int T_per_seq, pos0, causal, n_keys;
     int NH, NKV, G;
-    int kv_z_base;
     uint16_t* att;               // [rows][ld_att] f16 (GEMM operand)
     int ld_att;
     int* status;
@@ -278,14 +278,19 @@ struct AttnTcArgs {
 bool attn_tc_supported(int D);
 void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
                     int nseq, int D, cudaStream_t s);
+// head_dim 64, two query tiles per CTA in ping-pong (attn_tc2.cu)
+void launch_attn_tc2(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
+                     int nseq, cudaStream_t s);
 
-// Vt[z][d][key] = f16(V[z][key][d]) for keys < n_keys, 0 for keys in [n_keys, keys_pad):
-// V rows of index z = (z / nkv, z % nkv) start at v + (z/nkv)*v_z_stride + (z%nkv)*v_h_stride.
+// Vt[z][d][key] = f16(V[z][key][d]) and Kh[z][key][d] = f16(K[z][key][d]) for
+// keys < n_keys, 0 for keys in [n_keys, keys_pad): V (and K) rows of index
+// z = (z / nkv, z % nkv) start at v + (z/nkv)*v_z_stride + (z%nkv)*v_h_stride
+// (the same offsets from k).  kh may be null.
 struct VtArgs {
-    const uint16_t* v;
+    const uint16_t *v, *k;
     long long v_z_stride, v_h_stride;
     int nkv, D, n_keys, keys_pad;
-    uint16_t* vt;
+    uint16_t *vt, *kh;
 };
 void launch_vt(const VtArgs& a, int zs, cudaStream_t s);
 

@@ -86,6 +86,7 @@ class Workload:
     steps: int
     note: str = ""
     extra: dict = field(default_factory=dict)
+    weights_q8: int = 0      # 1: the layer matrices run as q8_0 blocks
 
 
 TINY = ModelShape("tiny-qwen2", vocab=256, hidden=64, layers=2, n_heads=4, n_kv_heads=2,
@@ -104,6 +105,9 @@ WORKLOADS = {
                      note="f32 weights N(0,0.02); bf16-rounded copy for the GPU"),
     "qwen2.5-0.5b": Workload("qwen2.5-0.5b", QWEN25_05B, batch=1, prompt=128, steps=128),
     "llama-3.2-1b": Workload("llama-3.2-1b", LLAMA32_1B, batch=1, prompt=2048, steps=256),
+    "qwen2.5-0.5b-q8_0": Workload("qwen2.5-0.5b-q8_0", QWEN25_05B, batch=1, prompt=128, steps=128,
+                                  note="layer matrices quantized to q8_0 at model creation",
+                                  weights_q8=1),
     "qwen2.5-0.5b-b64": Workload("qwen2.5-0.5b-b64", QWEN25_05B, batch=64, prompt=4096, steps=64),
     "qwen3-encoder": Workload("qwen3-encoder", QWEN3_ENC, batch=8, prompt=512, steps=0),
 }

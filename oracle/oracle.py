@@ -205,6 +205,23 @@ def q8_0_dequant(blocks) -> np.ndarray:
     return out
 
 
+LAYER_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+def q8_0_layer_weights(weights: dict, layers: int) -> dict:
+    """A model's weights with every layer matrix replaced by the f32 decode of
+    its q8_0 encoding (embedding, head, norms and biases as given): the
+    values a q8_0 model computes with."""
+    out = dict(weights)
+    for l in range(layers):
+        for m in LAYER_MATRICES:
+            k = f"layers.{l}.{m}"
+            a = out[k]
+            a = bf16_decode(a) if a.dtype == np.uint16 else np.asarray(a, dtype=np.float32)
+            out[k] = q8_0_dequant(q8_0_quantize(a)).reshape(a.shape)
+    return out
+
+
 def mean_pooled_head(hidden, w, b=None):
     """[PII] forward() sensitivity head over final-normed states hidden [T, H]:
     mean over positions, then . w[j] + b[j] for w [n_out, H] (f32 values)."""

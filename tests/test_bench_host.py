@@ -51,14 +51,16 @@ def test_kernel_names_of_a_trace(mangled, name):
     ("qwen2.5-0.5b", 1, ("k_fused_attn", "k_fused_mlp", "k_gemv")),
     ("llama-3.2-1b", 1, ("k_fused_attn", "k_fused_mlp", "k_gemv")),
     ("qwen2.5-0.5b", 64, ("k_gemm_tcp", "k_attn_decode_mma")),
+    ("qwen2.5-0.5b-q8_0", 1, ("k_gemv", "k_attn_decode_mma")),
 ])
 def test_kernel_family_bytes_add_up_to_the_step(key, B, fams):
     bench = _bench()
-    shape = synth.WORKLOADS[key].model
+    wl = synth.WORKLOADS[key]
+    shape = wl.model
     ctx = 4097 if B > 1 else 200
-    fam = bench.decode_family_bytes(shape, B, ctx)
+    fam = bench.decode_family_bytes(shape, B, ctx, bool(wl.weights_q8))
     total = sum(fam[f] for f in fams)
-    job = types.SimpleNamespace(wl=types.SimpleNamespace(model=shape), B=B)
+    job = types.SimpleNamespace(wl=types.SimpleNamespace(model=shape, weights_q8=wl.weights_q8), B=B)
     step = bench.DecodeJob.bytes_per_decode_step(job, ctx - 1)   # ctx_mid + 1 keys
     # the families add the f32 residual stream and count biases as f32; the
     # step model counts the norm vectors: both differences are < 0.5 %

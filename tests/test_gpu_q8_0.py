@@ -112,19 +112,6 @@ Q8_QWEN2 = synth.ModelShape("q8-qwen2", vocab=2000, hidden=448, layers=2, n_head
                             n_kv_heads=1, head_dim=64, ff=640, rope_theta=1e6, qkv_bias=1)
 Q8_D128 = synth.ModelShape("q8-d128", vocab=900, hidden=256, layers=2, n_heads=4, n_kv_heads=2,
                            head_dim=128, ff=384, rope_theta=1e6, qk_norm=1)
-MATS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
-
-
-def q8_oracle_weights(shape, w):
-    """The model's weights with every layer matrix replaced by the f32 decode of
-    its oracle q8_0 encoding (embedding, head and norms as given)."""
-    out = {k: O.bf16_decode(v) for k, v in w.items()}
-    for l in range(shape.layers):
-        for m in MATS:
-            k = f"layers.{l}.{m}"
-            a = out[k]
-            out[k] = O.q8_0_dequant(O.q8_0_quantize(a)).reshape(a.shape)
-    return out
 
 
 _models = {}
@@ -133,7 +120,7 @@ _models = {}
 def q8_models(shape):
     if shape.name not in _models:
         w = synth.weights_bf16(shape)
-        _models[shape.name] = (O.OracleModel(shape, q8_oracle_weights(shape, w)), O.OracleModel(shape, w),
+        _models[shape.name] = (O.OracleModel(shape, O.q8_0_layer_weights(w, shape.layers)), O.OracleModel(shape, w),
                                R.Model(shape, w, max_tokens=512, weights_q8=1))
     return _models[shape.name]
 
