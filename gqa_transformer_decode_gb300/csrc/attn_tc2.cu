@@ -2,18 +2,22 @@
 // tensor cores, two query tiles per CTA in ping-pong.
 //
 // The same computation as k_attn_tc (attn_tc.cu): per key tile of 128 keys,
-// S = Q . K^T into TMEM, the online softmax of each query row, P (f16) to
-// shared memory and O += P . V accumulated in TMEM, with the lazy rescaling
-// of O and l when a row's maximum moves by more than 2^8.  What differs is
-// the schedule.  One CTA holds two 128-row query tiles A and B of one head,
-// each with its own four softmax warps (one thread per query row, all 128
-// score columns), its own S and O columns of TMEM and its own P buffer, and
-// the MMA warp interleaves them:
-//     PV_A(j), S_A(j+1)   while the B warps turn S_B(j) into P_B(j)
-//     PV_B(j), S_B(j+1)   while the A warps turn S_A(j+1) into P_A(j+1)
+// S = Q . K^T into TMEM, the online softmax of each query row, P (f16) and
+// O += P . V accumulated in TMEM, with the lazy rescaling of O and l when a
+// row's maximum moves by more than 2^8.  What differs is the schedule, and
+// that P stays in tensor memory (the A operand of P . V read from TMEM).
+// One CTA holds two 128-row query tiles A and B of one head, each with its
+// own four softmax warps (one thread per query row, all 128 score columns)
+// and its own S, P and O columns of TMEM, and the MMA warp interleaves them:
+//     S_A(j+1), PV_A(j)   while the B warps turn S_B(j) into P_B(j)
+//     S_B(j+1), PV_B(j)   while the A warps turn S_A(j+1) into P_A(j+1)
 // so the tensor cores work on one tile while the CUDA cores exponentiate the
 // other (with one tile per CTA the two alternate and each idles while the
-// other runs).  Both tiles walk the key tiles of tile B (the later one); the
+// other runs).  S of the next key tile goes ahead of P . V of this one: a
+// softmax warp computes its row's P in registers while P . V(j) still reads
+// the TMEM copy of P(j), and writes P(j + 1) there once that is done.  (A
+// tcgen05.mma of M = 128, K = 16 takes ~112 cycles whatever N <= 128, so the
+// N = 64 P . V costs twice the N = 128 S and the tensor pipe sets the pace.)  Both tiles walk the key tiles of tile B (the later one); the
 // causal mask zeroes tile A's share of the last one.
 // Warp 0: TMA producer (f16 Q, the f16 copy Kh of the keys and the
 // transposed Vt, as k_attn_tc reads them); warp 1:
@@ -38,18 +42,19 @@ constexpr int P2_D = 64;
 
 struct P2Smem {
     static constexpr int TILE = P2_BQ * 128;            // 128 rows x 64 f16 (one swizzled block)
-    static constexpr int NSTG = 3;                      // K/V ring stages
+    static constexpr int NSTG = 4;                      // K/V ring stages
     static constexpr int K_BYTES = P2_BK * 128;         // 128 keys x 64 f16
     static constexpr int V_BLOCK = P2_D * 128;          // [64 dims][64 keys] f16
     static constexpr int V_BYTES = 2 * V_BLOCK;         // 128 keys
-    static constexpr int P_BYTES = 2 * P2_BQ * 128;     // [128 rows][128 keys] f16
     static constexpr int OFF_Q = 0;                     // Q_A, Q_B
     static constexpr int OFF_K = OFF_Q + 2 * TILE;
     static constexpr int OFF_V = OFF_K + NSTG * K_BYTES;
-    static constexpr int OFF_P = OFF_V + NSTG * V_BYTES;   // P_A, P_B
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NSTG * V_BYTES;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;     // + barriers, + alignment slack
-    static constexpr uint32_t TMEM_COLS = 512;             // S_A, S_B (128 each), O_A, O_B (64 each)
+    // TMEM columns: S_A, S_B (128 f32 each), O_A, O_B (64 f32 each), P_A, P_B
+    // (128 f16 each, packed two to a column)
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
 };
 
 __global__ void __launch_bounds__(P2_THREADS, 1)
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 7);
     int* sflag = reinterpret_cast<int*>(bar + 8);   // [0] failed, [1] issued, [2] consumed
     uint64_t* kv_full = bar + 10;   // [NSTG]
-    uint64_t* kv_empty = bar + 14;  // [NSTG]
+    uint64_t* kv_empty = bar + 16;  // [NSTG]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pt = gridDim.x - 1 - blockIdx.x;         // heaviest (last) tile pairs first
@@ -146,20 +151,18 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    umma_bf16(tmem + t * 128, sdesc_sw128(q0 + k * 32), sdesc_sw128(k0 + k * 32), idS,
-                              k ? 1u : 0u);
+                    umma_bf16(tmem + L::COL_S + t * 128, sdesc_sw128(q0 + k * 32), sdesc_sw128(k0 + k * 32),
+                              idS, k ? 1u : 0u);
                 umma_commit(&s_full[t]);
             };
-            auto mma_pv = [&](int t, int s, bool acc) {   // O_t += P_t . V(stage s)
-                const uint32_t p0 = smem_u32(sm + L::OFF_P + t * L::P_BYTES);
+            auto mma_pv = [&](int t, int s, bool acc) {   // O_t += P_t (TMEM) . V(stage s)
                 const uint32_t v0 = smem_u32(sm + L::OFF_V + s * L::V_BYTES);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_bf16(tmem + 256 + t * P2_D, sdesc_sw128(p0 + kb * P2_BQ * 128 + k * 32),
-                                  sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO,
-                                  (acc || kb || k) ? 1u : 0u);
+                        umma_f16_ts(tmem + L::COL_O + t * P2_D, tmem + L::COL_P + t * 64 + kb * 32 + k * 8,
+                                    sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO, (acc || kb || k) ? 1u : 0u);
                 umma_commit(&o_full[t]);
             };
             bool ok = mbar_wait(q_full, 0) && (nkt == 0 || mbar_wait(&kv_full[0], 0));
@@ -173,19 +176,21 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 const int s = j % NSTG;
                 const bool more = j + 1 < nkt;
                 const int s1 = (j + 1) % NSTG;
+                // S_t(j + 1) may overwrite S_t(j): p_full[t] says its row
+                // values have all been read
                 if (!mbar_wait(&p_full[0], (uint32_t)j & 1u)) break;
                 tc_fence_after();
-                mma_pv(0, s, j > 0);
                 if (more) {
                     if (!mbar_wait(&kv_full[s1], (uint32_t)((j + 1) / NSTG) & 1u)) break;
                     tc_fence_after();
                     mma_s(0, s1);
                 }
+                mma_pv(0, s, j > 0);
                 if (!mbar_wait(&p_full[1], (uint32_t)j & 1u)) break;
                 tc_fence_after();
+                if (more) mma_s(1, s1);
                 mma_pv(1, s, j > 0);
                 umma_commit(&kv_empty[s]);
-                if (more) mma_s(1, s1);
             }
             if (!ok || j < nkt) sflag[0] = 1;
             sflag[2] = j;
@@ -198,40 +203,46 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int row0 = q_first + t * P2_BQ;         // the tile's first row
         const int qp = a.pos0 + row0 + r;             // this row's position
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-        const uint32_t tS = tmem + t * 128 + lane_off;
-        const uint32_t tO = tmem + 256 + t * P2_D + lane_off;
+        const uint32_t tS = tmem + L::COL_S + t * 128 + lane_off;
+        const uint32_t tO = tmem + L::COL_O + t * P2_D + lane_off;
+        const uint32_t tP = tmem + L::COL_P + t * 64 + lane_off;
         const float sc_log2 = 1.4426950408889634f * rsqrtf((float)P2_D);
-        uint8_t* sP = sm + L::OFF_P + t * L::P_BYTES;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // p = 2^(s - mr) for the row's 128 scores of the tile (masked: 0), 64
-        // columns per TMEM load; P -> shared as two K-major blocks of 64 keys
-        // with the 128-byte swizzle.  Returns the row sum; mt = the tile's
-        // largest visible scaled score.
-        auto emit = [&](float mr, int lim, float& mt) -> float {
+        // columns per TMEM load, packed as f16 pairs into pk (keys 2c, 2c + 1
+        // in pk[c]).  Returns the row sum; mt = the tile's largest visible
+        // scaled score.  `masked` is warp-uniform: false when every row of
+        // the warp sees all 128 keys.
+        auto emit = [&](float mr, int lim, bool masked, float& mt, uint32_t (&pk)[64]) -> float {
             const float mo = mr == -INFINITY ? 0.f : mr;   // no visible key yet: every p is 0
             float rs = 0.f;
-#pragma unroll 1
+#pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 64) {
                 uint32_t v[64];
                 tmem_ld32(tS + c0, v);
                 tmem_ld32(tS + c0 + 32, v + 32);
                 tmem_ld_wait();
-                uint8_t* rowp = sP + (c0 >> 6) * P2_BQ * 128 + (r >> 3) * 1024 + (r & 7) * 128;
+                if (masked) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const int c = q * 8 + i;
+                    for (int c = 0; c < 64; c += 2) {
                         const float x0 = c0 + c < lim ? __uint_as_float(v[c]) * sc_log2 : -INFINITY;
                         const float x1 = c0 + c + 1 < lim ? __uint_as_float(v[c + 1]) * sc_log2 : -INFINITY;
                         mt = fmaxf(mt, fmaxf(x0, x1));
                         const float p0 = ex2(x0 - mo), p1 = ex2(x1 - mo);
                         rs += p0 + p1;
-                        pk[i / 2] = pack_f16x2(p0, p1);
+                        pk[(c0 + c) / 2] = pack_f16x2(p0, p1);
                     }
-                    *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const float x0 = __uint_as_float(v[c]) * sc_log2;
+                        const float x1 = __uint_as_float(v[c + 1]) * sc_log2;
+                        mt = fmaxf(mt, fmaxf(x0, x1));
+                        const float p0 = ex2(x0 - mo), p1 = ex2(x1 - mo);
+                        rs += p0 + p1;
+                        pk[(c0 + c) / 2] = pack_f16x2(p0, p1);
+                    }
                 }
             }
             return rs;
@@ -246,13 +257,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             int lim = a.n_keys - key0;                        // keys i < lim of the tile are visible
             if (a.causal) lim = min(lim, qp - key0 + 1);
             lim = max(0, min(P2_BK, lim));
-            if (j > 0) {   // PV(j-1) must be complete before O is touched or P is rewritten
-                if (!mbar_wait(&o_full[t], (uint32_t)(j - 1) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            } else {       // the first tile sets the reference maximum
+            const bool masked = !__all_sync(FULL_MASK, lim == P2_BK);
+            if (j == 0) {   // the first tile sets the reference maximum
                 float mt = -INFINITY;
 #pragma unroll
                 for (int c0 = 0; c0 < 128; c0 += 64) {
@@ -269,15 +275,27 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             // the reference maximum m moves (and O, l are rescaled) only when
             // the tile's maximum exceeds it by more than RESCALE (log2 units),
             // so p stays <= 2^RESCALE (f16-safe); then the tile is redone
+            uint32_t pk[64];
             float mt = -INFINITY;
-            float rs = emit(m, lim, mt);
+            float rs = emit(m, lim, masked, mt, pk);
             const bool move = mt > m + RESCALE;
-            if (__any_sync(FULL_MASK, move)) {
+            const bool any_move = __any_sync(FULL_MASK, move);
+            float corr = 1.f;
+            if (any_move) {
                 const float mnew = move ? mt : m;
-                const float corr = move ? exp2f(m - mnew) : 1.f;
+                corr = move ? exp2f(m - mnew) : 1.f;
                 float mt2 = -INFINITY;
-                rs = emit(mnew, lim, mt2);
-                if (j > 0) {
+                rs = emit(mnew, lim, masked, mt2, pk);
+                l *= corr;
+                m = mnew;
+            }
+            if (j > 0) {   // P . V(j - 1) must be complete before O is touched or P is rewritten
+                if (!mbar_wait(&o_full[t], (uint32_t)(j - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (any_move) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < P2_D; c0 += 16) {
                         uint32_t o[16];
@@ -287,12 +305,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                         for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
                         tmem_st16(tO + c0, o);
                     }
-                    tmem_st_wait();
                 }
-                l *= corr;
-                m = mnew;
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) tmem_st16(tP + c, pk + c);
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[t]);
             l += rs;
