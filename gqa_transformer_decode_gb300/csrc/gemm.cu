@@ -259,8 +259,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool encode_map_bf16(void* out, const void* ptr, int rank, const uint64_t* dims,
-                     const uint64_t* strides, const uint32_t* box) {
+static bool encode_map_t(void* out, const void* ptr, CUtensorMapDataType dt, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box) {
     auto enc = encode_fn();
     if (!enc || rank < 2 || rank > 5) return false;
     if (reinterpret_cast<uintptr_t>(ptr) & 15) return false;
@@ -275,11 +275,25 @@ bool encode_map_bf16(void* out, const void* ptr, int rank, const uint64_t* dims,
             st[i] = strides[i];
         }
     }
-    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), dt,
                      (cuuint32_t)rank, const_cast<void*>(ptr), d, st, bx, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_map_bf16(void* out, const void* ptr, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
+    return encode_map_t(out, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, dims, strides, box);
+}
+
+bool make_out_map(void* out, const void* ptr, int rows, int cols, int ld, bool f16) {
+    if (rows <= 0 || cols <= 0 || cols > ld) return false;
+    const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)ld * (f16 ? 2 : 4)};
+    const uint32_t box[2] = {f16 ? 64u : 32u, 128u};
+    return encode_map_t(out, ptr, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims,
+                        strides, box);
 }
 
 static bool make_map(void* out, const uint16_t* ptr, int rows, int ld, int K, int box_rows) {

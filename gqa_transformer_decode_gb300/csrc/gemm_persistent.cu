@@ -12,6 +12,10 @@
 // acc_empty[b] (128 epilogue arrivals -> MMA).  Every wait is bounded; a
 // timeout raises EMBER_ERR_TIMEOUT, drains the copies in flight and frees
 // TMEM.  Epilogues: bias store, residual add, SwiGLU (f16 out), argmax.
+// With an output tensor map the store / residual / SwiGLU epilogues stage
+// 32-column slices (f32) or the whole tile (f16) in a swizzled shared buffer
+// and write them with TMA (the residual as an f32 reduce-add), so the output
+// leaves in whole 128-byte lines instead of one 16-byte piece per row.
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -97,19 +101,116 @@ __device__ __forceinline__ void tile_epilogue(const GemmEpilogue& e, uint32_t tb
     }
 }
 
+constexpr int GP_STAGING = 32768;   // output staging: two 16 KB f32 slices or one f16 tile
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the same barrier, returning whether every epilogue thread passed `ok`
+__device__ __forceinline__ bool epi_bar_and(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
+// The same epilogues through TMA: thread `r` (0..127) holds tile row m0 + r.
+// f32 modes: 32-column slices alternate between the two 16 KB halves of stg
+// ([128 rows][32 f32], 16-byte chunk k of row r at chunk k ^ (r & 7), the
+// map's 128-byte swizzle); the slice written two slices ago must have been
+// read by its copy first.  SwiGLU: the tile's BN/2 f16 outputs per row as
+// BN/128 blocks of [128 rows][64 f16] in the same layout.  Rows >= M are
+// written as zeros (the map clips at its own row count).
+template <int BN>
+__device__ __forceinline__ void tile_epilogue_tma(const GemmEpilogue& e, const CUtensorMap* tmO, uint32_t tbase,
+                                                  int r, int m0, int n0, int M, int N, uint8_t* stg,
+                                                  bool& f16bad) {
+    const float wsc = pow2f(e.w_exp);
+    const bool live = m0 + r < M;
+    const bool leader = threadIdx.x == 64;   // first epilogue thread issues the copies
+    if (e.mode == EPI_SWIGLU) {
+        if (leader) bulk_wait_read<0>();
+        epi_bar();
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t u[32];
+            tmem_ld16(tbase + c, u);
+            tmem_ld16(tbase + c + 16, u + 16);
+            tmem_ld_wait();
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float g0 = __uint_as_float(u[4 * i]) * wsc, u0 = __uint_as_float(u[4 * i + 1]) * wsc;
+                const float g1 = __uint_as_float(u[4 * i + 2]) * wsc, u1 = __uint_as_float(u[4 * i + 3]) * wsc;
+                const float y0 = __fdividef(g0, 1.f + __expf(-g0)) * u0;
+                const float y1 = __fdividef(g1, 1.f + __expf(-g1)) * u1;
+                pk[i] = live && n0 + c + 4 * i < N ? pack_f16x2_chk(y0, y1, f16bad) : 0u;
+            }
+            uint8_t* rowp = stg + (c >> 7) * 16384 + r * 128;
+            const int k0 = (c & 127) >> 4;   // 16-byte chunk of the 32 outputs' first half
+            *reinterpret_cast<uint4*>(rowp + ((k0 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epi_bar();
+        if (leader) {
+            for (int b = 0; b < BN / 128; ++b)
+                if (n0 / 2 + b * 64 < N / 2) tma_store_2d(tmO, stg + b * 16384, n0 / 2 + b * 64, m0);
+            bulk_commit();
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t u[32];
+        tmem_ld16(tbase + c, u);
+        tmem_ld16(tbase + c + 16, u + 16);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = live ? __uint_as_float(u[i]) * wsc : 0.f;
+        if (e.mode == EPI_STORE && e.bias && live) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n0 + c + i < N) v[i] += e.bias[n0 + c + i];
+        }
+        uint8_t* buf = stg + ((c >> 5) & 1) * 16384;
+        if (leader) bulk_wait_read<1>();   // the copy of the slice before last has read buf
+        epi_bar();
+        uint8_t* rowp = buf + r * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(rowp + ((k ^ (r & 7)) << 4)) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epi_bar();
+        if (leader && n0 + c < N) {
+            if (e.mode == EPI_RESID) tma_reduce_add_2d(tmO, buf, n0 + c, m0);
+            else tma_store_2d(tmO, buf, n0 + c, m0);
+            bulk_commit();
+        }
+    }
+}
+
 }  // namespace
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(GP_THREADS, 1)
     k_gemm_tcp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               int M, int N, int K, uint32_t idesc, GemmEpilogue e, int* status) {
+               const __grid_constant__ CUtensorMap tmO, int M, int N, int K, uint32_t idesc, GemmEpilogue e,
+               int* status) {
     constexpr int A_BYTES = GP_BM * GP_BK * 2;
     constexpr int B_BYTES = BN * GP_BK * 2;
     constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* stg = smem + STAGES * STAGE_BYTES;   // output staging (1024-aligned)
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg + GP_STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;     // [2]
     uint64_t* acc_empty = acc_full + 2;      // [2]
@@ -227,12 +328,15 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         unsigned long long best = 0ull;
         int best_row = -1;
         bool f16bad = false;   // EPI_SWIGLU: an output beyond the f16 range
+        const bool tma_out = e.out_map && e.mode != EPI_ARGMAX && (e.mode != EPI_SWIGLU || BN >= 128);
         for (int li = 0; li < my_tiles; ++li) {
             const int b = li & 1;
             int m0, n0;
             tile_mn(li, m0, n0);
             const int row = m0 + q * 32 + lane;
-            if (!mbar_wait(&acc_full[b], (uint32_t)(li >> 1) & 1u)) {
+            bool got = mbar_wait(&acc_full[b], (uint32_t)(li >> 1) & 1u);
+            if (tma_out) got = epi_bar_and(got);   // the TMA epilogue's barriers need all 128 threads
+            if (!got) {
                 sflag[0] = 1;
                 break;
             }
@@ -242,14 +346,19 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
                 best = 0ull;
                 best_row = row;
             }
-            tile_epilogue<BN>(e, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), row, n0, M, N,
-                              best, f16bad);
+            if (tma_out)
+                tile_epilogue_tma<BN>(e, &tmO, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), q * 32 + lane,
+                                      m0, n0, M, N, stg, f16bad);
+            else
+                tile_epilogue<BN>(e, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), row, n0, M, N,
+                                  best, f16bad);
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
         }
         if (e.mode == EPI_ARGMAX && best && best_row >= 0 && best_row < M)
             atomicMax(e.keys + best_row, best);
         if (f16bad) raise_status(status, EMBER_ERR_RANGE);
+        if (tma_out && threadIdx.x == 64) bulk_wait<0>();   // every output copy complete before exit
     }
 
     tc_fence_before();
@@ -270,7 +379,7 @@ template <int BN, int STAGES>
 static void launch_p(const void* tmA, const void* tmB, int m_rows, int N, int K, uint32_t idesc,
                      const GemmEpilogue& e, int* status, int sms, cudaStream_t s) {
     constexpr int STAGE_BYTES = (GP_BM + BN) * GP_BK * 2;
-    constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    constexpr int SMEM = STAGES * STAGE_BYTES + GP_STAGING + 1024 + 256;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tcp<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -278,8 +387,10 @@ static void launch_p(const void* tmA, const void* tmB, int m_rows, int N, int K,
     }
     const int tiles = ((m_rows + GP_BM - 1) / GP_BM) * ((N + BN - 1) / BN);
     const int grid = tiles < sms ? tiles : sms;
+    static const CUtensorMap no_map{};   // unused when e.out_map is null
+    const CUtensorMap* tmO = e.out_map ? reinterpret_cast<const CUtensorMap*>(e.out_map) : &no_map;
     launch_k(k_gemm_tcp<BN, STAGES>, dim3(grid), dim3(GP_THREADS), SMEM, s,
-             *reinterpret_cast<const CUtensorMap*>(tmA), *reinterpret_cast<const CUtensorMap*>(tmB),
+             *reinterpret_cast<const CUtensorMap*>(tmA), *reinterpret_cast<const CUtensorMap*>(tmB), *tmO,
              m_rows, N, K, idesc, e, status);
 }
 

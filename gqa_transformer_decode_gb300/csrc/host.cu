@@ -182,6 +182,11 @@ struct ember_model {
     bool q_map_ok = false;
     int enc_positions = 0;
     GemmPlan p_head;   // tied head on bf16 final states (encode without labels)
+    // TMA maps over the many-row GEMM outputs: q/k/v (f32), the residual
+    // stream (f32, reduce-add) and the SwiGLU output (f16)
+    alignas(64) unsigned char omap_qkv[128];
+    alignas(64) unsigned char omap_x[128];
+    alignas(64) unsigned char omap_act[128];
     // fused batch-1 decode (two kernels per layer)
     FusedPlan fp;
     float* fx[2] = {nullptr, nullptr};             // residual stream copies [H]
@@ -487,6 +492,9 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     }
     if (!make_gemm_plan(m->p_head, m->hb, T, H, m->embed, V, H, H, false))
         return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (head)"));
+    if (!make_out_map(m->omap_qkv, m->qkv, T, m->qkv_n, m->qkv_n, false) ||
+        !make_out_map(m->omap_x, m->x, T, H, H, false) || !make_out_map(m->omap_act, m->act_b, T, F, F, true))
+        return cleanup(fail(EMBER_ERR_CUDA, "TMA tensor map encoding failed (GEMM outputs)"));
     if (attn_tc_supported(D)) {
         const uint64_t qd[2] = {(uint64_t)m->q, (uint64_t)T};
         const uint64_t qs[1] = {(uint64_t)m->q * 2};
@@ -701,6 +709,7 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     e.ldo = m->qkv_n;
     e.bias = c.qkv_bias ? L.bqkv : nullptr;
     e.w_exp = L.e_qkv;
+    e.out_map = m->omap_qkv;
     launch_gemm(L.p_qkv, n, e, m->status, s);
     RopeKVArgs r{};
     r.qkv = m->qkv;
@@ -772,6 +781,7 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     e.out_f32 = m->x;
     e.ldo = c.hidden;
     e.w_exp = L.e_o;
+    e.out_map = m->omap_x;
     launch_gemm(L.p_o, n, e, m->status, s);
     launch_rmsnorm_h(m->x, L.mlp_norm, eps, n, c.hidden, m->xb, m->status, s);
     e = GemmEpilogue{};
@@ -779,12 +789,14 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     e.out_h = m->act_b;
     e.ldo = c.ff;
     e.w_exp = L.e_gu;
+    e.out_map = m->omap_act;
     launch_gemm(L.p_gu, n, e, m->status, s);
     e = GemmEpilogue{};
     e.mode = EPI_RESID;
     e.out_f32 = m->x;
     e.ldo = c.hidden;
     e.w_exp = L.e_d;
+    e.out_map = m->omap_x;
     launch_gemm(L.p_d, n, e, m->status, s);
 }
 
@@ -1399,10 +1411,14 @@ extern "C" ember_status ember_gemm_bf16(const uint16_t* A, const uint16_t* Bm, f
     GemmPlan p;
     if (!make_gemm_plan(p, A, M, K, Bm, N, K, K, false))
         return fail(EMBER_ERR_INVALID_ARG, "TMA tensor map rejected (alignment?)");
+    alignas(64) unsigned char omap[128];
+    if (!make_out_map(omap, Dm, M, N, N, false))
+        return fail(EMBER_ERR_INVALID_ARG, "TMA tensor map rejected for D (alignment?)");
     GemmEpilogue e{};
     e.mode = EPI_STORE;
     e.out_f32 = Dm;
     e.ldo = N;
+    e.out_map = omap;   // copied into the launch's parameters
     launch_gemm(p, M, e, nullptr, (cudaStream_t)stream);
     CK(cudaGetLastError());
     return EMBER_OK;

@@ -225,7 +225,16 @@ struct GemmEpilogue {
     int ksplit;                  // set by launch_gemm: K split over grid.z (red.add outputs)
     int w_exp;                   // B is stored scaled by 2^-w_exp: products are multiplied by 2^w_exp
     int zeroed;                  // EPI_STORE: out_f32 is zero, so K may be split
+    // Host pointer to a tensor map over the output (make_out_map), or null.
+    // The many-row GEMM then writes its EPI_STORE / EPI_RESID / EPI_SWIGLU
+    // tiles through shared memory with TMA (EPI_RESID as an f32 reduce-add);
+    // the map's rows bound the rows written.
+    const void* out_map;
 };
+// Tensor map over an output [rows][ld] (cols <= ld) for GemmEpilogue.out_map:
+// f32 with 32 x 128 boxes, or f16 (the SwiGLU output) with 64 x 128 boxes,
+// 128-byte swizzle.  False if the driver rejects it.
+bool make_out_map(void* out, const void* ptr, int rows, int cols, int ld, bool f16);
 
 struct GemmPlan {
     alignas(64) unsigned char tmA[128];
