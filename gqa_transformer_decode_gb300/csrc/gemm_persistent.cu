@@ -16,6 +16,10 @@
 // 32-column slices (f32) or the whole tile (f16) in a swizzled shared buffer
 // and write them with TMA (the residual as an f32 reduce-add), so the output
 // leaves in whole 128-byte lines instead of one 16-byte piece per row.
+// The residual epilogue adds, so that GEMM is split stream-K style: CTA b
+// takes the b-th contiguous 1/gridDim share of the (tile, k-block) work, a
+// tile's k-range may be shared by two or three CTAs, and each adds its
+// partial sum (every SM busy whatever the tile count; no inter-CTA waits).
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -119,16 +123,17 @@ __device__ __forceinline__ bool epi_bar_and(bool ok) {
 }
 
 // The same epilogues through TMA: thread `r` (0..127) holds tile row m0 + r.
-// f32 modes: 32-column slices alternate between the two 16 KB halves of stg
-// ([128 rows][32 f32], 16-byte chunk k of row r at chunk k ^ (r & 7), the
-// map's 128-byte swizzle); the slice written two slices ago must have been
-// read by its copy first.  SwiGLU: the tile's BN/2 f16 outputs per row as
+// f32 modes: the slices the kernel writes (32 columns each; none past N)
+// alternate, by their running count `slice`, between the two 16 KB halves of
+// stg ([128 rows][32 f32], 16-byte chunk k of row r at chunk k ^ (r & 7), the
+// map's 128-byte swizzle); one copy (one bulk group) per slice, and the slice
+// written two slices ago must have been read by its copy first.  SwiGLU: the tile's BN/2 f16 outputs per row as
 // BN/128 blocks of [128 rows][64 f16] in the same layout.  Rows >= M are
 // written as zeros (the map clips at its own row count).
 template <int BN>
 __device__ __forceinline__ void tile_epilogue_tma(const GemmEpilogue& e, const CUtensorMap* tmO, uint32_t tbase,
                                                   int r, int m0, int n0, int M, int N, uint8_t* stg,
-                                                  bool& f16bad) {
+                                                  int& slice, bool& f16bad) {
     const float wsc = pow2f(e.w_exp);
     const bool live = m0 + r < M;
     const bool leader = threadIdx.x == 64;   // first epilogue thread issues the copies
@@ -165,7 +170,7 @@ __device__ __forceinline__ void tile_epilogue_tma(const GemmEpilogue& e, const C
         return;
     }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN && n0 + c < N; c += 32) {
         uint32_t u[32];
         tmem_ld16(tbase + c, u);
         tmem_ld16(tbase + c + 16, u + 16);
@@ -178,7 +183,8 @@ __device__ __forceinline__ void tile_epilogue_tma(const GemmEpilogue& e, const C
             for (int i = 0; i < 32; ++i)
                 if (n0 + c + i < N) v[i] += e.bias[n0 + c + i];
         }
-        uint8_t* buf = stg + ((c >> 5) & 1) * 16384;
+        uint8_t* buf = stg + (slice & 1) * 16384;
+        ++slice;
         if (leader) bulk_wait_read<1>();   // the copy of the slice before last has read buf
         epi_bar();
         uint8_t* rowp = buf + r * 128;
@@ -188,7 +194,7 @@ __device__ __forceinline__ void tile_epilogue_tma(const GemmEpilogue& e, const C
                 make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         epi_bar();
-        if (leader && n0 + c < N) {
+        if (leader) {
             if (e.mode == EPI_RESID) tma_reduce_add_2d(tmO, buf, n0 + c, m0);
             else tma_store_2d(tmO, buf, n0 + c, m0);
             bulk_commit();
@@ -221,10 +227,26 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     const int nk = (K + GP_BK - 1) / GP_BK;
     const int n_mt = (M + GP_BM - 1) / GP_BM, n_nt = (N + BN - 1) / BN;
     const int n_tiles = n_mt * n_nt;
-    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int pre = nk < STAGES ? nk : STAGES;   // weight blocks of the first tile issued early
-    auto tile_mn = [&](int li, int& m0, int& n0) {
-        const int t = (int)blockIdx.x + li * (int)gridDim.x;
+    // Work segments of this CTA: whole tiles b, b + grid, ... or, stream-K
+    // (residual epilogue through TMA), the k-blocks [w0, w1) of the
+    // tile-major (tile, k-block) sequence, cut at tile boundaries.
+    const bool sk = e.mode == EPI_RESID && e.out_map != nullptr;
+    const long long W = (long long)n_tiles * nk;
+    const long long w0 = sk ? W * blockIdx.x / gridDim.x : 0;
+    const long long w1 = sk ? W * (blockIdx.x + 1) / gridDim.x : 0;
+    const int my_tiles = sk ? (w1 > w0 ? (int)((w1 - 1) / nk - w0 / nk) + 1 : 0)
+                            : ((int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0);
+    auto tile_mn = [&](int li, int& m0, int& n0, int& kb0, int& kb1) {
+        int t;
+        if (sk) {
+            t = (int)(w0 / nk) + li;
+            kb0 = li == 0 ? (int)(w0 % nk) : 0;
+            kb1 = (int)((w1 - (long long)t * nk) < nk ? (w1 - (long long)t * nk) : nk);
+        } else {
+            t = (int)blockIdx.x + li * (int)gridDim.x;
+            kb0 = 0;
+            kb1 = nk;
+        }
         m0 = (t % n_mt) * GP_BM;
         n0 = (t / n_mt) * BN;
     };
@@ -243,12 +265,13 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         sflag[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (my_tiles > 0) {   // the first tile's weights do not depend on the previous kernel
-            int m0, n0;
-            tile_mn(0, m0, n0);
-            for (int kb = 0; kb < pre; ++kb) {
-                mbar_expect_tx(&full[kb], STAGE_BYTES);
-                tma_load_2d(smem + kb * STAGE_BYTES + A_BYTES, &tmB, kb * GP_BK, n0, &full[kb]);
+        if (my_tiles > 0) {   // the first segment's weights do not depend on the previous kernel
+            int m0, n0, kb0, kb1;
+            tile_mn(0, m0, n0, kb0, kb1);
+            const int pre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(&full[i], STAGE_BYTES);
+                tma_load_2d(smem + i * STAGE_BYTES + A_BYTES, &tmB, (kb0 + i) * GP_BK, n0, &full[i]);
             }
         }
     }
@@ -267,13 +290,15 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     pdl_wait();   // activations and the residual stream are the previous kernels' outputs
 
     if (warp == 0) {
-        if (lane == 0) {   // ---------------- TMA producer, k-blocks of all my tiles
+        if (lane == 0) {   // ---------------- TMA producer, k-blocks of all my segments
             int g = 0;     // global k-block count
             bool fail = false;
+            int pre = 0;   // B blocks of the first segment already issued
             for (int li = 0; li < my_tiles && !fail; ++li) {
-                int m0, n0;
-                tile_mn(li, m0, n0);
-                for (int kb = 0; kb < nk; ++kb, ++g) {
+                int m0, n0, kb0, kb1;
+                tile_mn(li, m0, n0, kb0, kb1);
+                if (li == 0) pre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     const int s = g % STAGES;
                     uint8_t* sa = smem + s * STAGE_BYTES;
                     if (g >= pre) {
@@ -297,13 +322,15 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
             bool fail = false;
             for (int li = 0; li < my_tiles && !fail; ++li) {
                 const int b = li & 1;
+                int m0, n0, kb0, kb1;
+                tile_mn(li, m0, n0, kb0, kb1);
                 if (!mbar_wait(&acc_empty[b], ((uint32_t)(li >> 1) & 1u) ^ 1u)) {
                     fail = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t acc = tmem + (uint32_t)(b * BN);
-                for (int kb = 0; kb < nk; ++kb, ++g) {
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     const int s = g % STAGES;
                     if (!mbar_wait(&full[s], (uint32_t)(g / STAGES) & 1u)) {
                         fail = true;
@@ -315,7 +342,7 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < GP_BK / 16; ++k)
                         umma_bf16(acc, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
+                                  (kb > kb0 || k > 0) ? 1u : 0u);
                     umma_commit(&empty[s]);   // the stage is free once these MMAs read it
                 }
                 if (!fail) umma_commit(&acc_full[b]);
@@ -328,11 +355,12 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         unsigned long long best = 0ull;
         int best_row = -1;
         bool f16bad = false;   // EPI_SWIGLU: an output beyond the f16 range
+        int slice = 0;         // f32 slices written through TMA so far
         const bool tma_out = e.out_map && e.mode != EPI_ARGMAX && (e.mode != EPI_SWIGLU || BN >= 128);
         for (int li = 0; li < my_tiles; ++li) {
             const int b = li & 1;
-            int m0, n0;
-            tile_mn(li, m0, n0);
+            int m0, n0, kb0, kb1;
+            tile_mn(li, m0, n0, kb0, kb1);
             const int row = m0 + q * 32 + lane;
             bool got = mbar_wait(&acc_full[b], (uint32_t)(li >> 1) & 1u);
             if (tma_out) got = epi_bar_and(got);   // the TMA epilogue's barriers need all 128 threads
@@ -348,7 +376,7 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
             }
             if (tma_out)
                 tile_epilogue_tma<BN>(e, &tmO, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), q * 32 + lane,
-                                      m0, n0, M, N, stg, f16bad);
+                                      m0, n0, M, N, stg, slice, f16bad);
             else
                 tile_epilogue<BN>(e, tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16), row, n0, M, N,
                                   best, f16bad);
@@ -386,7 +414,9 @@ static void launch_p(const void* tmA, const void* tmB, int m_rows, int N, int K,
         attr = true;
     }
     const int tiles = ((m_rows + GP_BM - 1) / GP_BM) * ((N + BN - 1) / BN);
-    const int grid = tiles < sms ? tiles : sms;
+    // stream-K (residual through TMA): every SM, as long as each gets a k-block
+    const long long work = e.mode == EPI_RESID && e.out_map ? (long long)tiles * ((K + GP_BK - 1) / GP_BK) : tiles;
+    const int grid = work < sms ? (int)work : sms;
     static const CUtensorMap no_map{};   // unused when e.out_map is null
     const CUtensorMap* tmO = e.out_map ? reinterpret_cast<const CUtensorMap*>(e.out_map) : &no_map;
     launch_k(k_gemm_tcp<BN, STAGES>, dim3(grid), dim3(GP_THREADS), SMEM, s,
