@@ -1072,16 +1072,16 @@ static void decode_enqueue(ember_model* m, ember_kv* kv, int B, const int32_t* s
             g.status = m->status;
             launch_gemv(g, s, m->sms);
         } else {
-            launch_rmsnorm_h(m->x, L.attn_norm, eps, B, c.hidden, m->xb, m->status, s);
+            // split K adds into a zeroed output: the norm kernel clears it
+            const bool qsplit = gemm_splits(L.p_qkv, B, EPI_STORE) > 1;
+            launch_rmsnorm_h(m->x, L.attn_norm, eps, B, c.hidden, m->xb, m->status, s,
+                             qsplit ? m->qkv : nullptr, m->qkv_n);
             GemmEpilogue e{};
             e.mode = EPI_STORE;
             e.out_f32 = m->qkv;
             e.ldo = m->qkv_n;
             e.bias = c.qkv_bias ? L.bqkv : nullptr;
-            if (gemm_splits(L.p_qkv, B, EPI_STORE) > 1) {   // split K adds into a zeroed output
-                cudaMemsetAsync(m->qkv, 0, (size_t)B * m->qkv_n * 4, s);
-                e.zeroed = 1;
-            }
+            e.zeroed = qsplit ? 1 : 0;
             e.w_exp = L.e_qkv;
             launch_gemm(L.p_qkv, B, e, m->status, s);
         }

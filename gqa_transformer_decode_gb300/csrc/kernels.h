@@ -141,9 +141,10 @@ void launch_finish(const FinishArgs& a, cudaStream_t s);
 void launch_set_cursor(int32_t* cursor, int seq, int pos, cudaStream_t s);
 
 // ------------------------------------------------------------- prefill side --
-// xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs)
+// xb[t] = f16(RMSNorm(x[t]) * w)   (A operand of the tensor-core GEMMs);
+// with zero set, also zero[t][0, zlen) = 0 (the next GEMM's split-K output)
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
-                      int* status, cudaStream_t s);
+                      int* status, cudaStream_t s, float* zero = nullptr, int zlen = 0);
 // xb[t] = bf16(RMSNorm(x[t]) * w)   (A operand of the tied-head GEMM)
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s);

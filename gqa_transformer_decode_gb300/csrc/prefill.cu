@@ -13,9 +13,12 @@ namespace ember {
 
 // ============================================================ RMSNorm rows ==
 // OUT: 0 = f32, 1 = f16 (projection GEMM operand), 2 = bf16 (tied-head GEMM operand)
+// zero (nullable): row t also clears zero[t * zlen, (t + 1) * zlen) -- the
+// split-K output of the GEMM that consumes this operand, so that no memset
+// node breaks the chain of programmatic launches.
 template <int OUT>
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w, float eps, int H,
-                                                 void* out, int* status) {
+                                                 void* out, int* status, float* zero, int zlen) {
     // one row per CTA; H % 4 == 0 and H <= 8192 (the weights are loaded into
     // registers before the wait, the row in one batch of 16-byte loads)
     constexpr int MAXV = 8;
@@ -29,6 +32,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* x, const float* w,
     }
     pdl_trigger();
     pdl_wait();
+    if (zero)
+        for (int i = threadIdx.x; i < zlen; i += 256) zero[(size_t)t * zlen + i] = 0.f;
     const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * H);
     float ss = 0.f;
 #pragma unroll
@@ -95,11 +100,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_warp(const float* x, const floa
 }
 
 void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
-                      int* status, cudaStream_t s) {
+                      int* status, cudaStream_t s, float* zero, int zlen) {
     const dim3 g((n + 7) / 8), b(256);
     // a warp per row pays off with many rows; a few rows (decode batches,
     // short prompts) keep a CTA per row so that they spread over the SMs
-    if (n >= 1024 && H % 128 == 0 && H <= 2048) {
+    if (!zero && n >= 1024 && H % 128 == 0 && H <= 2048) {
         switch (H / 128) {
 #define EMBER_RMS_WARP(NV) \
     case NV: launch_k(k_rmsnorm_warp<NV>, g, b, 0, s, x, w, eps, H, n, xb, status); return;
@@ -111,15 +116,15 @@ void launch_rmsnorm_h(const float* x, const float* w, float eps, int n, int H, u
             default: break;
         }
     }
-    launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, status);
+    launch_k(k_rmsnorm<1>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, status, zero, zlen);
 }
 void launch_rmsnorm_bf16(const float* x, const float* w, float eps, int n, int H, uint16_t* xb,
                          cudaStream_t s) {
-    launch_k(k_rmsnorm<2>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, (int*)nullptr);
+    launch_k(k_rmsnorm<2>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)xb, (int*)nullptr, (float*)nullptr, 0);
 }
 void launch_rmsnorm_f32(const float* x, const float* w, float eps, int n, int H, float* h,
                         cudaStream_t s) {
-    launch_k(k_rmsnorm<0>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h, (int*)nullptr);
+    launch_k(k_rmsnorm<0>, dim3(n), dim3(256), 0, s, x, w, eps, H, (void*)h, (int*)nullptr, (float*)nullptr, 0);
 }
 
 // =================================================== q/k norm, RoPE, K/V write ==
