@@ -459,7 +459,7 @@ bool attn_tc_supported(int D) { return D == 64 || D == 128; }
 void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
                     int nseq, int D, cudaStream_t s) {
     // more than one query tile per sequence: two tiles per CTA in ping-pong
-    if (D == 64 && a.T_per_seq > AT_BQ) launch_attn_tc2(map_q, map_k, map_vt, a, nseq, s);
+    if (a.T_per_seq > AT_BQ) launch_attn_tc2(map_q, map_k, map_vt, a, nseq, D, s);
     else if (D == 64) launch_at<64>(map_q, map_k, map_vt, a, nseq, s);
     else if (D == 128) launch_at<128>(map_q, map_k, map_vt, a, nseq, s);
 }

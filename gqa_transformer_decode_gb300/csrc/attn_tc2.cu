@@ -1,5 +1,5 @@
-// attn_tc2.cu -- whole-prompt GQA attention for head_dim 64 on the tcgen05
-// tensor cores, two query tiles per CTA in ping-pong.
+// attn_tc2.cu -- whole-prompt GQA attention for head_dim 64 and 128 on the
+// tcgen05 tensor cores, two query tiles per CTA in ping-pong.
 //
 // The same computation as k_attn_tc (attn_tc.cu): per key tile of 128 keys,
 // S = Q . K^T into TMEM, the online softmax of each query row, P (f16) and
@@ -8,7 +8,8 @@
 // that P stays in tensor memory (the A operand of P . V read from TMEM).
 // One CTA holds two 128-row query tiles A and B of one head, each with its
 // own four softmax warps (one thread per query row, all 128 score columns)
-// and its own S, P and O columns of TMEM, and the MMA warp interleaves them:
+// and its own S, P and O columns of TMEM, and the MMA warp interleaves them
+// (head_dim 64):
 //     S_A(j+1), PV_A(j)   while the B warps turn S_B(j) into P_B(j)
 //     S_B(j+1), PV_B(j)   while the A warps turn S_A(j+1) into P_A(j+1)
 // so the tensor cores work on one tile while the CUDA cores exponentiate the
@@ -17,7 +18,11 @@
 // softmax warp computes its row's P in registers while P . V(j) still reads
 // the TMEM copy of P(j), and writes P(j + 1) there once that is done.  (A
 // tcgen05.mma of M = 128, K = 16 takes ~112 cycles whatever N <= 128, so the
-// N = 64 P . V costs twice the N = 128 S and the tensor pipe sets the pace.)  Both tiles walk the key tiles of tile B (the later one); the
+// N = 64 P . V costs twice the N = 128 S and the tensor pipe sets the pace.)
+// With head_dim 128 the four accumulators fill the 512 TMEM columns, so P
+// is written over the first half of its tile's S columns and the order is
+// PV_t(j), S_t(j + 1) (the MMAs of one thread run in issue order, and S_t(j)
+// complete implies PV_t(j - 1) complete).  Both tiles walk the key tiles of tile B (the later one); the
 // causal mask zeroes tile A's share of the last one.
 // Warp 0: TMA producer (f16 Q, the f16 copy Kh of the keys and the
 // transposed Vt, as k_attn_tc reads them); warp 1:
@@ -38,29 +43,34 @@ namespace {
 constexpr int P2_THREADS = 320;
 constexpr int P2_BQ = 128;    // query rows per tile (two tiles per CTA)
 constexpr int P2_BK = 128;    // keys per tile
-constexpr int P2_D = 64;
 
+template <int D>
 struct P2Smem {
-    static constexpr int TILE = P2_BQ * 128;            // 128 rows x 64 f16 (one swizzled block)
-    static constexpr int NSTG = 4;                      // K/V ring stages
-    static constexpr int K_BYTES = P2_BK * 128;         // 128 keys x 64 f16
-    static constexpr int V_BLOCK = P2_D * 128;          // [64 dims][64 keys] f16
+    static constexpr int KB = D / 64;                   // 64-element blocks of a Q / K row
+    static constexpr int TILE = KB * P2_BQ * 128;       // one query tile: KB swizzled [128][64] blocks
+    static constexpr int NSTG = D == 64 ? 4 : 2;        // K/V ring stages
+    static constexpr int K_BYTES = KB * P2_BK * 128;    // 128 keys x D f16
+    static constexpr int V_BLOCK = D * 128;             // [D dims][64 keys] f16
     static constexpr int V_BYTES = 2 * V_BLOCK;         // 128 keys
     static constexpr int OFF_Q = 0;                     // Q_A, Q_B
     static constexpr int OFF_K = OFF_Q + 2 * TILE;
     static constexpr int OFF_V = OFF_K + NSTG * K_BYTES;
     static constexpr int OFF_BAR = OFF_V + NSTG * V_BYTES;
     static constexpr int TOTAL = OFF_BAR + 256 + 1024;     // + barriers, + alignment slack
-    // TMEM columns: S_A, S_B (128 f32 each), O_A, O_B (64 f32 each), P_A, P_B
-    // (128 f16 each, packed two to a column)
+    // TMEM columns: S_A, S_B (128 f32 each), O_A, O_B (D f32 each); P_A, P_B
+    // (128 f16 each, packed two to a column) in their own columns for head_dim
+    // 64, over the first half of S_A / S_B for 128
+    static constexpr bool ALIAS = D == 128;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0, COL_O = 256, COL_P = 384;
+    static constexpr uint32_t COL_S = 0, COL_O = 256;
+    static constexpr uint32_t col_p(int t) { return ALIAS ? COL_S + t * 128 : 384 + t * 64; }
 };
 
+template <int D>
 __global__ void __launch_bounds__(P2_THREADS, 1)
     k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, AttnTcArgs a) {
-    using L = P2Smem;
+    using L = P2Smem<D>;
     constexpr int NSTG = L::NSTG;
     extern __shared__ uint8_t p2_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p2_raw) + 1023) &
@@ -119,7 +129,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             auto issue = [&](int j) {
                 const int s = j % NSTG;
                 mbar_expect_tx(&kv_full[s], L::K_BYTES + L::V_BYTES);
-                tma_load_3d(sm + L::OFF_K + s * L::K_BYTES, &tmK, 0, j * P2_BK, vz, &kv_full[s]);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_3d(sm + L::OFF_K + s * L::K_BYTES + kb * P2_BK * 128, &tmK, kb * 64, j * P2_BK, vz,
+                                &kv_full[s]);
                 for (int kb = 0; kb < 2; ++kb)
                     tma_load_3d(sm + L::OFF_V + s * L::V_BYTES + kb * L::V_BLOCK, &tmV,
                                 j * P2_BK + kb * 64, 0, vz, &kv_full[s]);
@@ -127,7 +139,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
             const int qrow0 = z * a.T_per_seq + q_first;
             mbar_expect_tx(q_full, 2 * L::TILE);
             for (int t = 0; t < 2; ++t)
-                tma_load_2d(sm + L::OFF_Q + t * L::TILE, &tmQ, h * P2_D, qrow0 + t * P2_BQ, q_full);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_2d(sm + L::OFF_Q + t * L::TILE + kb * P2_BQ * 128, &tmQ, h * D + kb * 64,
+                                qrow0 + t * P2_BQ, q_full);
             int issued = 0;
             for (; issued < NSTG && issued < nkt; ++issued) issue(issued);
             bool fail = false;
@@ -145,14 +159,16 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {   // ------------------------------------------ MMA issuer
             constexpr uint32_t idS = idesc_f16(P2_BQ, P2_BK);
-            constexpr uint32_t idO = idesc_f16(P2_BQ, P2_D);
+            constexpr uint32_t idO = idesc_f16(P2_BQ, D);
             auto mma_s = [&](int t, int s) {   // S_t = Q_t . K(stage s)^T
                 const uint32_t q0 = smem_u32(sm + L::OFF_Q + t * L::TILE);
                 const uint32_t k0 = smem_u32(sm + L::OFF_K + s * L::K_BYTES);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_bf16(tmem + L::COL_S + t * 128, sdesc_sw128(q0 + k * 32), sdesc_sw128(k0 + k * 32),
-                              idS, k ? 1u : 0u);
+                for (int kb = 0; kb < L::KB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(tmem + L::COL_S + t * 128, sdesc_sw128(q0 + kb * P2_BQ * 128 + k * 32),
+                                  sdesc_sw128(k0 + kb * P2_BK * 128 + k * 32), idS, (kb | k) ? 1u : 0u);
                 umma_commit(&s_full[t]);
             };
             auto mma_pv = [&](int t, int s, bool acc) {   // O_t += P_t (TMEM) . V(stage s)
@@ -161,7 +177,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_f16_ts(tmem + L::COL_O + t * P2_D, tmem + L::COL_P + t * 64 + kb * 32 + k * 8,
+                        umma_f16_ts(tmem + L::COL_O + t * D, tmem + L::col_p(t) + kb * 32 + k * 8,
                                     sdesc_sw128(v0 + kb * L::V_BLOCK + k * 32), idO, (acc || kb || k) ? 1u : 0u);
                 umma_commit(&o_full[t]);
             };
@@ -177,19 +193,22 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 const bool more = j + 1 < nkt;
                 const int s1 = (j + 1) % NSTG;
                 // S_t(j + 1) may overwrite S_t(j): p_full[t] says its row
-                // values have all been read
+                // values have all been read.  With P over S (head_dim 128)
+                // P . V(j) must go first.
                 if (!mbar_wait(&p_full[0], (uint32_t)j & 1u)) break;
                 tc_fence_after();
+                if (L::ALIAS) mma_pv(0, s, j > 0);
                 if (more) {
                     if (!mbar_wait(&kv_full[s1], (uint32_t)((j + 1) / NSTG) & 1u)) break;
                     tc_fence_after();
                     mma_s(0, s1);
                 }
-                mma_pv(0, s, j > 0);
+                if (!L::ALIAS) mma_pv(0, s, j > 0);
                 if (!mbar_wait(&p_full[1], (uint32_t)j & 1u)) break;
                 tc_fence_after();
+                if (L::ALIAS) mma_pv(1, s, j > 0);
                 if (more) mma_s(1, s1);
-                mma_pv(1, s, j > 0);
+                if (!L::ALIAS) mma_pv(1, s, j > 0);
                 umma_commit(&kv_empty[s]);
             }
             if (!ok || j < nkt) sflag[0] = 1;
@@ -204,9 +223,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         const int qp = a.pos0 + row0 + r;             // this row's position
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
         const uint32_t tS = tmem + L::COL_S + t * 128 + lane_off;
-        const uint32_t tO = tmem + L::COL_O + t * P2_D + lane_off;
-        const uint32_t tP = tmem + L::COL_P + t * 64 + lane_off;
-        const float sc_log2 = 1.4426950408889634f * rsqrtf((float)P2_D);
+        const uint32_t tO = tmem + L::COL_O + t * D + lane_off;
+        const uint32_t tP = tmem + L::col_p(t) + lane_off;
+        const float sc_log2 = 1.4426950408889634f * rsqrtf((float)D);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // p = 2^(s - mr) for the row's 128 scores of the tile (masked: 0), 64
@@ -297,7 +316,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
                 tc_fence_after();
                 if (any_move) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < P2_D; c0 += 16) {
+                    for (int c0 = 0; c0 < D; c0 += 16) {
                         uint32_t o[16];
                         tmem_ld16(tO + c0, o);
                         tmem_ld_wait();
@@ -320,9 +339,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
         if (ok) {
             const float inv = 1.f / l;
             const bool live = row0 + r < a.T_per_seq;
-            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + row0 + r) * a.ld_att + h * P2_D;
+            uint16_t* out = a.att + (size_t)(z * a.T_per_seq + row0 + r) * a.ld_att + h * D;
 #pragma unroll
-            for (int c0 = 0; c0 < P2_D; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + c0, o);
                 tmem_ld_wait();
@@ -360,17 +379,24 @@ __global__ void __launch_bounds__(P2_THREADS, 1)
 
 }  // namespace
 
-void launch_attn_tc2(const void* mq, const void* mk, const void* mv, const AttnTcArgs& a, int nseq,
-                     cudaStream_t s) {
+template <int D>
+static void launch_pp(const void* mq, const void* mk, const void* mv, const AttnTcArgs& a, int nseq,
+                      cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_attn_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, P2Smem::TOTAL);
+        cudaFuncSetAttribute(k_attn_tc2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P2Smem<D>::TOTAL);
         attr = true;
     }
     dim3 grid((a.T_per_seq + 2 * P2_BQ - 1) / (2 * P2_BQ), a.NH, nseq);
-    launch_k(k_attn_tc2, grid, dim3(P2_THREADS), P2Smem::TOTAL, s,
+    launch_k(k_attn_tc2<D>, grid, dim3(P2_THREADS), P2Smem<D>::TOTAL, s,
              *reinterpret_cast<const CUtensorMap*>(mq), *reinterpret_cast<const CUtensorMap*>(mk),
              *reinterpret_cast<const CUtensorMap*>(mv), a);
+}
+
+void launch_attn_tc2(const void* mq, const void* mk, const void* mv, const AttnTcArgs& a, int nseq, int D,
+                     cudaStream_t s) {
+    if (D == 64) launch_pp<64>(mq, mk, mv, a, nseq, s);
+    else if (D == 128) launch_pp<128>(mq, mk, mv, a, nseq, s);
 }
 
 }  // namespace ember

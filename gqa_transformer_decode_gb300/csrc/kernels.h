@@ -288,9 +288,9 @@ struct AttnTcArgs {
 bool attn_tc_supported(int D);
 void launch_attn_tc(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
                     int nseq, int D, cudaStream_t s);
-// head_dim 64, two query tiles per CTA in ping-pong (attn_tc2.cu)
+// head_dim 64 / 128, two query tiles per CTA in ping-pong (attn_tc2.cu)
 void launch_attn_tc2(const void* map_q, const void* map_k, const void* map_vt, const AttnTcArgs& a,
-                     int nseq, cudaStream_t s);
+                     int nseq, int D, cudaStream_t s);
 
 // Vt[z][d][key] = f16(V[z][key][d]) and Kh[z][key][d] = f16(K[z][key][d]) for
 // keys < n_keys, 0 for keys in [n_keys, keys_pad): V (and K) rows of index
