@@ -360,7 +360,11 @@ static void launch_bn(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int*
 void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* status,
                  cudaStream_t s) {
     if (m_rows <= 0) return;
-    if (m_rows <= GEMM_BM) {   // one row tile: narrow tiles, K split for the additive epilogues
+    // one row tile: narrow tiles, K split for the additive epilogues -- except
+    // a wide argmax head (the tied LM head over the vocabulary), which the
+    // persistent kernel serves with 256-column tiles: a quarter of the tiles,
+    // so a quarter of the activation re-reads, and one key flush per row
+    if (m_rows <= GEMM_BM && !(e.mode == EPI_ARGMAX && p.N >= 16 * 256 && p.bn == 256)) {
         GemmEpilogue e2 = e;
         int ks = gemm_splits(p, m_rows, e.mode);
         if (e.mode == EPI_STORE && !e.zeroed) ks = 1;
