@@ -95,12 +95,33 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
     const int G = a.NH / a.NKV;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    // The caller's sequence indices are complete before the step starts, and
+    // the barriers are this CTA's own: both before the wait.
+    const int seq = a.seqs[b];
+    if (tid == 0) {
+        s_err = 0;
+        for (int st = 0; st < NS; ++st)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa_u32(&full[st])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     pdl_trigger();
     pdl_wait();
     const int tok_ok = __ldcg(a.tok_ok + b);
     const int pos = __ldcg(a.positions + b);   // both loads in flight together
+    // q of the G heads (rows >= G zero) and the new k / v: independent of the
+    // position, so their loads go out with it
+    constexpr int QPT = (16 * D + AM_THREADS - 1) / AM_THREADS;
+    float qreg[QPT];
+    const float* qkv = a.qkv + (size_t)b * a.ld_qkv;
+#pragma unroll
+    for (int j = 0; j < QPT; ++j) {
+        const int e = tid + j * AM_THREADS;
+        qreg[j] = (e < 16 * D && e / D < G) ? __ldcg(qkv + (size_t)g * G * D + e) : 0.f;
+    }
+    const float kvreg = tid < 2 * D ? __ldcg(qkv + (size_t)a.NH * D + (size_t)(tid / D) * a.NKV * D +
+                                              (size_t)g * D + tid % D)
+                                    : 0.f;
     if (!tok_ok) return;   // the embed kernel flagged this token
-    const int seq = a.seqs[b];
     const int n_keys = pos + 1;
     int per = (n_keys + gridDim.x - 1) / gridDim.x;
     per = per < AM_MIN_CHUNK ? AM_MIN_CHUNK : per;
@@ -120,14 +141,8 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
             tma3(kt + L::TILE + sb * AM_TK * 128, &v_map, sb * 64, lo + it * AM_TK, kz, &full[st]);
         }
     };
-    if (tid == 0) {
-        s_err = 0;
-        for (int st = 0; st < NS; ++st)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa_u32(&full[st])));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (tid == 0)
         for (int it = 0; it < NS && it < n_tiles; ++it) issue(it);
-    }
-    const float* qkv = a.qkv + (size_t)b * a.ld_qkv;
     const float* cs = a.cos_t + (size_t)pos * H2;
     const float* sn = a.sin_t + (size_t)pos * H2;
     const size_t head_off = (size_t)kz * a.max_len * D;
@@ -136,14 +151,12 @@ __global__ void __launch_bounds__(AM_THREADS) k_attn_decode_mma(const __grid_con
     const float qscale = 1.4426950408889634f * rsqrtf((float)D);   // scores in base 2
 
     // ---- q of the G heads (rows >= G zero), the new k / v; q/k norm; RoPE ----
-    for (int e = tid; e < 16 * D; e += AM_THREADS) {
-        const int h = e / D;
-        s_q[h][e % D] = h < G ? __ldcg(qkv + (size_t)g * G * D + e) : 0.f;
+#pragma unroll
+    for (int j = 0; j < QPT; ++j) {
+        const int e = tid + j * AM_THREADS;
+        if (e < 16 * D) s_q[e / D][e % D] = qreg[j];
     }
-    for (int e = tid; e < 2 * D; e += AM_THREADS) {
-        const int which = e / D, d = e % D;   // 0: k, 1: v
-        s_kv[which][d] = __ldcg(qkv + (size_t)a.NH * D + (size_t)which * a.NKV * D + (size_t)g * D + d);
-    }
+    if (tid < 2 * D) s_kv[tid / D][tid % D] = kvreg;   // 0: k, 1: v
     for (int e = tid; e < D; e += AM_THREADS) s_cs[e] = e < H2 ? cs[e] : sn[e - H2];
     __syncthreads();
     if (a.q_norm) {
