@@ -309,7 +309,7 @@ __device__ __forceinline__ float wdot4_f16(const uint4* r0, const uint4* r1, con
 
 // ================================================================== D1 ==
 constexpr int FA_KT = 128;     // keys per K/V tile (the TMA box height)
-constexpr int FA_C = 16;       // CTAs per cluster (one cluster per kv head)
+constexpr int FA_C = 16;       // CTAs per cluster at most (one cluster per kv head)
 constexpr int FA_SOLO = 384;   // up to this many keys one CTA of the cluster does the attention
 
 // Shared-memory plan of D1 (host and device compute it the same way).
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, G = a.NH / a.NKV;
-    constexpr int C = FA_C;
+    const int C = a.C;   // CTAs of the cluster (<= FA_C)
     const int Rg = (G + 2) * D;
     const bool res = a.resident != 0;
     const FaLayout Lo = fa_layout(D, G, H, a.nr, a.no, res, NW);
@@ -581,9 +581,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
                 if (a.bqkv) v += s_bias[ri];
                 if (solo) {
                     if (l8 == 0) st_async1(dsmem(&s_qkv[r0 + ri], 0), v, dsmem(&bar[3], 0));
-                } else {
-                    st_async1(dsmem(&s_qkv[r0 + ri], l8), v, dsmem(&bar[3], l8));
-                    st_async1(dsmem(&s_qkv[r0 + ri], l8 + 8), v, dsmem(&bar[3], l8 + 8));
+                } else {   // to every CTA of the cluster: lane l8 serves ranks l8, l8 + 8 (< C)
+                    for (int cc = l8; cc < C; cc += 8)
+                        st_async1(dsmem(&s_qkv[r0 + ri], cc), v, dsmem(&bar[3], cc));
                 }
             }
         }
@@ -849,20 +849,24 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
                 const int h = e / D, d = e % D;
                 // log-sum-exp merge of the C partials (empty ranges have l = 0); all
                 // 3*C remote loads are issued before the first is used
-                float mc[C], lc[C], oc[C];
+                float mc[FA_C], lc[FA_C], oc[FA_C];
 #pragma unroll
-                for (int cc = 0; cc < C; ++cc) {
-                    mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
-                    lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
-                    oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+                for (int cc = 0; cc < FA_C; ++cc) {
+                    mc[cc] = oc[cc] = 0.f;
+                    lc[cc] = 0.f;
+                    if (cc < C) {
+                        mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
+                        lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
+                        oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+                    }
                 }
                 float M = -INFINITY;
 #pragma unroll
-                for (int cc = 0; cc < C; ++cc)
+                for (int cc = 0; cc < FA_C; ++cc)
                     if (lc[cc] > 0.f) M = fmaxf(M, mc[cc]);
                 float Ls = 0.f, O = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < C; ++cc) {
+                for (int cc = 0; cc < FA_C; ++cc) {
                     if (lc[cc] > 0.f) {
                         const float f = exp2f(mc[cc] - M);
                         Ls = fmaf(lc[cc], f, Ls);
@@ -1379,6 +1383,43 @@ static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int nu
                                  : cudaOccupancyMaxActiveClusters(&n, k_fused_attn<128, 8, 8>, &cfg));
     if (e != cudaSuccess) return no("cluster occupancy query failed");
     if (n < 1) return no("a cluster of 16 CTAs does not fit");
+    // All NKV clusters should be on the chip at once: a cluster that finds no
+    // 16 SMs of one GPC free waits for another to finish (on a GB300, seven
+    // clusters of 16 fit: the eighth of a Llama-3.2-1B layer started 12 us
+    // late).  Fewer CTAs per cluster, each with more of the group's rows, as
+    // long as its shared memory allows.
+    // EMBER_FUSED_CLUSTER=c (8..15) asks for clusters of c CTAs outright (the
+    // same search, started there: tests reach the smaller clusters with it)
+    const char* want = getenv("EMBER_FUSED_CLUSTER");
+    const int cwant = want ? atoi(want) : 0;
+    if (!p.part && (n < NKV || (cwant >= 8 && cwant < C))) {
+        for (int c2 = (cwant >= 8 && cwant < C) ? cwant : C - 1; c2 >= 8; --c2) {
+            const int nr2 = ((G + 2) * D + c2 - 1) / c2, no2 = (H + c2 - 1) / c2;
+            int sm2 = fa_layout(D, G, H, nr2, no2, false).total;
+            if (sm2 < 116 * 1024) sm2 = 116 * 1024;
+            if (sm2 > 200 * 1024) break;
+            cfg.gridDim = dim3(c2, NKV);
+            cfg.dynamicSmemBytes = sm2;
+            at[0].val.clusterDim.x = c2;
+            int n2 = 0;
+            e = D == 64 ? (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n2, k_fused_attn<64, 4, 8>, &cfg)
+                                      : cudaOccupancyMaxActiveClusters(&n2, k_fused_attn<64, 8, 8>, &cfg))
+                        : (p.xi == 4 ? cudaOccupancyMaxActiveClusters(&n2, k_fused_attn<128, 4, 8>, &cfg)
+                                      : cudaOccupancyMaxActiveClusters(&n2, k_fused_attn<128, 8, 8>, &cfg));
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                e = cudaSuccess;
+                break;
+            }
+            if (n2 >= NKV || c2 == cwant) {
+                p.C = c2;
+                p.nr = nr2;
+                p.no = no2;
+                p.smem_attn = sm2;
+                break;
+            }
+        }
+    }
     p.ok = true;
     p.why = "";
     return true;

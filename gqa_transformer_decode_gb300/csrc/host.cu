@@ -287,9 +287,9 @@ ember_status ember_model_create(const ember_config* cfg, const ember_weights* w,
     if (c.causal && !c.weights_q8 && !(getenv("EMBER_NO_FUSED") && atoi(getenv("EMBER_NO_FUSED"))))
         fused_decode_plan(m->fp, H, c.n_heads, NKV, D, F, m->sms);
     if (getenv("EMBER_VERBOSE") && atoi(getenv("EMBER_VERBOSE")))
-        fprintf(stderr, "ember: fused batch-1 decode %s%s (%s, attention smem %d, MLP grid %d smem %d fc %d ns %d)\n",
+        fprintf(stderr, "ember: fused batch-1 decode %s%s (%s, clusters of %d, attention smem %d, MLP grid %d smem %d fc %d ns %d)\n",
                 m->fp.ok ? "on" : "off: ", m->fp.ok ? "" : m->fp.why,
-                m->fp.part ? "partitioned" : (m->fp.resident ? "resident MLP" : "MLP ring"), m->fp.smem_attn,
+                m->fp.part ? "partitioned" : (m->fp.resident ? "resident MLP" : "MLP ring"), m->fp.C, m->fp.smem_attn,
                 m->fp.mlp_grid, m->fp.smem_mlp, m->fp.fc, m->fp.ns);
 
     // ---- weights ----

@@ -329,6 +329,34 @@ def test_fused_batch1_decode_matches_oracle(shape, n_prompt, n_steps, seq, strea
     assert E.ember_kernel_launches() - l0 == 2 * shape.layers + 3
 
 
+@pytest.mark.parametrize("shape,n_prompt,cl", [(MID_LLAMA, 2100, 12), (MID_QWEN2, 500, 9),
+                                             (MID_D128, 700, 11)])
+def test_fused_batch1_decode_with_smaller_clusters(shape, n_prompt, cl, stream, monkeypatch):
+    """Batch-1 decode on clusters of fewer than 16 CTAs (the plan's choice
+    when 16-CTA clusters for every kv head do not fit on the chip at once),
+    over contexts past the single-CTA range so that every CTA of the cluster
+    takes keys, receives every q/k/v row and merges a slice of the heads."""
+    from gqa_transformer_decode_gb300 import ember as E
+    monkeypatch.setenv("EMBER_FUSED_CLUSTER", str(cl))
+    w = synth.weights_bf16(shape)
+    gm = R.Model(shape, w, max_tokens=max(512, n_prompt + 16))
+    monkeypatch.delenv("EMBER_FUSED_CLUSTER")
+    om = model_pair(shape)[1]
+    n_steps = 4
+    prompt = synth.prompt_ids(shape, n_prompt)
+    toks, olg, _ = om.greedy(prompt, n_steps)
+    kv = gm.kv_alloc(1, n_prompt + n_steps + 8)
+    glg, gam, _ = run_greedy_gpu(gm, kv, prompt, n_steps, toks[:-1], stream)
+    assert_close(olg, glg, "logits")
+    assert_tokens(olg, toks, gam, "greedy tokens")
+    l0 = E.ember_kernel_launches()   # still the fused path: embed, 2 per layer, head, finish
+    with torch.cuda.stream(stream):
+        gm.decode_step(kv, i32([0]), i32([toks[-1]]), i32([n_prompt + n_steps]), stream=stream)
+    assert gm.sync_status(stream) == 0
+    assert E.ember_kernel_launches() - l0 == 2 * shape.layers + 3
+    gm.close()
+
+
 def test_traced_decode_step_matches_the_step_and_names_its_launches(stream):
     """ember_decode_step_traced computes the same step (logits, argmax, cache
     cursor) as ember_decode_step and reports every launch in order: embed, an
