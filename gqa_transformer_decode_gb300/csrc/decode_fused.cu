@@ -954,13 +954,18 @@ __global__ void __launch_bounds__(FM_THREADS, 2) k_fused_mlp(FusedMlpArgs a) {
         prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
         prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
     }
-    // the first pf_late CTAs prefetch the chunks of the last pf_late CTAs,
-    // which launch only when the attention CTAs leave their SMs
-    if ((int)blockIdx.x < a.pf_late) {
-        const int lb = (int)gridDim.x - a.pf_late + (int)blockIdx.x;
-        for (int ch = lb + tid * (int)gridDim.x; ch < n_chunks; ch += FM_THREADS * (int)gridDim.x) {
-            prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
-            prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
+    // The last pf_late CTAs launch only when the attention CTAs leave their
+    // SMs; the E CTAs before them run beside the attention, so CTA b < E
+    // prefetches the chunks of late CTAs E + b, E + b + E, ... into L2 while
+    // the attention block computes.
+    {
+        const int E = (int)gridDim.x - a.pf_late;
+        if (a.pf_late > 0 && E > 0 && (int)blockIdx.x < E) {
+            for (int lb = E + (int)blockIdx.x; lb < (int)gridDim.x; lb += E)
+                for (int ch = lb + tid * (int)gridDim.x; ch < n_chunks; ch += FM_THREADS * (int)gridDim.x) {
+                    prefetch_l2(a.wgu + (size_t)ch * 2 * FC * H, (uint32_t)(4 * FC * H));
+                    prefetch_l2(a.wdT + (size_t)ch * FC * H, (uint32_t)(2 * FC * H));
+                }
         }
     }
     ResidualNorm rn;
@@ -1326,6 +1331,9 @@ static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int nu
         if (ns < 2) ns = 2;
         p.ns = ns;
         p.smem_mlp = ns * stage + fixed;
+        // without room beside an attention CTA, the MLP CTAs on the
+        // attention's SMs start late: the others prefetch their chunks
+        if (!coresident) p.pf_late = C * NKV < p.mlp_grid ? C * NKV : 0;
     }
     if (p.smem_mlp > 227 * 1024) return no("MLP ring does not fit shared memory");
     }   // !p.part
@@ -1416,6 +1424,7 @@ static bool plan_impl(FusedPlan& p, int H, int NH, int NKV, int D, int F, int nu
                 p.nr = nr2;
                 p.no = no2;
                 p.smem_attn = sm2;
+                if (p.pf_late) p.pf_late = c2 * NKV < p.mlp_grid ? c2 * NKV : 0;   // the attention's SMs
                 break;
             }
         }

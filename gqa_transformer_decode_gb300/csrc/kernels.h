@@ -325,7 +325,7 @@ struct FusedPlan {
     bool part = false;       // partitioned: attention and MLP blocks on disjoint SMs, all weights resident
     int zs = ZSLOTS;         // copies of the MLP block's split-K accumulator (1..ZSLOTS)
     int mlp_delay_ns = 0;    // partitioned: MLP weight copies start this long after the CTA arrives
-    int pf_late = 0;         // CTAs whose chunks the first CTAs prefetch to L2 (resident plan)
+    int pf_late = 0;         // MLP CTAs that start after the attention (their chunks are prefetched to L2)
     bool ok = false;
     const char* why = "not planned";   // reason when !ok
 };
@@ -378,7 +378,7 @@ struct FusedMlpArgs {
     float* z_acc;
     int* status;
     int ns;
-    int pf_late;                 // the first pf_late CTAs prefetch the last pf_late CTAs' chunks to L2
+    int pf_late;                 // the last pf_late CTAs start late: the others prefetch their chunks to L2
     int load_delay_ns;           // partitioned plan: delay of the weight copies after the CTA arrives
     int gu_exp, d_exp;           // storage scales of wgu / wdT (2^-e), undone on the products
     int zs;                      // accumulator copies to add into (CTA index % zs)
