@@ -304,9 +304,13 @@ static bool make_map(void* out, const uint16_t* ptr, int rows, int ld, int K, in
     return encode_map_bf16(out, ptr, 2, dims, strides, box);
 }
 
+// N tile of the many-row GEMM: an M = 128, N = 256 tcgen05.mma takes ~171
+// cycles against ~112 for N = 128 (the minimum per instruction), so 256
+// columns do 31 % more work per cycle -- worth a partly empty last tile
+// unless N is small
 static int pick_bn(int N) {
     if (N <= 64) return 64;
-    if (N <= 1024) return 128;
+    if (N <= 512) return 128;
     return 256;
 }
 

@@ -73,6 +73,25 @@ def test_qwen25_05b_prefill_and_decode(stream):
     assert all(gam[i] == first_argmax(glg[i]) for i in range(len(gam)))
 
 
+def test_qwen25_05b_q8_0_weights(stream):
+    """Qwen2.5-0.5B shape with q8_0 layer weights (the bench's q8_0 line):
+    the 128-token prompt (tensor-core GEMMs on the f16 copy of the decoded
+    values) and 16 greedy steps (q8_0 GEMVs) against the oracle run on the
+    decoded weights."""
+    name = "qwen2.5-0.5b"
+    shape = synth.WORKLOADS[name].model
+    w = weights(name)
+    prompt = synth.prompt_ids(shape, 128)
+    om = O.OracleModel(shape, O.q8_0_layer_weights(w, shape.layers))
+    toks, olg, _ = om.greedy(prompt, 16, kv_bf16=True)
+    m = R.Model(shape, w, max_tokens=128, weights_q8=1)
+    kv = m.kv_alloc(1, 128 + 24)
+    glg, gam, _ = greedy_gpu(m, kv, prompt, toks[:-1], stream)
+    assert_close(olg, glg, "q8_0 logits")
+    assert_tokens(olg, toks, gam, "q8_0 greedy tokens")
+    assert all(gam[i] == first_argmax(glg[i]) for i in range(len(gam)))
+
+
 def test_llama32_1b_prefix_and_full_prompt(stream):
     """Llama-3.2-1B shape: a 128-token prefix and 4 steps against the oracle;
     the benchmark's 2048-token prefill then reproduces the prefix's hidden
