@@ -373,10 +373,11 @@ __global__ void __launch_bounds__(256) k_vt(VtArgs a) {
         uint16_t* kd = a.kh + (size_t)z * a.keys_pad * D;
         for (int e = threadIdx.x; e < 64 * D; e += blockDim.x) {
             const int k = e / D, d = e % D;
-            if (key0 + k < a.keys_pad)
-                kd[(size_t)(key0 + k) * D + d] =
-                    key0 + k < a.n_keys ? __half_as_ushort(__float2half_rn(bf16_to_f32(ks[(size_t)(key0 + k) * D + d])))
-                                        : (uint16_t)0;
+            const int key = key0 + k;
+            if (key < a.keys_pad && (key < a.kh_from || key >= a.n_keys))
+                kd[(size_t)key * D + d] =
+                    key < a.n_keys ? __half_as_ushort(__float2half_rn(bf16_to_f32(ks[(size_t)key * D + d])))
+                                   : (uint16_t)0;
         }
     }
 }
@@ -421,6 +422,7 @@ __global__ void __launch_bounds__(256) k_vt16(VtArgs a) {
         for (int e = threadIdx.x; e < 64 * C8; e += blockDim.x) {
             const int k = e / C8, c = e % C8;
             if (key0 + k >= a.keys_pad) continue;
+            if (key0 + k >= a.kh_from && key0 + k < a.n_keys) continue;   // written by the RoPE kernel
             uint4 u = make_uint4(0, 0, 0, 0);
             if (key0 + k < a.n_keys) {
                 const uint4 b = *reinterpret_cast<const uint4*>(ks + (size_t)(key0 + k) * D + 8 * c);

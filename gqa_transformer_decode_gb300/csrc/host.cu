@@ -730,6 +730,10 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
     r.vc = cv.v;
     r.seq_stride = cv.seq_stride;
     r.head_stride = cv.head_stride;
+    if (cv.kh_map && cv.vt_map) {   // the attention's f16 K rows of the new tokens
+        r.kh = cv.kh;
+        r.kh_pad = cv.keys_pad;
+    }
     launch_rope_kv(r, s);
     if (cv.kh_map && cv.vt_map) {   // tensor-core attention
         const int nseq = n / cv.T_per_seq;
@@ -745,6 +749,7 @@ static void layer_tc(ember_model* m, int l, int n, const CacheView& cv, cudaStre
         va.n_keys = n_keys;
         va.keys_pad = cv.keys_pad;
         va.vt = cv.vt;
+        va.kh_from = cv.pos0;   // Kh of the new tokens came with the RoPE kernel
         launch_vt(va, nseq * c.n_kv_heads, s);
         AttnTcArgs ta{};
         ta.T_per_seq = cv.T_per_seq;

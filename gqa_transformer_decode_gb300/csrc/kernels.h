@@ -169,6 +169,11 @@ struct RopeKVArgs {
     uint16_t* kc;
     uint16_t* vc;
     long long seq_stride, head_stride;
+    // nullable: the f16 copy of each new K row (the value the bf16 cache
+    // holds) also goes to kh[(z * NKV + g) * kh_pad + pos][D], the tensor-core
+    // attention's K operand
+    uint16_t* kh;
+    int kh_pad;
 };
 void launch_rope_kv(const RopeKVArgs& a, cudaStream_t s);
 
@@ -295,12 +300,14 @@ void launch_attn_tc2(const void* map_q, const void* map_k, const void* map_vt, c
 // Vt[z][d][key] = f16(V[z][key][d]) and Kh[z][key][d] = f16(K[z][key][d]) for
 // keys < n_keys, 0 for keys in [n_keys, keys_pad): V (and K) rows of index
 // z = (z / nkv, z % nkv) start at v + (z/nkv)*v_z_stride + (z%nkv)*v_h_stride
-// (the same offsets from k).  kh may be null.
+// (the same offsets from k).  kh may be null; Kh rows in [kh_from, n_keys)
+// are left alone (the RoPE kernel wrote them).
 struct VtArgs {
     const uint16_t *v, *k;
     long long v_z_stride, v_h_stride;
     int nkv, D, n_keys, keys_pad;
     uint16_t *vt, *kh;
+    int kh_from;
 };
 void launch_vt(const VtArgs& a, int zs, cudaStream_t s);
 

@@ -167,6 +167,13 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
                     dst = a.q_out + (size_t)t * nq + h * D;
                 } else {
                     dst = a.kc + z * a.seq_stride + (h - a.NH) * a.head_stride + (long long)pos * D;
+                    if (a.kh) {   // the same bf16 values, as f16
+                        uint16_t* kd = a.kh + ((size_t)(z * a.NKV + h - a.NH) * a.kh_pad + pos) * D;
+                        *reinterpret_cast<uint2*>(kd + i0) =
+                            make_uint2(pack_f16x2(bf16_lo(lo.x), bf16_hi(lo.x)), pack_f16x2(bf16_lo(lo.y), bf16_hi(lo.y)));
+                        *reinterpret_cast<uint2*>(kd + H2 + i0) =
+                            make_uint2(pack_f16x2(bf16_lo(hi.x), bf16_hi(hi.x)), pack_f16x2(bf16_lo(hi.y), bf16_hi(hi.y)));
+                    }
                 }
                 *reinterpret_cast<uint2*>(dst + i0) = lo;
                 *reinterpret_cast<uint2*>(dst + H2 + i0) = hi;
@@ -221,6 +228,17 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
                 dst[i0] = isq ? f32_to_f16(r0[0]) : f32_to_bf16(r0[0]);
                 dst[H2 + i0] = isq ? f32_to_f16(r1[0]) : f32_to_bf16(r1[0]);
             }
+            if (!isq && a.kh) {   // the same bf16 values, as f16
+                uint16_t* kd = a.kh + ((size_t)(z * a.NKV + h - a.NH) * a.kh_pad + pos) * D;
+                if (PPL == 2) {
+                    const uint32_t b0 = pack_bf16x2(r0[0], r0[1]), b1 = pack_bf16x2(r1[0], r1[1]);
+                    *reinterpret_cast<uint32_t*>(kd + i0) = pack_f16x2(bf16_lo(b0), bf16_hi(b0));
+                    *reinterpret_cast<uint32_t*>(kd + H2 + i0) = pack_f16x2(bf16_lo(b1), bf16_hi(b1));
+                } else {
+                    kd[i0] = f32_to_f16(bf16_to_f32(f32_to_bf16(r0[0])));
+                    kd[H2 + i0] = f32_to_f16(bf16_to_f32(f32_to_bf16(r1[0])));
+                }
+            }
         }
         for (int f = tid * 4; f < nkv; f += blockDim.x * 4) {   // V rows: bf16 into the cache
             const int g = f / D, d = f % D;
@@ -260,6 +278,11 @@ __global__ void __launch_bounds__(128) k_rope_kv(RopeKVArgs a) {
             uint16_t* kr = a.kc + z * a.seq_stride + g * a.head_stride + (long long)pos * D;
             kr[i] = f32_to_bf16(r0);
             kr[i + H2] = f32_to_bf16(r1);
+            if (a.kh) {   // the same bf16 values, as f16
+                uint16_t* kd = a.kh + ((size_t)(z * a.NKV + g) * a.kh_pad + pos) * D;
+                kd[i] = f32_to_f16(bf16_to_f32(kr[i]));
+                kd[i + H2] = f32_to_f16(bf16_to_f32(kr[i + H2]));
+            }
         }
     }
     for (int e = tid; e < nkv; e += blockDim.x) {
