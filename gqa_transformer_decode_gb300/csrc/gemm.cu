@@ -4,8 +4,11 @@
 //   D[M,N] = A[M,K] . B[N,K]^T      A: activations (bf16, K contiguous)
 //                                   B: weights, HF [out, in] (bf16, K contiguous)
 //
-// One CTA computes a BM x BN tile (BM = 128 rows of A = 128 TMEM lanes, BN f32
-// accumulator columns).  Warp roles:
+// k_gemm_tc serves calls of at most one row tile (decode batches up to 128
+// tokens, narrow heads), with 64-column tiles and the K range split over
+// grid.z for the additive epilogues; more rows go to the persistent kernel
+// (gemm_persistent.cu).  One CTA computes a BM x BN tile (BM = 128 rows of
+// A = 128 TMEM lanes, BN f32 accumulator columns).  Warp roles:
 //   warp 0   one thread issues the TMA loads of A and B k-blocks (BK = 64
 //            elements = one 128-byte swizzle span) into a STAGES-deep ring;
 //   warp 1   allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
@@ -21,8 +24,6 @@
 // (SwiGLU) and down (+residual) of ember scripts/reference_forward.py
 // forward(), in the whole-sequence form of LowLlamaBasic reference.py.
 #include <cudaTypedefs.h>
-
-#include <cstdlib>
 
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -376,19 +377,10 @@ void launch_gemm(const GemmPlan& p, int m_rows, const GemmEpilogue& e, int* stat
         launch_bn<64, 8>(p, m_rows, e2, status, s, ks);
         return;
     }
-    // persistent tiles with a double-buffered accumulator (EMBER_GEMM_TILED=1: one CTA per tile)
-    static const bool tiled = getenv("EMBER_GEMM_TILED") && atoi(getenv("EMBER_GEMM_TILED"));
-    if (!tiled) {
-        const uint32_t idesc = p.f16 ? (p.bn == 64 ? idesc_f16(GEMM_BM, 64) : p.bn == 128 ? idesc_f16(GEMM_BM, 128) : idesc_f16(GEMM_BM, 256))
-                                     : (p.bn == 64 ? idesc_bf16(GEMM_BM, 64) : p.bn == 128 ? idesc_bf16(GEMM_BM, 128) : idesc_bf16(GEMM_BM, 256));
-        launch_gemm_persistent(p.tmA, p.tmB, p.bn, m_rows, p.N, p.K, idesc, e, status, p.sms, s);
-        return;
-    }
-    switch (p.bn) {
-        case 64: launch_bn<64, 8>(p, m_rows, e, status, s); break;
-        case 128: launch_bn<128, 6>(p, m_rows, e, status, s); break;
-        default: launch_bn<256, 4>(p, m_rows, e, status, s); break;
-    }
+    // many rows: persistent tiles with a double-buffered accumulator
+    const uint32_t idesc = p.f16 ? (p.bn == 64 ? idesc_f16(GEMM_BM, 64) : p.bn == 128 ? idesc_f16(GEMM_BM, 128) : idesc_f16(GEMM_BM, 256))
+                                 : (p.bn == 64 ? idesc_bf16(GEMM_BM, 64) : p.bn == 128 ? idesc_bf16(GEMM_BM, 128) : idesc_bf16(GEMM_BM, 256));
+    launch_gemm_persistent(p.tmA, p.tmB, p.bn, m_rows, p.N, p.K, idesc, e, status, p.sms, s);
 }
 
 }  // namespace ember
