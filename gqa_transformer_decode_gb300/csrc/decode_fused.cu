@@ -70,6 +70,12 @@ __device__ __forceinline__ void st_async4(uint32_t addr, float a, float b, float
                  "r"(bar)
                  : "memory");
 }
+// 8-byte store (two 32-bit words), 8 bytes on the remote mbarrier
+__device__ __forceinline__ void st_async2u(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void st_async1(uint32_t addr, float a, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
                  "r"(__float_as_uint(a)), "r"(bar)
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + Lo.x);  // normed input, f16
     float* s_qkv = reinterpret_cast<float*>(sm + Lo.qkv);    // [G*D q | D k | D v]
     float* s_part = reinterpret_cast<float*>(sm + Lo.part);  // [G][m, l, acc[D]]
-    float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads
+    float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads (f32; f16 from a solo CTA 0)
     uint8_t* sQh = sm + Lo.qh;                                 // [16][D] f16, swizzled
     float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [NW][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
@@ -554,7 +560,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
             issue_tile(lo, 0, kz);
         }
         if (attn_cta) mbar_expect_tx(&bar[3], (uint32_t)(Rg * 4));
-        mbar_expect_tx(&bar[4], (uint32_t)(GD * 4));
+        mbar_expect_tx(&bar[4], (uint32_t)(GD * (solo ? 2 : 4)));
     }
     float cs_v = 0.f;   // RoPE row of pos (cos | sin), stored to shared memory after the rows
     if (attn_cta && ok && tid < D)
@@ -805,7 +811,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
             }
         }
         __syncthreads();
-        if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA
+        if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA,
+                      // already rounded to the f16 of the o_proj operand (half the bytes to send)
+            bool bad = false;
+            uint16_t* s_atth = reinterpret_cast<uint16_t*>(s_att);
             for (int e = 4 * tid; e < GD; e += 4 * NTH) {   // D % 4 == 0: one head per quad
                 const int hh = e / D, d = e % D;
                 float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
@@ -821,9 +830,11 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
                 const float l = s_ml[2 * hh + 1];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 O0 *= inv; O1 *= inv; O2 *= inv; O3 *= inv;
-#pragma unroll
-                for (int cc = 0; cc < C; ++cc) st_async4(dsmem(&s_att[e], cc), O0, O1, O2, O3, dsmem(&bar[4], cc));
+                const uint32_t h01 = pack_f16x2_chk(O0, O1, bad), h23 = pack_f16x2_chk(O2, O3, bad);
+#pragma unroll 4
+                for (int cc = 0; cc < C; ++cc) st_async2u(dsmem(&s_atth[e], cc), h01, h23, dsmem(&bar[4], cc));
             }
+            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
         } else {
         // this CTA's partial (m, l, acc) per head, for the merge across the cluster
         for (int e = tid; e < G * (D + 2); e += NTH) {
@@ -888,9 +899,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
     {
         XRegs<XI> xr;
-        bool bad = false;
-        xr.load_f32(s_att, GD / 8, bad);
-        if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+        if (solo) {
+            xr.load(reinterpret_cast<const uint16_t*>(s_att), GD / 8);
+        } else {
+            bool bad = false;
+            xr.load_f32(s_att, GD / 8, bad);
+            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
+        }
         const int nrow = o1 - o0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
         for (int base = warp * 4; base < nrow; base += NTH / 8) {   // 4 rows per warp
