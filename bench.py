@@ -334,7 +334,9 @@ NCU_TRAFFIC = {}
 # bytes), from an ncu capture of this build's kernels (dram__bytes_read.sum +
 # dram__bytes_write.sum of every launch in the "decode/" range, one step of
 # 51 launches); a workload without a capture of the current kernels reports null.
-NCU_STEP_TRAFFIC = {"qwen2.5-0.5b": 996055433, "llama-3.2-1b": 2555069312}
+# (The last batch-1 captures predate the f16 cluster broadcast of the fused
+# attention's merged heads, so no workload has one.)
+NCU_STEP_TRAFFIC = {}
 
 
 def decode_roofline(job, hbm_peak):

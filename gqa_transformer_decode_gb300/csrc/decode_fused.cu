@@ -62,15 +62,9 @@ __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
-// 16-byte store into the shared memory of a CTA of this cluster whose
-// completion counts 16 bytes on that CTA's mbarrier (both addresses from mapa)
-__device__ __forceinline__ void st_async4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
-                 "r"(bar)
-                 : "memory");
-}
-// 8-byte store (two 32-bit words), 8 bytes on the remote mbarrier
+// 8-byte store (two 32-bit words) into the shared memory of a CTA of this
+// cluster whose completion counts 8 bytes on that CTA's mbarrier (both
+// addresses from mapa)
 __device__ __forceinline__ void st_async2u(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
                  "r"(a), "r"(b), "r"(bar)
@@ -240,21 +234,6 @@ struct XRegs {
             v[i] = c < n8 ? reinterpret_cast<const uint4*>(xh)[c] : make_uint4(0, 0, 0, 0);
         }
     }
-    __device__ __forceinline__ void load_f32(const float* x, int n8, bool& bad) {  // f32 input, rounded to f16
-        const int lane = threadIdx.x & 31;
-#pragma unroll
-        for (int i = 0; i < XI; ++i) {
-            const int c = lane + 32 * i;
-            if (c < n8) {
-                const float4 a = reinterpret_cast<const float4*>(x)[2 * c];
-                const float4 b = reinterpret_cast<const float4*>(x)[2 * c + 1];
-                v[i] = make_uint4(pack_f16x2_chk(a.x, a.y, bad), pack_f16x2_chk(a.z, a.w, bad),
-                                  pack_f16x2_chk(b.x, b.y, bad), pack_f16x2_chk(b.z, b.w, bad));
-            } else {
-                v[i] = make_uint4(0, 0, 0, 0);
-            }
-        }
-    }
 };
 // Two f16 products accumulated in f32 (fma.rn.f32.f16 takes f16 operands,
 // which are exact in f32, so this rounds exactly like fmaf on the converted
@@ -382,7 +361,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
     uint16_t* s_xh = reinterpret_cast<uint16_t*>(sm + Lo.x);  // normed input, f16
     float* s_qkv = reinterpret_cast<float*>(sm + Lo.qkv);    // [G*D q | D k | D v]
     float* s_part = reinterpret_cast<float*>(sm + Lo.part);  // [G][m, l, acc[D]]
-    float* s_att = reinterpret_cast<float*>(sm + Lo.att);    // [G*D] merged heads (f32; f16 from a solo CTA 0)
+    uint16_t* s_atth = reinterpret_cast<uint16_t*>(sm + Lo.att);   // [G*D] merged heads, f16
     uint8_t* sQh = sm + Lo.qh;                                 // [16][D] f16, swizzled
     float* s_wm = reinterpret_cast<float*>(sm + Lo.wm);      // [NW][G][D + 2]
     float* s_red = reinterpret_cast<float*>(sm + Lo.red);
@@ -560,7 +539,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
             issue_tile(lo, 0, kz);
         }
         if (attn_cta) mbar_expect_tx(&bar[3], (uint32_t)(Rg * 4));
-        mbar_expect_tx(&bar[4], (uint32_t)(GD * (solo ? 2 : 4)));
+        mbar_expect_tx(&bar[4], (uint32_t)(GD * 2));
     }
     float cs_v = 0.f;   // RoPE row of pos (cos | sin), stored to shared memory after the rows
     if (attn_cta && ok && tid < D)
@@ -811,10 +790,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
             }
         }
         __syncthreads();
-        if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA,
-                      // already rounded to the f16 of the o_proj operand (half the bytes to send)
-            bool bad = false;
-            uint16_t* s_atth = reinterpret_cast<uint16_t*>(s_att);
+        // the merged heads go out already rounded to the f16 of the o_proj
+        // operand (half the bytes of f32; the range check is the sender's)
+        bool bad = false;
+        if (solo) {   // CTA 0 holds the whole softmax: normalise and send the heads to every CTA
             for (int e = 4 * tid; e < GD; e += 4 * NTH) {   // D % 4 == 0: one head per quad
                 const int hh = e / D, d = e % D;
                 float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
@@ -834,7 +813,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
 #pragma unroll 4
                 for (int cc = 0; cc < C; ++cc) st_async2u(dsmem(&s_atth[e], cc), h01, h23, dsmem(&bar[4], cc));
             }
-            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
         } else {
         // this CTA's partial (m, l, acc) per head, for the merge across the cluster
         for (int e = tid; e < G * (D + 2); e += NTH) {
@@ -852,60 +830,61 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) k_fused_attn(const _
         }
         cluster_sync_all();   // every CTA's partial is in its shared memory
 
-        // ---- merge: CTA r merges elements [r*ne, (r+1)*ne) and broadcasts them ----
+        // ---- merge: CTA r merges element pairs [r*np, (r+1)*np) and broadcasts them ----
         {
-            const int ne = (GD + C - 1) / C;
-            const int e = r * ne + tid;
-            if (tid < ne && e < GD) {
+            const int GP = GD / 2;   // D is even: a pair never straddles two heads
+            const int np = (GP + C - 1) / C;
+            const int pi = r * np + tid;
+            if (tid < np && pi < GP) {
+                const int e = 2 * pi;
                 const int h = e / D, d = e % D;
                 // log-sum-exp merge of the C partials (empty ranges have l = 0); all
-                // 3*C remote loads are issued before the first is used
-                float mc[FA_C], lc[FA_C], oc[FA_C];
+                // 4*C remote loads are issued before the first is used
+                float mc[FA_C], lc[FA_C], oa[FA_C], ob[FA_C];
 #pragma unroll
                 for (int cc = 0; cc < FA_C; ++cc) {
-                    mc[cc] = oc[cc] = 0.f;
+                    mc[cc] = oa[cc] = ob[cc] = 0.f;
                     lc[cc] = 0.f;
                     if (cc < C) {
                         mc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2)], cc));
                         lc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 1], cc));
-                        oc[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+                        oa[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 2 + d], cc));
+                        ob[cc] = ld_dsmem(dsmem(&s_part[h * (D + 2) + 3 + d], cc));
                     }
                 }
                 float M = -INFINITY;
 #pragma unroll
                 for (int cc = 0; cc < FA_C; ++cc)
                     if (lc[cc] > 0.f) M = fmaxf(M, mc[cc]);
-                float Ls = 0.f, O = 0.f;
+                float Ls = 0.f, Oa = 0.f, Ob = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < FA_C; ++cc) {
                     if (lc[cc] > 0.f) {
                         const float f = exp2f(mc[cc] - M);
                         Ls = fmaf(lc[cc], f, Ls);
-                        O = fmaf(oc[cc], f, O);
+                        Oa = fmaf(oa[cc], f, Oa);
+                        Ob = fmaf(ob[cc], f, Ob);
                     }
                 }
-                O = Ls > 0.f ? O / Ls : 0.f;
-#pragma unroll
-                for (int cc = 0; cc < C; ++cc) st_async1(dsmem(&s_att[e], cc), O, dsmem(&bar[4], cc));
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                const uint32_t hab = pack_f16x2_chk(Oa * inv, Ob * inv, bad);
+#pragma unroll 4
+                for (int cc = 0; cc < C; ++cc)
+                    st_async1(dsmem(&s_atth[e], cc), __uint_as_float(hab), dsmem(&bar[4], cc));
             }
         }
         }   // !solo
+        if (bad) raise_status(a.status, EMBER_ERR_RANGE);
     }   // attn_cta
-    // the merged heads, GD floats from the cluster; a CTA leaves only after
-    // every store aimed at its shared memory has landed
+    // the merged heads, GD f16 values from the cluster; a CTA leaves only
+    // after every store aimed at its shared memory has landed
     if (!mbar_wait_cluster(&bar[4], 0)) s_err = 1;
 
     // ---- o_proj: this CTA's rows of the group's column block, into the residual ----
     if (o1 > o0 && !mbar_wait(&bar[2], 0)) s_err = 1;
     {
         XRegs<XI> xr;
-        if (solo) {
-            xr.load(reinterpret_cast<const uint16_t*>(s_att), GD / 8);
-        } else {
-            bool bad = false;
-            xr.load_f32(s_att, GD / 8, bad);
-            if (bad) raise_status(a.status, EMBER_ERR_RANGE);
-        }
+        xr.load(s_atth, GD / 8);
         const int nrow = o1 - o0;
         const int my = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
         for (int base = warp * 4; base < nrow; base += NTH / 8) {   // 4 rows per warp
