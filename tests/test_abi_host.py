@@ -41,9 +41,9 @@ def test_kv_bytes_matches_the_pages_worked_example():
     assert abs(f32_bytes / 2 / 2 ** 20 - g["stated_total_mb"]) < 0.5
 
 
-def _create(shape, **over):
+def _create(shape, weights_q8=0, **over):
     d = {**shape.asdict(), **over}
-    cfg = E.make_config(d)
+    cfg = E.make_config(d, weights_q8=weights_q8)
     w = E.ember_weights()
     out = C.c_void_p()
     st = E.load().ember_model_create(C.byref(cfg), C.byref(w), C.byref(out))
@@ -70,3 +70,16 @@ def test_missing_weights_are_reported():
 def test_unsupported_shapes_say_so():
     st, err = _create(synth.TINY, head_dim=24, n_heads=4, n_kv_heads=2)
     assert st == 8 and "head_dim" in err
+
+
+@pytest.mark.parametrize("q8,over,status,msg", [
+    (2, dict(), 1, "weights_q8 must be 0 or 1"),
+    # q8_0 blocks of 32 along every layer matrix's input dimension
+    (1, dict(hidden=112, n_heads=7, n_kv_heads=1, head_dim=16, ff=160), 8, "multiples of 32"),
+    (0, dict(n_heads=34, n_kv_heads=2), 8, "GQA group > 16"),
+    (0, dict(hidden=8200), 8, "hidden > 8192"),
+    (0, dict(hidden=100), 8, "multiples of 8"),
+])
+def test_limits_and_the_q8_0_flag_are_checked_before_any_device_work(q8, over, status, msg):
+    st, err = _create(synth.TINY, weights_q8=q8, **over)
+    assert st == status and msg in err, (st, err)
