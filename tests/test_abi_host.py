@@ -83,3 +83,35 @@ def test_unsupported_shapes_say_so():
 def test_limits_and_the_q8_0_flag_are_checked_before_any_device_work(q8, over, status, msg):
     st, err = _create(synth.TINY, weights_q8=q8, **over)
     assert st == status and msg in err, (st, err)
+
+
+def _zero_args(f):
+    """NULL for every pointer, 0 for every number, following the binding's
+    argument types."""
+    out = []
+    for t in f.argtypes:
+        if t in (C.c_float, C.c_double):
+            out.append(t(0.0))
+        elif t in (C.c_int32, C.c_int64, C.c_uint32, C.c_uint64, C.c_size_t):
+            out.append(t(0))
+        else:
+            out.append(None)
+    return out
+
+
+def test_every_status_entry_rejects_null_arguments_before_device_work():
+    """Each ember_status entry point answers INVALID_ARG (with a message) when
+    its handles / buffers are NULL, without reaching the CUDA runtime."""
+    lib = E.load()
+    status_entries = [n for n in declared_symbols()
+                      if getattr(lib, n).restype is C.c_int and getattr(lib, n).argtypes]
+    assert len(status_entries) >= 15, status_entries
+    for n in status_entries:
+        f = getattr(lib, n)
+        st = f(*_zero_args(f))
+        assert st == 1, (n, st, E.last_error())
+        assert E.last_error(), n
+    # the void destructors accept NULL; the size query answers 0
+    lib.ember_model_destroy(None)
+    lib.ember_kv_free(None)
+    assert lib.ember_kv_bytes(None, 1, 1) == 0
